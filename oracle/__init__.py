@@ -1,0 +1,172 @@
+"""fp64 CPU oracle for paged decode attention (test infrastructure).
+
+Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's CPU
+baseline may import this package.  The product path (the CUDA library and its
+Python binding) never does, and this package never imports the product.
+
+The arithmetic lives in ``pa_oracle.c`` (plain loops in double, OpenMP over
+independent (row, head) items).  This module only compiles it, marshals numpy
+arrays and converts error codes.  Each function documents which passage of
+the pages it follows; the C file has the full list of readings.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pa_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "libpa_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile pa_oracle.c with gcc (-O2, OpenMP) into oracle/_build/libpa_oracle.so."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def bind(path: str):
+    """Load a compiled oracle library and declare its C signatures."""
+    lib = ctypes.CDLL(path)
+    P, I, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
+    lib.pa_oracle_gqa.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, D, I, I, P, P, P, P, I]
+    lib.pa_oracle_gqa_span.argtypes = [P, P, P, P, I, I, I, I, I, I, I, D, I, P, P, P, P, P, P, I]
+    lib.pa_oracle_merge.argtypes = [I, I, P, P, P, P]
+    lib.pa_oracle_mla.argtypes = [P, P, P, P, P, P, I, I, I, I, I, D, I, P, P, P, P, P, P, I]
+    lib.pa_oracle_num_threads.argtypes = []
+    for f in ("pa_oracle_gqa", "pa_oracle_gqa_span", "pa_oracle_merge", "pa_oracle_mla",
+              "pa_oracle_num_threads"):
+        getattr(lib, f).restype = ctypes.c_int
+    return lib
+
+
+def _load(lib=None):
+    global _lib
+    if lib is not None:
+        return lib
+    with _lock:
+        if _lib is None:
+            _lib = bind(build())
+    return _lib
+
+
+def num_threads(lib=None) -> int:
+    return int(_load(lib).pa_oracle_num_threads())
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _items(B, H, rows):
+    if rows is None:
+        bb, hh = np.meshgrid(np.arange(B), np.arange(H), indexing="ij")
+        return _c(bb.ravel(), np.int32), _c(hh.ravel(), np.int32)
+    rows = np.asarray(rows, dtype=np.int64).reshape(-1, 2)
+    return _c(rows[:, 0], np.int32), _c(rows[:, 1], np.int32)
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise ValueError(f"oracle {what} rejected its inputs (code {rc})")
+
+
+def gqa(q, k_pool, v_pool, block_table, context_lens, scale: float, window: int = 0,
+        rows=None, threads: int = 0, lib=None):
+    """GQA paged decode in fp64.
+
+    q [B, Hq, D], pools [pages, P, Hkv, D] (bf16 bit patterns, uint16), block_table
+    [B, max_pages] int32, context_lens [B] int32.  ``rows``: optional list of (b, h)
+    pairs; default all.  Returns (o [n, D] float64, lse [n] float64).
+    Query head h reads KV head h // (Hq // Hkv); with window W > 0 a row of length
+    L attends to its W most recent keys.
+    """
+    q, k_pool, v_pool = _c(q, np.uint16), _c(k_pool, np.uint16), _c(v_pool, np.uint16)
+    bt, lens = _c(block_table, np.int32), _c(context_lens, np.int32)
+    B, Hq, D = q.shape
+    npg, P, Hkv, D2 = k_pool.shape
+    assert D2 == D and v_pool.shape == k_pool.shape and bt.shape[0] == B
+    ib, ih = _items(B, Hq, rows)
+    n = ib.shape[0]
+    o = np.zeros((n, D), dtype=np.float64)
+    lse = np.zeros(n, dtype=np.float64)
+    rc = _load(lib).pa_oracle_gqa(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(bt), _ptr(lens), B, Hq,
+                               Hkv, D, P, npg, bt.shape[1], float(scale), int(window), n,
+                               _ptr(ib), _ptr(ih), _ptr(o), _ptr(lse), int(threads))
+    _check(rc, "gqa")
+    return o, lse
+
+
+def gqa_span(q, k_pool, v_pool, block_table, scale: float, items, threads: int = 0, lib=None):
+    """Attention of (b, h) over the explicit logical token span [t0, t1): items = [(b, h, t0, t1)]."""
+    q, k_pool, v_pool = _c(q, np.uint16), _c(k_pool, np.uint16), _c(v_pool, np.uint16)
+    bt = _c(block_table, np.int32)
+    B, Hq, D = q.shape
+    npg, P, Hkv, _ = k_pool.shape
+    it = np.asarray(items, dtype=np.int64).reshape(-1, 4)
+    ib, ih = _c(it[:, 0], np.int32), _c(it[:, 1], np.int32)
+    t0, t1 = _c(it[:, 2], np.int64), _c(it[:, 3], np.int64)
+    n = it.shape[0]
+    o = np.zeros((n, D), dtype=np.float64)
+    lse = np.zeros(n, dtype=np.float64)
+    rc = _load(lib).pa_oracle_gqa_span(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(bt), B, Hq, Hkv, D, P,
+                                    npg, bt.shape[1], float(scale), n, _ptr(ib), _ptr(ih), _ptr(t0),
+                                    _ptr(t1), _ptr(o), _ptr(lse), int(threads))
+    _check(rc, "gqa_span")
+    return o, lse
+
+
+def merge(parts_o, parts_lse, lib=None):
+    """LSE merge of split partials in ascending split order; empty splits carry lse = -inf."""
+    po = _c(parts_o, np.float64)
+    pl = _c(parts_lse, np.float64)
+    n, D = po.shape
+    o = np.zeros(D, dtype=np.float64)
+    lse = np.zeros(1, dtype=np.float64)
+    _check(_load(lib).pa_oracle_merge(n, D, _ptr(po), _ptr(pl), _ptr(o), _ptr(lse)), "merge")
+    return o, float(lse[0])
+
+
+def mla(q, cache, w_uk, w_uv, block_table, context_lens, scale: float, rows=None,
+        threads: int = 0, intermediates: bool = False, lib=None):
+    """MLA absorbed decode in fp64 (the seven steps of the absorbed schedule, no bf16 landings).
+
+    q [B, H, 192] (nope 128 || rope 64), cache [pages, P, 576], w_uk / w_uv [H, 128, 512].
+    Returns (o [n, 128], lse [n]) and, with ``intermediates``, also (q_lat [n, 512], o_lat [n, 512]).
+    """
+    q, cache = _c(q, np.uint16), _c(cache, np.uint16)
+    w_uk, w_uv = _c(w_uk, np.uint16), _c(w_uv, np.uint16)
+    bt, lens = _c(block_table, np.int32), _c(context_lens, np.int32)
+    B, H, QD = q.shape
+    npg, P, CD = cache.shape
+    assert QD == 192 and CD == 576 and w_uk.shape == (H, 128, 512) and w_uv.shape == (H, 128, 512)
+    ib, ih = _items(B, H, rows)
+    n = ib.shape[0]
+    o = np.zeros((n, 128), dtype=np.float64)
+    lse = np.zeros(n, dtype=np.float64)
+    ql = np.zeros((n, 512), dtype=np.float64) if intermediates else None
+    ol = np.zeros((n, 512), dtype=np.float64) if intermediates else None
+    rc = _load(lib).pa_oracle_mla(_ptr(q), _ptr(cache), _ptr(w_uk), _ptr(w_uv), _ptr(bt), _ptr(lens), B, H,
+                               P, npg, bt.shape[1], float(scale), n, _ptr(ib), _ptr(ih), _ptr(o),
+                               _ptr(lse), _ptr(ql) if ql is not None else None,
+                               _ptr(ol) if ol is not None else None, int(threads))
+    _check(rc, "mla")
+    if intermediates:
+        return o, lse, ql, ol
+    return o, lse

@@ -1,0 +1,340 @@
+"""Seeded synthetic inputs for paged decode attention.
+
+This module is the one piece shared by the CUDA path's tests/bench and the
+fp64 oracle's tests.  It only *draws numbers and lays them out*: it holds none
+of the attention arithmetic (no dot products, no softmax, no merge).
+
+Recipe (all counter-based, so any element can be regenerated on its own):
+
+* ``splitmix64``: output ``i`` of stream ``s`` is ``mix(s + (i + 1) * GOLDEN)``
+  (Steele, Lea, Flood, "Fast splittable pseudorandom number generators",
+  OOPSLA 2014; the finaliser is the published variant-13 mixer).
+* ``normal``: Box-Muller (cosine branch) on two consecutive outputs,
+  ``u1 = (x >> 11 + 1) * 2^-53`` in (0, 1], ``u2 = (y >> 11) * 2^-53`` in [0, 1).
+* bf16 values: float64 normal * std -> float32 (RNE) -> bf16 (RNE), stored as
+  raw ``uint16`` bit patterns.  Both sides of every parity test consume exactly
+  these bits.
+* context lengths: uniform integers on an inclusive range, or log-uniform as
+  ``floor(exp(U(ln a, ln b)))``, or a fixed list.
+* page pool: holds ``sum_b ceil(L_b / P)`` pages times an oversize factor.  A
+  seeded Fisher-Yates permutation assigns physical pages to logical pages.
+  Every slot that the attention must not read (unused pool pages, the tail of
+  each row's last page, pages wholly outside a sliding window) is filled with a
+  bf16 NaN, so a stray read poisons the result.
+* Data is drawn per *logical* (row, token, head, dim) coordinate, so the same
+  seed gives the same logical cache under any physical page permutation.
+
+The workloads mirror the decode shapes of the pages: the Llama-3-8B / Qwen3-32B
+GQA geometries and the 576-wide (512 latent + 64 rope) MLA cache of
+DeepSeek-V2-Lite named in the vllm.cpp kernel-matrix rows KERNEL-ATTN-FA2 and
+KERNEL-ATTN-MLA-SPARSE.  No public dataset is involved.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional, Sequence
+
+import numpy as np
+
+GOLDEN = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+BF16_NAN = np.uint16(0x7FC0)
+
+# stream tags: one independent splitmix64 stream per drawn quantity
+TAG_Q, TAG_K, TAG_V, TAG_LENS, TAG_PERM, TAG_CACHE, TAG_WUK, TAG_WUV = range(1, 9)
+
+
+def _mix(z: np.ndarray) -> np.ndarray:
+    z = (z ^ (z >> np.uint64(30))) * _M1
+    z = (z ^ (z >> np.uint64(27))) * _M2
+    return z ^ (z >> np.uint64(31))
+
+
+def splitmix64(state: int, index: np.ndarray) -> np.ndarray:
+    """Outputs ``index`` (0-based, uint64 array) of the splitmix64 stream seeded with ``state``."""
+    idx = np.asarray(index, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        return _mix(np.uint64(state) + (idx + np.uint64(1)) * GOLDEN)
+
+
+def stream_seed(seed: int, tag: int) -> int:
+    """Seed of the independent sub-stream ``tag`` of the workload seed ``seed``."""
+    with np.errstate(over="ignore"):
+        return int(splitmix64(seed, np.array([tag], dtype=np.uint64))[0])
+
+
+def uniform01(state: int, index: np.ndarray) -> np.ndarray:
+    """Uniform doubles in [0, 1) from the top 53 bits of each stream output."""
+    return (splitmix64(state, index) >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+
+
+def normal(state: int, index: np.ndarray) -> np.ndarray:
+    """Standard normal doubles, one per ``index``; uses stream outputs 2i and 2i+1."""
+    idx = np.asarray(index, dtype=np.uint64)
+    x = splitmix64(state, idx * np.uint64(2))
+    y = splitmix64(state, idx * np.uint64(2) + np.uint64(1))
+    u1 = ((x >> np.uint64(11)).astype(np.float64) + 1.0) * (2.0 ** -53)
+    u2 = (y >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+    return np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * math.pi * u2)
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to bf16 (round-to-nearest-even); NaN stays a quiet NaN."""
+    f = np.ascontiguousarray(x, dtype=np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    rounded = (u + np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)
+    out = rounded.astype(np.uint16)
+    nan = np.isnan(f)
+    if nan.any():
+        out[nan] = BF16_NAN
+    return out
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Widen raw bf16 bit patterns to float32 (exact)."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def normal_bf16(state: int, index: np.ndarray, std: float = 1.0) -> np.ndarray:
+    return f32_to_bf16_bits((normal(state, index) * std).astype(np.float32))
+
+
+def _normal_bf16_range(state: int, start: int, n: int, std: float, chunk: int = 1 << 18) -> np.ndarray:
+    """bf16 normals for stream indices [start, start + n), drawn in cache-sized chunks."""
+    out = np.empty(n, dtype=np.uint16)
+    for s in range(0, n, chunk):
+        e = min(n, s + chunk)
+        out[s:e] = normal_bf16(state, np.arange(start + s, start + e, dtype=np.uint64), std)
+    return out
+
+
+def _normal_bf16_dense(state: int, n: int, std: float) -> np.ndarray:
+    return _normal_bf16_range(state, 0, n, std)
+
+
+def permutation(state: int, n: int) -> np.ndarray:
+    """Seeded Fisher-Yates shuffle of range(n) (Durstenfeld form, j drawn from [0, i])."""
+    perm = np.arange(n, dtype=np.int64)
+    if n <= 1:
+        return perm
+    u = uniform01(state, np.arange(n, dtype=np.uint64))
+    for i in range(n - 1, 0, -1):
+        j = int(u[i] * (i + 1))
+        perm[i], perm[j] = perm[j], perm[i]
+    return perm
+
+
+def context_lengths(seed: int, batch: int, dist: str, lo: int = 0, hi: int = 0,
+                    values: Optional[Sequence[int]] = None) -> np.ndarray:
+    """Per-row context lengths: ``fixed`` list, ``uniform`` on [lo, hi], or ``loguniform`` on [lo, hi]."""
+    if dist == "fixed":
+        assert values is not None and len(values) == batch
+        return np.asarray(values, dtype=np.int32)
+    u = uniform01(stream_seed(seed, TAG_LENS), np.arange(batch, dtype=np.uint64))
+    if dist == "uniform":
+        lens = lo + np.floor(u * (hi - lo + 1)).astype(np.int64)
+    elif dist == "loguniform":
+        lens = np.floor(np.exp(math.log(lo) + u * (math.log(hi) - math.log(lo)))).astype(np.int64)
+    else:
+        raise ValueError(dist)
+    return np.clip(lens, lo, hi).astype(np.int32)
+
+
+def visible_range(L: int, window: int) -> tuple:
+    """Token range [lo, L) a query row attends to: the W most recent keys when window W > 0."""
+    lo = max(0, L - window) if window > 0 else 0
+    return lo, L
+
+
+@dataclasses.dataclass
+class PagedLayout:
+    """Block table + pool geometry shared by the GQA and MLA workloads."""
+    page_size: int
+    context_lens: np.ndarray          # [B] int32
+    block_table: np.ndarray           # [B, max_pages_per_seq] int32, -1 past the row's pages
+    num_pages: int                    # physical pages in the pool
+    logical_page_of_row: np.ndarray   # [B] first global logical page index of each row
+    phys_of_logical: np.ndarray       # [total logical pages] physical page id
+
+    @property
+    def batch(self) -> int:
+        return int(self.context_lens.shape[0])
+
+    @property
+    def max_pages_per_seq(self) -> int:
+        return int(self.block_table.shape[1])
+
+
+def make_layout(seed: int, context_lens: np.ndarray, page_size: int, pool_factor: int = 1,
+                scramble: bool = True, extra_table_cols: int = 0) -> PagedLayout:
+    lens = np.asarray(context_lens, dtype=np.int32)
+    B = lens.shape[0]
+    pages = [(int(L) + page_size - 1) // page_size for L in lens]
+    total = int(sum(pages))
+    num_pages = max(1, total * pool_factor)
+    perm = permutation(stream_seed(seed, TAG_PERM), num_pages) if scramble else np.arange(num_pages)
+    phys_of_logical = perm[:total].astype(np.int32)
+    max_pages = max(1, max(pages) + extra_table_cols)
+    table = np.full((B, max_pages), -1, dtype=np.int32)
+    first = np.zeros(B, dtype=np.int64)
+    off = 0
+    for b in range(B):
+        first[b] = off
+        table[b, : pages[b]] = phys_of_logical[off: off + pages[b]]
+        off += pages[b]
+    return PagedLayout(page_size, lens, table, num_pages, first, phys_of_logical)
+
+
+def _fill_pool(state: int, layout: PagedLayout, row_width: int, std: float, window: int,
+               visible_only: bool) -> np.ndarray:
+    """Pool [num_pages, P, row_width] bf16 bits; values drawn per logical (page, slot, element)."""
+    P = layout.page_size
+    pool = np.full((layout.num_pages, P, row_width), BF16_NAN, dtype=np.uint16)
+    per_page = P * row_width
+    for b in range(layout.batch):
+        L = int(layout.context_lens[b])
+        if L == 0:
+            continue
+        lo, hi = visible_range(L, window) if visible_only else (0, L)
+        p0, p1 = lo // P, (hi + P - 1) // P
+        g0 = int(layout.logical_page_of_row[b])
+        vals = _normal_bf16_range(state, (g0 + p0) * per_page, (p1 - p0) * per_page, std)
+        vals = vals.reshape(p1 - p0, P, row_width)
+        flat = vals.reshape((p1 - p0) * P, row_width)
+        # poison the slots of the visited pages that lie outside [lo, hi)
+        flat[: lo - p0 * P] = BF16_NAN
+        flat[hi - p0 * P:] = BF16_NAN
+        pool[layout.block_table[b, p0:p1]] = vals
+    return pool
+
+
+@dataclasses.dataclass
+class GQAWorkload:
+    name: str
+    seed: int
+    q: np.ndarray            # [B, Hq, D] bf16 bits
+    k_pool: np.ndarray       # [num_pages, P, Hkv, D] bf16 bits
+    v_pool: np.ndarray       # [num_pages, P, Hkv, D] bf16 bits
+    layout: PagedLayout
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    scale: float
+    window: int
+    k_std: float = 1.0
+
+    @property
+    def batch(self):
+        return self.layout.batch
+
+    def visible_tokens(self) -> int:
+        return int(sum(visible_range(int(L), self.window)[1] - visible_range(int(L), self.window)[0]
+                       for L in self.layout.context_lens))
+
+    def algorithmic_bytes(self) -> int:
+        """Bytes the method must move: every visible K and V row of each kv head, all of q, and the output."""
+        kv = self.visible_tokens() * self.num_kv_heads * self.head_dim * 2 * 2
+        qb = self.batch * self.num_q_heads * self.head_dim * 2
+        ob = self.batch * self.num_q_heads * (self.head_dim * 2 + 4)
+        return kv + qb + ob
+
+
+def make_gqa(seed: int, context_lens, num_q_heads: int, num_kv_heads: int, head_dim: int,
+             page_size: int, window: int = 0, k_std: float = 1.0, pool_factor: int = 1,
+             scale: Optional[float] = None, scramble: bool = True, name: str = "gqa",
+             visible_only: bool = True, extra_table_cols: int = 0) -> GQAWorkload:
+    lens = np.asarray(context_lens, dtype=np.int32)
+    layout = make_layout(seed, lens, page_size, pool_factor, scramble, extra_table_cols)
+    B = lens.shape[0]
+    q = _normal_bf16_dense(stream_seed(seed, TAG_Q), B * num_q_heads * head_dim, 1.0)
+    q = q.reshape(B, num_q_heads, head_dim)
+    w = num_kv_heads * head_dim
+    k = _fill_pool(stream_seed(seed, TAG_K), layout, w, k_std, window, visible_only)
+    v = _fill_pool(stream_seed(seed, TAG_V), layout, w, 1.0, window, visible_only)
+    k = k.reshape(layout.num_pages, page_size, num_kv_heads, head_dim)
+    v = v.reshape(layout.num_pages, page_size, num_kv_heads, head_dim)
+    if scale is None:
+        scale = 1.0 / math.sqrt(head_dim)
+    return GQAWorkload(name, seed, q, k, v, layout, num_q_heads, num_kv_heads, head_dim,
+                       float(scale), int(window), float(k_std))
+
+
+MLA_NOPE, MLA_ROPE, MLA_LATENT, MLA_VDIM = 128, 64, 512, 128
+MLA_QDIM = MLA_NOPE + MLA_ROPE          # 192
+MLA_CDIM = MLA_LATENT + MLA_ROPE        # 576
+
+
+@dataclasses.dataclass
+class MLAWorkload:
+    name: str
+    seed: int
+    q: np.ndarray       # [B, H, 192] bf16 bits: q_nope (128) || q_rope (64)
+    cache: np.ndarray   # [num_pages, P, 576] bf16 bits: latent (512) || rope key (64)
+    w_uk: np.ndarray    # [H, 128, 512] bf16 bits, W_UK[h][d][j]
+    w_uv: np.ndarray    # [H, 128, 512] bf16 bits, W_UV[h][dv][j]
+    layout: PagedLayout
+    num_heads: int
+    scale: float
+
+    @property
+    def batch(self):
+        return self.layout.batch
+
+    def visible_tokens(self) -> int:
+        return int(sum(int(L) for L in self.layout.context_lens))
+
+    def algorithmic_bytes(self, with_weights: bool = True) -> int:
+        c = self.visible_tokens() * MLA_CDIM * 2
+        qb = self.batch * self.num_heads * MLA_QDIM * 2
+        ob = self.batch * self.num_heads * (MLA_VDIM * 2 + 4)
+        wb = 2 * self.num_heads * MLA_NOPE * MLA_LATENT * 2 if with_weights else 0
+        return c + qb + ob + wb
+
+
+def make_mla(seed: int, context_lens, num_heads: int, page_size: int, w_std: float = 0.02,
+             scale: Optional[float] = None, scramble: bool = True, pool_factor: int = 1,
+             name: str = "mla") -> MLAWorkload:
+    lens = np.asarray(context_lens, dtype=np.int32)
+    layout = make_layout(seed, lens, page_size, pool_factor, scramble)
+    B = lens.shape[0]
+    q = _normal_bf16_dense(stream_seed(seed, TAG_Q), B * num_heads * MLA_QDIM, 1.0)
+    q = q.reshape(B, num_heads, MLA_QDIM)
+    cache = _fill_pool(stream_seed(seed, TAG_CACHE), layout, MLA_CDIM, 1.0, 0, True)
+    n_w = num_heads * MLA_NOPE * MLA_LATENT
+    w_uk = _normal_bf16_dense(stream_seed(seed, TAG_WUK), n_w, w_std).reshape(num_heads, MLA_NOPE, MLA_LATENT)
+    w_uv = _normal_bf16_dense(stream_seed(seed, TAG_WUV), n_w, w_std).reshape(num_heads, MLA_VDIM, MLA_LATENT)
+    if scale is None:
+        scale = 1.0 / math.sqrt(MLA_QDIM)
+    return MLAWorkload(name, seed, q, cache, w_uk, w_uv, layout, num_heads, float(scale))
+
+
+# ---------------------------------------------------------------------------
+# The five workloads of the build (seed = 20260 + index).  Shapes follow the
+# decode geometries the pages discuss; see the design doc for the recipe table.
+# ---------------------------------------------------------------------------
+WORKLOADS = ("tiny", "llama3-8b", "qwen3-32b", "hd256-window", "mla")
+
+
+def workload(name: str, seed: Optional[int] = None, scramble: bool = True):
+    i = WORKLOADS.index(name)
+    seed = 20260 + i if seed is None else seed
+    if name == "tiny":
+        lens = context_lengths(seed, 6, "fixed", values=[1, 31, 32, 33, 64, 100])
+        return make_gqa(seed, lens, 8, 2, 128, 32, name=name, scramble=scramble)
+    if name == "llama3-8b":
+        lens = context_lengths(seed, 8, "uniform", 512, 4096)
+        return make_gqa(seed, lens, 32, 8, 128, 16, k_std=0.5, pool_factor=2, name=name,
+                        scramble=scramble)
+    if name == "qwen3-32b":
+        lens = context_lengths(seed, 32, "loguniform", 128, 16384)
+        return make_gqa(seed, lens, 64, 8, 128, 32, name=name, scramble=scramble)
+    if name == "hd256-window":
+        lens = context_lengths(seed, 16, "uniform", 2048, 32768)
+        return make_gqa(seed, lens, 16, 4, 256, 32, window=4096, name=name, scramble=scramble)
+    if name == "mla":
+        lens = context_lengths(seed, 16, "uniform", 1024, 8192)
+        return make_mla(seed, lens, 128, 64, name=name, scramble=scramble)
+    raise KeyError(name)
