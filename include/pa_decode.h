@@ -1,0 +1,170 @@
+/*
+ * pa_decode.h -- C ABI of the paged decode attention library (GB300, sm_103a).
+ *
+ * Single-token decode (and speculative-verify) attention of a batch of query
+ * rows against a paged bf16 KV cache, in two variants:
+ *
+ *   pa_decode_gqa           grouped-query attention, optional sliding window
+ *   pa_decode_mla_absorbed  multi-head latent attention in the absorbed form
+ *
+ * The operations are the ones the following pages describe:
+ *   - paged cache: K/V pools [pages, block_size, Hkv, D], per-request
+ *     seq_lens, and a block table (vllm.cpp kernel-matrix, rows
+ *     KERNEL-ATTN-PAGED and KERNEL-ATTN-DFLASH-PAGED-BLOCK);
+ *   - query heads sharing one KV head, served by one CTA per (batch, KV head)
+ *     so that every KV page is read once per group (vllm.cpp PR #49 "flip
+ *     decode GQA group-swap default ON", mechanism paragraph);
+ *   - f32 online softmax over the KV sequence and the HasWindow arm
+ *     (vllm.cpp PR #425 "head_dim-128 arm for the warp-split-KV decode
+ *     kernel", description and limitations list);
+ *   - split-KV over the sequence with a separate combine step that merges
+ *     splits in a fixed ascending order, no atomics, empty splits skipped
+ *     (kernel-matrix rows KERNEL-ATTN-FA2 and KERNEL-ATTN-MLA-SPARSE);
+ *   - the absorbed MLA schedule q_lat = q_nope.W_UK || q_rope, scores over
+ *     the 576-wide latent cache, o_lat = sum p c, o = W_UV.o_lat (pegainfer
+ *     PR #938 "warp-cooperative two-pass MLA absorbed decode kernel",
+ *     Schedule section, steps 1-7; kernel-matrix row KERNEL-ATTN-MLA-SPARSE,
+ *     weight absorption as two batched contractions);
+ *   - the raw pointer / shape / scalar / workspace / stream calling
+ *     convention of the planned drop-in kernel ABI (kernel-matrix preamble).
+ *
+ * Conventions shared by every entry point
+ *   - Every data pointer is DEVICE memory owned by the caller; the library
+ *     allocates nothing and keeps no state between calls (re-entrant).  The
+ *     only library state is the optional per-host-thread profiling hook.
+ *   - Tensors are dense, row-major, in the layouts written beside each
+ *     argument.  bf16 means IEEE bfloat16 bit patterns.  q, pools, cache,
+ *     weights, out and workspace must be 16-byte aligned; block_table,
+ *     context_lens and lse 4-byte aligned.  Misalignment returns
+ *     PA_ERR_MISALIGNED before anything is launched.
+ *   - Calls are asynchronous on `stream` (no host synchronisation) except
+ *     pa_read_device_status.
+ *   - Scores are scale * q.k in fp32; probabilities and accumulators are
+ *     fp32; out is rounded to bf16 (round to nearest even); lse is the
+ *     natural-log log-sum-exp of the scores in fp32, -inf for an empty row
+ *     (whose out is 0).
+ *   - Row b attends to logical tokens [lo, L) with L = context_lens[b] and
+ *     lo = max(0, L - window) when window > 0 (the `window` most recent keys,
+ *     current token included), else lo = 0.  Logical token t lives in
+ *     physical page block_table[b][t / page_size], slot t % page_size.
+ *     Table entries past a row's last visible page are never read.
+ *   - Preconditions the host cannot check (they live in device memory):
+ *     0 <= context_lens[b] <= max_context_len and every visited table entry
+ *     in [0, num_pages).  A violation never traps: the kernel records a bit
+ *     in the workspace's device status word (pa_read_device_status), clamps
+ *     the length / skips the page, and the output of that row is unspecified.
+ *   - num_splits: 0 = automatic (the library balances page-aligned chunks of
+ *     all rows over the SMs); n > 0 = every row is cut into n page-aligned
+ *     chunks of ceil(pages / n) pages, trailing chunks possibly empty.  For a
+ *     fixed num_splits (and fixed inputs) results are bitwise reproducible
+ *     from run to run and independent of the physical page order; different
+ *     split counts agree within rounding.
+ *   - Workspace: at least pa_workspace_size(...) bytes of device memory for
+ *     the same (kind, shape, max_context_len, page_size, num_splits).  Its
+ *     contents need no initialisation and are overwritten by each call;
+ *     calls sharing one workspace must be ordered on one stream.
+ */
+#ifndef PA_DECODE_H
+#define PA_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes of every entry point. */
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARGUMENT = -1, /* a size <= 0 where one is needed, Hq % Hkv != 0, NULL pointer, ... */
+  PA_ERR_UNSUPPORTED = -2,      /* head_dim not 64/128/256, page_size not a power of two in [1, 256], ... */
+  PA_ERR_MISALIGNED = -3,       /* a pointer breaks the alignment rule above */
+  PA_ERR_WORKSPACE_TOO_SMALL = -4,
+  PA_ERR_CUDA = -5              /* a CUDA runtime call or launch failed (cudaGetLastError is left set) */
+} pa_status;
+
+typedef enum { PA_KIND_GQA = 0, PA_KIND_MLA_ABSORBED = 1 } pa_kind;
+
+/* Bits of the device status word (see pa_read_device_status). */
+#define PA_DEV_BAD_PAGE 0x1u /* a visited block-table entry was outside [0, num_pages) */
+#define PA_DEV_BAD_LEN 0x2u  /* a context length was < 0 or > max_context_len */
+#define PA_DEV_TIMEOUT 0x4u  /* a bounded wait inside a kernel gave up (never expected) */
+
+/*
+ * Bytes of device workspace a call with these arguments needs.  For
+ * PA_KIND_MLA_ABSORBED, num_q_heads is the head count and num_kv_heads /
+ * head_dim are ignored.  Returns 0 for arguments the matching decode call
+ * would reject.
+ */
+size_t pa_workspace_size(int kind, int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                         int max_context_len, int page_size, int num_splits);
+
+/*
+ * GQA paged decode.
+ *   q            [batch, num_q_heads, head_dim] bf16
+ *   k_pool       [num_pages, page_size, num_kv_heads, head_dim] bf16
+ *   v_pool       same shape as k_pool
+ *   block_table  [batch, max_pages_per_seq] int32, logical page -> physical page
+ *   context_lens [batch] int32
+ *   out          [batch, num_q_heads, head_dim] bf16 (written)
+ *   lse          [batch, num_q_heads] fp32 natural-log LSE (written), or NULL
+ * Query head h reads KV head h / (num_q_heads / num_kv_heads).
+ * head_dim in {64, 128, 256}; page_size a power of two in [1, 256];
+ * max_pages_per_seq >= ceil(max_context_len / page_size); window <= 0 means
+ * no window; num_splits in [0, 1024].  batch == 0 is a no-op returning PA_OK.
+ */
+int pa_decode_gqa(const void *q, const void *k_pool, const void *v_pool,
+                  const int32_t *block_table, const int32_t *context_lens, void *out, float *lse,
+                  int batch, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+                  int num_pages, int max_pages_per_seq, int max_context_len, float scale,
+                  int window, int num_splits, void *workspace, size_t workspace_bytes,
+                  cudaStream_t stream);
+
+/*
+ * MLA absorbed decode (DeepSeek-V2-style geometry: 128 nope + 64 rope query
+ * dims, 512 latent + 64 rope cache dims, 128 value dims per head).
+ *   q            [batch, num_heads, 192] bf16: q_nope (128) || q_rope (64)
+ *   cache        [num_pages, page_size, 576] bf16: latent c (512) || rope key (64)
+ *   w_uk         [num_heads, 128, 512] bf16, W_UK[h][d][j]: q_lat[j] = sum_d q_nope[d] W_UK[h][d][j]
+ *   w_uv         [num_heads, 128, 512] bf16, W_UV[h][v][j]: o[v] = sum_j W_UV[h][v][j] o_lat[j]
+ *   block_table, context_lens as for GQA (one latent head shared by all heads)
+ *   out          [batch, num_heads, 128] bf16 (written)
+ *   lse          [batch, num_heads] fp32 (written), or NULL
+ * page_size a power of two in [1, 256]; num_splits as for GQA.
+ */
+int pa_decode_mla_absorbed(const void *q, const void *cache, const void *w_uk, const void *w_uv,
+                           const int32_t *block_table, const int32_t *context_lens, void *out,
+                           float *lse, int batch, int num_heads, int page_size, int num_pages,
+                           int max_pages_per_seq, int max_context_len, float scale,
+                           int num_splits, void *workspace, size_t workspace_bytes,
+                           cudaStream_t stream);
+
+/* Static text for a pa_status value (never NULL). */
+const char *pa_status_string(int status);
+
+/*
+ * Synchronises `stream`, then copies the device status word of `workspace`
+ * (as left by the last call that used it) into *out_bits (PA_DEV_* bits).
+ * Returns PA_ERR_CUDA if the copy or the synchronisation fails.
+ */
+int pa_read_device_status(const void *workspace, cudaStream_t stream, uint32_t *out_bits);
+
+/*
+ * Measurement hook: on the calling host thread, subsequent decode calls
+ * record `before_main` just before and `after_main` just after the launch of
+ * their dominant kernel (the split-KV attention kernel), on the call's
+ * stream.  Pass NULL, NULL to switch it off.  Events are owned by the caller.
+ */
+int pa_set_profile_events(cudaEvent_t before_main, cudaEvent_t after_main);
+
+/* Number of kernel launches the last decode call on this host thread issued. */
+int pa_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_DECODE_H */

@@ -1,0 +1,310 @@
+// pa_api.cu -- the C ABI (include/pa_decode.h): argument validation, workspace
+// layout, TMA tensor-map encoding and the launch sequence of each call.
+//
+// Every check that can be made on the host is made before anything is
+// launched, so an invalid call returns an error code with no device work and
+// no CUDA call at all.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "pa_decode.h"
+#include "pa_gqa.cuh"
+#include "pa_launch.h"
+#include "pa_mla.h"
+
+namespace pa {
+cudaError_t launch_gqa_split_d64(int GP, int grid, const CUtensorMap &, const CUtensorMap &, const GqaArgs &,
+                                 cudaStream_t);
+cudaError_t launch_gqa_split_d128(int GP, int grid, const CUtensorMap &, const CUtensorMap &, const GqaArgs &,
+                                  cudaStream_t);
+cudaError_t launch_gqa_split_d256(int GP, int grid, const CUtensorMap &, const CUtensorMap &, const GqaArgs &,
+                                  cudaStream_t);
+cudaError_t launch_gqa_combine_d64(const CombineArgs &, cudaStream_t);
+cudaError_t launch_gqa_combine_d128(const CombineArgs &, cudaStream_t);
+cudaError_t launch_gqa_combine_d256(const CombineArgs &, cudaStream_t);
+}  // namespace pa
+
+namespace {
+
+using namespace pa;
+
+constexpr int kMinChunkTokens = 128;  // automatic mode: smallest split, in tokens
+constexpr int kItemsPerCta = 8;       // automatic mode: work items per persistent CTA
+constexpr int kMaxSplits = 1024;      // largest accepted explicit num_splits
+
+thread_local cudaEvent_t t_ev_before = nullptr;
+thread_local cudaEvent_t t_ev_after = nullptr;
+thread_local int t_last_launches = 0;
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+int ilog2(int x) {
+  int l = 0;
+  while ((1 << l) < x) ++l;
+  return l;
+}
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int gqa_stage_tokens_of(int D) { return 32768 / (2 * D * 2); }
+
+struct GqaPlan {
+  int GP, nsub, max_splits, min_chunk_pages, chunk_align;
+  size_t off_rows, off_items, off_part_lse, off_part_o, total;
+};
+
+// Shape checks shared by pa_workspace_size and pa_decode_gqa; PA_OK or an error code.
+int gqa_shape(int batch, int Hq, int Hkv, int D, int max_ctx, int P, int num_splits, GqaPlan *pl) {
+  if (batch < 0 || Hq <= 0 || Hkv <= 0 || max_ctx < 0 || num_splits < 0) return PA_ERR_INVALID_ARGUMENT;
+  if (Hq % Hkv != 0) return PA_ERR_INVALID_ARGUMENT;
+  if (num_splits > kMaxSplits) return PA_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128 && D != 256) return PA_ERR_UNSUPPORTED;
+  if (!is_pow2(P) || P > 256) return PA_ERR_UNSUPPORTED;
+  const int G = Hq / Hkv;
+  pl->GP = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8;
+  pl->nsub = (G + pl->GP - 1) / pl->GP;
+  const int ST = gqa_stage_tokens_of(D);
+  pl->chunk_align = P >= ST ? 1 : ST / P;
+  int mcp = kMinChunkTokens / P;
+  if (mcp < 1) mcp = 1;
+  pl->min_chunk_pages = (int)round_up((size_t)mcp, (size_t)pl->chunk_align);
+  const long long max_pages = max_ctx == 0 ? 1 : ((long long)max_ctx + P - 1) / P;
+  pl->max_splits = num_splits > 0 ? num_splits : (int)((max_pages + pl->min_chunk_pages - 1) / pl->min_chunk_pages);
+  if (pl->max_splits < 1) pl->max_splits = 1;
+  const size_t B = (size_t)(batch > 0 ? batch : 1);
+  const size_t items = B * (size_t)Hkv * (size_t)pl->nsub * (size_t)pl->max_splits;
+  if (items > (size_t)INT32_MAX) return PA_ERR_UNSUPPORTED;
+  size_t off = sizeof(WsHeader);
+  pl->off_rows = off;
+  off = round_up(off + B * sizeof(RowInfo), 256);
+  pl->off_items = off;
+  off = round_up(off + items * sizeof(WorkItem), 256);
+  pl->off_part_lse = off;
+  off = round_up(off + B * (size_t)Hq * pl->max_splits * sizeof(float), 256);
+  pl->off_part_o = off;
+  off = round_up(off + B * (size_t)Hq * pl->max_splits * (size_t)D * sizeof(float), 256);
+  pl->total = off;
+  return PA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 4-D map over a [num_pages, P, H, D] bf16 pool, box = (D, 1 head, BH tokens, 1 page).
+bool encode_pool_map(CUtensorMap *m, const void *base, int num_pages, int P, int H, int D, int BH) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)P, (cuuint64_t)num_pages};
+  cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)P * H * D * 2};
+  cuuint32_t box[4] = {(cuuint32_t)D, 1u, (cuuint32_t)BH, 1u};
+  cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  static int cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (dev < 0 || dev >= 64) return -1;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+
+}  // namespace
+
+extern "C" {
+
+size_t pa_workspace_size(int kind, int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                         int max_context_len, int page_size, int num_splits) {
+  if (kind == PA_KIND_GQA) {
+    GqaPlan pl;
+    if (gqa_shape(batch, num_q_heads, num_kv_heads, head_dim, max_context_len, page_size, num_splits, &pl) !=
+        PA_OK)
+      return 0;
+    return pl.total;
+  }
+  if (kind == PA_KIND_MLA_ABSORBED) {
+    return pa::mla_workspace_size(batch, num_q_heads, max_context_len, page_size, num_splits);
+  }
+  return 0;
+}
+
+int pa_decode_gqa(const void *q, const void *k_pool, const void *v_pool, const int32_t *block_table,
+                  const int32_t *context_lens, void *out, float *lse, int batch, int num_q_heads,
+                  int num_kv_heads, int head_dim, int page_size, int num_pages, int max_pages_per_seq,
+                  int max_context_len, float scale, int window, int num_splits, void *workspace,
+                  size_t workspace_bytes, cudaStream_t stream) {
+  t_last_launches = 0;
+  if (batch == 0) return PA_OK;
+  GqaPlan pl;
+  int rc = gqa_shape(batch, num_q_heads, num_kv_heads, head_dim, max_context_len, page_size, num_splits, &pl);
+  if (rc != PA_OK) return rc;
+  if (!q || !k_pool || !v_pool || !block_table || !context_lens || !out || !workspace)
+    return PA_ERR_INVALID_ARGUMENT;
+  if (num_pages <= 0 || max_pages_per_seq <= 0 || !std::isfinite(scale)) return PA_ERR_INVALID_ARGUMENT;
+  if ((long long)max_pages_per_seq * page_size < (long long)max_context_len) return PA_ERR_INVALID_ARGUMENT;
+  if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16) ||
+      !aligned(workspace, 16) || !aligned(block_table, 4) || !aligned(context_lens, 4) ||
+      (lse && !aligned(lse, 4)))
+    return PA_ERR_MISALIGNED;
+  if (workspace_bytes < pl.total) return PA_ERR_WORKSPACE_TOO_SMALL;
+
+  const int D = head_dim, P = page_size;
+  const int ST = gqa_stage_tokens_of(D);
+  const int BH = P < ST ? P : ST;
+  CUtensorMap tm_k, tm_v;
+  if (!encode_pool_map(&tm_k, k_pool, num_pages, P, num_kv_heads, D, BH) ||
+      !encode_pool_map(&tm_v, v_pool, num_pages, P, num_kv_heads, D, BH))
+    return PA_ERR_UNSUPPORTED;
+  const int sms = sm_count();
+  if (sms <= 0) return PA_ERR_CUDA;
+
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  WsHeader *hdr = reinterpret_cast<WsHeader *>(ws);
+  RowInfo *rows = reinterpret_cast<RowInfo *>(ws + pl.off_rows);
+  WorkItem *items = reinterpret_cast<WorkItem *>(ws + pl.off_items);
+  float *part_lse = reinterpret_cast<float *>(ws + pl.off_part_lse);
+  float *part_o = reinterpret_cast<float *>(ws + pl.off_part_o);
+
+  const long long max_items = (long long)batch * num_kv_heads * pl.nsub * pl.max_splits;
+  const int grid = (int)(max_items < sms ? max_items : sms);
+
+  PlanArgs pa_;
+  pa_.context_lens = context_lens;
+  pa_.batch = batch;
+  pa_.heads_per_row = num_kv_heads * pl.nsub;
+  pa_.page_size = P;
+  pa_.log2_page = ilog2(P);
+  pa_.window = window > 0 ? window : 0;
+  pa_.max_context_len = max_context_len;
+  pa_.num_splits = num_splits;
+  pa_.max_splits = pl.max_splits;
+  pa_.target_items = grid * kItemsPerCta;
+  pa_.min_chunk_pages = pl.min_chunk_pages;
+  pa_.chunk_align = pl.chunk_align;
+  pa_.hdr = hdr;
+  pa_.rows = rows;
+  pa_.items = items;
+
+  GqaArgs ga;
+  ga.q = static_cast<const uint16_t *>(q);
+  ga.block_table = block_table;
+  ga.out = static_cast<uint16_t *>(out);
+  ga.lse = lse;
+  ga.part_o = part_o;
+  ga.part_lse = part_lse;
+  ga.hdr = hdr;
+  ga.items = items;
+  ga.rows = rows;
+  ga.max_pages_per_seq = max_pages_per_seq;
+  ga.num_pages = num_pages;
+  ga.Hq = num_q_heads;
+  ga.Hkv = num_kv_heads;
+  ga.G = num_q_heads / num_kv_heads;
+  ga.nsub = pl.nsub;
+  ga.page_size = P;
+  ga.log2_page = ilog2(P);
+  ga.max_splits = pl.max_splits;
+  ga.qscale = scale * LOG2E;
+
+  CombineArgs ca;
+  ca.out = static_cast<uint16_t *>(out);
+  ca.lse = lse;
+  ca.part_o = part_o;
+  ca.part_lse = part_lse;
+  ca.rows = rows;
+  ca.batch = batch;
+  ca.Hq = num_q_heads;
+  ca.D = D;
+  ca.max_splits = pl.max_splits;
+
+  cudaError_t e = launch_plan(pa_, stream);
+  if (e != cudaSuccess) return PA_ERR_CUDA;
+  ++t_last_launches;
+  if (t_ev_before && cudaEventRecord(t_ev_before, stream) != cudaSuccess) return PA_ERR_CUDA;
+  switch (D) {
+    case 64: e = launch_gqa_split_d64(pl.GP, grid, tm_k, tm_v, ga, stream); break;
+    case 128: e = launch_gqa_split_d128(pl.GP, grid, tm_k, tm_v, ga, stream); break;
+    default: e = launch_gqa_split_d256(pl.GP, grid, tm_k, tm_v, ga, stream); break;
+  }
+  if (e != cudaSuccess) return PA_ERR_CUDA;
+  ++t_last_launches;
+  if (t_ev_after && cudaEventRecord(t_ev_after, stream) != cudaSuccess) return PA_ERR_CUDA;
+  switch (D) {
+    case 64: e = launch_gqa_combine_d64(ca, stream); break;
+    case 128: e = launch_gqa_combine_d128(ca, stream); break;
+    default: e = launch_gqa_combine_d256(ca, stream); break;
+  }
+  if (e != cudaSuccess) return PA_ERR_CUDA;
+  ++t_last_launches;
+  return PA_OK;
+}
+
+int pa_decode_mla_absorbed(const void *q, const void *cache, const void *w_uk, const void *w_uv,
+                           const int32_t *block_table, const int32_t *context_lens, void *out, float *lse,
+                           int batch, int num_heads, int page_size, int num_pages, int max_pages_per_seq,
+                           int max_context_len, float scale, int num_splits, void *workspace,
+                           size_t workspace_bytes, cudaStream_t stream) {
+  t_last_launches = 0;
+  int launches = 0;
+  const int rc = pa::mla_decode(q, cache, w_uk, w_uv, block_table, context_lens, out, lse, batch, num_heads,
+                                page_size, num_pages, max_pages_per_seq, max_context_len, scale, num_splits,
+                                workspace, workspace_bytes, stream, t_ev_before, t_ev_after, &launches);
+  t_last_launches = launches;
+  return rc;
+}
+
+const char *pa_status_string(int status) {
+  switch (status) {
+    case PA_OK: return "ok";
+    case PA_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case PA_ERR_UNSUPPORTED: return "unsupported shape or parameter";
+    case PA_ERR_MISALIGNED: return "misaligned pointer";
+    case PA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case PA_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+int pa_read_device_status(const void *workspace, cudaStream_t stream, uint32_t *out_bits) {
+  if (!workspace || !out_bits) return PA_ERR_INVALID_ARGUMENT;
+  if (!aligned(workspace, 16)) return PA_ERR_MISALIGNED;
+  uint32_t v = 0;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return PA_ERR_CUDA;
+  if (cudaMemcpy(&v, workspace, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return PA_ERR_CUDA;
+  *out_bits = v;
+  return PA_OK;
+}
+
+int pa_set_profile_events(cudaEvent_t before_main, cudaEvent_t after_main) {
+  if ((before_main == nullptr) != (after_main == nullptr)) return PA_ERR_INVALID_ARGUMENT;
+  t_ev_before = before_main;
+  t_ev_after = after_main;
+  return PA_OK;
+}
+
+int pa_last_launch_count(void) { return t_last_launches; }
+
+}  // extern "C"

@@ -82,6 +82,7 @@ def lse_max_abs(got, ref) -> float:
     g = np.asarray(got, dtype=np.float64).ravel()
     r = np.asarray(ref, dtype=np.float64).ravel()
     both_inf = np.isinf(g) & np.isinf(r) & (np.sign(g) == np.sign(r))
-    d = np.where(both_inf, 0.0, np.abs(g - r))
+    with np.errstate(invalid="ignore"):
+        d = np.where(both_inf, 0.0, np.abs(g - r))
     d = np.where(np.isnan(d), np.inf, d)
     return float(d.max()) if d.size else 0.0
