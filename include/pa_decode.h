@@ -18,8 +18,8 @@
  *     (vllm.cpp PR #425 "head_dim-128 arm for the warp-split-KV decode
  *     kernel", description and limitations list);
  *   - split-KV over the sequence with a separate combine step that merges
- *     splits in a fixed ascending order, no atomics, empty splits skipped
- *     (kernel-matrix rows KERNEL-ATTN-FA2 and KERNEL-ATTN-MLA-SPARSE);
+ *     splits in a fixed ascending order, no atomics on the data, empty splits
+ *     skipped (kernel-matrix rows KERNEL-ATTN-FA2 and KERNEL-ATTN-MLA-SPARSE);
  *   - the absorbed MLA schedule q_lat = q_nope.W_UK || q_rope, scores over
  *     the 576-wide latent cache, o_lat = sum p c, o = W_UV.o_lat (pegainfer
  *     PR #938 "warp-cooperative two-pass MLA absorbed decode kernel",
@@ -80,7 +80,7 @@ extern "C" {
 typedef enum {
   PA_OK = 0,
   PA_ERR_INVALID_ARGUMENT = -1, /* a size <= 0 where one is needed, Hq % Hkv != 0, NULL pointer, ... */
-  PA_ERR_UNSUPPORTED = -2,      /* head_dim not 64/128/256, page_size not a power of two in [1, 256], ... */
+  PA_ERR_UNSUPPORTED = -2,      /* head_dim not 64/128/256, page_size not an accepted power of two, ... */
   PA_ERR_MISALIGNED = -3,       /* a pointer breaks the alignment rule above */
   PA_ERR_WORKSPACE_TOO_SMALL = -4,
   PA_ERR_CUDA = -5              /* a CUDA runtime call or launch failed (cudaGetLastError is left set) */
@@ -112,7 +112,7 @@ size_t pa_workspace_size(int kind, int batch, int num_q_heads, int num_kv_heads,
  *   out          [batch, num_q_heads, head_dim] bf16 (written)
  *   lse          [batch, num_q_heads] fp32 natural-log LSE (written), or NULL
  * Query head h reads KV head h / (num_q_heads / num_kv_heads).
- * head_dim in {64, 128, 256}; page_size a power of two in [1, 256];
+ * head_dim in {64, 128, 256}; page_size a power of two in [8, 256];
  * max_pages_per_seq >= ceil(max_context_len / page_size); window <= 0 means
  * no window; num_splits in [0, 1024].  batch == 0 is a no-op returning PA_OK.
  */

@@ -16,24 +16,13 @@
 #include "pa_launch.h"
 #include "pa_mla.h"
 
-namespace pa {
-cudaError_t launch_gqa_split_d64(int GP, int grid, const CUtensorMap &, const CUtensorMap &, const GqaArgs &,
-                                 cudaStream_t);
-cudaError_t launch_gqa_split_d128(int GP, int grid, const CUtensorMap &, const CUtensorMap &, const GqaArgs &,
-                                  cudaStream_t);
-cudaError_t launch_gqa_split_d256(int GP, int grid, const CUtensorMap &, const CUtensorMap &, const GqaArgs &,
-                                  cudaStream_t);
-cudaError_t launch_gqa_combine_d64(const CombineArgs &, cudaStream_t);
-cudaError_t launch_gqa_combine_d128(const CombineArgs &, cudaStream_t);
-cudaError_t launch_gqa_combine_d256(const CombineArgs &, cudaStream_t);
-}  // namespace pa
-
 namespace {
 
 using namespace pa;
 
-constexpr int kMinChunkTokens = 128;  // automatic mode: smallest split, in tokens
+constexpr int kMinChunkTokens = 256;  // automatic mode: smallest split, in tokens
 constexpr int kItemsPerCta = 8;       // automatic mode: work items per persistent CTA
+constexpr int kStageTokens = 64;      // tokens per stage of the split kernel (all head dims)
 constexpr int kMaxSplits = 1024;      // largest accepted explicit num_splits
 
 thread_local cudaEvent_t t_ev_before = nullptr;
@@ -49,10 +38,8 @@ int ilog2(int x) {
 }
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-int gqa_stage_tokens_of(int D) { return 32768 / (2 * D * 2); }
-
 struct GqaPlan {
-  int GP, nsub, max_splits, min_chunk_pages, chunk_align;
+  int nsub, max_splits, min_chunk_pages, chunk_align;
   size_t off_rows, off_items, off_part_lse, off_part_o, total;
 };
 
@@ -62,11 +49,10 @@ int gqa_shape(int batch, int Hq, int Hkv, int D, int max_ctx, int P, int num_spl
   if (Hq % Hkv != 0) return PA_ERR_INVALID_ARGUMENT;
   if (num_splits > kMaxSplits) return PA_ERR_UNSUPPORTED;
   if (D != 64 && D != 128 && D != 256) return PA_ERR_UNSUPPORTED;
-  if (!is_pow2(P) || P > 256) return PA_ERR_UNSUPPORTED;
+  if (!is_pow2(P) || P < 8 || P > 256) return PA_ERR_UNSUPPORTED;
   const int G = Hq / Hkv;
-  pl->GP = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8;
-  pl->nsub = (G + pl->GP - 1) / pl->GP;
-  const int ST = gqa_stage_tokens_of(D);
+  pl->nsub = (G + 15) / 16;  // query heads per tensor-core tile: 16
+  const int ST = kStageTokens;
   pl->chunk_align = P >= ST ? 1 : ST / P;
   int mcp = kMinChunkTokens / P;
   if (mcp < 1) mcp = 1;
@@ -104,16 +90,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 4-D map over a [num_pages, P, H, D] bf16 pool, box = (D, 1 head, BH tokens, 1 page).
+// 4-D map over a [num_pages, P, H, D] bf16 pool; box = (64 dims, 1 head, BH tokens, 1 page),
+// written to shared memory with the 128-byte swizzle (one box row is 128 bytes).
 bool encode_pool_map(CUtensorMap *m, const void *base, int num_pages, int P, int H, int D, int BH) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)P, (cuuint64_t)num_pages};
   cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)P * H * D * 2};
-  cuuint32_t box[4] = {(cuuint32_t)D, 1u, (cuuint32_t)BH, 1u};
+  cuuint32_t box[4] = {64u, 1u, (cuuint32_t)BH, 1u};
   cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -172,7 +159,7 @@ int pa_decode_gqa(const void *q, const void *k_pool, const void *v_pool, const i
   if (workspace_bytes < pl.total) return PA_ERR_WORKSPACE_TOO_SMALL;
 
   const int D = head_dim, P = page_size;
-  const int ST = gqa_stage_tokens_of(D);
+  const int ST = kStageTokens;
   const int BH = P < ST ? P : ST;
   CUtensorMap tm_k, tm_v;
   if (!encode_pool_map(&tm_k, k_pool, num_pages, P, num_kv_heads, D, BH) ||
@@ -207,6 +194,10 @@ int pa_decode_gqa(const void *q, const void *k_pool, const void *v_pool, const i
   pa_.hdr = hdr;
   pa_.rows = rows;
   pa_.items = items;
+  pa_.out = static_cast<uint16_t *>(out);
+  pa_.lse = lse;
+  pa_.out_heads = num_q_heads;
+  pa_.out_dim = D;
 
   GqaArgs ga;
   ga.q = static_cast<const uint16_t *>(q);
@@ -217,7 +208,6 @@ int pa_decode_gqa(const void *q, const void *k_pool, const void *v_pool, const i
   ga.part_lse = part_lse;
   ga.hdr = hdr;
   ga.items = items;
-  ga.rows = rows;
   ga.max_pages_per_seq = max_pages_per_seq;
   ga.num_pages = num_pages;
   ga.Hq = num_q_heads;
@@ -237,7 +227,6 @@ int pa_decode_gqa(const void *q, const void *k_pool, const void *v_pool, const i
   ca.rows = rows;
   ca.batch = batch;
   ca.Hq = num_q_heads;
-  ca.D = D;
   ca.max_splits = pl.max_splits;
 
   cudaError_t e = launch_plan(pa_, stream);
@@ -245,9 +234,9 @@ int pa_decode_gqa(const void *q, const void *k_pool, const void *v_pool, const i
   ++t_last_launches;
   if (t_ev_before && cudaEventRecord(t_ev_before, stream) != cudaSuccess) return PA_ERR_CUDA;
   switch (D) {
-    case 64: e = launch_gqa_split_d64(pl.GP, grid, tm_k, tm_v, ga, stream); break;
-    case 128: e = launch_gqa_split_d128(pl.GP, grid, tm_k, tm_v, ga, stream); break;
-    default: e = launch_gqa_split_d256(pl.GP, grid, tm_k, tm_v, ga, stream); break;
+    case 64: e = launch_gqa_split_d64(grid, tm_k, tm_v, ga, stream); break;
+    case 128: e = launch_gqa_split_d128(grid, tm_k, tm_v, ga, stream); break;
+    default: e = launch_gqa_split_d256(grid, tm_k, tm_v, ga, stream); break;
   }
   if (e != cudaSuccess) return PA_ERR_CUDA;
   ++t_last_launches;

@@ -27,14 +27,17 @@ struct WsHeader {
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
 // Work item of the split-KV kernels: one (row, head subgroup) and a
-// page-aligned chunk [page_begin, page_end) of the row's visible pages.
+// page-aligned chunk [page_begin, page_end) of the row's visible pages, with
+// the row facts the kernels need (so fetching an item is a single load).
 struct WorkItem {
   int32_t b;
-  int32_t sub;        // head subgroup (GQA) / unused (MLA)
+  int32_t sub;        // KV head x head subgroup (GQA) / head group (MLA)
   int32_t split;      // chunk index within the row
   int32_t page_begin;
   int32_t page_end;
-  int32_t pad[3];
+  int32_t tok_lo;     // attended tokens of the chunk: [tok_lo, tok_hi)
+  int32_t tok_hi;
+  int32_t splits;     // (row's split count << 16) | row's non-empty split count
 };
 static_assert(sizeof(WorkItem) == 32, "work item is 32 bytes");
 
@@ -155,6 +158,38 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
   __nv_bfloat16 h = __float2bfloat16_rn(x);
   return *reinterpret_cast<uint16_t *>(&h);
 }
+
+// ldmatrix: four 8x8 b16 matrices; lane 8i + r gives the shared address of row r of matrix i.
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// D += A(16x16, row) * B(16x8, col), bf16 inputs, fp32 accumulation.
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two fp32 -> one bf16x2 (round to nearest even); `lo` lands in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Programmatic dependent launch: wait for the preceding grid / let the next one start.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
 
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;

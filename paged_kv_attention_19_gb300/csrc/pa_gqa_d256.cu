@@ -1,52 +1,48 @@
-// pa_gqa_d256.cu -- head_dim 256 instantiations of the GQA split-KV and combine kernels.
+// pa_gqa_d256.cu -- head_dim 256 instantiations of the GQA split-KV and combine kernels and their launchers.
 #include "pa_gqa.cuh"
 #include "pa_launch.h"
 
 namespace pa {
 
-template <int GP>
-static cudaError_t launch_split_gp(int grid, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                                   const GqaArgs &a, cudaStream_t stream) {
-  using C = GqaCfg<256, GP>;
+namespace {
+// Both kernels are launched as programmatic dependents of the kernel before them: their
+// prologue overlaps its tail and they wait (griddepcontrol.wait) before reading its output.
+cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, int smem, cudaStream_t stream, cudaLaunchAttribute *attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+}  // namespace
+
+cudaError_t launch_gqa_split_d256(int grid, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const GqaArgs &a,
+                                 cudaStream_t stream) {
+  using C = GqaCfg<256>;
   constexpr int smem = GqaSmem<C>::BYTES;
   static int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(gqa_split_kernel<256, GP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(gqa_split_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  gqa_split_kernel<256, GP><<<grid, C::THREADS, smem, stream>>>(tm_k, tm_v, a);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_gqa_split_d256(int GP, int grid, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                                 const GqaArgs &a, cudaStream_t stream) {
-  switch (GP) {
-    case 1: return launch_split_gp<1>(grid, tm_k, tm_v, a, stream);
-    case 2: return launch_split_gp<2>(grid, tm_k, tm_v, a, stream);
-    case 4: return launch_split_gp<4>(grid, tm_k, tm_v, a, stream);
-    case 8: return launch_split_gp<8>(grid, tm_k, tm_v, a, stream);
-    default: return cudaErrorInvalidValue;
-  }
-}
-
-int gqa_split_smem_bytes_d256(int GP) {
-  switch (GP) {
-    case 1: return GqaSmem<GqaCfg<256, 1>>::BYTES;
-    case 2: return GqaSmem<GqaCfg<256, 2>>::BYTES;
-    case 4: return GqaSmem<GqaCfg<256, 4>>::BYTES;
-    case 8: return GqaSmem<GqaCfg<256, 8>>::BYTES;
-    default: return 0;
-  }
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(C::THREADS), smem, stream, attr);
+  return cudaLaunchKernelEx(&cfg, gqa_split_kernel<256>, tm_k, tm_v, a);
 }
 
 cudaError_t launch_gqa_combine_d256(const CombineArgs &a, cudaStream_t stream) {
   const int warps = a.batch * a.Hq;
-  const int blocks = (warps + 7) / 8;
-  combine_kernel<256><<<blocks, 256, 0, stream>>>(a);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pdl_config(dim3((warps + 3) / 4), dim3(128), 0, stream, attr);
+  return cudaLaunchKernelEx(&cfg, gqa_combine_kernel<256>, a);
 }
 
 }  // namespace pa

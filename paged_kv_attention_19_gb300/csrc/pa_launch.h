@@ -6,16 +6,17 @@
 
 namespace pa {
 struct GqaArgs;
-struct CombineArgs;
 struct PlanArgs;
-
-// Shared-memory bytes and thread count of the split kernel for (D, GP).
-int gqa_split_smem_bytes(int D, int GP);
-int gqa_split_threads();
-int gqa_stage_tokens(int D);
+struct CombineArgs;
 
 cudaError_t launch_plan(const PlanArgs &a, cudaStream_t stream);
-cudaError_t launch_gqa_split(int D, int GP, int grid, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                             const GqaArgs &a, cudaStream_t stream);
-cudaError_t launch_gqa_combine(int D, const CombineArgs &a, cudaStream_t stream);
+cudaError_t launch_gqa_split_d64(int grid, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const GqaArgs &a,
+                                 cudaStream_t stream);
+cudaError_t launch_gqa_split_d128(int grid, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const GqaArgs &a,
+                                  cudaStream_t stream);
+cudaError_t launch_gqa_split_d256(int grid, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const GqaArgs &a,
+                                  cudaStream_t stream);
+cudaError_t launch_gqa_combine_d64(const CombineArgs &a, cudaStream_t stream);
+cudaError_t launch_gqa_combine_d128(const CombineArgs &a, cudaStream_t stream);
+cudaError_t launch_gqa_combine_d256(const CombineArgs &a, cudaStream_t stream);
 }  // namespace pa

@@ -299,15 +299,7 @@ __global__ void __launch_bounds__(MlaCfg::THREADS, 1)
 }
 
 // ----------------------------------------------------------------------------- tensor-core projections
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(uint16_t lo, uint16_t hi) {
+__device__ __forceinline__ uint32_t pack_u16(uint16_t lo, uint16_t hi) {
   return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
@@ -344,9 +336,9 @@ __global__ void __launch_bounds__(128) q_absorb_kernel(const uint16_t *q, const 
       for (int nt = 0; nt < 4; ++nt) {
         const int n = warp * 32 + nt * 8 + g;
         uint32_t bf[2];
-        bf[0] = pack_bf16(w[k0 + 2 * tq][n], w[k0 + 2 * tq + 1][n]);
-        bf[1] = pack_bf16(w[k0 + 8 + 2 * tq][n], w[k0 + 9 + 2 * tq][n]);
-        mma_bf16_16816(acc[nt], af, bf);
+        bf[0] = pack_u16(w[k0 + 2 * tq][n], w[k0 + 2 * tq + 1][n]);
+        bf[1] = pack_u16(w[k0 + 8 + 2 * tq][n], w[k0 + 9 + 2 * tq][n]);
+        mma_bf16_16816(acc[nt], af, bf[0], bf[1]);
       }
     }
 #pragma unroll
@@ -432,7 +424,7 @@ __global__ void __launch_bounds__(128) mla_out_kernel(const MlaOutArgs a) {
         uint32_t bf[2];
         bf[0] = *reinterpret_cast<const uint32_t *>(wv + (size_t)v * MLA_LAT + k0 + 2 * tq);
         bf[1] = *reinterpret_cast<const uint32_t *>(wv + (size_t)v * MLA_LAT + k0 + 8 + 2 * tq);
-        mma_bf16_16816(acc[nt], af, bf);
+        mma_bf16_16816(acc[nt], af, bf[0], bf[1]);
       }
     }
     const int r0 = m0 + g, r1 = m0 + g + 8;
@@ -441,10 +433,10 @@ __global__ void __launch_bounds__(128) mla_out_kernel(const MlaOutArgs a) {
       const int col = warp * 32 + nt * 8 + 2 * tq;
       if (r0 < a.B)
         *reinterpret_cast<uint32_t *>(a.out + ((size_t)r0 * a.H + h) * MLA_V + col) =
-            pack_bf16(f32_to_bf16_bits(acc[nt][0]), f32_to_bf16_bits(acc[nt][1]));
+            pack_u16(f32_to_bf16_bits(acc[nt][0]), f32_to_bf16_bits(acc[nt][1]));
       if (r1 < a.B)
         *reinterpret_cast<uint32_t *>(a.out + ((size_t)r1 * a.H + h) * MLA_V + col) =
-            pack_bf16(f32_to_bf16_bits(acc[nt][2]), f32_to_bf16_bits(acc[nt][3]));
+            pack_u16(f32_to_bf16_bits(acc[nt][2]), f32_to_bf16_bits(acc[nt][3]));
     }
     __syncthreads();
   }
@@ -594,6 +586,10 @@ int mla_decode(const void *q, const void *cache, const void *w_uk, const void *w
   pa_.hdr = hdr;
   pa_.rows = rows;
   pa_.items = items;
+  pa_.out = nullptr;  // rows without keys are written by mla_out_kernel
+  pa_.lse = nullptr;
+  pa_.out_heads = 0;
+  pa_.out_dim = 0;
   if (launch_plan(pa_, stream) != cudaSuccess) return PA_ERR_CUDA;
   ++*launches;
 

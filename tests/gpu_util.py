@@ -1,12 +1,12 @@
 """Helpers of the GPU parity tests: upload a seeded workload, run the CUDA path
-through the C ABI binding, and compare with the fp64 oracle."""
+through the C ABI binding, and compare with the fp64 oracle (imported only by
+the comparison helpers, so the benchmark can reuse the upload helpers)."""
 from __future__ import annotations
 
 import numpy as np
 import torch
 
 import compare
-import oracle
 import synth
 
 
@@ -55,6 +55,7 @@ class GqaDev:
 
 
 def gqa_oracle(w: synth.GQAWorkload, rows=None, window=None):
+    import oracle
     return oracle.gqa(w.q, w.k_pool, w.v_pool, w.layout.block_table, w.layout.context_lens, w.scale,
                       w.window if window is None else window, rows=rows)
 
@@ -104,6 +105,7 @@ class MlaDev:
 
 
 def check_mla(w, out_bits, lse, rows=None):
+    import oracle
     B, H, _ = w.q.shape
     ro, rl = oracle.mla(w.q, w.cache, w.w_uk, w.w_uv, w.layout.block_table, w.layout.context_lens, w.scale,
                         rows=rows)

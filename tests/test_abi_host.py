@@ -1,0 +1,127 @@
+"""The C ABI without a GPU: the library builds and loads, exports every function
+include/pa_decode.h declares, and rejects bad arguments on the host (no CUDA
+call happens before these checks)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pa_decode.h")
+
+
+@pytest.fixture(scope="module")
+def pa():
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("pa_build", os.path.join(ROOT, "paged_kv_attention_19_gb300", "build.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod.build()
+    import paged_kv_attention_19_gb300 as pkg
+    return pkg
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    for required in ("pa_workspace_size", "pa_decode_gqa", "pa_decode_mla_absorbed", "pa_status_string",
+                     "pa_read_device_status"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(pa):
+    out = subprocess.run(["nm", "-D", "--defined-only", pa.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\bT (pa_[a-z0-9_]+)\b", out))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    # and the binding declares a signature for each of them
+    assert set(declared_functions()) <= set(pa.SIGNATURES)
+
+
+def test_status_strings(pa):
+    assert pa.pa_status_string(0) == "ok"
+    for code in (-1, -2, -3, -4, -5):
+        assert pa.pa_status_string(code) not in ("ok", "unknown status")
+    assert pa.pa_status_string(42) == "unknown status"
+
+
+def test_workspace_size(pa):
+    g = pa.pa_workspace_size(pa.PA_KIND_GQA, 32, 64, 8, 128, 16384, 32, 0)
+    assert g > 0
+    assert pa.pa_workspace_size(pa.PA_KIND_GQA, 32, 64, 8, 128, 16384, 32, 4) > 0
+    # grows with the batch and with an explicit split count
+    assert pa.pa_workspace_size(pa.PA_KIND_GQA, 64, 64, 8, 128, 16384, 32, 0) > g
+    assert pa.pa_workspace_size(pa.PA_KIND_GQA, 32, 64, 8, 128, 16384, 32, 512) > g
+    # rejected shapes report 0
+    assert pa.pa_workspace_size(pa.PA_KIND_GQA, 32, 64, 7, 128, 16384, 32, 0) == 0     # Hq % Hkv
+    assert pa.pa_workspace_size(pa.PA_KIND_GQA, 32, 64, 8, 96, 16384, 32, 0) == 0      # head_dim
+    assert pa.pa_workspace_size(pa.PA_KIND_GQA, 32, 64, 8, 128, 16384, 48, 0) == 0     # page size
+    assert pa.pa_workspace_size(pa.PA_KIND_GQA, 32, 64, 8, 128, 16384, 32, 2000) == 0  # num_splits
+    assert pa.pa_workspace_size(pa.PA_KIND_MLA_ABSORBED, 16, 128, 0, 0, 8192, 64, 0) > 0
+    assert pa.pa_workspace_size(pa.PA_KIND_MLA_ABSORBED, 16, 0, 0, 0, 8192, 64, 0) == 0
+    assert pa.pa_workspace_size(7, 16, 128, 1, 128, 8192, 64, 0) == 0
+
+
+def _gqa(pa, **kw):
+    a = dict(q=0x10000, k=0x20000, v=0x30000, bt=0x40000, lens=0x50000, out=0x60000, lse=None, batch=2, hq=8,
+             hkv=2, d=128, p=16, pages=10, maxp=5, maxctx=80, scale=0.1, window=0, splits=0, ws=0x70000,
+             wsb=1 << 30)
+    a.update(kw)
+    return pa.lib.pa_decode_gqa(a["q"], a["k"], a["v"], a["bt"], a["lens"], a["out"], a["lse"], a["batch"],
+                                a["hq"], a["hkv"], a["d"], a["p"], a["pages"], a["maxp"], a["maxctx"], a["scale"],
+                                a["window"], a["splits"], a["ws"], a["wsb"], None)
+
+
+def test_gqa_host_validation(pa):
+    assert _gqa(pa, batch=0) == pa.PA_OK                       # empty batch: no-op
+    assert _gqa(pa, batch=-1) == pa.PA_ERR_INVALID_ARGUMENT
+    assert _gqa(pa, hkv=3) == pa.PA_ERR_INVALID_ARGUMENT        # 8 % 3 != 0
+    assert _gqa(pa, hq=0) == pa.PA_ERR_INVALID_ARGUMENT
+    assert _gqa(pa, d=96) == pa.PA_ERR_UNSUPPORTED
+    assert _gqa(pa, p=4) == pa.PA_ERR_UNSUPPORTED
+    assert _gqa(pa, p=24) == pa.PA_ERR_UNSUPPORTED
+    assert _gqa(pa, splits=1025) == pa.PA_ERR_UNSUPPORTED
+    assert _gqa(pa, splits=-1) == pa.PA_ERR_INVALID_ARGUMENT
+    assert _gqa(pa, q=None) == pa.PA_ERR_INVALID_ARGUMENT
+    assert _gqa(pa, ws=None) == pa.PA_ERR_INVALID_ARGUMENT
+    assert _gqa(pa, pages=0) == pa.PA_ERR_INVALID_ARGUMENT
+    assert _gqa(pa, maxp=4) == pa.PA_ERR_INVALID_ARGUMENT      # 4 pages of 16 < 80 tokens
+    assert _gqa(pa, scale=float("nan")) == pa.PA_ERR_INVALID_ARGUMENT
+    assert _gqa(pa, q=0x10002) == pa.PA_ERR_MISALIGNED
+    assert _gqa(pa, k=0x20008) == pa.PA_ERR_MISALIGNED
+    assert _gqa(pa, bt=0x40002) == pa.PA_ERR_MISALIGNED
+    assert _gqa(pa, lse=0x80001) == pa.PA_ERR_MISALIGNED
+    assert _gqa(pa, wsb=1024) == pa.PA_ERR_WORKSPACE_TOO_SMALL
+
+
+def _mla(pa, **kw):
+    a = dict(q=0x10000, c=0x20000, wk=0x30000, wv=0x40000, bt=0x50000, lens=0x60000, out=0x70000, lse=None,
+             batch=2, h=16, p=64, pages=10, maxp=5, maxctx=300, scale=0.07, splits=0, ws=0x80000, wsb=1 << 30)
+    a.update(kw)
+    return pa.lib.pa_decode_mla_absorbed(a["q"], a["c"], a["wk"], a["wv"], a["bt"], a["lens"], a["out"], a["lse"],
+                                         a["batch"], a["h"], a["p"], a["pages"], a["maxp"], a["maxctx"], a["scale"],
+                                         a["splits"], a["ws"], a["wsb"], None)
+
+
+def test_mla_host_validation(pa):
+    assert _mla(pa, batch=0) == pa.PA_OK
+    assert _mla(pa, h=0) == pa.PA_ERR_INVALID_ARGUMENT
+    assert _mla(pa, p=48) == pa.PA_ERR_UNSUPPORTED
+    assert _mla(pa, wk=None) == pa.PA_ERR_INVALID_ARGUMENT
+    assert _mla(pa, maxp=4) == pa.PA_ERR_INVALID_ARGUMENT
+    assert _mla(pa, c=0x20004) == pa.PA_ERR_MISALIGNED
+    assert _mla(pa, wsb=16) == pa.PA_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_profile_hook_arguments(pa):
+    assert pa.lib.pa_set_profile_events(None, None) == pa.PA_OK
+    assert pa.lib.pa_set_profile_events(ctypes.c_void_p(0x1234), None) == pa.PA_ERR_INVALID_ARGUMENT
+    assert pa.lib.pa_read_device_status(None, None, None) == pa.PA_ERR_INVALID_ARGUMENT

@@ -21,18 +21,30 @@ def test_tiny_workload_all_rows():
 
 
 @pytest.mark.parametrize("D", [64, 128, 256])
-@pytest.mark.parametrize("hq,hkv", [(8, 2), (8, 1), (4, 4), (16, 2), (6, 2), (24, 2)])
+@pytest.mark.parametrize("hq,hkv", [(8, 2), (8, 1), (4, 4), (16, 2), (6, 2), (24, 2), (32, 2), (40, 2), (64, 4)])
 def test_context_ladder(D, hq, hkv):
     w = synth.make_gqa(100 + D + hq, LADDER, hq, hkv, D, 32, k_std=1.0)
     o, l = gu.GqaDev(w).run()
     gu.check_gqa(w, o, l)
 
 
-@pytest.mark.parametrize("P", [1, 2, 8, 16, 64, 128, 256])
+@pytest.mark.parametrize("P", [8, 16, 64, 128, 256])
 def test_page_sizes(P):
     w = synth.make_gqa(200 + P, LADDER, 8, 2, 128, P)
     o, l = gu.GqaDev(w).run()
     gu.check_gqa(w, o, l)
+
+
+def test_page_size_below_eight_is_rejected():
+    import paged_kv_attention_19_gb300 as pa
+    assert pa.pa_workspace_size(pa.PA_KIND_GQA, 2, 8, 2, 128, 100, 4, 0) == 0
+    w = synth.make_gqa(210, [40, 70], 8, 2, 128, 4)
+    g = gu.GqaDev(w)
+    out = torch.empty(w.q.shape, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    with pytest.raises(pa.PaError) as e:
+        pa.pa_decode_gqa(g.q, g.k, g.v, g.bt, g.lens, out, None, scale=w.scale, workspace=ws)
+    assert e.value.status == pa.PA_ERR_UNSUPPORTED
 
 
 @pytest.mark.parametrize("D", [128, 256])
