@@ -142,6 +142,38 @@ int pa_decode_mla_absorbed(const void *q, const void *cache, const void *w_uk, c
                            int num_splits, void *workspace, size_t workspace_bytes,
                            cudaStream_t stream);
 
+/*
+ * GQA paged decode without a caller-provided workspace.  The pages describe
+ * no counterpart of this entry point: it exists for callers that cannot
+ * allocate device memory when they call the decode (an engine whose device
+ * memory is all held by its own pool, a plug-in that is handed only its input
+ * and output pointers, a latency-critical path that must not pay for
+ * cudaMalloc's possible device synchronisation).
+ *
+ * Arguments, layouts, results and error codes are those of pa_decode_gqa;
+ * the workspace is a fixed device array of PA_NOALLOC_SCRATCH_BYTES inside
+ * this library, which every GPU that loads the library keeps allocated until
+ * the process exits.  Nothing is allocated or freed by the call.
+ *   - A call whose pa_workspace_size(PA_KIND_GQA, ...) exceeds
+ *     PA_NOALLOC_SCRATCH_BYTES returns PA_ERR_WORKSPACE_TOO_SMALL before any
+ *     device work (pass a smaller batch, or a num_splits that needs less).
+ *   - The first call on a device looks up the array's device address on that
+ *     (current) device and caches it; make that first call before starting
+ *     any stream capture on the device.
+ *   - All calls on a device share the one array.  Nothing in it has to start
+ *     at zero (each call's planner rewrites the parts the kernels read before
+ *     they read them), but two calls that may overlap on the GPU race on it:
+ *     order them on one stream, or use pa_decode_gqa with separate workspaces.
+ *   - The array keeps the last call's contents; pa_read_device_status cannot
+ *     reach it, so this entry point offers no device status word.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (32u << 20) /* 32 MiB per device */
+int pa_decode_gqa_noalloc(const void *q, const void *k_pool, const void *v_pool,
+                          const int32_t *block_table, const int32_t *context_lens, void *out,
+                          float *lse, int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                          int page_size, int num_pages, int max_pages_per_seq, int max_context_len,
+                          float scale, int window, int num_splits, cudaStream_t stream);
+
 /* Static text for a pa_status value (never NULL). */
 const char *pa_status_string(int status);
 

@@ -37,6 +37,7 @@ SIGNATURES = {
     "pa_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I, _I, _I]),
     "pa_decode_gqa": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _Z, _P]),
     "pa_decode_mla_absorbed": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P]),
+    "pa_decode_gqa_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
     "pa_status_string": (ctypes.c_char_p, [_I]),
     "pa_read_device_status": (_I, [_P, _P, _U32P]),
     "pa_set_profile_events": (_I, [_P, _P]),
