@@ -53,8 +53,12 @@
  *     in [0, num_pages).  A violation never traps: the kernel records a bit
  *     in the workspace's device status word (pa_read_device_status), clamps
  *     the length / skips the page, and the output of that row is unspecified.
- *   - num_splits: 0 = automatic (the library balances page-aligned chunks of
- *     all rows over the SMs); n > 0 = every row is cut into n page-aligned
+ *   - num_splits, GQA: the visible keys of every (row, KV head) sequence,
+ *     flattened row by row, are cut into that many equal contiguous shares,
+ *     each handled by one CTA and merged in ascending order where a sequence
+ *     spans several shares; 0 = automatic (one share per SM, at most 256),
+ *     n in [1, 4096] = n shares.  MLA: 0 = automatic (page-aligned chunks
+ *     balanced over the SMs); n > 0 = every row is cut into n page-aligned
  *     chunks of ceil(pages / n) pages, trailing chunks possibly empty.  For a
  *     fixed num_splits (and fixed inputs) results are bitwise reproducible
  *     from run to run and independent of the physical page order; different
@@ -62,7 +66,10 @@
  *   - Workspace: at least pa_workspace_size(...) bytes of device memory for
  *     the same (kind, shape, max_context_len, page_size, num_splits).  Its
  *     contents need no initialisation and are overwritten by each call;
- *     calls sharing one workspace must be ordered on one stream.
+ *     calls sharing one workspace must be ordered on one stream.  The GQA
+ *     workspace depends on head_dim and num_splits only (two fp32 partial
+ *     results of 16 heads per share: 16 KB per share at head_dim 128, about
+ *     4.2 MB in automatic mode); the MLA one grows with batch and context.
  */
 #ifndef PA_DECODE_H
 #define PA_DECODE_H
@@ -114,7 +121,7 @@ size_t pa_workspace_size(int kind, int batch, int num_q_heads, int num_kv_heads,
  * Query head h reads KV head h / (num_q_heads / num_kv_heads).
  * head_dim in {64, 128, 256}; page_size a power of two in [8, 256];
  * max_pages_per_seq >= ceil(max_context_len / page_size); window <= 0 means
- * no window; num_splits in [0, 1024].  batch == 0 is a no-op returning PA_OK.
+ * no window; num_splits in [0, 4096].  batch == 0 is a no-op returning PA_OK.
  */
 int pa_decode_gqa(const void *q, const void *k_pool, const void *v_pool,
                   const int32_t *block_table, const int32_t *context_lens, void *out, float *lse,
@@ -133,7 +140,7 @@ int pa_decode_gqa(const void *q, const void *k_pool, const void *v_pool,
  *   block_table, context_lens as for GQA (one latent head shared by all heads)
  *   out          [batch, num_heads, 128] bf16 (written)
  *   lse          [batch, num_heads] fp32 (written), or NULL
- * page_size a power of two in [1, 256]; num_splits as for GQA.
+ * page_size a power of two in [1, 256]; num_splits in [0, 1024] (chunks per row, see above).
  */
 int pa_decode_mla_absorbed(const void *q, const void *cache, const void *w_uk, const void *w_uv,
                            const int32_t *block_table, const int32_t *context_lens, void *out,
@@ -156,7 +163,8 @@ int pa_decode_mla_absorbed(const void *q, const void *cache, const void *w_uk, c
  * the process exits.  Nothing is allocated or freed by the call.
  *   - A call whose pa_workspace_size(PA_KIND_GQA, ...) exceeds
  *     PA_NOALLOC_SCRATCH_BYTES returns PA_ERR_WORKSPACE_TOO_SMALL before any
- *     device work (pass a smaller batch, or a num_splits that needs less).
+ *     device work.  Automatic mode (num_splits 0) always fits; an explicit
+ *     num_splits fits up to about 2000 shares at head_dim 128 (1000 at 256).
  *   - The first call on a device looks up the array's device address on that
  *     (current) device and caches it; make that first call before starting
  *     any stream capture on the device.

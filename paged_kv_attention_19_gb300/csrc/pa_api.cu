@@ -15,15 +15,17 @@
 #include "pa_gqa.cuh"
 #include "pa_launch.h"
 #include "pa_mla.h"
+#include "pa_plan.cuh"
 
 namespace {
 
 using namespace pa;
 
-constexpr int kMinChunkTokens = 256;  // automatic mode: smallest split, in tokens
-constexpr int kItemsPerCta = 8;       // automatic mode: work items per persistent CTA
-constexpr int kStageTokens = 64;      // tokens per stage of the split kernel (all head dims)
-constexpr int kMaxSplits = 1024;      // largest accepted explicit num_splits
+constexpr int kMaxSplits = 4096;     // largest accepted explicit num_splits (partitions)
+constexpr int kAutoPartsMax = 256;   // automatic mode: one partition per SM, at most this many
+// Fixed cost of one piece of work in the GQA partition (the Q load and the end-of-piece
+// merge, about 1.5 us of one SM), expressed as the KV bytes the SM streams meanwhile.
+constexpr long long kPieceCostBytes = 64 << 10;
 
 thread_local cudaEvent_t t_ev_before = nullptr;
 thread_local cudaEvent_t t_ev_after = nullptr;
@@ -38,12 +40,18 @@ int ilog2(int x) {
 }
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Tokens per stage of the split kernel for a head_dim (must match GqaCfg<D>::ST).
+int gqa_stage_tokens(int D) { return D <= 128 ? 64 : 32; }
+
 struct GqaPlan {
-  int nsub, max_splits, min_chunk_pages, chunk_align;
-  size_t off_rows, off_items, off_part_lse, off_part_o, total;
+  int nsub, nparts_max;
+  size_t off_desc, off_part_lse, off_part_o, total;
 };
 
 // Shape checks shared by pa_workspace_size and pa_decode_gqa; PA_OK or an error code.
+// The workspace holds the header, one descriptor per partition and two fp32
+// partial slots (16 heads x head_dim, plus their LSEs) per partition: its size
+// depends on head_dim and the partition count only, not on batch or context.
 int gqa_shape(int batch, int Hq, int Hkv, int D, int max_ctx, int P, int num_splits, GqaPlan *pl) {
   if (batch < 0 || Hq <= 0 || Hkv <= 0 || max_ctx < 0 || num_splits < 0) return PA_ERR_INVALID_ARGUMENT;
   if (Hq % Hkv != 0) return PA_ERR_INVALID_ARGUMENT;
@@ -52,26 +60,15 @@ int gqa_shape(int batch, int Hq, int Hkv, int D, int max_ctx, int P, int num_spl
   if (!is_pow2(P) || P < 8 || P > 256) return PA_ERR_UNSUPPORTED;
   const int G = Hq / Hkv;
   pl->nsub = (G + 15) / 16;  // query heads per tensor-core tile: 16
-  const int ST = kStageTokens;
-  pl->chunk_align = P >= ST ? 1 : ST / P;
-  int mcp = kMinChunkTokens / P;
-  if (mcp < 1) mcp = 1;
-  pl->min_chunk_pages = (int)round_up((size_t)mcp, (size_t)pl->chunk_align);
-  const long long max_pages = max_ctx == 0 ? 1 : ((long long)max_ctx + P - 1) / P;
-  pl->max_splits = num_splits > 0 ? num_splits : (int)((max_pages + pl->min_chunk_pages - 1) / pl->min_chunk_pages);
-  if (pl->max_splits < 1) pl->max_splits = 1;
-  const size_t B = (size_t)(batch > 0 ? batch : 1);
-  const size_t items = B * (size_t)Hkv * (size_t)pl->nsub * (size_t)pl->max_splits;
-  if (items > (size_t)INT32_MAX) return PA_ERR_UNSUPPORTED;
+  pl->nparts_max = num_splits > 0 ? num_splits : kAutoPartsMax;
+  const size_t np = (size_t)pl->nparts_max;
   size_t off = sizeof(WsHeader);
-  pl->off_rows = off;
-  off = round_up(off + B * sizeof(RowInfo), 256);
-  pl->off_items = off;
-  off = round_up(off + items * sizeof(WorkItem), 256);
+  pl->off_desc = off;
+  off = round_up(off + np * sizeof(GqaPartDesc), 256);
   pl->off_part_lse = off;
-  off = round_up(off + B * (size_t)Hq * pl->max_splits * sizeof(float), 256);
+  off = round_up(off + np * 2 * PART_HEADS * sizeof(float), 256);
   pl->off_part_o = off;
-  off = round_up(off + B * (size_t)Hq * pl->max_splits * (size_t)D * sizeof(float), 256);
+  off = round_up(off + np * 2 * PART_HEADS * (size_t)D * sizeof(float), 256);
   pl->total = off;
   return PA_OK;
 }
@@ -100,6 +97,20 @@ bool encode_pool_map(CUtensorMap *m, const void *base, int num_pages, int P, int
   cuuint32_t box[4] = {64u, 1u, (cuuint32_t)BH, 1u};
   cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 2-D map over q viewed as [batch * Hq rows, D] bf16; box = (64 dims, 16 rows), 128-byte swizzle.
+bool encode_q_map(CUtensorMap *m, const void *base, long long rows, int D) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+  cuuint32_t box[2] = {64u, (cuuint32_t)PART_HEADS};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -159,64 +170,48 @@ int pa_decode_gqa(const void *q, const void *k_pool, const void *v_pool, const i
   if (workspace_bytes < pl.total) return PA_ERR_WORKSPACE_TOO_SMALL;
 
   const int D = head_dim, P = page_size;
-  const int ST = kStageTokens;
-  const int BH = P < ST ? P : ST;
-  CUtensorMap tm_k, tm_v;
+  const int ST = gqa_stage_tokens(D);
+  const int BH = P < ST ? P : ST;  // tokens per TMA box = per work unit
+  CUtensorMap tm_k, tm_v, tm_q;
   if (!encode_pool_map(&tm_k, k_pool, num_pages, P, num_kv_heads, D, BH) ||
-      !encode_pool_map(&tm_v, v_pool, num_pages, P, num_kv_heads, D, BH))
+      !encode_pool_map(&tm_v, v_pool, num_pages, P, num_kv_heads, D, BH) ||
+      !encode_q_map(&tm_q, q, (long long)batch * num_q_heads, D))
     return PA_ERR_UNSUPPORTED;
   const int sms = sm_count();
   if (sms <= 0) return PA_ERR_CUDA;
+  const int nparts = num_splits > 0 ? num_splits : (sms < kAutoPartsMax ? sms : kAutoPartsMax);
 
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   WsHeader *hdr = reinterpret_cast<WsHeader *>(ws);
-  RowInfo *rows = reinterpret_cast<RowInfo *>(ws + pl.off_rows);
-  WorkItem *items = reinterpret_cast<WorkItem *>(ws + pl.off_items);
+  GqaPartDesc *desc = reinterpret_cast<GqaPartDesc *>(ws + pl.off_desc);
   float *part_lse = reinterpret_cast<float *>(ws + pl.off_part_lse);
   float *part_o = reinterpret_cast<float *>(ws + pl.off_part_o);
-
-  const long long max_items = (long long)batch * num_kv_heads * pl.nsub * pl.max_splits;
-  const int grid = (int)(max_items < sms ? max_items : sms);
-
-  PlanArgs pa_;
-  pa_.context_lens = context_lens;
-  pa_.batch = batch;
-  pa_.heads_per_row = num_kv_heads * pl.nsub;
-  pa_.page_size = P;
-  pa_.log2_page = ilog2(P);
-  pa_.window = window > 0 ? window : 0;
-  pa_.max_context_len = max_context_len;
-  pa_.num_splits = num_splits;
-  pa_.max_splits = pl.max_splits;
-  pa_.target_items = grid * kItemsPerCta;
-  pa_.min_chunk_pages = pl.min_chunk_pages;
-  pa_.chunk_align = pl.chunk_align;
-  pa_.hdr = hdr;
-  pa_.rows = rows;
-  pa_.items = items;
-  pa_.out = static_cast<uint16_t *>(out);
-  pa_.lse = lse;
-  pa_.out_heads = num_q_heads;
-  pa_.out_dim = D;
 
   GqaArgs ga;
   ga.q = static_cast<const uint16_t *>(q);
   ga.block_table = block_table;
+  ga.context_lens = context_lens;
   ga.out = static_cast<uint16_t *>(out);
   ga.lse = lse;
   ga.part_o = part_o;
   ga.part_lse = part_lse;
-  ga.hdr = hdr;
-  ga.items = items;
+  ga.desc = desc;
+  ga.batch = batch;
   ga.max_pages_per_seq = max_pages_per_seq;
   ga.num_pages = num_pages;
+  ga.max_context_len = max_context_len;
+  ga.window = window > 0 ? window : 0;
   ga.Hq = num_q_heads;
   ga.Hkv = num_kv_heads;
   ga.G = num_q_heads / num_kv_heads;
   ga.nsub = pl.nsub;
-  ga.page_size = P;
   ga.log2_page = ilog2(P);
-  ga.max_splits = pl.max_splits;
+  ga.log2_bh = ilog2(BH);
+  ga.nparts = nparts;
+  {
+    const long long unit_bytes = (long long)BH * D * 4;  // K and V of one unit of one KV head
+    ga.piece_cost = (int)((kPieceCostBytes + unit_bytes - 1) / unit_bytes);
+  }
   ga.qscale = scale * LOG2E;
 
   CombineArgs ca;
@@ -224,19 +219,19 @@ int pa_decode_gqa(const void *q, const void *k_pool, const void *v_pool, const i
   ca.lse = lse;
   ca.part_o = part_o;
   ca.part_lse = part_lse;
-  ca.rows = rows;
-  ca.batch = batch;
+  ca.desc = desc;
+  ca.status = &hdr->status;
   ca.Hq = num_q_heads;
-  ca.max_splits = pl.max_splits;
+  ca.G = ga.G;
+  ca.nsub = pl.nsub;
+  ca.nparts = nparts;
 
-  cudaError_t e = launch_plan(pa_, stream);
-  if (e != cudaSuccess) return PA_ERR_CUDA;
-  ++t_last_launches;
+  cudaError_t e;
   if (t_ev_before && cudaEventRecord(t_ev_before, stream) != cudaSuccess) return PA_ERR_CUDA;
   switch (D) {
-    case 64: e = launch_gqa_split_d64(grid, tm_k, tm_v, ga, stream); break;
-    case 128: e = launch_gqa_split_d128(grid, tm_k, tm_v, ga, stream); break;
-    default: e = launch_gqa_split_d256(grid, tm_k, tm_v, ga, stream); break;
+    case 64: e = launch_gqa_split_d64(nparts, tm_k, tm_v, tm_q, ga, stream); break;
+    case 128: e = launch_gqa_split_d128(nparts, tm_k, tm_v, tm_q, ga, stream); break;
+    default: e = launch_gqa_split_d256(nparts, tm_k, tm_v, tm_q, ga, stream); break;
   }
   if (e != cudaSuccess) return PA_ERR_CUDA;
   ++t_last_launches;

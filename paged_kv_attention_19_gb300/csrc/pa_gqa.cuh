@@ -1,6 +1,5 @@
-// pa_gqa.cuh -- GQA paged decode, split-KV attention and combine kernels
-// (sm_103a), plus the work-list types shared with the planner (pa_plan.cu) and
-// the MLA path.
+// pa_gqa.cuh -- GQA paged decode: the split-KV attention kernel and the split
+// combine kernel (sm_103a).
 //
 // Method (what is computed) follows the pages: a query row of length L reads
 // its keys through the block table; the query heads sharing one KV head are
@@ -13,123 +12,125 @@
 // data (vllm.cpp kernel-matrix, rows KERNEL-ATTN-FA2 and KERNEL-ATTN-MLA-SPARSE).
 //
 // GB300 design (how):
-//   * one persistent CTA per SM: the last warp is a TMA producer that pulls
-//     work items (row, KV head, 16-head subgroup, page-aligned chunk) from a
-//     device queue and issues 4-D tensor-map copies of whole page fragments
-//     into a ring of shared-memory stages (64 tokens of K and V each), with
-//     the 128-byte swizzle so tensor-core fragment loads are bank-conflict
-//     free.  Block-table entries are read 32 pages at a time into a register
-//     window (lane l holds entry l) with the next window already in flight,
-//     and the next item is fetched in dependent steps spread over the current
-//     item's stages, so no stage waits on a global load;
-//   * the consumer warps take 16 tokens of every stage per token group (four
-//     groups per stage; for head_dim <= 128 two warps share a group, both
-//     computing its scores and each accumulating half of the P.V columns, so
-//     two warps per SM sub-partition hide each other's latency).  The group's
-//     (up to 16) query heads are the M rows of mma.sync m16n8k16 bf16 tiles,
-//     so S = Q K^T and O += P V cost one tensor-core instruction per 8 tokens
-//     x 16 dims.  The online softmax (running max with a lazy rescale, fp32
-//     denominator) runs on the CUDA cores; P is rounded to bf16 only as the
-//     MMA operand;
-//   * at the end of an item the token groups merge through the consumed stage
-//     buffer; a single-split row writes the final bf16 output and LSE, a split
-//     writes an fp32 partial (normalised output + LSE);
+//   * static, balanced partition.  The visible keys of every (row, KV head,
+//     16-head subgroup) sequence are cut into units of one TMA box (min(page,
+//     stage) tokens).  All units, flattened row by row, are divided into
+//     `nparts` equal contiguous ranges, one per CTA (one CTA per SM by
+//     default), so every SM streams the same number of KV bytes.  Each CTA
+//     finds its range from the context lengths in a short prologue: no
+//     planner launch, no work queue, no atomics, identical from run to run.
+//     A range is a list of pieces (maximal runs of one sequence); only its
+//     first and last piece can be part of a sequence that another CTA also
+//     touches, so a CTA leaves at most two partial results;
+//   * the last warp is a TMA producer: it walks the CTA's pieces, keeps 32
+//     block-table entries in a register window (the next window and the next
+//     piece's first window already in flight), and issues 4-D tensor-map
+//     copies of page fragments into a ring of shared-memory stages (K and V
+//     of 64 tokens, 32 for head_dim 256) with the 128-byte swizzle, so the
+//     tensor-core fragment loads are bank-conflict free.  The ring takes all
+//     of shared memory (224 KB) to keep ~200 KB of copies in flight per SM;
+//   * the consumer warps take 16 tokens of every stage per token group; two
+//     warps share a group, both computing its scores and each accumulating
+//     half of the P.V columns.  The group's (up to 16) query heads are the M
+//     rows of mma.sync m16n8k16 bf16 tiles, so S = Q K^T and O += P V cost one
+//     tensor-core instruction per 8 tokens x 16 dims.  The online softmax
+//     (running max with a lazy rescale, fp32 denominator) runs on the CUDA
+//     cores; P is rounded to bf16 only as the MMA operand.  Q is read from
+//     global memory into registers at the start of a piece (the producer has
+//     prefetched it to L2), so no shared memory is spent on it;
+//   * at the end of a piece the token groups merge through the consumed stage
+//     buffer; a piece that covers its whole sequence writes the final bf16
+//     output and LSE, any other writes an fp32 partial (normalised output +
+//     LSE) to one of the CTA's two slots;
 //   * the combine kernel (a programmatic dependent launch, so its launch hides
-//     under the split kernel's tail) merges the splits of every row with two
-//     or more of them, one warp per (row, query head), in ascending order.
+//     under the split kernel's tail) merges every split sequence over the
+//     CTAs that hold its pieces, in ascending order.
 #pragma once
 
 #include "pa_common.cuh"
 
 namespace pa {
 
-struct RowInfo {
-  int32_t lo, L;             // visible token range [lo, L)
-  int32_t page_lo, page_hi;  // visible pages [page_lo, page_hi)
-  int32_t nsplit;            // splits of this row (0: no visible key)
-  int32_t chunk;             // pages per split
-  int32_t full_off;          // exclusive prefix of full chunks over rows
-  int32_t tail_off;          // exclusive prefix of tail chunks over rows
+// What each split CTA leaves for the combine kernel.
+struct GqaPartDesc {
+  int32_t last_b;   // row of the CTA's last piece
+  int32_t last_hs;  // KV head x subgroup (kv_head * nsub + sub) of the last piece
+  uint32_t flags;   // bits 0-15: pieces of the CTA (saturating); DESC_* bits
+  uint32_t status;  // PA_DEV_* bits seen by the CTA
 };
-static_assert(sizeof(RowInfo) == 32, "row info is 32 bytes");
-
-struct PlanArgs {
-  const int32_t *context_lens;
-  int batch, heads_per_row;  // (KV head, subgroup) pairs per row (GQA) or head groups (MLA)
-  int page_size, log2_page, window, max_context_len;
-  int num_splits;            // 0 = automatic
-  int max_splits;            // workspace capacity per row
-  int target_items;          // automatic mode: aim for this many items
-  int min_chunk_pages;       // automatic mode: smallest chunk
-  int chunk_align;           // automatic mode: chunk is a multiple of this
-  WsHeader *hdr;
-  RowInfo *rows;
-  WorkItem *items;
-  uint16_t *out;             // rows without keys get out = 0, lse = -inf (or null: not written)
-  float *lse;
-  int out_heads, out_dim;
-};
-
-// Non-empty splits of a row.
-__device__ __forceinline__ int row_nonempty(const RowInfo &r) {
-  const int pages = r.page_hi - r.page_lo;
-  return pages > 0 ? (pages + r.chunk - 1) / r.chunk : 0;
-}
+static_assert(sizeof(GqaPartDesc) == 16, "descriptor is 16 bytes");
+constexpr uint32_t DESC_PIECES = 0xffffu;
+constexpr uint32_t DESC_LAST_STARTS = 1u << 16;  // the last piece begins its sequence
+constexpr uint32_t DESC_LAST_ENDS = 1u << 17;    // the last piece ends its sequence
+constexpr uint32_t DESC_FIRST_ENDS = 1u << 18;   // the first piece ends its sequence
+constexpr int PART_HEADS = 16;                   // heads per partial slot (one subgroup)
 
 struct GqaArgs {
   const uint16_t *q;            // [B, Hq, D] bf16
   const int32_t *block_table;   // [B, max_pages_per_seq]
+  const int32_t *context_lens;  // [B]
   uint16_t *out;                // [B, Hq, D] bf16
   float *lse;                   // [B, Hq] or null
-  float *part_o;                // [B, Hq, max_splits, D]
-  float *part_lse;              // [B, Hq, max_splits], log2 units
-  WsHeader *hdr;
-  const WorkItem *items;
-  int max_pages_per_seq, num_pages;
+  float *part_o;                // [nparts, 2, 16, D] fp32
+  float *part_lse;              // [nparts, 2, 16] fp32, log2 units
+  GqaPartDesc *desc;            // [nparts]
+  int batch, max_pages_per_seq, num_pages, max_context_len, window;
   int Hq, Hkv, G, nsub;
-  int page_size, log2_page;
-  int max_splits;
+  int log2_page, log2_bh;       // page size and tokens per unit (TMA box), as powers of two
+  int piece_cost;               // partition cost of starting a piece, in units
+  int nparts;
   float qscale;                 // scale * log2(e)
 };
 
 template <int D_>
 struct GqaCfg {
   static constexpr int D = D_;
-  static constexpr int M = 16;                     // MMA rows = query heads per subgroup
-  static constexpr int TG = 4;                     // token groups per stage
-  static constexpr int DSPLIT = D <= 128 ? 2 : 1;  // warps sharing a token group (each: D / DSPLIT of P.V)
+  static constexpr int M = PART_HEADS;             // MMA rows = query heads per subgroup
+  static constexpr int ST = D <= 128 ? 64 : 32;    // tokens per stage
+  static constexpr int TW = 16;                    // tokens per token group per stage
+  static constexpr int TG = ST / TW;               // token groups per stage
+  static constexpr int DSPLIT = 2;                 // warps sharing a token group (each: D / 2 of P.V)
   static constexpr int NCW = TG * DSPLIT;          // consumer warps
   static constexpr int THREADS = (NCW + 1) * 32;   // + producer warp
-  static constexpr int TW = 16;                    // tokens per token group per stage
-  static constexpr int ST = TG * TW;               // tokens per stage
   static constexpr int NT_PV = D / 8 / DSPLIT;     // P.V n-tiles per warp
   static constexpr int NQ = D / 64;                // 128-byte swizzle planes along D
   static constexpr int PLANE = ST * 128;           // bytes of one plane (ST rows x 64 dims)
   static constexpr int KV_BYTES = NQ * PLANE;      // K (or V) of one stage
   static constexpr int STAGE_BYTES = 2 * KV_BYTES;
-  static constexpr int NS = (196608 / STAGE_BYTES) < 8 ? (196608 / STAGE_BYTES) : 8;
-  static constexpr int QBYTES = M * D * 2;
+  static constexpr int RING_BUDGET = 229376;       // 224 KB of stages
+  static constexpr int NS = (RING_BUDGET / STAGE_BYTES) < 16 ? (RING_BUDGET / STAGE_BYTES) : 16;
   static constexpr int NACC = 2;                   // independent QK accumulators
   static_assert(M * D * 4 * TG <= STAGE_BYTES, "merge area fits in one stage");
 };
 
 struct alignas(16) StageMeta {
-  int32_t end, first, last, masked;
-  int32_t b, g, sub, split;
-  int32_t tok0, tok_lo, tok_hi, ghead;  // ghead: real heads of the subgroup
-  uint32_t badmask;                     // bit k: box k of the stage was not loaded
-  int32_t nsplit, ne, pad0;             // splits / non-empty splits of the item's row
+  int32_t end, first, last, masked;  // first: a stage holding the piece's query rows only
+  int32_t b, hq0, ghead, slot;  // slot: -1 = whole sequence (final output), else partial slot 0 / 1
+  int32_t tok0, tok_lo, tok_hi, pad0;
+  uint32_t badmask;             // bit k: box k of the stage was not loaded
+  int32_t pad1, pad2, pad3;
+};
+static_assert(sizeof(StageMeta) == 64, "stage meta is 64 bytes");
+
+// Small shared state of a CTA outside the ring.
+struct GqaMisc {
+  uint32_t status;
+  int32_t found_b;
+  long long found_off;
+  GqaPartDesc desc;
+  long long warp_part[10];
 };
 
 template <class C>
 struct GqaSmem {
   static constexpr int OFF_STAGE = 0;
-  static constexpr int OFF_Q = OFF_STAGE + C::NS * C::STAGE_BYTES;
-  static constexpr int OFF_ML = OFF_Q + C::NS * C::QBYTES;
+  static constexpr int OFF_ML = OFF_STAGE + C::NS * C::STAGE_BYTES;
   static constexpr int OFF_META = OFF_ML + C::TG * C::M * 2 * 4;
   static constexpr int OFF_BAR = OFF_META + C::NS * (int)sizeof(StageMeta);
-  static constexpr int USED = OFF_BAR + 2 * C::NS * 8;
+  static constexpr int OFF_MISC = OFF_BAR + 2 * C::NS * 8;
+  static constexpr int USED = OFF_MISC + (int)sizeof(GqaMisc);
   static constexpr int BYTES = USED + 1024;  // slack to align the base to 1024 bytes
+  static_assert(BYTES <= 232448, "fits the 227 KB opt-in shared memory of one CTA");
 };
 
 // Byte offset of 16-byte chunk `chunk` (along D) of token row `tok` in a
@@ -140,10 +141,58 @@ __device__ __forceinline__ uint32_t kv_off(int tok, int chunk) {
   return (uint32_t)((chunk >> 3) * C::PLANE + tok * 128 + (((chunk & 7) ^ (tok & 7)) << 4));
 }
 
+// Visible units of a row of length L: [*u_lo, u_lo + return value).
+__device__ __forceinline__ int row_units(int L, int window, int log2_bh, int *u_lo) {
+  const int lo = (window > 0 && L > window) ? L - window : 0;
+  *u_lo = lo >> log2_bh;
+  return L > 0 ? ((L + (1 << log2_bh) - 1) >> log2_bh) - *u_lo : 0;
+}
+
+__device__ __forceinline__ int clamp_len(int L, int max_len) { return min(max(L, 0), max_len); }
+
+// Block-wide sum / exclusive scan of 64-bit values (all threads of the CTA take part).
+__device__ __forceinline__ long long block_sum64(long long v, long long *warp_part) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
+  if (lane == 0) warp_part[warp] = v;
+  __syncthreads();
+  long long t = 0;
+  for (int w = 0; w < nw; ++w) t += warp_part[w];
+  __syncthreads();
+  return t;
+}
+
+__device__ __forceinline__ long long block_scan64(long long v, long long *excl, long long *warp_part) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(FULL, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_part[warp] = x;
+  __syncthreads();
+  long long before = 0, t = 0;
+  for (int w = 0; w < nw; ++w) {
+    if (w < warp) before += warp_part[w];
+    t += warp_part[w];
+  }
+  __syncthreads();
+  *excl = before + x - v;
+  return t;
+}
+
+// One piece: units [ub, ue) of sequence (b, hs); lo / L: the row's visible token range.
+struct Piece {
+  int b, hs, ub, ue, lo, L;
+  bool starts, ends;
+};
+
 template <int D>
 __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
     gqa_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                     const GqaArgs a) {
+                     const __grid_constant__ CUtensorMap tm_q, const GqaArgs a) {
   using C = GqaCfg<D>;
   using S = GqaSmem<C>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -152,101 +201,243 @@ __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::OFF_BAR);
   uint64_t *empty = full + C::NS;
   StageMeta *meta = reinterpret_cast<StageMeta *>(smem + S::OFF_META);
+  GqaMisc *misc = reinterpret_cast<GqaMisc *>(smem + S::OFF_MISC);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
+  const int HS = a.Hkv * a.nsub;
   if (tid == 0) {
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], C::NCW);
     }
     fence_mbar_init();
+    misc->status = 0;
+    misc->found_b = -1;
   }
   if (warp == C::NCW && lane == 0) {
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
+    prefetch_tensormap(&tm_q);
   }
   __syncthreads();
-  pdl_wait();               // the plan written by the previous kernel is visible from here on
+  pdl_wait();               // inputs written by the stream's previous kernel are visible from here on
   pdl_launch_dependents();  // the combine kernel may be scheduled; it waits for this grid to finish
-  uint32_t *status = &a.hdr->status;
+  uint32_t *status = &misc->status;
+
+  // ---------------------------------------------- prologue: this CTA's range
+  // Sequence (b, hs) costs w_b = n_b + piece_cost units (0 when n_b == 0); the cost axis,
+  // flattened row by row, is cut into nparts equal ranges.  A range position inside the
+  // first piece_cost units of a sequence maps to no key: those units stand for the fixed
+  // cost of starting a piece (loading Q, merging the token groups at its end).
+  auto seq_cost = [&](int L, int *n_out) {
+    int ul;
+    const int n = row_units(L, a.window, a.log2_bh, &ul);
+    *n_out = n;
+    return n > 0 ? n + a.piece_cost : 0;
+  };
+  long long W = 0;  // total cost
+  if (a.batch <= C::THREADS) {
+    // one pass: every row in one thread
+    long long v = 0;
+    if (tid < a.batch) {
+      const int L0 = a.context_lens[tid];
+      if (L0 < 0 || L0 > a.max_context_len) atomicOr(status, PA_DEV_BAD_LEN);
+      int n;
+      v = (long long)seq_cost(clamp_len(L0, a.max_context_len), &n) * HS;
+    }
+    long long ex;
+    W = block_scan64(v, &ex, misc->warp_part);
+    const long long x0 = (long long)blockIdx.x * W / a.nparts;
+    if (v > 0 && x0 >= ex && x0 < ex + v && x0 < ((long long)blockIdx.x + 1) * W / a.nparts) {
+      misc->found_b = tid;
+      misc->found_off = x0 - ex;
+    }
+  } else {
+    long long local = 0;
+    for (int b = tid; b < a.batch; b += C::THREADS) {
+      const int L0 = a.context_lens[b];
+      if (L0 < 0 || L0 > a.max_context_len) atomicOr(status, PA_DEV_BAD_LEN);
+      int n;
+      local += seq_cost(clamp_len(L0, a.max_context_len), &n);
+    }
+    W = block_sum64(local, misc->warp_part) * HS;
+    const long long x0 = (long long)blockIdx.x * W / a.nparts;
+    if (x0 < ((long long)blockIdx.x + 1) * W / a.nparts) {
+      long long base = 0;
+      for (int b0 = 0; b0 < a.batch; b0 += C::THREADS) {
+        const int b = b0 + tid;
+        long long v = 0;
+        if (b < a.batch) {
+          int n;
+          v = (long long)seq_cost(clamp_len(a.context_lens[b], a.max_context_len), &n) * HS;
+        }
+        long long ex;
+        const long long tot = block_scan64(v, &ex, misc->warp_part);
+        if (v > 0 && x0 >= base + ex && x0 < base + ex + v) {
+          misc->found_b = b;
+          misc->found_off = x0 - base - ex;
+        }
+        base += tot;
+        __syncthreads();
+        if (misc->found_b >= 0) break;
+      }
+    }
+  }
+  const long long x_begin = (long long)blockIdx.x * W / a.nparts;
+  const long long x_end = ((long long)blockIdx.x + 1) * W / a.nparts;
+  // rows without a visible key: out = 0, lse = -inf (rows b = blockIdx.x mod nparts)
+  for (int b = blockIdx.x; b < a.batch; b += a.nparts) {
+    int ul;
+    if (row_units(clamp_len(a.context_lens[b], a.max_context_len), a.window, a.log2_bh, &ul) != 0) continue;
+    uint4 *o = reinterpret_cast<uint4 *>(a.out + (size_t)b * a.Hq * D);
+    for (int e = tid; e < a.Hq * D / 8; e += C::THREADS) o[e] = make_uint4(0, 0, 0, 0);
+    if (a.lse)
+      for (int h = tid; h < a.Hq; h += C::THREADS) a.lse[(size_t)b * a.Hq + h] = -INFINITY;
+  }
+  __syncthreads();
 
   if (warp == C::NCW) {
     // ------------------------------------------------------------ producer
-    const int n_items = (int)a.hdr->n_items;
-    const int P = a.page_size;
-    const int BH = P < C::ST ? P : C::ST;  // tokens per box
-    const int nbox = C::ST / BH;
+    const int P = 1 << a.log2_page;
+    const int nbox = C::ST >> a.log2_bh;  // boxes (units) per stage
     uint32_t j = 0;
     bool ok = true;
-    // next-item fetch: 0 idle, 1 ticket taken, 2 descriptor loaded, 3 first window loaded
-    int pstate = 0;
-    uint32_t nticket = 0;
-    int nidx = 0, nwin = 0;
-    WorkItem nit = {};
-    auto step = [&]() {
-      if (pstate == 0) {
-        if (lane == 0) nticket = atomicAdd(&a.hdr->item_counter, 1u);
-        pstate = 1;
-      } else if (pstate == 1) {
-        nidx = __shfl_sync(FULL, (int)nticket, 0);
-        if (nidx < n_items) nit = a.items[nidx];
-        pstate = 2;
-      } else if (pstate == 2) {
-        if (nidx < n_items) {
-          const int np = nit.page_end - nit.page_begin;
-          nwin = lane < np ? a.block_table[(size_t)nit.b * a.max_pages_per_seq + nit.page_begin + lane] : 0;
-        }
-        pstate = 3;
+    long long R = misc->found_b >= 0 ? x_end - x_begin : 0;  // cost still to walk
+    int npieces = 0;
+    Piece last_piece = {};
+    bool first_ends = false;
+    // lens window: lane l holds the clamped length of row rb + l
+    int rb = max(misc->found_b, 0);
+    int lwin = rb + lane < a.batch ? clamp_len(a.context_lens[rb + lane], a.max_context_len) : 0;
+    auto len_of = [&](int row) {  // rows only move forward
+      while (row >= rb + 32) {
+        rb += 32;
+        lwin = rb + lane < a.batch ? clamp_len(a.context_lens[rb + lane], a.max_context_len) : 0;
       }
+      return __shfl_sync(FULL, lwin, row - rb);
     };
-    step();
-    step();
-    step();
-    while (ok) {
-      if (nidx >= n_items) {
+    // walk position: sequence (it_b, it_hs), `it_in` cost units into it
+    int it_b = rb, it_hs = 0, it_in = 0;
+    if (R > 0) {
+      int n;
+      const int w = seq_cost(len_of(it_b), &n);
+      it_hs = (int)(misc->found_off / w);
+      it_in = (int)(misc->found_off % w);
+    }
+    // the next piece that holds at least one key; false once the range is walked
+    auto take_piece = [&](Piece &p) {
+      while (R > 0) {
+        const int L = len_of(it_b);
+        int n;
+        const int w = seq_cost(L, &n);
+        const int take = (int)min((long long)(w - it_in), R);
+        const int u0 = max(0, it_in - a.piece_cost), u1 = max(0, it_in + take - a.piece_cost);
+        const int b = it_b, hs = it_hs;
+        R -= take;
+        it_in += take;
+        if (it_in == w && R > 0) {
+          it_in = 0;
+          if (++it_hs == HS) {
+            it_hs = 0;
+            int nn;
+            do {
+              ++it_b;
+            } while (it_b < a.batch - 1 && seq_cost(len_of(it_b), &nn) == 0);
+          }
+        }
+        if (u1 > u0) {
+          int ul;
+          row_units(L, a.window, a.log2_bh, &ul);
+          p.b = b;
+          p.hs = hs;
+          p.L = L;
+          p.lo = (a.window > 0 && L > a.window) ? L - a.window : 0;
+          p.ub = ul + u0;
+          p.ue = ul + u1;
+          p.starts = u0 == 0;
+          p.ends = u1 == n;
+          return true;
+        }
+      }
+      return false;
+    };
+    auto q_head0 = [&](const Piece &p) { return (p.hs / a.nsub) * a.G + (p.hs % a.nsub) * C::M; };
+    auto q_heads = [&](const Piece &p) { return min(C::M, a.G - (p.hs % a.nsub) * C::M); };
+    // block-table window 0 of a piece (lane l: entry l of its first page)
+    auto piece_window = [&](const Piece &p) {
+      const int pb = (p.ub << a.log2_bh) >> a.log2_page;
+      const int pe = (((p.ue << a.log2_bh) - 1) >> a.log2_page) + 1;
+      return lane < pe - pb ? a.block_table[(size_t)p.b * a.max_pages_per_seq + pb + lane] : 0;
+    };
+    Piece cur = {}, nxt = {};
+    bool has_cur = take_piece(cur);
+    int cwin0 = 0, nwin0 = 0;
+    bool has_next = false;
+    if (has_cur) {
+      cwin0 = piece_window(cur);
+      has_next = take_piece(nxt);
+      if (has_next) nwin0 = piece_window(nxt);
+    }
+    while (has_cur && ok) {
+      // ---- emit the stages of `cur`
+      const int g = cur.hs / a.nsub;
+      const int ghead = q_heads(cur);
+      const int hq0 = q_head0(cur);
+      const int slot = (cur.starts && cur.ends) ? -1 : (npieces == 0 ? 0 : 1);
+      const int T0 = cur.ub << a.log2_bh;
+      const int tok_lo = max(cur.lo, T0), tok_hi = min(cur.L, cur.ue << a.log2_bh);
+      const int n_stages = (cur.ue - cur.ub + nbox - 1) / nbox;
+      const int pb = T0 >> a.log2_page;
+      const int npages = ((((cur.ue << a.log2_bh) - 1) >> a.log2_page) + 1) - pb;
+      const int32_t *bt_piece = a.block_table + (size_t)cur.b * a.max_pages_per_seq + pb;
+      int cwin = cwin0, wi = 0;
+      int fwin = (lane + 32 < npages) ? bt_piece[32 + lane] : 0;  // window 1, in flight
+      {
+        // the piece's query rows: a stage of their own (16 rows from row b * Hq + hq0; rows
+        // past ghead belong to other heads or are zero-filled, and are masked by the consumers)
         const int s = j % C::NS;
         const uint32_t u = j / C::NS;
         if (u > 0) ok = mbar_wait(&empty[s], (u - 1) & 1, status);
-        if (ok && lane == 0) {
-          meta[s].end = 1;
-          mbar_arrive(&full[s]);
+        if (!ok) break;
+        if (lane == 0) {
+          StageMeta &m = meta[s];
+          m.end = 0;
+          m.first = 1;
+          m.last = 0;
+          m.b = cur.b;
+          m.hq0 = hq0;
+          m.ghead = ghead;
+          mbar_arrive_expect_tx(&full[s], (uint32_t)(C::NQ * C::M * 128));
+          uint8_t *qdst = smem + S::OFF_STAGE + s * C::STAGE_BYTES;
+#pragma unroll
+          for (int dq = 0; dq < C::NQ; ++dq)
+            tma_load_2d(qdst + dq * (C::M * 128), &tm_q, dq * 64, cur.b * a.Hq + hq0, &full[s]);
         }
-        break;
+        __syncwarp();
+        ++j;
       }
-      const WorkItem it = nit;
-      int cwin = nwin;  // block-table window `wi` of this item
-      int wi = 0;
-      pstate = 0;
-      step();  // take the next ticket right away
-      const int g = it.sub / a.nsub, sub = it.sub % a.nsub;
-      const int ghead = min(C::M, a.G - sub * C::M);
-      const int npages = it.page_end - it.page_begin;
-      const int T0 = it.page_begin * P, T1 = it.page_end * P;
-      const int tok_lo = it.tok_lo, tok_hi = it.tok_hi;
-      const int n_stages = (T1 - T0 + C::ST - 1) / C::ST;
-      const int32_t *bt_item = a.block_table + (size_t)it.b * a.max_pages_per_seq + it.page_begin;
-      int fwin = (lane + 32 < npages) ? bt_item[32 + lane] : 0;  // window wi + 1, in flight
-      const int nsplit = it.splits >> 16, ne = it.splits & 0xffff;
       for (int t = 0; t < n_stages && ok; ++t, ++j) {
         const int s = j % C::NS;
         const uint32_t u = j / C::NS;
         if (u > 0) ok = mbar_wait(&empty[s], (u - 1) & 1, status);
         if (!ok) break;
-        const int tok0 = T0 + t * C::ST;
-        // the pages of one stage never straddle a 32-page window
-        const int pwin = ((tok0 - T0) >> a.log2_page) >> 5;
+        const int unit0 = cur.ub + t * nbox;
+        const int tok0 = unit0 << a.log2_bh;
+        // the pages of one stage never straddle a 32-page window (nbox divides 32)
+        const int pwin = ((tok0 >> a.log2_page) - pb) >> 5;
         while (wi < pwin) {
           cwin = fwin;
           ++wi;
-          const int nxt = 32 * (wi + 1) + lane;
-          fwin = nxt < npages ? bt_item[nxt] : 0;
+          const int nx = 32 * (wi + 1) + lane;
+          fwin = nx < npages ? bt_piece[nx] : 0;
         }
+        const int unit = unit0 + lane;
+        const int btok = unit << a.log2_bh;
+        const int prel = (btok >> a.log2_page) - pb;
+        const int phys = __shfl_sync(FULL, cwin, prel & 31);
         bool load = false, isbad = false;
-        const int btok = tok0 + lane * BH;
-        const int pi = (btok - T0) >> a.log2_page;  // page index within the item
-        const int phys = __shfl_sync(FULL, cwin, pi & 31);
-        if (lane < nbox && btok < tok_hi && btok + BH > tok_lo) {
+        if (lane < nbox && unit < cur.ue) {
           if (phys < 0 || phys >= a.num_pages) {
             isbad = true;
             atomicOr(status, PA_DEV_BAD_PAGE);
@@ -256,281 +447,309 @@ __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
         }
         const uint32_t bad = __ballot_sync(FULL, isbad);
         const int nvalid = __popc(__ballot_sync(FULL, load));
-        const bool first = (t == 0), last = (t == n_stages - 1);
+        const bool last = (t == n_stages - 1);
         uint8_t *kdst = smem + S::OFF_STAGE + s * C::STAGE_BYTES;
         if (lane == 0) {
           StageMeta &m = meta[s];
           m.end = 0;
-          m.first = first;
+          m.first = 0;
           m.last = last;
-          m.b = it.b;
-          m.g = g;
-          m.sub = sub;
-          m.split = it.split;
+          m.b = cur.b;
+          m.hq0 = hq0;
+          m.ghead = ghead;
+          m.slot = slot;
           m.tok0 = tok0;
           m.tok_lo = tok_lo;
           m.tok_hi = tok_hi;
-          m.ghead = ghead;
           m.badmask = bad;
-          m.nsplit = nsplit;
-          m.ne = ne;
           m.masked = (tok0 < tok_lo) || (tok0 + C::ST > tok_hi) || bad != 0;
-          const uint32_t qbytes = first ? (uint32_t)(ghead * D * 2) : 0u;
-          mbar_arrive_expect_tx(&full[s], (uint32_t)nvalid * (uint32_t)(BH * D * 2 * 2) + qbytes);
-          if (first) {
-            const uint16_t *qsrc = a.q + ((size_t)it.b * a.Hq + (size_t)g * a.G + (size_t)sub * C::M) * D;
-            bulk_load(smem + S::OFF_Q + s * C::QBYTES, qsrc, qbytes, &full[s]);
-          }
+          mbar_arrive_expect_tx(&full[s], (uint32_t)nvalid * (uint32_t)((D * 2 * 2) << a.log2_bh));
         }
         __syncwarp();
         if (load) {
-          const int slot = btok & (P - 1);
+          const int pslot = btok & (P - 1);
+          uint8_t *dst = kdst + (lane << a.log2_bh) * 128;
 #pragma unroll
           for (int dq = 0; dq < C::NQ; ++dq) {
-            uint8_t *dst = kdst + dq * C::PLANE + lane * BH * 128;
-            tma_load_4d(dst, &tm_k, dq * 64, g, slot, phys, &full[s]);
-            tma_load_4d(dst + C::KV_BYTES, &tm_v, dq * 64, g, slot, phys, &full[s]);
+            tma_load_4d(dst + dq * C::PLANE, &tm_k, dq * 64, g, pslot, phys, &full[s]);
+            tma_load_4d(dst + dq * C::PLANE + C::KV_BYTES, &tm_v, dq * 64, g, pslot, phys, &full[s]);
           }
         }
-        // advance the next-item fetch at stages ~n/3 and ~2n/3, so each dependent load has a
-        // third of the item's stages to land before its value is needed
-        if (pstate < 3 && (t + 1) * 3 >= pstate * n_stages) step();
       }
-      while (pstate < 3) step();
+      if (!ok) break;
+      if (npieces == 0) first_ends = cur.ends;
+      if (npieces < (int)DESC_PIECES) ++npieces;
+      last_piece = cur;
+      has_cur = has_next;
+      if (!has_cur) break;
+      cur = nxt;
+      cwin0 = nwin0;
+      has_next = take_piece(nxt);
+      if (has_next) nwin0 = piece_window(nxt);
+    }
+    if (ok) {
+      // end marker
+      const int s = j % C::NS;
+      const uint32_t u = j / C::NS;
+      if (u > 0) ok = mbar_wait(&empty[s], (u - 1) & 1, status);
+      if (ok && lane == 0) {
+        meta[s].end = 1;
+        mbar_arrive(&full[s]);
+      }
     }
     if (!ok) {
       // A wait gave up: let the copies this warp issued land before the CTA exits.
       const uint32_t first = j > (uint32_t)C::NS ? j - C::NS : 0u;
       for (uint32_t i = first; i < j; ++i) mbar_wait(&full[i % C::NS], (i / C::NS) & 1, status);
     }
-    return;
-  }
-
-  // -------------------------------------------------------------- consumers
-  const int ct = tid;                               // consumer thread index
-  const int g8 = lane >> 2, tq = lane & 3;          // MMA fragment row / column pair
-  const int lm_mat = lane >> 3, lm_row = lane & 7;  // ldmatrix: matrix / row this lane addresses
-  const int tgrp = warp % C::TG;                    // token group of this warp
-  const int dh = warp / C::TG;                      // which 1/DSPLIT of the P.V columns it owns
-  const int wbase = tgrp * C::TW;                   // first stage token of this warp
-  const int nd0 = dh * C::NT_PV;                    // first P.V n-tile of this warp
-  float *sm_ml = reinterpret_cast<float *>(smem + S::OFF_ML);
-  const float TAU = 8.f;
-
-  uint32_t qa[D / 16][4];   // Q A-fragments (rows = heads)
-  float acc[C::NT_PV][4];   // O C-fragments of this warp's columns: [n-tile][row g8 x2, row g8+8 x2]
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  int ghead = 0;
-
-  for (uint32_t j = 0;; ++j) {
-    const int s = j % C::NS;
-    if (!mbar_wait(&full[s], (j / C::NS) & 1, status)) break;
-    const StageMeta &mt = meta[s];
-    if (mt.end) break;
-    const uint32_t kbase = smem_u32(smem + S::OFF_STAGE + s * C::STAGE_BYTES);
-    const uint32_t vbase = kbase + C::KV_BYTES;
-    if (mt.first) {
-      ghead = mt.ghead;
-      const uint16_t *qs = reinterpret_cast<const uint16_t *>(smem + S::OFF_Q + s * C::QBYTES);
-#pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        const int c0 = ks * 16 + 2 * tq;
-        qa[ks][0] = g8 < ghead ? *reinterpret_cast<const uint32_t *>(qs + g8 * D + c0) : 0u;
-        qa[ks][1] = g8 + 8 < ghead ? *reinterpret_cast<const uint32_t *>(qs + (g8 + 8) * D + c0) : 0u;
-        qa[ks][2] = g8 < ghead ? *reinterpret_cast<const uint32_t *>(qs + g8 * D + c0 + 8) : 0u;
-        qa[ks][3] = g8 + 8 < ghead ? *reinterpret_cast<const uint32_t *>(qs + (g8 + 8) * D + c0 + 8) : 0u;
-      }
-#pragma unroll
-      for (int n = 0; n < C::NT_PV; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-      m0 = m1 = -INFINITY;
-      l0 = l1 = 0.f;
+    if (lane == 0) {
+      misc->desc.last_b = last_piece.b;
+      misc->desc.last_hs = last_piece.hs;
+      misc->desc.flags = (uint32_t)npieces | (last_piece.starts ? DESC_LAST_STARTS : 0u) |
+                         (last_piece.ends ? DESC_LAST_ENDS : 0u) | (first_ends ? DESC_FIRST_ENDS : 0u);
     }
+  } else {
+    // ------------------------------------------------------------ consumers
+    const int ct = tid;                               // consumer thread index
+    const int g8 = lane >> 2, tq = lane & 3;          // MMA fragment row / column pair
+    const int lm_mat = lane >> 3, lm_row = lane & 7;  // ldmatrix: matrix / row this lane addresses
+    const int tgrp = warp % C::TG;                    // token group of this warp
+    const int dh = warp / C::TG;                      // which half of the P.V columns it owns
+    const int wbase = tgrp * C::TW;                   // first stage token of this warp
+    const int nd0 = dh * C::NT_PV;                    // first P.V n-tile of this warp
+    float *sm_ml = reinterpret_cast<float *>(smem + S::OFF_ML);
+    const float TAU = 8.f;
+    const int bh_tokens = 1 << a.log2_bh;
 
-    // ---- S = Q K^T for the group's 16 tokens (two n-tiles of 8); the k-steps are
-    // spread over NACC independent accumulators so no long chain of dependent MMAs forms
-    float sv[2][4];
-    {
-      float sp[C::NACC][2][4];
+    uint32_t qa[D / 16][4];  // Q A-fragments (rows = heads)
+    float acc[C::NT_PV][4];  // O C-fragments of this warp's columns: [n-tile][row g8 x2, row g8+8 x2]
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    int ghead = 0;
+    for (uint32_t j = 0;; ++j) {
+      const int s = j % C::NS;
+      if (!mbar_wait(&full[s], (j / C::NS) & 1, status)) break;
+      const StageMeta &mt = meta[s];
+      if (mt.end) break;
+      const uint32_t kbase = smem_u32(smem + S::OFF_STAGE + s * C::STAGE_BYTES);
+      const uint32_t vbase = kbase + C::KV_BYTES;
+      if (mt.first) {
+        // a new piece: its query rows into the A-fragments (ldmatrix from the 128-byte
+        // swizzled planes of 16 rows x 64 dims), fresh softmax state, and the stage goes back
+        ghead = mt.ghead;
+        const uint32_t qbase = kbase;
 #pragma unroll
-      for (int q = 0; q < C::NACC; ++q)
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) sp[q][nt][0] = sp[q][nt][1] = sp[q][nt][2] = sp[q][nt][3] = 0.f;
-#pragma unroll
-      for (int ks2 = 0; ks2 < D / 32; ++ks2) {
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          uint32_t b[4];
-          ldmatrix_x4(b, kbase + kv_off<C>(wbase + nt * 8 + lm_row, 4 * ks2 + lm_mat));
-          mma_bf16_16816(sp[(2 * ks2) % C::NACC][nt], qa[2 * ks2], b[0], b[1]);
-          mma_bf16_16816(sp[(2 * ks2 + 1) % C::NACC][nt], qa[2 * ks2 + 1], b[2], b[3]);
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const int row = (lm_mat & 1) * 8 + lm_row, chunk = 2 * ks + (lm_mat >> 1);
+          ldmatrix_x4(qa[ks], qbase + (chunk >> 3) * (C::M * 128) + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
         }
+#pragma unroll
+        for (int n = 0; n < C::NT_PV; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+        m0 = m1 = -INFINITY;
+        l0 = l1 = 0.f;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        continue;
       }
+
+      // ---- S = Q K^T for the group's 16 tokens (two n-tiles of 8); the k-steps are
+      // spread over NACC independent accumulators so no long chain of dependent MMAs forms
+      float sv[2][4];
+      {
+        float sp[C::NACC][2][4];
+#pragma unroll
+        for (int q = 0; q < C::NACC; ++q)
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) sp[q][nt][0] = sp[q][nt][1] = sp[q][nt][2] = sp[q][nt][3] = 0.f;
+#pragma unroll
+        for (int ks2 = 0; ks2 < D / 32; ++ks2) {
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            uint32_t b[4];
+            ldmatrix_x4(b, kbase + kv_off<C>(wbase + nt * 8 + lm_row, 4 * ks2 + lm_mat));
+            mma_bf16_16816(sp[(2 * ks2) % C::NACC][nt], qa[2 * ks2], b[0], b[1]);
+            mma_bf16_16816(sp[(2 * ks2 + 1) % C::NACC][nt], qa[2 * ks2 + 1], b[2], b[3]);
+          }
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float x = sp[0][nt][e];
+#pragma unroll
+            for (int q = 1; q < C::NACC; ++q) x += sp[q][nt][e];
+            sv[nt][e] = x;
+          }
+      }
+      const bool masked = mt.masked;
+      // scale, mask (invalid tokens and padded head rows -> -inf)
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          float x = sp[0][nt][e];
-#pragma unroll
-          for (int q = 1; q < C::NACC; ++q) x += sp[q][nt][e];
-          sv[nt][e] = x;
+          const float v = sv[nt][e] * a.qscale;
+          const int row = (e < 2) ? g8 : g8 + 8;
+          bool valid = row < ghead;
+          if (masked) {
+            const int stok = wbase + nt * 8 + 2 * tq + (e & 1);
+            const int ltok = mt.tok0 + stok;
+            valid = valid && ltok >= mt.tok_lo && ltok < mt.tok_hi && !((mt.badmask >> (stok / bh_tokens)) & 1u);
+          }
+          sv[nt][e] = valid ? v : -INFINITY;
         }
-    }
-    const bool masked = mt.masked;
-    const int bh_tokens = a.page_size < C::ST ? a.page_size : C::ST;
-    // scale, mask (invalid tokens and padded head rows -> -inf)
+      // ---- online softmax per head row (rows g8 and g8 + 8)
+      float x0 = fmaxf(fmaxf(sv[0][0], sv[0][1]), fmaxf(sv[1][0], sv[1][1]));
+      float x1 = fmaxf(fmaxf(sv[0][2], sv[0][3]), fmaxf(sv[1][2], sv[1][3]));
+      x0 = fmaxf(x0, __shfl_xor_sync(FULL, x0, 1));
+      x0 = fmaxf(x0, __shfl_xor_sync(FULL, x0, 2));
+      x1 = fmaxf(x1, __shfl_xor_sync(FULL, x1, 1));
+      x1 = fmaxf(x1, __shfl_xor_sync(FULL, x1, 2));
+      if (__any_sync(FULL, (x0 > m0 + TAU) || (x1 > m1 + TAU))) {
+        const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+        const float a0 = (n0 == -INFINITY) ? 1.f : fast_exp2(m0 - n0);
+        const float a1 = (n1 == -INFINITY) ? 1.f : fast_exp2(m1 - n1);
+        m0 = n0;
+        m1 = n1;
+        l0 *= a0;
+        l1 *= a1;
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+        for (int n = 0; n < C::NT_PV; ++n) {
+          acc[n][0] *= a0;
+          acc[n][1] *= a0;
+          acc[n][2] *= a1;
+          acc[n][3] *= a1;
+        }
+      }
+      uint32_t pa[4];
+      {
+        float p[2][4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float v = sv[nt][e] * a.qscale;
-        const int row = (e < 2) ? g8 : g8 + 8;
-        bool valid = row < ghead;
-        if (masked) {
-          const int stok = wbase + nt * 8 + 2 * tq + (e & 1);
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float mr = (e < 2) ? m0 : m1;
+            p[nt][e] = (sv[nt][e] == -INFINITY) ? 0.f : fast_exp2(sv[nt][e] - mr);
+          }
+        pa[0] = pack_bf16x2(p[0][0], p[0][1]);
+        pa[1] = pack_bf16x2(p[0][2], p[0][3]);
+        pa[2] = pack_bf16x2(p[1][0], p[1][1]);
+        pa[3] = pack_bf16x2(p[1][2], p[1][3]);
+        // the denominator (and so the LSE) sums the fp32 weights; only the MMA operand is rounded
+        l0 += (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
+        l1 += (p[0][2] + p[0][3]) + (p[1][2] + p[1][3]);
+      }
+      if (masked) {
+        // V rows of keys that are not attended (outside [lo, L), unloaded boxes) may hold
+        // anything, NaN included: zero this warp's columns of them so that 0 x row stays 0.
+        uint8_t *vgen = smem + S::OFF_STAGE + s * C::STAGE_BYTES + C::KV_BYTES;
+        constexpr int CPW = C::NQ * 8 / C::DSPLIT;  // 16-byte chunks of a row owned by this warp
+        for (int e = lane; e < C::TW * CPW; e += 32) {
+          const int stok = wbase + e / CPW;
+          const int chunk = dh * CPW + e % CPW;
           const int ltok = mt.tok0 + stok;
-          valid = valid && ltok >= mt.tok_lo && ltok < mt.tok_hi && !((mt.badmask >> (stok / bh_tokens)) & 1u);
+          if (ltok < mt.tok_lo || ltok >= mt.tok_hi || ((mt.badmask >> (stok / bh_tokens)) & 1u))
+            *reinterpret_cast<uint4 *>(vgen + kv_off<C>(stok, chunk)) = make_uint4(0, 0, 0, 0);
         }
-        sv[nt][e] = valid ? v : -INFINITY;
+        __syncwarp();
       }
-    // ---- online softmax per head row (rows g8 and g8 + 8)
-    float x0 = fmaxf(fmaxf(sv[0][0], sv[0][1]), fmaxf(sv[1][0], sv[1][1]));
-    float x1 = fmaxf(fmaxf(sv[0][2], sv[0][3]), fmaxf(sv[1][2], sv[1][3]));
-    x0 = fmaxf(x0, __shfl_xor_sync(FULL, x0, 1));
-    x0 = fmaxf(x0, __shfl_xor_sync(FULL, x0, 2));
-    x1 = fmaxf(x1, __shfl_xor_sync(FULL, x1, 1));
-    x1 = fmaxf(x1, __shfl_xor_sync(FULL, x1, 2));
-    if (__any_sync(FULL, (x0 > m0 + TAU) || (x1 > m1 + TAU))) {
-      const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
-      const float a0 = (n0 == -INFINITY) ? 1.f : fast_exp2(m0 - n0);
-      const float a1 = (n1 == -INFINITY) ? 1.f : fast_exp2(m1 - n1);
-      m0 = n0;
-      m1 = n1;
-      l0 *= a0;
-      l1 *= a1;
+      // ---- O += P V (k = the group's 16 tokens), this warp's columns
+      {
+        const int tok = wbase + (lm_mat & 1) * 8 + lm_row;
 #pragma unroll
-      for (int n = 0; n < C::NT_PV; ++n) {
-        acc[n][0] *= a0;
-        acc[n][1] *= a0;
-        acc[n][2] *= a1;
-        acc[n][3] *= a1;
-      }
-    }
-    uint32_t pa[4];
-    {
-      float p[2][4];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float mr = (e < 2) ? m0 : m1;
-          p[nt][e] = (sv[nt][e] == -INFINITY) ? 0.f : fast_exp2(sv[nt][e] - mr);
+        for (int nd = 0; nd < C::NT_PV; nd += 2) {
+          uint32_t b[4];
+          ldmatrix_x4_trans(b, vbase + kv_off<C>(tok, nd0 + nd + (lm_mat >> 1)));
+          mma_bf16_16816(acc[nd], pa, b[0], b[1]);
+          mma_bf16_16816(acc[nd + 1], pa, b[2], b[3]);
         }
-      pa[0] = pack_bf16x2(p[0][0], p[0][1]);
-      pa[1] = pack_bf16x2(p[0][2], p[0][3]);
-      pa[2] = pack_bf16x2(p[1][0], p[1][1]);
-      pa[3] = pack_bf16x2(p[1][2], p[1][3]);
-      // the denominator (and so the LSE) sums the fp32 weights; only the MMA operand is rounded
-      l0 += (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
-      l1 += (p[0][2] + p[0][3]) + (p[1][2] + p[1][3]);
-    }
-    if (masked) {
-      // V rows of keys that are not attended (outside [lo, L), unloaded boxes) may hold
-      // anything, NaN included: zero this warp's columns of them so that 0 x row stays 0.
-      uint8_t *vgen = smem + S::OFF_STAGE + s * C::STAGE_BYTES + C::KV_BYTES;
-      constexpr int CPW = C::NQ * 8 / C::DSPLIT;  // 16-byte chunks of a row owned by this warp
-      for (int e = lane; e < C::TW * CPW; e += 32) {
-        const int stok = wbase + e / CPW;
-        const int chunk = dh * CPW + e % CPW;
-        const int ltok = mt.tok0 + stok;
-        if (ltok < mt.tok_lo || ltok >= mt.tok_hi || ((mt.badmask >> (stok / bh_tokens)) & 1u))
-          *reinterpret_cast<uint4 *>(vgen + kv_off<C>(stok, chunk)) = make_uint4(0, 0, 0, 0);
+      }
+
+      if (mt.last) {
+        // ---- end of a piece: merge the token groups through this stage's buffer
+        l0 += __shfl_xor_sync(FULL, l0, 1);
+        l0 += __shfl_xor_sync(FULL, l0, 2);
+        l1 += __shfl_xor_sync(FULL, l1, 1);
+        l1 += __shfl_xor_sync(FULL, l1, 2);
+        named_bar(1, C::NCW * 32);  // all warps are done reading this stage
+        float *mg = reinterpret_cast<float *>(smem + S::OFF_STAGE + s * C::STAGE_BYTES);
+        // merge-area column of (head h, dim d) is d ^ (4 (h & 7)): rows of one fragment hit distinct banks
+#pragma unroll
+        for (int n = 0; n < C::NT_PV; ++n) {
+          const int d = ((nd0 + n) * 8 + 2 * tq) ^ (4 * g8);
+          *reinterpret_cast<float2 *>(mg + (tgrp * C::M + g8) * D + d) = make_float2(acc[n][0], acc[n][1]);
+          *reinterpret_cast<float2 *>(mg + (tgrp * C::M + g8 + 8) * D + d) = make_float2(acc[n][2], acc[n][3]);
+        }
+        if (tq == 0 && dh == 0) {  // both column halves of a token group hold the same (m, l)
+          sm_ml[(tgrp * C::M + g8) * 2] = m0;
+          sm_ml[(tgrp * C::M + g8) * 2 + 1] = l0;
+          sm_ml[(tgrp * C::M + g8 + 8) * 2] = m1;
+          sm_ml[(tgrp * C::M + g8 + 8) * 2 + 1] = l1;
+        }
+        named_bar(1, C::NCW * 32);
+        // each thread: 4 consecutive dims of one head; token-group weights
+        // exp2(m_w - M) / sum_w l_w exp2(m_w - M), computed by every thread of the head
+        const int slot = mt.slot;
+        const size_t pi = (size_t)blockIdx.x * 2 + (slot > 0 ? 1 : 0);  // partial slot (when slot >= 0)
+        for (int e = ct; e < ghead * (D / 4); e += C::NCW * 32) {
+          const int h = e / (D / 4), d4 = (e % (D / 4)) * 4;
+          float mw[C::TG], M = -INFINITY;
+#pragma unroll
+          for (int w = 0; w < C::TG; ++w) {
+            mw[w] = sm_ml[(w * C::M + h) * 2];
+            M = fmaxf(M, mw[w]);
+          }
+          float L = 0.f;
+          float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int w = 0; w < C::TG; ++w) {
+            const float wt = (mw[w] == -INFINITY) ? 0.f : fast_exp2(mw[w] - M);
+            L += sm_ml[(w * C::M + h) * 2 + 1] * wt;
+            const float4 x = *reinterpret_cast<const float4 *>(mg + (w * C::M + h) * D + (d4 ^ (4 * (h & 7))));
+            o.x += wt * x.x;
+            o.y += wt * x.y;
+            o.z += wt * x.z;
+            o.w += wt * x.w;
+          }
+          const float inv = L > 0.f ? 1.f / L : 0.f;
+          const size_t bh = (size_t)mt.b * a.Hq + mt.hq0 + h;
+          if (slot < 0) {
+            uint2 v;
+            v.x = pack_bf16x2(o.x * inv, o.y * inv);
+            v.y = pack_bf16x2(o.z * inv, o.w * inv);
+            *reinterpret_cast<uint2 *>(a.out + bh * D + d4) = v;
+          } else {
+            *reinterpret_cast<float4 *>(a.part_o + (pi * C::M + h) * D + d4) =
+                make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+          }
+          if (d4 == 0) {
+            const float lse2 = (M == -INFINITY || L == 0.f) ? -INFINITY : M + __log2f(L);
+            if (slot < 0) {
+              if (a.lse) a.lse[bh] = lse2 * LN2;
+            } else {
+              a.part_lse[pi * C::M + h] = lse2;
+            }
+          }
+        }
+        // no CTA barrier before the release: every warp arrives on the stage's empty barrier
+        // after its own reads, and the producer refills the stage only once all have arrived
+        fence_proxy_async_smem();  // generic writes to the stage buffer precede its next TMA fill
+      } else if (masked) {
+        fence_proxy_async_smem();  // the zeroed V rows precede the next TMA fill of this stage
       }
       __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
     }
-    // ---- O += P V (k = the group's 16 tokens), this warp's columns
-    {
-      const int tok = wbase + (lm_mat & 1) * 8 + lm_row;
-#pragma unroll
-      for (int nd = 0; nd < C::NT_PV; nd += 2) {
-        uint32_t b[4];
-        ldmatrix_x4_trans(b, vbase + kv_off<C>(tok, nd0 + nd + (lm_mat >> 1)));
-        mma_bf16_16816(acc[nd], pa, b[0], b[1]);
-        mma_bf16_16816(acc[nd + 1], pa, b[2], b[3]);
-      }
-    }
+  }
 
-    if (mt.last) {
-      // ---- end of item: merge the token groups through this stage's buffer
-      l0 += __shfl_xor_sync(FULL, l0, 1);
-      l0 += __shfl_xor_sync(FULL, l0, 2);
-      l1 += __shfl_xor_sync(FULL, l1, 1);
-      l1 += __shfl_xor_sync(FULL, l1, 2);
-      named_bar(1, C::NCW * 32);  // all warps are done reading this stage
-      float *mg = reinterpret_cast<float *>(smem + S::OFF_STAGE + s * C::STAGE_BYTES);
-      // merge-area column of (head h, dim d) is d ^ (4 (h & 7)): rows of one fragment hit distinct banks
-#pragma unroll
-      for (int n = 0; n < C::NT_PV; ++n) {
-        const int d = ((nd0 + n) * 8 + 2 * tq) ^ (4 * g8);
-        *reinterpret_cast<float2 *>(mg + (tgrp * C::M + g8) * D + d) = make_float2(acc[n][0], acc[n][1]);
-        *reinterpret_cast<float2 *>(mg + (tgrp * C::M + g8 + 8) * D + d) = make_float2(acc[n][2], acc[n][3]);
-      }
-      if (tq == 0 && dh == 0) {  // both column halves of a token group hold the same (m, l)
-        sm_ml[(tgrp * C::M + g8) * 2] = m0;
-        sm_ml[(tgrp * C::M + g8) * 2 + 1] = l0;
-        sm_ml[(tgrp * C::M + g8 + 8) * 2] = m1;
-        sm_ml[(tgrp * C::M + g8 + 8) * 2 + 1] = l1;
-      }
-      named_bar(1, C::NCW * 32);
-      const bool direct = mt.nsplit == 1;
-      const int hq0 = mt.g * a.G + mt.sub * C::M;
-      // per head: weight of each token group, exp2(m_w - M) / sum_w l_w exp2(m_w - M)
-      if (ct < ghead) {
-        const int h = ct;
-        float mw[C::TG], lw[C::TG], M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < C::TG; ++w) {
-          mw[w] = sm_ml[(w * C::M + h) * 2];
-          lw[w] = sm_ml[(w * C::M + h) * 2 + 1];
-          M = fmaxf(M, mw[w]);
-        }
-        float L = 0.f, wt[C::TG];
-#pragma unroll
-        for (int w = 0; w < C::TG; ++w) {
-          wt[w] = (mw[w] == -INFINITY) ? 0.f : fast_exp2(mw[w] - M);
-          L += lw[w] * wt[w];
-        }
-        const float inv = L > 0.f ? 1.f / L : 0.f;
-        const float lse2 = (M == -INFINITY || L == 0.f) ? -INFINITY : M + __log2f(L);
-        const size_t bh = (size_t)mt.b * a.Hq + hq0 + h;
-        if (direct) {
-          if (a.lse) a.lse[bh] = lse2 * LN2;
-        } else {
-          a.part_lse[bh * a.max_splits + mt.split] = lse2;
-        }
-        // each thread only rewrites the m-slots of its own head, which only it reads
-#pragma unroll
-        for (int w = 0; w < C::TG; ++w) sm_ml[(w * C::M + h) * 2] = wt[w] * inv;
-      }
-      named_bar(1, C::NCW * 32);
-      for (int e = ct; e < ghead * D; e += C::NCW * 32) {
-        const int h = e / D, d = e % D;
-        float o = 0.f;
-#pragma unroll
-        for (int w = 0; w < C::TG; ++w) o += mg[(w * C::M + h) * D + (d ^ (4 * (h & 7)))] * sm_ml[(w * C::M + h) * 2];
-        const size_t bh = (size_t)mt.b * a.Hq + hq0 + h;
-        if (direct) {
-          a.out[bh * D + d] = f32_to_bf16_bits(o);
-        } else {
-          a.part_o[(bh * a.max_splits + mt.split) * D + d] = o;
-        }
-      }
-      named_bar(1, C::NCW * 32);
-      fence_proxy_async_smem();  // generic writes to the stage buffer precede its next TMA fill
-    } else if (masked) {
-      fence_proxy_async_smem();  // the zeroed V rows precede the next TMA fill of this stage
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
+  __syncthreads();
+  if (tid == 0) {
+    GqaPartDesc d = misc->desc;
+    d.status = misc->status;
+    a.desc[blockIdx.x] = d;
+  }
+  if ((misc->desc.flags & DESC_PIECES) == 0) {
+    // no work: leave slot 0 empty (lse -inf, output 0), so a merge that spans this CTA adds nothing
+    for (int e = tid; e < C::M * D; e += C::THREADS) a.part_o[(size_t)blockIdx.x * 2 * C::M * D + e] = 0.f;
+    for (int h = tid; h < C::M; h += C::THREADS) a.part_lse[(size_t)blockIdx.x * 2 * C::M + h] = -INFINITY;
   }
 }
 
@@ -539,69 +758,96 @@ struct CombineArgs {
   float *lse;
   const float *part_o;
   const float *part_lse;
-  const RowInfo *rows;
-  int batch, Hq, max_splits;
+  const GqaPartDesc *desc;
+  uint32_t *status;  // the workspace status word: OR of every CTA's bits
+  int Hq, G, nsub, nparts;
 };
 
-// One warp per (row, query head) with >= 2 splits: weights exp2(lse_c - M) for
-// every non-empty split c (one lane each), then o = sum_c w_c o_c / sum_c w_c
-// in ascending c, each lane owning D/32 consecutive dims.
+// One block per split CTA c.  Block c merges the sequence that CTA c's last
+// piece begins, if that piece does not also end it: the sequence's pieces are
+// CTA c's slot (1 if the CTA has several pieces, else 0) and slot 0 of every
+// following CTA up to the first one whose first piece ends the sequence.
+// Warp w handles heads w, w + 4, ...: weights exp2(lse_k - M), then
+// o = sum_k w_k o_k / sum_k w_k in ascending k, each lane owning D/32 dims.
 template <int D>
 __global__ void __launch_bounds__(128) gqa_combine_kernel(const CombineArgs a) {
-  __shared__ float s_w[4][1024 + 1];
-  pdl_wait();  // the split kernel's partials are visible from here on
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int wid = blockIdx.x * 4 + warp;
-  if (wid >= a.batch * a.Hq) return;
-  const RowInfo ri = a.rows[wid / a.Hq];
-  if (ri.nsplit <= 1) return;  // written by the split kernel or the planner
-  const int ne = row_nonempty(ri);
-  const size_t bh = (size_t)wid;
-  const float *pl = a.part_lse + bh * a.max_splits;
-  float *w = s_w[warp];
-  float M = -INFINITY;
-  for (int c = lane; c < ne; c += 32) M = fmaxf(M, pl[c]);
+  pdl_wait();  // the split kernel's partials and descriptors are visible from here on
+  const int c = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (c == 0 && warp == 0) {
+    uint32_t s = 0;
+    for (int i = lane; i < a.nparts; i += 32) s |= a.desc[i].status;
 #pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, o));
-  float Z = 0.f;
-  for (int c = lane; c < ne; c += 32) {
-    const float lc = pl[c];
-    const float wc = (lc == -INFINITY || M == -INFINITY) ? 0.f : fast_exp2(lc - M);
-    w[c] = wc;
-    Z += wc;
+    for (int o = 16; o >= 1; o >>= 1) s |= __shfl_xor_sync(FULL, s, o);
+    if (lane == 0) *a.status = s;
   }
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) Z += __shfl_xor_sync(FULL, Z, o);
-  __syncwarp();
+  const GqaPartDesc d0 = a.desc[c];
+  const uint32_t np = d0.flags & DESC_PIECES;
+  if (np == 0 || !(d0.flags & DESC_LAST_STARTS) || (d0.flags & DESC_LAST_ENDS)) return;
+  int c_last = -1;
+  for (int base = c + 1; base < a.nparts && c_last < 0; base += 32) {
+    const int i = base + lane;
+    bool hit = false;
+    if (i < a.nparts) {
+      const uint32_t f = a.desc[i].flags;
+      hit = (f & DESC_PIECES) != 0 && (f & DESC_FIRST_ENDS) != 0;
+    }
+    const uint32_t m = __ballot_sync(FULL, hit);
+    if (m) c_last = base + __ffs(m) - 1;
+  }
+  if (c_last < 0) return;  // not reachable for a consistent partition
+  const int first_slot = np >= 2 ? 1 : 0;
+  const int g = d0.last_hs / a.nsub, sub = d0.last_hs % a.nsub;
+  const int hq0 = g * a.G + sub * PART_HEADS;
+  const int ghead = min(PART_HEADS, a.G - sub * PART_HEADS);
+  const int k = c_last - c + 1;
   constexpr int PER = D / 32;  // 2, 4 or 8 consecutive dims per lane
-  float acc[PER];
+  for (int h = warp; h < ghead; h += 4) {
+    float M = -INFINITY;
+    for (int i = lane; i < k; i += 32) {
+      const size_t pi = i == 0 ? (size_t)c * 2 + first_slot : (size_t)(c + i) * 2;
+      M = fmaxf(M, a.part_lse[pi * PART_HEADS + h]);
+    }
 #pragma unroll
-  for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-  // every split c < ne was written (finite), so the loads need no guard and stay independent
-  const float *po = a.part_o + bh * a.max_splits * D + lane * PER;
-#pragma unroll 16
-  for (int c = 0; c < ne; ++c) {
-    const float wc = w[c];
-    if constexpr (PER == 2) {
-      const float2 x = *reinterpret_cast<const float2 *>(po + (size_t)c * D);
-      acc[0] += wc * x.x;
-      acc[1] += wc * x.y;
-    } else {
+    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, o));
+    float Z = 0.f;
+    for (int i = lane; i < k; i += 32) {
+      const size_t pi = i == 0 ? (size_t)c * 2 + first_slot : (size_t)(c + i) * 2;
+      const float l = a.part_lse[pi * PART_HEADS + h];
+      Z += (l == -INFINITY || M == -INFINITY) ? 0.f : fast_exp2(l - M);
+    }
 #pragma unroll
-      for (int e = 0; e < PER; e += 4) {
-        const float4 x = *reinterpret_cast<const float4 *>(po + (size_t)c * D + e);
-        acc[e] += wc * x.x;
-        acc[e + 1] += wc * x.y;
-        acc[e + 2] += wc * x.z;
-        acc[e + 3] += wc * x.w;
+    for (int o = 16; o >= 1; o >>= 1) Z += __shfl_xor_sync(FULL, Z, o);
+    float acc[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+#pragma unroll 4
+    for (int i = 0; i < k; ++i) {
+      const size_t pi = i == 0 ? (size_t)c * 2 + first_slot : (size_t)(c + i) * 2;
+      const float l = a.part_lse[pi * PART_HEADS + h];
+      const float wc = (l == -INFINITY || M == -INFINITY) ? 0.f : fast_exp2(l - M);
+      const float *po = a.part_o + (pi * PART_HEADS + h) * D + lane * PER;
+      if constexpr (PER == 2) {
+        const float2 x = *reinterpret_cast<const float2 *>(po);
+        acc[0] += wc * x.x;
+        acc[1] += wc * x.y;
+      } else {
+#pragma unroll
+        for (int e = 0; e < PER; e += 4) {
+          const float4 x = *reinterpret_cast<const float4 *>(po + e);
+          acc[e] += wc * x.x;
+          acc[e + 1] += wc * x.y;
+          acc[e + 2] += wc * x.z;
+          acc[e + 3] += wc * x.w;
+        }
       }
     }
-  }
-  const float inv = Z > 0.f ? 1.f / Z : 0.f;
-  uint32_t *dst = reinterpret_cast<uint32_t *>(a.out + bh * D + lane * PER);
+    const float inv = Z > 0.f ? 1.f / Z : 0.f;
+    const size_t bh = (size_t)d0.last_b * a.Hq + hq0 + h;
+    uint32_t *dst = reinterpret_cast<uint32_t *>(a.out + bh * D + lane * PER);
 #pragma unroll
-  for (int e = 0; e < PER; e += 2) dst[e / 2] = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
-  if (lane == 0 && a.lse) a.lse[bh] = (M == -INFINITY || Z == 0.f) ? -INFINITY : (M + __log2f(Z)) * LN2;
+    for (int e = 0; e < PER; e += 2) dst[e / 2] = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+    if (lane == 0 && a.lse) a.lse[bh] = (M == -INFINITY || Z == 0.f) ? -INFINITY : (M + __log2f(Z)) * LN2;
+  }
 }
 
 }  // namespace pa

@@ -5,8 +5,9 @@
 namespace pa {
 
 namespace {
-// Both kernels are launched as programmatic dependents of the kernel before them: their
-// prologue overlaps its tail and they wait (griddepcontrol.wait) before reading its output.
+// Both kernels are launched as programmatic dependents of the kernel before them: the
+// combine kernel's launch overlaps the split kernel's tail and waits (griddepcontrol.wait)
+// before reading its output; the split kernel reads nothing an earlier kernel of the call wrote.
 cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, int smem, cudaStream_t stream, cudaLaunchAttribute *attr) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
@@ -21,8 +22,8 @@ cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, int smem, cudaStream_t stre
 }
 }  // namespace
 
-cudaError_t launch_gqa_split_d64(int grid, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const GqaArgs &a,
-                                 cudaStream_t stream) {
+cudaError_t launch_gqa_split_d64(int grid, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const CUtensorMap &tm_q,
+                                  const GqaArgs &a, cudaStream_t stream) {
   using C = GqaCfg<64>;
   constexpr int smem = GqaSmem<C>::BYTES;
   static int configured_device = -1;
@@ -35,13 +36,12 @@ cudaError_t launch_gqa_split_d64(int grid, const CUtensorMap &tm_k, const CUtens
   }
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(C::THREADS), smem, stream, attr);
-  return cudaLaunchKernelEx(&cfg, gqa_split_kernel<64>, tm_k, tm_v, a);
+  return cudaLaunchKernelEx(&cfg, gqa_split_kernel<64>, tm_k, tm_v, tm_q, a);
 }
 
 cudaError_t launch_gqa_combine_d64(const CombineArgs &a, cudaStream_t stream) {
-  const int warps = a.batch * a.Hq;
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = pdl_config(dim3((warps + 3) / 4), dim3(128), 0, stream, attr);
+  cudaLaunchConfig_t cfg = pdl_config(dim3(a.nparts), dim3(128), 0, stream, attr);
   return cudaLaunchKernelEx(&cfg, gqa_combine_kernel<64>, a);
 }
 

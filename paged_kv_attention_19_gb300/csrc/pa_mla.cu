@@ -30,7 +30,7 @@
 #include <cmath>
 #include <mutex>
 
-#include "pa_gqa.cuh"
+#include "pa_plan.cuh"
 #include "pa_launch.h"
 #include "pa_mla.h"
 

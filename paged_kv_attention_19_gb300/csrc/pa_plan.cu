@@ -1,4 +1,4 @@
-// pa_plan.cu -- the work-list planner shared by the GQA and MLA split-KV kernels.
+// pa_plan.cu -- the work-list planner of the MLA split-KV kernel.
 //
 // Turns the device-resident context lengths into page-aligned work items
 // without a host round trip.  Automatic mode picks one chunk length so the
@@ -9,7 +9,7 @@
 // the shorter tail chunks, so the dynamic queue of the split kernel ends with
 // short work.  The planner also resets the queue cursor and writes the output
 // of rows that have no key to attend (out = 0, lse = -inf).
-#include "pa_gqa.cuh"
+#include "pa_plan.cuh"
 #include "pa_launch.h"
 
 namespace pa {

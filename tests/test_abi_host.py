@@ -54,17 +54,23 @@ def test_status_strings(pa):
 
 
 def test_workspace_size(pa):
-    g = pa.pa_workspace_size(pa.PA_KIND_GQA, 32, 64, 8, 128, 16384, 32, 0)
+    ws = lambda *a: pa.pa_workspace_size(pa.PA_KIND_GQA, *a)
+    g = ws(32, 64, 8, 128, 16384, 32, 0)
     assert g > 0
-    assert pa.pa_workspace_size(pa.PA_KIND_GQA, 32, 64, 8, 128, 16384, 32, 4) > 0
-    # grows with the batch and with an explicit split count
-    assert pa.pa_workspace_size(pa.PA_KIND_GQA, 64, 64, 8, 128, 16384, 32, 0) > g
-    assert pa.pa_workspace_size(pa.PA_KIND_GQA, 32, 64, 8, 128, 16384, 32, 512) > g
+    # two partial slots of 16 heads per share: independent of batch, heads and context,
+    # growing with head_dim and with an explicit share count (automatic mode: 256 shares)
+    assert ws(64, 64, 8, 128, 16384, 32, 0) == g
+    assert ws(32, 64, 8, 128, 131072, 32, 0) == g
+    assert ws(32, 64, 8, 128, 16384, 32, 256) == g
+    assert 256 * 2 * 16 * 128 * 4 <= g < 256 * 2 * 16 * 128 * 4 + (1 << 16)
+    assert ws(32, 64, 8, 128, 16384, 32, 4) < g
+    assert ws(32, 64, 8, 128, 16384, 32, 512) > g
+    assert ws(32, 64, 8, 256, 16384, 32, 0) > g
     # rejected shapes report 0
-    assert pa.pa_workspace_size(pa.PA_KIND_GQA, 32, 64, 7, 128, 16384, 32, 0) == 0     # Hq % Hkv
-    assert pa.pa_workspace_size(pa.PA_KIND_GQA, 32, 64, 8, 96, 16384, 32, 0) == 0      # head_dim
-    assert pa.pa_workspace_size(pa.PA_KIND_GQA, 32, 64, 8, 128, 16384, 48, 0) == 0     # page size
-    assert pa.pa_workspace_size(pa.PA_KIND_GQA, 32, 64, 8, 128, 16384, 32, 2000) == 0  # num_splits
+    assert ws(32, 64, 7, 128, 16384, 32, 0) == 0     # Hq % Hkv
+    assert ws(32, 64, 8, 96, 16384, 32, 0) == 0      # head_dim
+    assert ws(32, 64, 8, 128, 16384, 48, 0) == 0     # page size
+    assert ws(32, 64, 8, 128, 16384, 32, 4097) == 0  # num_splits
     assert pa.pa_workspace_size(pa.PA_KIND_MLA_ABSORBED, 16, 128, 0, 0, 8192, 64, 0) > 0
     assert pa.pa_workspace_size(pa.PA_KIND_MLA_ABSORBED, 16, 0, 0, 0, 8192, 64, 0) == 0
     assert pa.pa_workspace_size(7, 16, 128, 1, 128, 8192, 64, 0) == 0
@@ -88,7 +94,7 @@ def test_gqa_host_validation(pa):
     assert _gqa(pa, d=96) == pa.PA_ERR_UNSUPPORTED
     assert _gqa(pa, p=4) == pa.PA_ERR_UNSUPPORTED
     assert _gqa(pa, p=24) == pa.PA_ERR_UNSUPPORTED
-    assert _gqa(pa, splits=1025) == pa.PA_ERR_UNSUPPORTED
+    assert _gqa(pa, splits=4097) == pa.PA_ERR_UNSUPPORTED
     assert _gqa(pa, splits=-1) == pa.PA_ERR_INVALID_ARGUMENT
     assert _gqa(pa, q=None) == pa.PA_ERR_INVALID_ARGUMENT
     assert _gqa(pa, ws=None) == pa.PA_ERR_INVALID_ARGUMENT

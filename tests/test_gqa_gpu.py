@@ -10,7 +10,7 @@ import synth
 pytestmark = pytest.mark.gpu
 
 LADDER = [1, 31, 32, 33, 64, 100, 685, 1000]
-SPLITS = [1, 2, 3, 4, 5, 8, 16, 17, 64, 300, 512]
+SPLITS = [1, 2, 3, 4, 5, 8, 16, 17, 64, 152, 300, 512, 4096]
 
 
 def test_tiny_workload_all_rows():
@@ -85,6 +85,25 @@ def test_num_splits_sweep():
         # different split counts agree within rounding
         st = compare.compare(o, ref_o)
         assert st.max_abs <= compare.MAX_ABS
+
+
+@pytest.mark.parametrize("splits", [0, 2, 7, 64, 152, 1000])
+def test_shares_spanning_rows_and_heads(splits):
+    """Shares whose ranges start and end inside sequences, cover several whole sequences, or hold
+    nothing; one long sequence spread over many shares; empty rows between; two 16-head subgroups."""
+    w = synth.make_gqa(510 + splits, [20000, 1, 0, 3, 7000, 64, 0, 129], 40, 2, 128, 16)
+    o, l = gu.GqaDev(w).run(num_splits=splits)
+    gu.check_gqa(w, o, l)
+
+
+def test_fewer_query_rows_than_one_tile():
+    """batch * Hq below the 16 query rows one tensor-core tile holds."""
+    w = synth.make_gqa(520, [77], 8, 2, 128, 16)
+    o, l = gu.GqaDev(w).run()
+    gu.check_gqa(w, o, l)
+    w = synth.make_gqa(521, [300], 4, 1, 64, 32)
+    o, l = gu.GqaDev(w).run(num_splits=3)
+    gu.check_gqa(w, o, l)
 
 
 def test_run_to_run_bitwise():

@@ -47,10 +47,10 @@ def test_noalloc_matches_workspace_entry_point_twice(window):
 
 def test_noalloc_refuses_a_workspace_larger_than_its_scratch():
     import paged_kv_attention_19_gb300 as pa
-    B, Hq, Hkv, D, P, max_ctx = 64, 64, 8, 128, 16, 131072
-    assert pa.pa_workspace_size(pa.PA_KIND_GQA, B, Hq, Hkv, D, max_ctx, P, 0) > (32 << 20)
+    B, Hq, Hkv, D, P, max_ctx, splits = 4, 16, 4, 256, 16, 4096, 4096
+    assert pa.pa_workspace_size(pa.PA_KIND_GQA, B, Hq, Hkv, D, max_ctx, P, splits) > (32 << 20)
     x = torch.empty(16, dtype=torch.uint8, device="cuda")  # never read: the call stops on the host
     rc = pa.lib.pa_decode_gqa_noalloc(x.data_ptr(), x.data_ptr(), x.data_ptr(), x.data_ptr(), x.data_ptr(),
                                       x.data_ptr(), None, B, Hq, Hkv, D, P, 1 << 20, max_ctx // P, max_ctx,
-                                      0.1, 0, 0, torch.cuda.current_stream().cuda_stream)
+                                      0.1, 0, splits, torch.cuda.current_stream().cuda_stream)
     assert rc == pa.PA_ERR_WORKSPACE_TOO_SMALL
