@@ -24,8 +24,8 @@ using namespace pa;
 constexpr int kMaxSplits = 4096;     // largest accepted explicit num_splits (partitions)
 constexpr int kAutoPartsMax = 256;   // automatic mode: one partition per SM, at most this many
 // Fixed cost of one piece of work in the GQA partition (the Q load and the end-of-piece
-// merge, about 1.5 us of one SM), expressed as the KV bytes the SM streams meanwhile.
-constexpr long long kPieceCostBytes = 64 << 10;
+// merge, about 0.8 us of one SM), expressed as the KV bytes the SM streams meanwhile.
+constexpr long long kPieceCostBytes = 32 << 10;
 
 thread_local cudaEvent_t t_ev_before = nullptr;
 thread_local cudaEvent_t t_ev_after = nullptr;
@@ -209,6 +209,10 @@ int pa_decode_gqa(const void *q, const void *k_pool, const void *v_pool, const i
   ga.log2_bh = ilog2(BH);
   ga.nparts = nparts;
   {
+    const int hs = num_kv_heads * pl.nsub;
+    ga.hg = hs < nparts ? hs : nparts;
+  }
+  {
     const long long unit_bytes = (long long)BH * D * 4;  // K and V of one unit of one KV head
     ga.piece_cost = (int)((kPieceCostBytes + unit_bytes - 1) / unit_bytes);
   }
@@ -225,6 +229,7 @@ int pa_decode_gqa(const void *q, const void *k_pool, const void *v_pool, const i
   ca.G = ga.G;
   ca.nsub = pl.nsub;
   ca.nparts = nparts;
+  ca.hg = ga.hg;
 
   cudaError_t e;
   if (t_ev_before && cudaEventRecord(t_ev_before, stream) != cudaSuccess) return PA_ERR_CUDA;

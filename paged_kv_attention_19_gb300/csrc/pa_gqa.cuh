@@ -78,7 +78,8 @@ struct GqaArgs {
   int Hq, Hkv, G, nsub;
   int log2_page, log2_bh;       // page size and tokens per unit (TMA box), as powers of two
   int piece_cost;               // partition cost of starting a piece, in units
-  int nparts;
+  int nparts;                   // CTAs (shares); groups of hg consecutive CTAs
+  int hg;                       // CTAs per group: min(Hkv * nsub, nparts)
   float qscale;                 // scale * log2(e)
 };
 
@@ -226,17 +227,24 @@ __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
   uint32_t *status = &misc->status;
 
   // ---------------------------------------------- prologue: this CTA's range
-  // Sequence (b, hs) costs w_b = n_b + piece_cost units (0 when n_b == 0); the cost axis,
-  // flattened row by row, is cut into nparts equal ranges.  A range position inside the
-  // first piece_cost units of a sequence maps to no key: those units stand for the fixed
-  // cost of starting a piece (loading Q, merging the token groups at its end).
+  // The CTAs form NG groups of HG = min(HS, nparts) consecutive CTAs; CTA r of a group
+  // serves KV-head subgroups r, r + HG, ... .  A row's column cost is w_b = n_b +
+  // piece_cost units (0 when n_b == 0); the column axis (rows in order) is cut into NG
+  // equal ranges, one per group, so the HG CTAs of a group stream the same pages (each
+  // its own head) at about the same time and every CTA streams the same cost.  A position
+  // inside the first piece_cost units of a row maps to no key: those units stand for the
+  // fixed cost of a piece (its query stage, the merge at its end).  With NG >= 2 each CTA
+  // serves exactly one subgroup (HG == HS); with NG == 1 every piece is a whole sequence.
   auto seq_cost = [&](int L, int *n_out) {
     int ul;
     const int n = row_units(L, a.window, a.log2_bh, &ul);
     *n_out = n;
     return n > 0 ? n + a.piece_cost : 0;
   };
-  long long W = 0;  // total cost
+  const int HG = a.hg, NG = a.nparts / a.hg;
+  const int grp = (int)blockIdx.x / HG, hr = (int)blockIdx.x % HG;
+  const bool member = grp < NG;  // CTAs past the last full group get no work
+  long long W = 0;  // total column cost
   if (a.batch <= C::THREADS) {
     // one pass: every row in one thread
     long long v = 0;
@@ -244,14 +252,14 @@ __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
       const int L0 = a.context_lens[tid];
       if (L0 < 0 || L0 > a.max_context_len) atomicOr(status, PA_DEV_BAD_LEN);
       int n;
-      v = (long long)seq_cost(clamp_len(L0, a.max_context_len), &n) * HS;
+      v = seq_cost(clamp_len(L0, a.max_context_len), &n);
     }
     long long ex;
     W = block_scan64(v, &ex, misc->warp_part);
-    const long long x0 = (long long)blockIdx.x * W / a.nparts;
-    if (v > 0 && x0 >= ex && x0 < ex + v && x0 < ((long long)blockIdx.x + 1) * W / a.nparts) {
+    const long long xb = (long long)grp * W / NG, xe = ((long long)grp + 1) * W / NG;
+    if (member && v > 0 && xb >= ex && xb < ex + v && xb < xe) {
       misc->found_b = tid;
-      misc->found_off = x0 - ex;
+      misc->found_off = xb - ex;
     }
   } else {
     long long local = 0;
@@ -261,22 +269,22 @@ __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
       int n;
       local += seq_cost(clamp_len(L0, a.max_context_len), &n);
     }
-    W = block_sum64(local, misc->warp_part) * HS;
-    const long long x0 = (long long)blockIdx.x * W / a.nparts;
-    if (x0 < ((long long)blockIdx.x + 1) * W / a.nparts) {
+    W = block_sum64(local, misc->warp_part);
+    const long long xb = (long long)grp * W / NG, xe = ((long long)grp + 1) * W / NG;
+    if (member && xb < xe) {
       long long base = 0;
       for (int b0 = 0; b0 < a.batch; b0 += C::THREADS) {
         const int b = b0 + tid;
         long long v = 0;
         if (b < a.batch) {
           int n;
-          v = (long long)seq_cost(clamp_len(a.context_lens[b], a.max_context_len), &n) * HS;
+          v = seq_cost(clamp_len(a.context_lens[b], a.max_context_len), &n);
         }
         long long ex;
         const long long tot = block_scan64(v, &ex, misc->warp_part);
-        if (v > 0 && x0 >= base + ex && x0 < base + ex + v) {
+        if (v > 0 && xb >= base + ex && xb < base + ex + v) {
           misc->found_b = b;
-          misc->found_off = x0 - base - ex;
+          misc->found_off = xb - base - ex;
         }
         base += tot;
         __syncthreads();
@@ -284,8 +292,8 @@ __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
       }
     }
   }
-  const long long x_begin = (long long)blockIdx.x * W / a.nparts;
-  const long long x_end = ((long long)blockIdx.x + 1) * W / a.nparts;
+  const long long x_begin = member ? (long long)grp * W / NG : 0;
+  const long long x_end = member ? ((long long)grp + 1) * W / NG : 0;
   // rows without a visible key: out = 0, lse = -inf (rows b = blockIdx.x mod nparts)
   for (int b = blockIdx.x; b < a.batch; b += a.nparts) {
     int ul;
@@ -303,54 +311,55 @@ __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
     const int nbox = C::ST >> a.log2_bh;  // boxes (units) per stage
     uint32_t j = 0;
     bool ok = true;
-    long long R = misc->found_b >= 0 ? x_end - x_begin : 0;  // cost still to walk
+    const int b_first = max(misc->found_b, 0);
+    const int in_first = misc->found_b >= 0 ? (int)misc->found_off : 0;
+    long long R = misc->found_b >= 0 ? x_end - x_begin : 0;  // column cost still to walk for it_hs
     int npieces = 0;
     Piece last_piece = {};
     bool first_ends = false;
     // lens window: lane l holds the clamped length of row rb + l
-    int rb = max(misc->found_b, 0);
+    int rb = b_first;
     int lwin = rb + lane < a.batch ? clamp_len(a.context_lens[rb + lane], a.max_context_len) : 0;
-    auto len_of = [&](int row) {  // rows only move forward
-      while (row >= rb + 32) {
-        rb += 32;
+    auto len_of = [&](int row) {
+      if (row < rb || row >= rb + 32) {
+        rb = row;
         lwin = rb + lane < a.batch ? clamp_len(a.context_lens[rb + lane], a.max_context_len) : 0;
       }
       return __shfl_sync(FULL, lwin, row - rb);
     };
-    // walk position: sequence (it_b, it_hs), `it_in` cost units into it
-    int it_b = rb, it_hs = 0, it_in = 0;
-    if (R > 0) {
-      int n;
-      const int w = seq_cost(len_of(it_b), &n);
-      it_hs = (int)(misc->found_off / w);
-      it_in = (int)(misc->found_off % w);
-    }
-    // the next piece that holds at least one key; false once the range is walked
+    // walk position: subgroup it_hs, row it_b, `it_in` cost units into the row
+    int it_hs = hr, it_b = b_first, it_in = in_first;
+    // the next piece that holds at least one key; false once the range is walked for every
+    // subgroup of this CTA
     auto take_piece = [&](Piece &p) {
-      while (R > 0) {
+      while (true) {
+        if (R == 0) {
+          it_hs += HG;
+          if (misc->found_b < 0 || it_hs >= HS) return false;
+          R = x_end - x_begin;
+          it_b = b_first;
+          it_in = in_first;
+        }
         const int L = len_of(it_b);
         int n;
         const int w = seq_cost(L, &n);
         const int take = (int)min((long long)(w - it_in), R);
         const int u0 = max(0, it_in - a.piece_cost), u1 = max(0, it_in + take - a.piece_cost);
-        const int b = it_b, hs = it_hs;
+        const int b = it_b;
         R -= take;
         it_in += take;
         if (it_in == w && R > 0) {
           it_in = 0;
-          if (++it_hs == HS) {
-            it_hs = 0;
-            int nn;
-            do {
-              ++it_b;
-            } while (it_b < a.batch - 1 && seq_cost(len_of(it_b), &nn) == 0);
-          }
+          int nn;
+          do {
+            ++it_b;
+          } while (it_b < a.batch - 1 && seq_cost(len_of(it_b), &nn) == 0);
         }
         if (u1 > u0) {
           int ul;
           row_units(L, a.window, a.log2_bh, &ul);
           p.b = b;
-          p.hs = hs;
+          p.hs = it_hs;
           p.L = L;
           p.lo = (a.window > 0 && L > a.window) ? L - a.window : 0;
           p.ub = ul + u0;
@@ -360,7 +369,6 @@ __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
           return true;
         }
       }
-      return false;
     };
     auto q_head0 = [&](const Piece &p) { return (p.hs / a.nsub) * a.G + (p.hs % a.nsub) * C::M; };
     auto q_heads = [&](const Piece &p) { return min(C::M, a.G - (p.hs % a.nsub) * C::M); };
@@ -760,13 +768,14 @@ struct CombineArgs {
   const float *part_lse;
   const GqaPartDesc *desc;
   uint32_t *status;  // the workspace status word: OR of every CTA's bits
-  int Hq, G, nsub, nparts;
+  int Hq, G, nsub, nparts, hg;
 };
 
 // One block per split CTA c.  Block c merges the sequence that CTA c's last
 // piece begins, if that piece does not also end it: the sequence's pieces are
-// CTA c's slot (1 if the CTA has several pieces, else 0) and slot 0 of every
-// following CTA up to the first one whose first piece ends the sequence.
+// CTA c's slot (1 if the CTA has several pieces, else 0) and slot 0 of CTAs
+// c + hg, c + 2 hg, ... (the same head in the following groups) up to the
+// first one whose first piece ends the sequence.
 // Warp w handles heads w, w + 4, ...: weights exp2(lse_k - M), then
 // o = sum_k w_k o_k / sum_k w_k in ascending k, each lane owning D/32 dims.
 template <int D>
@@ -783,35 +792,35 @@ __global__ void __launch_bounds__(128) gqa_combine_kernel(const CombineArgs a) {
   const GqaPartDesc d0 = a.desc[c];
   const uint32_t np = d0.flags & DESC_PIECES;
   if (np == 0 || !(d0.flags & DESC_LAST_STARTS) || (d0.flags & DESC_LAST_ENDS)) return;
-  int c_last = -1;
-  for (int base = c + 1; base < a.nparts && c_last < 0; base += 32) {
-    const int i = base + lane;
+  // the later pieces of the sequence are in CTAs c + hg, c + 2 hg, ... (same head, next groups)
+  int k = -1;  // pieces: CTA c + i hg holds piece i, i < k
+  for (int base = 1; c + base * a.hg < a.nparts && k < 0; base += 32) {
+    const int i = c + (base + lane) * a.hg;
     bool hit = false;
     if (i < a.nparts) {
       const uint32_t f = a.desc[i].flags;
       hit = (f & DESC_PIECES) != 0 && (f & DESC_FIRST_ENDS) != 0;
     }
     const uint32_t m = __ballot_sync(FULL, hit);
-    if (m) c_last = base + __ffs(m) - 1;
+    if (m) k = base + __ffs(m);
   }
-  if (c_last < 0) return;  // not reachable for a consistent partition
+  if (k < 0) return;  // not reachable for a consistent partition
   const int first_slot = np >= 2 ? 1 : 0;
   const int g = d0.last_hs / a.nsub, sub = d0.last_hs % a.nsub;
   const int hq0 = g * a.G + sub * PART_HEADS;
   const int ghead = min(PART_HEADS, a.G - sub * PART_HEADS);
-  const int k = c_last - c + 1;
   constexpr int PER = D / 32;  // 2, 4 or 8 consecutive dims per lane
   for (int h = warp; h < ghead; h += 4) {
     float M = -INFINITY;
     for (int i = lane; i < k; i += 32) {
-      const size_t pi = i == 0 ? (size_t)c * 2 + first_slot : (size_t)(c + i) * 2;
+      const size_t pi = i == 0 ? (size_t)c * 2 + first_slot : (size_t)(c + i * a.hg) * 2;
       M = fmaxf(M, a.part_lse[pi * PART_HEADS + h]);
     }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, o));
     float Z = 0.f;
     for (int i = lane; i < k; i += 32) {
-      const size_t pi = i == 0 ? (size_t)c * 2 + first_slot : (size_t)(c + i) * 2;
+      const size_t pi = i == 0 ? (size_t)c * 2 + first_slot : (size_t)(c + i * a.hg) * 2;
       const float l = a.part_lse[pi * PART_HEADS + h];
       Z += (l == -INFINITY || M == -INFINITY) ? 0.f : fast_exp2(l - M);
     }
@@ -822,7 +831,7 @@ __global__ void __launch_bounds__(128) gqa_combine_kernel(const CombineArgs a) {
     for (int e = 0; e < PER; ++e) acc[e] = 0.f;
 #pragma unroll 4
     for (int i = 0; i < k; ++i) {
-      const size_t pi = i == 0 ? (size_t)c * 2 + first_slot : (size_t)(c + i) * 2;
+      const size_t pi = i == 0 ? (size_t)c * 2 + first_slot : (size_t)(c + i * a.hg) * 2;
       const float l = a.part_lse[pi * PART_HEADS + h];
       const float wc = (l == -INFINITY || M == -INFINITY) ? 0.f : fast_exp2(l - M);
       const float *po = a.part_o + (pi * PART_HEADS + h) * D + lane * PER;
