@@ -45,7 +45,7 @@ METRIC = "µs/call and achieved HBM GB/s (frac of ~8 TB/s) for paged decode atte
 FLUSH_BYTES = 512 << 20
 CLEAN_BYTES = 512 << 20
 DEFAULT_WORKLOAD = "qwen3-32b"
-WORKLOADS = ["tiny", "llama3-8b", "qwen3-32b", "hd256-window", "mla"]
+WORKLOADS = ["tiny", "llama3-8b", "qwen3-32b", "hd256-window", "mla", "kv-write"]
 # sources of the kernel each roofline line profiles (a change voids its committed ncu traffic)
 KERNEL_SOURCES = {"gqa": ("pa_gqa.cuh", "pa_common.cuh"),
                   "mla": ("pa_mla.cu", "pa_plan.cu", "pa_plan.cuh", "pa_common.cuh")}
@@ -111,6 +111,11 @@ def ncu_traffic(workload: str):
 
 def describe(w, name):
     import synth
+    if isinstance(w, synth.KVWriteWorkload):
+        return {"workload": name, "tokens": w.num_tokens, "kv_heads": int(w.k.shape[1]),
+                "head_dim": int(w.k.shape[2]), "page_size": w.page_size, "pool_pages": w.num_pages,
+                "slots": "prefill order: token t at position t % P of page perm[t // P]",
+                "algorithmic_bytes": w.algorithmic_bytes(), "seed": w.seed}
     if isinstance(w, synth.MLAWorkload):
         return {"workload": name, "batch": w.batch, "heads": w.num_heads, "q_dim": 192, "cache_dim": 576,
                 "v_dim": 128, "page_size": w.layout.page_size, "context": "uniform[1024,8192]",
@@ -188,6 +193,14 @@ class OracleSample:
         import oracle
         import synth
         self.cores = oracle.num_threads()
+        if isinstance(w, synth.KVWriteWorkload):
+            # the oracle writes token by token into copies of the pools: time it on all tokens
+            kp, vp = w.empty_pool(), w.empty_pool()
+            self.fn = lambda rows: oracle.kv_write(w.k, w.v, w.slots, kp, vp)
+            self.rows, self.bytes = None, w.algorithmic_bytes()
+            self.desc = f"all {w.num_tokens} tokens of the {name} workload"
+            self.cores = 1
+            return
         is_mla = isinstance(w, synth.MLAWorkload)
         H = w.num_heads if is_mla else w.num_q_heads
         rows_all = [(b, h) for b in range(w.batch) for h in range(H)]
@@ -267,23 +280,42 @@ def run_ours(args, rank, local_rank, world):
     w = synth.workload(args.workload)
     cfg = describe(w, args.workload)
     is_mla = isinstance(w, synth.MLAWorkload)
-    d = gu.MlaDev(w) if is_mla else gu.GqaDev(w)
-    B = w.batch
-    if is_mla:
+    is_write = isinstance(w, synth.KVWriteWorkload)
+    # per workload: the device inputs a step copies in end to end, the outputs it reads back,
+    # and call(*inputs) running the step on device tensors
+    if is_write:
+        ins = [gu.dev(w.k), gu.dev(w.v), torch.from_numpy(w.slots).cuda()]
+        kp = gu.dev(w.empty_pool())
+        vp = None if w.mla else gu.dev(w.empty_pool())
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        outs = [status]
+        if w.mla:
+            def call(c, r, s):
+                pa.pa_mla_cache_write(c, r, s, kp, status=status)
+        else:
+            def call(k, v, s):
+                pa.pa_kv_write(k, v, s, kp, vp, status=status)
+    elif is_mla:
+        d = gu.MlaDev(w)
+        B = w.batch
         out = torch.empty(B, w.num_heads, 128, dtype=torch.bfloat16, device="cuda")
         lse = torch.empty(B, w.num_heads, dtype=torch.float32, device="cuda")
         ws = pa.workspace_for_mla(d.q, d.cache, d.bt, args.num_splits)
+        ins, outs = [d.q, d.bt, d.lens], [out, lse]
 
-        def call(q, bt, lens, o, l):
-            pa.pa_decode_mla_absorbed(q, d.cache, d.wuk, d.wuv, bt, lens, o, l, scale=w.scale, workspace=ws,
+        def call(q, bt, lens):
+            pa.pa_decode_mla_absorbed(q, d.cache, d.wuk, d.wuv, bt, lens, out, lse, scale=w.scale, workspace=ws,
                                       num_splits=args.num_splits)
     else:
+        d = gu.GqaDev(w)
+        B = w.batch
         out = torch.empty(w.q.shape, dtype=torch.bfloat16, device="cuda")
         lse = torch.empty(B, w.num_q_heads, dtype=torch.float32, device="cuda")
         ws = pa.workspace_for_gqa(d.q, d.k, d.bt, args.num_splits)
+        ins, outs = [d.q, d.bt, d.lens], [out, lse]
 
-        def call(q, bt, lens, o, l):
-            pa.pa_decode_gqa(q, d.k, d.v, bt, lens, o, l, scale=w.scale, window=w.window, workspace=ws,
+        def call(q, bt, lens):
+            pa.pa_decode_gqa(q, d.k, d.v, bt, lens, out, lse, scale=w.scale, window=w.window, workspace=ws,
                              num_splits=args.num_splits)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     clean = torch.zeros(CLEAN_BYTES // 4, dtype=torch.float32, device="cuda")
@@ -306,7 +338,7 @@ def run_ours(args, rank, local_rank, world):
     clocks.start()
     for _ in range(args.warmup):
         flush_l2()
-        call(d.q, d.bt, d.lens, out, lse)
+        call(*ins)
     launches_per_call = pa.pa_last_launch_count()
     torch.cuda.synchronize()
 
@@ -320,12 +352,12 @@ def run_ours(args, rank, local_rank, world):
     for i in range(args.steps):
         flush_l2()
         evs[i][0].record(stream)
-        call(d.q, d.bt, d.lens, out, lse)
+        call(*ins)
         evs[i][1].record(stream)
     for i in range(args.steps):
         flush_l2()
         pa.pa_set_profile_events(*kev[i])
-        call(d.q, d.bt, d.lens, out, lse)
+        call(*ins)
     torch.cuda.synchronize()
     clocks.t1 = time.time()
     barrier()
@@ -339,14 +371,13 @@ def run_ours(args, rank, local_rank, world):
 
     # ---- end to end through the C ABI with host buffers
     pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-    q_h, bt_h, lens_h = pin(d.q), pin(d.bt), pin(d.lens)
-    q_h.copy_(d.q)
-    bt_h.copy_(d.bt)
-    lens_h.copy_(d.lens)
-    out_h, lse_h = pin(out), pin(lse)
-    q_d, bt_d, lens_d = torch.empty_like(d.q), torch.empty_like(d.bt), torch.empty_like(d.lens)
-    h2d = q_h.numel() * q_h.element_size() + bt_h.numel() * 4 + lens_h.numel() * 4
-    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
+    ins_h = [pin(t) for t in ins]
+    for h, t in zip(ins_h, ins):
+        h.copy_(t)
+    outs_h = [pin(t) for t in outs]
+    ins_d = [torch.empty_like(t) for t in ins]
+    h2d = sum(t.numel() * t.element_size() for t in ins_h)
+    d2h = sum(t.numel() * t.element_size() for t in outs_h)
     e2e_steps = max(1, min(args.steps, 200))
     eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(e2e_steps)]
     barrier()
@@ -354,12 +385,11 @@ def run_ours(args, rank, local_rank, world):
     for i in range(e2e_steps):
         flush_l2()
         eev[i][0].record(stream)
-        q_d.copy_(q_h, non_blocking=True)
-        bt_d.copy_(bt_h, non_blocking=True)
-        lens_d.copy_(lens_h, non_blocking=True)
-        call(q_d, bt_d, lens_d, out, lse)
-        out_h.copy_(out, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
+        for dd, h in zip(ins_d, ins_h):
+            dd.copy_(h, non_blocking=True)
+        call(*ins_d)
+        for h, dd in zip(outs_h, outs):
+            h.copy_(dd, non_blocking=True)
         eev[i][1].record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -378,7 +408,7 @@ def run_ours(args, rank, local_rank, world):
         "config": dict(cfg, num_splits=args.num_splits or "auto", parallelism=f"replicas x{world}",
                        l2="between timed calls, outside the timed events: a 512 MB buffer written, then another 512 MB read"),
         "roofline": {"bound": "alu" if is_mla else "hbm",
-                     "kernel": "mla_split_kernel" if is_mla else "gqa_split_kernel",
+                     "kernel": "kv_write_kernel" if is_write else "mla_split_kernel" if is_mla else "gqa_split_kernel",
                      "achieved": round(kernel_gbs, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(kernel_gbs / peak, 4), "peak_source": f"hbm_gbs of {peak_kind}",
                      "kernel_us": round(kms * 1000, 2), "traffic": ncu_traffic(args.workload)},

@@ -99,6 +99,7 @@ typedef enum { PA_KIND_GQA = 0, PA_KIND_MLA_ABSORBED = 1 } pa_kind;
 #define PA_DEV_BAD_PAGE 0x1u /* a visited block-table entry was outside [0, num_pages) */
 #define PA_DEV_BAD_LEN 0x2u  /* a context length was < 0 or > max_context_len */
 #define PA_DEV_TIMEOUT 0x4u  /* a bounded wait inside a kernel gave up (never expected) */
+#define PA_DEV_BAD_SLOT 0x8u /* a cache write named a slot at or past num_pages * page_size */
 
 /*
  * Bytes of device workspace a call with these arguments needs.  For
@@ -181,6 +182,38 @@ int pa_decode_gqa_noalloc(const void *q, const void *k_pool, const void *v_pool,
                           float *lse, int batch, int num_q_heads, int num_kv_heads, int head_dim,
                           int page_size, int num_pages, int max_pages_per_seq, int max_context_len,
                           float scale, int window, int num_splits, cudaStream_t stream);
+
+/*
+ * Paged KV write: puts the keys and values of new tokens into their slots of
+ * the paged pools, the step that precedes the decode (vllm.cpp kernel-matrix,
+ * row KERNEL-KV-CACHE, ReshapeAndCache).
+ *   k, v          [num_tokens, num_kv_heads, head_dim] bf16 (read)
+ *   slot_mapping  [num_tokens] int64: token t goes to physical page
+ *                 slot / page_size, slot slot % page_size; a negative slot is a
+ *                 padding token and is skipped
+ *   k_pool, v_pool [num_pages, page_size, num_kv_heads, head_dim] bf16 (written
+ *                 at the named slots only; everything else is left untouched)
+ *   status        optional device word (NULL: none); a slot at or past
+ *                 num_pages * page_size is skipped and sets PA_DEV_BAD_SLOT
+ * head_dim a multiple of 8 up to 1024.  The slots of one call must be distinct
+ * (two tokens naming one slot leave either token's row there).  A pure copy:
+ * the written bits equal the input bits.  num_tokens == 0 is a no-op.
+ */
+int pa_kv_write(const void *k, const void *v, const int64_t *slot_mapping, void *k_pool, void *v_pool,
+                int num_tokens, int num_kv_heads, int head_dim, int page_size, int num_pages,
+                uint32_t *status, cudaStream_t stream);
+
+/*
+ * MLA cache write: the 576-wide cache row of each new token is its latent
+ * (512) followed by its rope key (64) (vllm.cpp kernel-matrix, row
+ * KERNEL-KV-CACHE, ConcatAndCacheMla).
+ *   c_lat   [num_tokens, 512] bf16, k_rope [num_tokens, 64] bf16 (read)
+ *   cache   [num_pages, page_size, 576] bf16 (written at the named slots only)
+ * slot_mapping and status as for pa_kv_write.
+ */
+int pa_mla_cache_write(const void *c_lat, const void *k_rope, const int64_t *slot_mapping, void *cache,
+                       int num_tokens, int page_size, int num_pages, uint32_t *status,
+                       cudaStream_t stream);
 
 /* Static text for a pa_status value (never NULL). */
 const char *pa_status_string(int status);

@@ -170,3 +170,33 @@ def mla(q, cache, w_uk, w_uv, block_table, context_lens, scale: float, rows=None
     if intermediates:
         return o, lse, ql, ol
     return o, lse
+
+
+def kv_write(k, v, slots, k_pool, v_pool):
+    """Paged KV write (vllm.cpp kernel-matrix, row KERNEL-KV-CACHE, ReshapeAndCache): for every
+    token t with slot s = slots[t] >= 0, the row of physical page s // P, position s % P of each
+    pool becomes token t's row.  Negative slots are padding.  Returns new pools (inputs untouched);
+    bit patterns are copied, so the result is exact."""
+    kp, vp = k_pool.copy(), v_pool.copy()
+    P = kp.shape[1]
+    for t in range(len(slots)):
+        s = int(slots[t])
+        if s < 0:
+            continue
+        kp[s // P, s % P] = k[t]
+        vp[s // P, s % P] = v[t]
+    return kp, vp
+
+
+def mla_cache_write(c_lat, k_rope, slots, cache):
+    """MLA cache write (same row, ConcatAndCacheMla): the 576-wide row of token t is its 512
+    latent values followed by its 64 rope-key values."""
+    out = cache.copy()
+    P = out.shape[1]
+    for t in range(len(slots)):
+        s = int(slots[t])
+        if s < 0:
+            continue
+        out[s // P, s % P, :512] = c_lat[t]
+        out[s // P, s % P, 512:] = k_rope[t]
+    return out

@@ -6,7 +6,8 @@ There is no CPU fallback: importing this package fails with ImportError if the
 library has not been built (``python paged_kv_attention_19_gb300/build.py``).
 
 Names follow the C ABI: ``pa_workspace_size``, ``pa_decode_gqa``,
-``pa_decode_mla_absorbed``, ``pa_status_string``, ``pa_read_device_status``,
+``pa_decode_mla_absorbed``, ``pa_decode_gqa_noalloc``, ``pa_kv_write``,
+``pa_mla_cache_write``, ``pa_status_string``, ``pa_read_device_status``,
 ``pa_set_profile_events``, ``pa_last_launch_count``.  The tensor-taking
 functions accept torch tensors (device memory, the layouts of the header) and
 infer every size from their shapes.
@@ -30,6 +31,7 @@ PA_KIND_MLA_ABSORBED = 1
 PA_DEV_BAD_PAGE = 0x1
 PA_DEV_BAD_LEN = 0x2
 PA_DEV_TIMEOUT = 0x4
+PA_DEV_BAD_SLOT = 0x8
 
 # Every symbol include/pa_decode.h declares, with its ctypes signature.
 _P, _I, _F, _Z, _U32P = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.POINTER(ctypes.c_uint32)
@@ -38,6 +40,8 @@ SIGNATURES = {
     "pa_decode_gqa": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _Z, _P]),
     "pa_decode_mla_absorbed": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P]),
     "pa_decode_gqa_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
+    "pa_kv_write": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
+    "pa_mla_cache_write": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "pa_status_string": (ctypes.c_char_p, [_I]),
     "pa_read_device_status": (_I, [_P, _P, _U32P]),
     "pa_set_profile_events": (_I, [_P, _P]),
@@ -130,6 +134,24 @@ def pa_decode_mla_absorbed(q, cache, w_uk, w_uv, block_table, context_lens, out,
                                     int(max_context_len), float(scale), int(num_splits), _ptr(workspace),
                                     workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "pa_decode_mla_absorbed")
+
+
+def pa_kv_write(k, v, slot_mapping, k_pool, v_pool, *, status=None, stream=None) -> None:
+    """Paged KV write.  k, v [T, Hkv, D] bf16; slot_mapping [T] int64 (negative: padding, skipped);
+    pools [pages, P, Hkv, D] bf16 (written at the named slots); status: optional uint32 device
+    word that gets PA_DEV_BAD_SLOT for a slot past the pool."""
+    T, Hkv, D = k.shape
+    num_pages, P, _, _ = k_pool.shape
+    _check(lib.pa_kv_write(_ptr(k), _ptr(v), _ptr(slot_mapping), _ptr(k_pool), _ptr(v_pool), T, Hkv, D, P,
+                           num_pages, _ptr(status), _stream(stream)), "pa_kv_write")
+
+
+def pa_mla_cache_write(c_lat, k_rope, slot_mapping, cache, *, status=None, stream=None) -> None:
+    """MLA cache write.  c_lat [T, 512], k_rope [T, 64] bf16; cache [pages, P, 576] bf16."""
+    T = c_lat.shape[0]
+    num_pages, P, _ = cache.shape
+    _check(lib.pa_mla_cache_write(_ptr(c_lat), _ptr(k_rope), _ptr(slot_mapping), _ptr(cache), T, P, num_pages,
+                                  _ptr(status), _stream(stream)), "pa_mla_cache_write")
 
 
 def pa_read_device_status(workspace, stream=None) -> int:

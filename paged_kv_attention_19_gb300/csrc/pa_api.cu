@@ -132,6 +132,14 @@ int sm_count() {
 
 }  // namespace
 
+namespace pa {
+void note_launches(int n) { t_last_launches = n; }
+cudaError_t profile_mark(bool before, cudaStream_t stream) {
+  cudaEvent_t e = before ? t_ev_before : t_ev_after;
+  return e ? cudaEventRecord(e, stream) : cudaSuccess;
+}
+}  // namespace pa
+
 extern "C" {
 
 size_t pa_workspace_size(int kind, int batch, int num_q_heads, int num_kv_heads, int head_dim,

@@ -5,6 +5,10 @@
 #include <cuda_runtime.h>
 
 namespace pa {
+// Bookkeeping of the profiling hook and launch counter of the C ABI (pa_api.cu).
+void note_launches(int n);
+cudaError_t profile_mark(bool before, cudaStream_t stream);
+
 struct GqaArgs;
 struct PlanArgs;
 struct CombineArgs;

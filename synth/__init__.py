@@ -43,7 +43,7 @@ _M2 = np.uint64(0x94D049BB133111EB)
 BF16_NAN = np.uint16(0x7FC0)
 
 # stream tags: one independent splitmix64 stream per drawn quantity
-TAG_Q, TAG_K, TAG_V, TAG_LENS, TAG_PERM, TAG_CACHE, TAG_WUK, TAG_WUV = range(1, 9)
+TAG_Q, TAG_K, TAG_V, TAG_LENS, TAG_PERM, TAG_CACHE, TAG_WUK, TAG_WUV, TAG_SLOT = range(1, 10)
 
 
 def _mix(z: np.ndarray) -> np.ndarray:
@@ -315,7 +315,61 @@ def make_mla(seed: int, context_lens, num_heads: int, page_size: int, w_std: flo
 # The five workloads of the build (seed = 20260 + index).  Shapes follow the
 # decode geometries the pages discuss; see the design doc for the recipe table.
 # ---------------------------------------------------------------------------
-WORKLOADS = ("tiny", "llama3-8b", "qwen3-32b", "hd256-window", "mla")
+@dataclasses.dataclass
+class KVWriteWorkload:
+    """New tokens' K and V (or MLA latent + rope key) and their cache slots.
+
+    Slots follow a prefill: token t is position t % page_size of page
+    perm[t // page_size], the pages of a seeded permutation of the pool; every
+    ``pad_every``-th token (if > 0) is a padding token with slot -1.  The pool
+    starts as bf16 NaN everywhere, so a write to a wrong slot shows."""
+    name: str
+    seed: int
+    k: np.ndarray         # [T, Hkv, D] uint16 bf16 bits (MLA: c_lat [T, 512])
+    v: np.ndarray         # [T, Hkv, D] uint16 (MLA: k_rope [T, 64])
+    slots: np.ndarray     # [T] int64
+    num_pages: int
+    page_size: int
+    mla: bool = False
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.slots.shape[0])
+
+    def pool_shape(self):
+        if self.mla:
+            return (self.num_pages, self.page_size, 576)
+        return (self.num_pages, self.page_size) + tuple(self.k.shape[1:])
+
+    def empty_pool(self) -> np.ndarray:
+        return np.full(self.pool_shape(), BF16_NAN, dtype=np.uint16)
+
+    def algorithmic_bytes(self) -> int:
+        """Bytes read (new rows of the written tokens) plus bytes written (the same rows)."""
+        written = int((self.slots >= 0).sum())
+        row = (576 * 2) if self.mla else 2 * int(np.prod(self.k.shape[1:])) * 2
+        return 2 * written * row
+
+
+def make_kv_write(seed: int, num_tokens: int, num_kv_heads: int, head_dim: int, page_size: int,
+                  num_pages: int, pad_every: int = 0, mla: bool = False, name: str = "kv-write") -> KVWriteWorkload:
+    assert num_tokens <= num_pages * page_size
+    perm = permutation(stream_seed(seed, TAG_PERM), num_pages)
+    t = np.arange(num_tokens, dtype=np.int64)
+    slots = perm[t // page_size] * page_size + t % page_size
+    if pad_every > 0:
+        slots[pad_every - 1::pad_every] = -1
+    if mla:
+        k = _normal_bf16_dense(stream_seed(seed, TAG_CACHE), num_tokens * 512, 1.0).reshape(num_tokens, 512)
+        v = _normal_bf16_dense(stream_seed(seed, TAG_K), num_tokens * 64, 1.0).reshape(num_tokens, 64)
+    else:
+        n = num_tokens * num_kv_heads * head_dim
+        k = _normal_bf16_dense(stream_seed(seed, TAG_K), n, 1.0).reshape(num_tokens, num_kv_heads, head_dim)
+        v = _normal_bf16_dense(stream_seed(seed, TAG_V), n, 1.0).reshape(num_tokens, num_kv_heads, head_dim)
+    return KVWriteWorkload(name, seed, k, v, slots.astype(np.int64), num_pages, page_size, mla)
+
+
+WORKLOADS = ("tiny", "llama3-8b", "qwen3-32b", "hd256-window", "mla", "kv-write")
 
 
 def workload(name: str, seed: Optional[int] = None, scramble: bool = True):
@@ -337,4 +391,7 @@ def workload(name: str, seed: Optional[int] = None, scramble: bool = True):
     if name == "mla":
         lens = context_lengths(seed, 16, "uniform", 1024, 8192)
         return make_mla(seed, lens, 128, 64, name=name, scramble=scramble)
+    if name == "kv-write":
+        # a 16384-token prefill chunk into a Qwen3-32B-shaped cache (8 KV heads, D 128, page 32)
+        return make_kv_write(seed, 16384, 8, 128, 32, 1024, name=name)
     raise KeyError(name)

@@ -131,3 +131,25 @@ def test_profile_hook_arguments(pa):
     assert pa.lib.pa_set_profile_events(None, None) == pa.PA_OK
     assert pa.lib.pa_set_profile_events(ctypes.c_void_p(0x1234), None) == pa.PA_ERR_INVALID_ARGUMENT
     assert pa.lib.pa_read_device_status(None, None, None) == pa.PA_ERR_INVALID_ARGUMENT
+
+
+def test_kv_write_host_validation(pa):
+    kw = lambda **a: pa.lib.pa_kv_write(a.get("k", 0x10000), a.get("v", 0x20000), a.get("s", 0x30000),
+                                        a.get("kp", 0x40000), a.get("vp", 0x50000), a.get("T", 4),
+                                        a.get("H", 2), a.get("D", 64), a.get("P", 16), a.get("pages", 4),
+                                        a.get("st", None), None)
+    assert kw(T=0) == pa.PA_OK
+    assert kw(T=-1) == pa.PA_ERR_INVALID_ARGUMENT
+    assert kw(H=0) == pa.PA_ERR_INVALID_ARGUMENT
+    assert kw(D=60) == pa.PA_ERR_UNSUPPORTED
+    assert kw(k=None) == pa.PA_ERR_INVALID_ARGUMENT
+    assert kw(k=0x10008) == pa.PA_ERR_MISALIGNED
+    assert kw(s=0x30004) == pa.PA_ERR_MISALIGNED
+    assert kw(st=0x60002) == pa.PA_ERR_MISALIGNED
+    mw = lambda **a: pa.lib.pa_mla_cache_write(a.get("c", 0x10000), a.get("r", 0x20000), a.get("s", 0x30000),
+                                               a.get("cache", 0x40000), a.get("T", 4), a.get("P", 16),
+                                               a.get("pages", 4), None, None)
+    assert mw(T=0) == pa.PA_OK
+    assert mw(P=0) == pa.PA_ERR_INVALID_ARGUMENT
+    assert mw(cache=None) == pa.PA_ERR_INVALID_ARGUMENT
+    assert mw(r=0x20008) == pa.PA_ERR_MISALIGNED
