@@ -45,7 +45,7 @@ METRIC = "µs/call and achieved HBM GB/s (frac of ~8 TB/s) for paged decode atte
 FLUSH_BYTES = 512 << 20
 CLEAN_BYTES = 512 << 20
 DEFAULT_WORKLOAD = "qwen3-32b"
-WORKLOADS = ["tiny", "llama3-8b", "qwen3-32b", "hd256-window", "mla", "kv-write"]
+WORKLOADS = ["tiny", "llama3-8b", "qwen3-32b", "hd256-window", "mla", "kv-write", "qwen3-32b-verify4"]
 # sources of the kernel each roofline line profiles (a change voids its committed ncu traffic)
 KERNEL_SOURCES = {"gqa": ("pa_gqa.cuh", "pa_common.cuh"),
                   "mla": ("pa_mla.cu", "pa_plan.cu", "pa_plan.cuh", "pa_common.cuh")}
@@ -122,8 +122,11 @@ def describe(w, name):
                 "visible_tokens": w.visible_tokens(), "algorithmic_bytes": w.algorithmic_bytes(),
                 "algorithmic_bytes_without_weights": w.algorithmic_bytes(with_weights=False), "seed": w.seed}
     ctx = {"tiny": "fixed{1,31,32,33,64,100}", "llama3-8b": "uniform[512,4096]",
-           "qwen3-32b": "loguniform[128,16384]", "hd256-window": "uniform[2048,32768], window 4096"}[name]
-    return {"workload": name, "batch": w.batch, "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
+           "qwen3-32b": "loguniform[128,16384]", "hd256-window": "uniform[2048,32768], window 4096",
+           "qwen3-32b-verify4": "loguniform[128,16384] (the qwen3-32b lengths), 4 query positions per row, "
+                                "causal among them"}[name]
+    return {"workload": name, "batch": w.batch, "query_positions": w.num_query, "q_heads": w.num_q_heads,
+            "kv_heads": w.num_kv_heads,
             "head_dim": w.head_dim, "page_size": w.layout.page_size, "context": ctx, "window": w.window,
             "visible_tokens": w.visible_tokens(), "algorithmic_bytes": w.algorithmic_bytes(), "seed": w.seed}
 
@@ -203,11 +206,17 @@ class OracleSample:
             return
         is_mla = isinstance(w, synth.MLAWorkload)
         H = w.num_heads if is_mla else w.num_q_heads
+        Q = 1 if is_mla else w.num_query
         rows_all = [(b, h) for b in range(w.batch) for h in range(H)]
         win = 0 if is_mla else w.window
-        vis = [synth.visible_range(int(L), win) for L in w.layout.context_lens]
+        vis = [synth.visible_range(int(L), win, Q) for L in w.layout.context_lens]
         total_work = sum(hi - lo for lo, hi in vis) * H
-        if is_mla:
+        if Q > 1:
+            # every query position of a sampled (row, head)
+            self.fn = lambda rows: oracle.verify_gqa(w.q, w.k_pool, w.v_pool, w.layout.block_table,
+                                                     w.layout.context_lens, w.scale, w.window,
+                                                     rows=[(b, i, h) for b, h in rows for i in range(Q)])
+        elif is_mla:
             self.fn = lambda rows: oracle.mla(w.q, w.cache, w.w_uk, w.w_uv, w.layout.block_table,
                                               w.layout.context_lens, w.scale, rows=rows)
         else:
@@ -308,15 +317,15 @@ def run_ours(args, rank, local_rank, world):
                                       num_splits=args.num_splits)
     else:
         d = gu.GqaDev(w)
-        B = w.batch
         out = torch.empty(w.q.shape, dtype=torch.bfloat16, device="cuda")
-        lse = torch.empty(B, w.num_q_heads, dtype=torch.float32, device="cuda")
+        lse = torch.empty(w.q.shape[:-1], dtype=torch.float32, device="cuda")
         ws = pa.workspace_for_gqa(d.q, d.k, d.bt, args.num_splits)
         ins, outs = [d.q, d.bt, d.lens], [out, lse]
+        entry = pa.pa_verify_gqa if w.num_query > 1 else pa.pa_decode_gqa
 
         def call(q, bt, lens):
-            pa.pa_decode_gqa(q, d.k, d.v, bt, lens, out, lse, scale=w.scale, window=w.window, workspace=ws,
-                             num_splits=args.num_splits)
+            entry(q, d.k, d.v, bt, lens, out, lse, scale=w.scale, window=w.window, workspace=ws,
+                  num_splits=args.num_splits)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     clean = torch.zeros(CLEAN_BYTES // 4, dtype=torch.float32, device="cuda")
 

@@ -132,6 +132,30 @@ int pa_decode_gqa(const void *q, const void *k_pool, const void *v_pool,
                   cudaStream_t stream);
 
 /*
+ * GQA multi-query (speculative-verify) decode: the Q newest tokens of every row
+ * are queries, causal among themselves, and all of them share one walk over the
+ * row's pages (vllm.cpp kernel-matrix, row KERNEL-ATTN-DFLASH-PAGED-BLOCK: the
+ * block's queries causal within it over the paged cache; pegainfer PR #938's
+ * verify launches).
+ *   q            [batch, num_query, num_q_heads, head_dim] bf16
+ *   out          [batch, num_query, num_q_heads, head_dim] bf16 (written)
+ *   lse          [batch, num_query, num_q_heads] fp32 (written), or NULL
+ *   context_lens [batch]: L, the row's length including its num_query new tokens
+ * Query position i of a row sits at logical position L - num_query + i and
+ * attends to keys [lo, L - num_query + 1 + i), lo = max(0, that - window) under a
+ * window: the result of each (row, position) equals pa_decode_gqa on a row of
+ * length L - num_query + 1 + i (0 or less: out = 0, lse = -inf).  Every other
+ * argument, the workspace (same size as for pa_decode_gqa) and the error codes
+ * are those of pa_decode_gqa; num_query in [1, 64] (1 is pa_decode_gqa).
+ */
+int pa_verify_gqa(const void *q, const void *k_pool, const void *v_pool,
+                  const int32_t *block_table, const int32_t *context_lens, void *out, float *lse,
+                  int batch, int num_query, int num_q_heads, int num_kv_heads, int head_dim,
+                  int page_size, int num_pages, int max_pages_per_seq, int max_context_len,
+                  float scale, int window, int num_splits, void *workspace, size_t workspace_bytes,
+                  cudaStream_t stream);
+
+/*
  * MLA absorbed decode (DeepSeek-V2-style geometry: 128 nope + 64 rope query
  * dims, 512 latent + 64 rope cache dims, 128 value dims per head).
  *   q            [batch, num_heads, 192] bf16: q_nope (128) || q_rope (64)

@@ -113,6 +113,26 @@ def gqa(q, k_pool, v_pool, block_table, context_lens, scale: float, window: int 
     return o, lse
 
 
+def verify_gqa(q, k_pool, v_pool, block_table, context_lens, scale: float, window: int = 0,
+               rows=None, threads: int = 0, lib=None):
+    """Multi-query (speculative-verify) GQA decode: q [B, Q, Hq, D] holds the Q newest tokens of
+    each row, so query position i of a row of length L sits at logical position L - Q + i and
+    attends to the keys up to and including its own (the W most recent of them under a window):
+    exactly the decode of a row of length L - Q + 1 + i (kernel-matrix row
+    KERNEL-ATTN-DFLASH-PAGED-BLOCK, causal within the block; pegainfer PR #938's verify path).
+    The oracle is that definition written out: every (row, position) becomes a decode row with
+    its own length over the same block table.  ``rows``: optional (b, i, h) triples.  Returns
+    (o [n, D], lse [n]) in (b, i, h) order."""
+    q = _c(q, np.uint16)
+    B, Q, Hq, D = q.shape
+    bt, lens = _c(block_table, np.int32), _c(context_lens, np.int32)
+    qv = q.reshape(B * Q, Hq, D)
+    btv = np.repeat(bt, Q, axis=0)
+    lensv = np.maximum(np.repeat(lens, Q) - Q + 1 + np.tile(np.arange(Q, dtype=np.int32), B), 0).astype(np.int32)
+    rv = None if rows is None else [(b * Q + i, h) for b, i, h in rows]
+    return gqa(qv, k_pool, v_pool, btv, lensv, scale, window, rows=rv, threads=threads, lib=lib)
+
+
 def gqa_span(q, k_pool, v_pool, block_table, scale: float, items, threads: int = 0, lib=None):
     """Attention of (b, h) over the explicit logical token span [t0, t1): items = [(b, h, t0, t1)]."""
     q, k_pool, v_pool = _c(q, np.uint16), _c(k_pool, np.uint16), _c(v_pool, np.uint16)

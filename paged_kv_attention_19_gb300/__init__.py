@@ -6,7 +6,7 @@ There is no CPU fallback: importing this package fails with ImportError if the
 library has not been built (``python paged_kv_attention_19_gb300/build.py``).
 
 Names follow the C ABI: ``pa_workspace_size``, ``pa_decode_gqa``,
-``pa_decode_mla_absorbed``, ``pa_decode_gqa_noalloc``, ``pa_kv_write``,
+``pa_decode_mla_absorbed``, ``pa_verify_gqa``, ``pa_decode_gqa_noalloc``, ``pa_kv_write``,
 ``pa_mla_cache_write``, ``pa_status_string``, ``pa_read_device_status``,
 ``pa_set_profile_events``, ``pa_last_launch_count``.  The tensor-taking
 functions accept torch tensors (device memory, the layouts of the header) and
@@ -40,6 +40,8 @@ SIGNATURES = {
     "pa_decode_gqa": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _Z, _P]),
     "pa_decode_mla_absorbed": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P]),
     "pa_decode_gqa_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
+    "pa_verify_gqa": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _Z,
+                           _P]),
     "pa_kv_write": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
     "pa_mla_cache_write": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "pa_status_string": (ctypes.c_char_p, [_I]),
@@ -120,6 +122,22 @@ def pa_decode_gqa(q, k_pool, v_pool, block_table, context_lens, out, lse=None, *
     _check(rc, "pa_decode_gqa")
 
 
+def pa_verify_gqa(q, k_pool, v_pool, block_table, context_lens, out, lse=None, *, scale: float,
+                  workspace, window: int = 0, num_splits: int = 0, max_context_len=None, stream=None) -> None:
+    """GQA multi-query verify.  q [B, Q, Hq, D]; out [B, Q, Hq, D]; lse [B, Q, Hq] or None;
+    context_lens count the Q new tokens; the rest as for pa_decode_gqa."""
+    B, Q, Hq, D = q.shape
+    num_pages, P, Hkv, _ = k_pool.shape
+    max_pages = block_table.shape[1]
+    if max_context_len is None:
+        max_context_len = max_pages * P
+    rc = lib.pa_verify_gqa(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table), _ptr(context_lens),
+                           _ptr(out), _ptr(lse), B, Q, Hq, Hkv, D, P, num_pages, max_pages, int(max_context_len),
+                           float(scale), int(window), int(num_splits), _ptr(workspace),
+                           workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "pa_verify_gqa")
+
+
 def pa_decode_mla_absorbed(q, cache, w_uk, w_uv, block_table, context_lens, out, lse=None, *, scale: float,
                            workspace, num_splits: int = 0, max_context_len=None, stream=None) -> None:
     """MLA absorbed decode.  q [B, H, 192], cache [pages, P, 576], w_uk / w_uv [H, 128, 512] bf16;
@@ -179,7 +197,7 @@ def pa_last_launch_count() -> int:
 def workspace_for_gqa(q, k_pool, block_table, num_splits: int = 0, max_context_len=None, device=None):
     """Allocate a uint8 device workspace sized for a pa_decode_gqa call with these tensors."""
     import torch
-    B, Hq, D = q.shape
+    B, Hq, D = q.shape[0], q.shape[-2], q.shape[-1]
     _, P, Hkv, _ = k_pool.shape
     mcl = block_table.shape[1] * P if max_context_len is None else max_context_len
     n = pa_workspace_size(PA_KIND_GQA, B, Hq, Hkv, D, mcl, P, num_splits)

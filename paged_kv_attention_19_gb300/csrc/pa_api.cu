@@ -23,6 +23,7 @@ using namespace pa;
 
 constexpr int kMaxSplits = 4096;     // largest accepted explicit num_splits (partitions)
 constexpr int kAutoPartsMax = 256;   // automatic mode: one partition per SM, at most this many
+constexpr int kMaxQueryPositions = 64;  // verify: query positions per row
 // Fixed cost of one piece of work in the GQA partition (the Q load and the end-of-piece
 // merge, about 0.8 us of one SM), expressed as the KV bytes the SM streams meanwhile.
 constexpr long long kPieceCostBytes = 32 << 10;
@@ -102,15 +103,16 @@ bool encode_pool_map(CUtensorMap *m, const void *base, int num_pages, int P, int
   return r == CUDA_SUCCESS;
 }
 
-// 2-D map over q viewed as [batch * Hq rows, D] bf16; box = (64 dims, 16 rows), 128-byte swizzle.
-bool encode_q_map(CUtensorMap *m, const void *base, long long rows, int D) {
+// 3-D map over q viewed as [batch * Q positions, Hq, D] bf16; box = (64 dims, gt heads, qt
+// positions), 128-byte swizzle: the qt x gt rows of one tile land as consecutive 128-byte rows.
+bool encode_q_map(CUtensorMap *m, const void *base, long long positions, int Hq, int D, int gt, int qt) {
   auto fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-  cuuint32_t box[2] = {64u, (cuuint32_t)PART_HEADS};
-  cuuint32_t estr[2] = {1u, 1u};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hq, (cuuint64_t)positions};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hq * D * 2};
+  cuuint32_t box[3] = {64u, (cuuint32_t)gt, (cuuint32_t)qt};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -157,12 +159,18 @@ size_t pa_workspace_size(int kind, int batch, int num_q_heads, int num_kv_heads,
   return 0;
 }
 
-int pa_decode_gqa(const void *q, const void *k_pool, const void *v_pool, const int32_t *block_table,
-                  const int32_t *context_lens, void *out, float *lse, int batch, int num_q_heads,
-                  int num_kv_heads, int head_dim, int page_size, int num_pages, int max_pages_per_seq,
-                  int max_context_len, float scale, int window, int num_splits, void *workspace,
-                  size_t workspace_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// GQA decode (Q == 1) and verify (Q > 1 query positions per row, causal among them).
+int gqa_call(const void *q, const void *k_pool, const void *v_pool, const int32_t *block_table,
+             const int32_t *context_lens, void *out, float *lse, int batch, int Q, int num_q_heads,
+             int num_kv_heads, int head_dim, int page_size, int num_pages, int max_pages_per_seq,
+             int max_context_len, float scale, int window, int num_splits, void *workspace,
+             size_t workspace_bytes, cudaStream_t stream) {
   t_last_launches = 0;
+  if (Q <= 0 || Q > kMaxQueryPositions) return Q <= 0 ? PA_ERR_INVALID_ARGUMENT : PA_ERR_UNSUPPORTED;
   if (batch == 0) return PA_OK;
   GqaPlan pl;
   int rc = gqa_shape(batch, num_q_heads, num_kv_heads, head_dim, max_context_len, page_size, num_splits, &pl);
@@ -180,10 +188,15 @@ int pa_decode_gqa(const void *q, const void *k_pool, const void *v_pool, const i
   const int D = head_dim, P = page_size;
   const int ST = gqa_stage_tokens(D);
   const int BH = P < ST ? P : ST;  // tokens per TMA box = per work unit
+  // query tiles of at most 16 MMA rows: qt positions x gt heads of one KV head's group
+  const int G = num_q_heads / num_kv_heads;
+  const int gt = G < PART_HEADS ? G : PART_HEADS;
+  const int qt = G < PART_HEADS ? (Q < PART_HEADS / G ? Q : PART_HEADS / G) : 1;
+  const int ntile = G < PART_HEADS ? (Q + qt - 1) / qt : Q * pl.nsub;
   CUtensorMap tm_k, tm_v, tm_q;
   if (!encode_pool_map(&tm_k, k_pool, num_pages, P, num_kv_heads, D, BH) ||
       !encode_pool_map(&tm_v, v_pool, num_pages, P, num_kv_heads, D, BH) ||
-      !encode_q_map(&tm_q, q, (long long)batch * num_q_heads, D))
+      !encode_q_map(&tm_q, q, (long long)batch * Q, num_q_heads, D, gt, qt))
     return PA_ERR_UNSUPPORTED;
   const int sms = sm_count();
   if (sms <= 0) return PA_ERR_CUDA;
@@ -213,11 +226,15 @@ int pa_decode_gqa(const void *q, const void *k_pool, const void *v_pool, const i
   ga.Hkv = num_kv_heads;
   ga.G = num_q_heads / num_kv_heads;
   ga.nsub = pl.nsub;
+  ga.Q = Q;
+  ga.gt = gt;
+  ga.qt = qt;
+  ga.ntile = ntile;
   ga.log2_page = ilog2(P);
   ga.log2_bh = ilog2(BH);
   ga.nparts = nparts;
   {
-    const int hs = num_kv_heads * pl.nsub;
+    const int hs = num_kv_heads * ntile;
     ga.hg = hs < nparts ? hs : nparts;
   }
   {
@@ -238,6 +255,10 @@ int pa_decode_gqa(const void *q, const void *k_pool, const void *v_pool, const i
   ca.nsub = pl.nsub;
   ca.nparts = nparts;
   ca.hg = ga.hg;
+  ca.Q = Q;
+  ca.gt = gt;
+  ca.qt = qt;
+  ca.ntile = ntile;
 
   cudaError_t e;
   if (t_ev_before && cudaEventRecord(t_ev_before, stream) != cudaSuccess) return PA_ERR_CUDA;
@@ -257,6 +278,30 @@ int pa_decode_gqa(const void *q, const void *k_pool, const void *v_pool, const i
   if (e != cudaSuccess) return PA_ERR_CUDA;
   ++t_last_launches;
   return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_decode_gqa(const void *q, const void *k_pool, const void *v_pool, const int32_t *block_table,
+                  const int32_t *context_lens, void *out, float *lse, int batch, int num_q_heads,
+                  int num_kv_heads, int head_dim, int page_size, int num_pages, int max_pages_per_seq,
+                  int max_context_len, float scale, int window, int num_splits, void *workspace,
+                  size_t workspace_bytes, cudaStream_t stream) {
+  return gqa_call(q, k_pool, v_pool, block_table, context_lens, out, lse, batch, 1, num_q_heads, num_kv_heads,
+                  head_dim, page_size, num_pages, max_pages_per_seq, max_context_len, scale, window, num_splits,
+                  workspace, workspace_bytes, stream);
+}
+
+int pa_verify_gqa(const void *q, const void *k_pool, const void *v_pool, const int32_t *block_table,
+                  const int32_t *context_lens, void *out, float *lse, int batch, int num_query,
+                  int num_q_heads, int num_kv_heads, int head_dim, int page_size, int num_pages,
+                  int max_pages_per_seq, int max_context_len, float scale, int window, int num_splits,
+                  void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return gqa_call(q, k_pool, v_pool, block_table, context_lens, out, lse, batch, num_query, num_q_heads,
+                  num_kv_heads, head_dim, page_size, num_pages, max_pages_per_seq, max_context_len, scale, window,
+                  num_splits, workspace, workspace_bytes, stream);
 }
 
 int pa_decode_mla_absorbed(const void *q, const void *cache, const void *w_uk, const void *w_uv,

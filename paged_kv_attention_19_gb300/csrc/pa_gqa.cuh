@@ -54,7 +54,7 @@ namespace pa {
 // What each split CTA leaves for the combine kernel.
 struct GqaPartDesc {
   int32_t last_b;   // row of the CTA's last piece
-  int32_t last_hs;  // KV head x subgroup (kv_head * nsub + sub) of the last piece
+  int32_t last_hs;  // KV head x tile (kv_head * ntile + tile) of the last piece
   uint32_t flags;   // bits 0-15: pieces of the CTA (saturating); DESC_* bits
   uint32_t status;  // PA_DEV_* bits seen by the CTA
 };
@@ -76,10 +76,12 @@ struct GqaArgs {
   GqaPartDesc *desc;            // [nparts]
   int batch, max_pages_per_seq, num_pages, max_context_len, window;
   int Hq, Hkv, G, nsub;
+  int Q;                        // query positions per row (1: decode; > 1: verify, causal within them)
+  int gt, qt, ntile;            // a tile of MMA rows: qt positions x gt heads; ntile tiles per KV head
   int log2_page, log2_bh;       // page size and tokens per unit (TMA box), as powers of two
   int piece_cost;               // partition cost of starting a piece, in units
   int nparts;                   // CTAs (shares); groups of hg consecutive CTAs
-  int hg;                       // CTAs per group: min(Hkv * nsub, nparts)
+  int hg;                       // CTAs per group: min(Hkv * ntile, nparts)
   float qscale;                 // scale * log2(e)
 };
 
@@ -107,9 +109,9 @@ struct GqaCfg {
 struct alignas(16) StageMeta {
   int32_t end, first, last, masked;  // first: a stage holding the piece's query rows only
   int32_t b, hq0, ghead, slot;  // slot: -1 = whole sequence (final output), else partial slot 0 / 1
-  int32_t tok0, tok_lo, tok_hi, pad0;
+  int32_t tok0, tok_lo, tok_hi, L;  // L: the row's length (query position i attends below L - Q + 1 + i)
   uint32_t badmask;             // bit k: box k of the stage was not loaded
-  int32_t pad1, pad2, pad3;
+  int32_t i0, nq, pad0;         // the tile's positions [i0, i0 + nq); ghead: its heads
 };
 static_assert(sizeof(StageMeta) == 64, "stage meta is 64 bytes");
 
@@ -142,14 +144,44 @@ __device__ __forceinline__ uint32_t kv_off(int tok, int chunk) {
   return (uint32_t)((chunk >> 3) * C::PLANE + tok * 128 + (((chunk & 7) ^ (tok & 7)) << 4));
 }
 
-// Visible units of a row of length L: [*u_lo, u_lo + return value).
-__device__ __forceinline__ int row_units(int L, int window, int log2_bh, int *u_lo) {
-  const int lo = (window > 0 && L > window) ? L - window : 0;
+// Units of a row of length L that some of its Q query positions attend to:
+// [*u_lo, u_lo + return value), the union of the positions' key ranges.
+__device__ __forceinline__ int row_units(int L, int Q, int window, int log2_bh, int *u_lo) {
+  const int lo = window > 0 ? max(L - Q + 1 - window, 0) : 0;
   *u_lo = lo >> log2_bh;
   return L > 0 ? ((L + (1 << log2_bh) - 1) >> log2_bh) - *u_lo : 0;
 }
 
 __device__ __forceinline__ int clamp_len(int L, int max_len) { return min(max(L, 0), max_len); }
+
+// Tile t of a KV head's query rows: positions [i0, i0 + nq), heads [h0, h0 + nh) of the
+// group (h0 relative to the group's first head).  MMA row r is position i0 + r / gt, head
+// h0 + r % gt; it is a real row when r / gt < nq and r % gt < nh.
+struct Tile {
+  int i0, nq, h0, nh;
+};
+__device__ __forceinline__ Tile tile_of(int t, int G, int nsub, int Q, int qt) {
+  Tile x;
+  if (G < 16) {
+    x.i0 = t * qt;
+    x.nq = min(qt, Q - x.i0);
+    x.h0 = 0;
+    x.nh = G;
+  } else {
+    x.i0 = t / nsub;
+    x.nq = 1;
+    x.h0 = (t % nsub) * 16;
+    x.nh = min(16, G - x.h0);
+  }
+  return x;
+}
+
+// Keys of query position i of a row of length L holding Q new tokens: [lo, hi) with
+// hi = L - Q + 1 + i (the position itself included) and lo = max(0, hi - window) under a window.
+__device__ __forceinline__ int pos_hi(int L, int Q, int i) { return max(L - Q + 1 + i, 0); }
+__device__ __forceinline__ int pos_lo(int L, int Q, int i, int window) {
+  return window > 0 ? max(pos_hi(L, Q, i) - window, 0) : 0;
+}
 
 // Block-wide sum / exclusive scan of 64-bit values (all threads of the CTA take part).
 __device__ __forceinline__ long long block_sum64(long long v, long long *warp_part) {
@@ -190,7 +222,8 @@ struct Piece {
   bool starts, ends;
 };
 
-template <int D>
+// MQ: several query positions per row (verify); false compiles the decode-only row logic.
+template <int D, bool MQ>
 __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
     gqa_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_q, const GqaArgs a) {
@@ -206,7 +239,7 @@ __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int HS = a.Hkv * a.nsub;
+  const int HS = a.Hkv * a.ntile;  // sequences per row: KV heads x tiles
   if (tid == 0) {
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(&full[s], 1);
@@ -237,7 +270,7 @@ __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
   // serves exactly one subgroup (HG == HS); with NG == 1 every piece is a whole sequence.
   auto seq_cost = [&](int L, int *n_out) {
     int ul;
-    const int n = row_units(L, a.window, a.log2_bh, &ul);
+    const int n = row_units(L, a.Q, a.window, a.log2_bh, &ul);
     *n_out = n;
     return n > 0 ? n + a.piece_cost : 0;
   };
@@ -297,11 +330,11 @@ __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
   // rows without a visible key: out = 0, lse = -inf (rows b = blockIdx.x mod nparts)
   for (int b = blockIdx.x; b < a.batch; b += a.nparts) {
     int ul;
-    if (row_units(clamp_len(a.context_lens[b], a.max_context_len), a.window, a.log2_bh, &ul) != 0) continue;
-    uint4 *o = reinterpret_cast<uint4 *>(a.out + (size_t)b * a.Hq * D);
-    for (int e = tid; e < a.Hq * D / 8; e += C::THREADS) o[e] = make_uint4(0, 0, 0, 0);
+    if (row_units(clamp_len(a.context_lens[b], a.max_context_len), a.Q, a.window, a.log2_bh, &ul) != 0) continue;
+    uint4 *o = reinterpret_cast<uint4 *>(a.out + (size_t)b * a.Q * a.Hq * D);
+    for (int e = tid; e < a.Q * a.Hq * D / 8; e += C::THREADS) o[e] = make_uint4(0, 0, 0, 0);
     if (a.lse)
-      for (int h = tid; h < a.Hq; h += C::THREADS) a.lse[(size_t)b * a.Hq + h] = -INFINITY;
+      for (int h = tid; h < a.Q * a.Hq; h += C::THREADS) a.lse[(size_t)b * a.Q * a.Hq + h] = -INFINITY;
   }
   __syncthreads();
 
@@ -357,11 +390,11 @@ __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
         }
         if (u1 > u0) {
           int ul;
-          row_units(L, a.window, a.log2_bh, &ul);
+          row_units(L, a.Q, a.window, a.log2_bh, &ul);
           p.b = b;
           p.hs = it_hs;
           p.L = L;
-          p.lo = (a.window > 0 && L > a.window) ? L - a.window : 0;
+          p.lo = pos_lo(L, a.Q, 0, a.window);
           p.ub = ul + u0;
           p.ue = ul + u1;
           p.starts = u0 == 0;
@@ -370,8 +403,7 @@ __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
         }
       }
     };
-    auto q_head0 = [&](const Piece &p) { return (p.hs / a.nsub) * a.G + (p.hs % a.nsub) * C::M; };
-    auto q_heads = [&](const Piece &p) { return min(C::M, a.G - (p.hs % a.nsub) * C::M); };
+    auto tile = [&](const Piece &p) { return tile_of(p.hs % a.ntile, a.G, a.nsub, a.Q, a.qt); };
     // block-table window 0 of a piece (lane l: entry l of its first page)
     auto piece_window = [&](const Piece &p) {
       const int pb = (p.ub << a.log2_bh) >> a.log2_page;
@@ -389,9 +421,11 @@ __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
     }
     while (has_cur && ok) {
       // ---- emit the stages of `cur`
-      const int g = cur.hs / a.nsub;
-      const int ghead = q_heads(cur);
-      const int hq0 = q_head0(cur);
+      const int g = cur.hs / a.ntile;
+      const Tile tl = tile(cur);
+      const int hq0 = g * a.G + tl.h0;
+      // the tile's tightest key bounds: its first position ends first, its last starts last
+      const int hi_min = pos_hi(cur.L, a.Q, tl.i0), lo_max = pos_lo(cur.L, a.Q, tl.i0 + tl.nq - 1, a.window);
       const int slot = (cur.starts && cur.ends) ? -1 : (npieces == 0 ? 0 : 1);
       const int T0 = cur.ub << a.log2_bh;
       const int tok_lo = max(cur.lo, T0), tok_hi = min(cur.L, cur.ue << a.log2_bh);
@@ -402,8 +436,9 @@ __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
       int cwin = cwin0, wi = 0;
       int fwin = (lane + 32 < npages) ? bt_piece[32 + lane] : 0;  // window 1, in flight
       {
-        // the piece's query rows: a stage of their own (16 rows from row b * Hq + hq0; rows
-        // past ghead belong to other heads or are zero-filled, and are masked by the consumers)
+        // the piece's query rows: a stage of their own (a qt x gt box of (position, head) rows
+        // from position i0 and head hq0; rows of other heads or positions are masked by the
+        // consumers)
         const int s = j % C::NS;
         const uint32_t u = j / C::NS;
         if (u > 0) ok = mbar_wait(&empty[s], (u - 1) & 1, status);
@@ -415,12 +450,15 @@ __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
           m.last = 0;
           m.b = cur.b;
           m.hq0 = hq0;
-          m.ghead = ghead;
-          mbar_arrive_expect_tx(&full[s], (uint32_t)(C::NQ * C::M * 128));
+          m.ghead = tl.nh;
+          m.i0 = tl.i0;
+          m.nq = tl.nq;
+          m.L = cur.L;
+          mbar_arrive_expect_tx(&full[s], (uint32_t)(C::NQ * a.gt * a.qt * 128));
           uint8_t *qdst = smem + S::OFF_STAGE + s * C::STAGE_BYTES;
 #pragma unroll
           for (int dq = 0; dq < C::NQ; ++dq)
-            tma_load_2d(qdst + dq * (C::M * 128), &tm_q, dq * 64, cur.b * a.Hq + hq0, &full[s]);
+            tma_load_3d(qdst + dq * (C::M * 128), &tm_q, dq * 64, hq0, cur.b * a.Q + tl.i0, &full[s]);
         }
         __syncwarp();
         ++j;
@@ -464,13 +502,16 @@ __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
           m.last = last;
           m.b = cur.b;
           m.hq0 = hq0;
-          m.ghead = ghead;
+          m.ghead = tl.nh;
+          m.i0 = tl.i0;
+          m.nq = tl.nq;
+          m.L = cur.L;
           m.slot = slot;
           m.tok0 = tok0;
           m.tok_lo = tok_lo;
           m.tok_hi = tok_hi;
           m.badmask = bad;
-          m.masked = (tok0 < tok_lo) || (tok0 + C::ST > tok_hi) || bad != 0;
+          m.masked = (tok0 < max(tok_lo, lo_max)) || (tok0 + C::ST > min(tok_hi, hi_min)) || bad != 0;
           mbar_arrive_expect_tx(&full[s], (uint32_t)nvalid * (uint32_t)((D * 2 * 2) << a.log2_bh));
         }
         __syncwarp();
@@ -532,7 +573,9 @@ __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
     uint32_t qa[D / 16][4];  // Q A-fragments (rows = heads)
     float acc[C::NT_PV][4];  // O C-fragments of this warp's columns: [n-tile][row g8 x2, row g8+8 x2]
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    int ghead = 0;
+    // this thread's two fragment rows (g8, g8 + 8): real row?, key bounds [lo, hi) of its position
+    bool rv0 = false, rv1 = false;
+    int lo0 = 0, hi0 = 0, lo1 = 0, hi1 = 0;
     for (uint32_t j = 0;; ++j) {
       const int s = j % C::NS;
       if (!mbar_wait(&full[s], (j / C::NS) & 1, status)) break;
@@ -543,7 +586,18 @@ __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
       if (mt.first) {
         // a new piece: its query rows into the A-fragments (ldmatrix from the 128-byte
         // swizzled planes of 16 rows x 64 dims), fresh softmax state, and the stage goes back
-        ghead = mt.ghead;
+        if constexpr (MQ) {
+          const int iq0 = g8 / a.gt, hh0 = g8 % a.gt, iq1 = (g8 + 8) / a.gt, hh1 = (g8 + 8) % a.gt;
+          rv0 = iq0 < mt.nq && hh0 < mt.ghead;
+          rv1 = iq1 < mt.nq && hh1 < mt.ghead;
+          lo0 = pos_lo(mt.L, a.Q, mt.i0 + iq0, a.window);
+          hi0 = pos_hi(mt.L, a.Q, mt.i0 + iq0);
+          lo1 = pos_lo(mt.L, a.Q, mt.i0 + iq1, a.window);
+          hi1 = pos_hi(mt.L, a.Q, mt.i0 + iq1);
+        } else {  // one position: row r is head r, and the piece's bounds are the row's
+          rv0 = g8 < mt.ghead;
+          rv1 = g8 + 8 < mt.ghead;
+        }
         const uint32_t qbase = kbase;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
@@ -595,12 +649,12 @@ __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float v = sv[nt][e] * a.qscale;
-          const int row = (e < 2) ? g8 : g8 + 8;
-          bool valid = row < ghead;
+          bool valid = (e < 2) ? rv0 : rv1;
           if (masked) {
             const int stok = wbase + nt * 8 + 2 * tq + (e & 1);
             const int ltok = mt.tok0 + stok;
             valid = valid && ltok >= mt.tok_lo && ltok < mt.tok_hi && !((mt.badmask >> (stok / bh_tokens)) & 1u);
+            if constexpr (MQ) valid = valid && ltok >= ((e < 2) ? lo0 : lo1) && ltok < ((e < 2) ? hi0 : hi1);
           }
           sv[nt][e] = valid ? v : -INFINITY;
         }
@@ -693,12 +747,14 @@ __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
           sm_ml[(tgrp * C::M + g8 + 8) * 2 + 1] = l1;
         }
         named_bar(1, C::NCW * 32);
-        // each thread: 4 consecutive dims of one head; token-group weights
-        // exp2(m_w - M) / sum_w l_w exp2(m_w - M), computed by every thread of the head
+        // each thread: 4 consecutive dims of one row; token-group weights
+        // exp2(m_w - M) / sum_w l_w exp2(m_w - M), computed by every thread of the row
         const int slot = mt.slot;
         const size_t pi = (size_t)blockIdx.x * 2 + (slot > 0 ? 1 : 0);  // partial slot (when slot >= 0)
-        for (int e = ct; e < ghead * (D / 4); e += C::NCW * 32) {
-          const int h = e / (D / 4), d4 = (e % (D / 4)) * 4;
+        const int nrows = MQ ? mt.nq * a.gt : mt.ghead;
+        for (int e = ct; e < nrows * (D / 4); e += C::NCW * 32) {
+          const int h = e / (D / 4), d4 = (e % (D / 4)) * 4;  // h: the MMA row
+          if (MQ && h % a.gt >= mt.ghead) continue;          // not a head of this tile
           float mw[C::TG], M = -INFINITY;
 #pragma unroll
           for (int w = 0; w < C::TG; ++w) {
@@ -718,7 +774,8 @@ __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
             o.w += wt * x.w;
           }
           const float inv = L > 0.f ? 1.f / L : 0.f;
-          const size_t bh = (size_t)mt.b * a.Hq + mt.hq0 + h;
+          const size_t bh = MQ ? ((size_t)mt.b * a.Q + mt.i0 + h / a.gt) * a.Hq + mt.hq0 + h % a.gt
+                               : (size_t)mt.b * a.Hq + mt.hq0 + h;
           if (slot < 0) {
             uint2 v;
             v.x = pack_bf16x2(o.x * inv, o.y * inv);
@@ -769,6 +826,7 @@ struct CombineArgs {
   const GqaPartDesc *desc;
   uint32_t *status;  // the workspace status word: OR of every CTA's bits
   int Hq, G, nsub, nparts, hg;
+  int Q, gt, qt, ntile;
 };
 
 // One block per split CTA c.  Block c merges the sequence that CTA c's last
@@ -806,11 +864,12 @@ __global__ void __launch_bounds__(128) gqa_combine_kernel(const CombineArgs a) {
   }
   if (k < 0) return;  // not reachable for a consistent partition
   const int first_slot = np >= 2 ? 1 : 0;
-  const int g = d0.last_hs / a.nsub, sub = d0.last_hs % a.nsub;
-  const int hq0 = g * a.G + sub * PART_HEADS;
-  const int ghead = min(PART_HEADS, a.G - sub * PART_HEADS);
+  const int g = d0.last_hs / a.ntile;
+  const Tile tl = tile_of(d0.last_hs % a.ntile, a.G, a.nsub, a.Q, a.qt);
+  const int hq0 = g * a.G + tl.h0;
   constexpr int PER = D / 32;  // 2, 4 or 8 consecutive dims per lane
-  for (int h = warp; h < ghead; h += 4) {
+  for (int h = warp; h < tl.nq * a.gt; h += 4) {  // h: the MMA row
+    if (h % a.gt >= tl.nh) continue;
     float M = -INFINITY;
     for (int i = lane; i < k; i += 32) {
       const size_t pi = i == 0 ? (size_t)c * 2 + first_slot : (size_t)(c + i * a.hg) * 2;
@@ -851,7 +910,7 @@ __global__ void __launch_bounds__(128) gqa_combine_kernel(const CombineArgs a) {
       }
     }
     const float inv = Z > 0.f ? 1.f / Z : 0.f;
-    const size_t bh = (size_t)d0.last_b * a.Hq + hq0 + h;
+    const size_t bh = ((size_t)d0.last_b * a.Q + tl.i0 + h / a.gt) * a.Hq + hq0 + h % a.gt;
     uint32_t *dst = reinterpret_cast<uint32_t *>(a.out + bh * D + lane * PER);
 #pragma unroll
     for (int e = 0; e < PER; e += 2) dst[e / 2] = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);

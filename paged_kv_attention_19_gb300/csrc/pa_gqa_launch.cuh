@@ -1,0 +1,60 @@
+// pa_gqa_launch.cuh -- host launchers of the GQA split-KV and combine kernels, instantiated
+// once per head_dim by pa_gqa_d{64,128,256}.cu (one translation unit each, built in parallel).
+#pragma once
+
+#include "pa_gqa.cuh"
+#include "pa_launch.h"
+
+namespace pa {
+
+// Both kernels are launched as programmatic dependents of the kernel before them: the
+// combine kernel's launch overlaps the split kernel's tail and waits (griddepcontrol.wait)
+// before reading its output; the split kernel waits the same way before it reads its inputs.
+inline cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, int smem, cudaStream_t stream,
+                                     cudaLaunchAttribute *attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+template <int D, bool MQ>
+cudaError_t launch_split(int grid, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const CUtensorMap &tm_q,
+                         const GqaArgs &a, cudaStream_t stream) {
+  using C = GqaCfg<D>;
+  constexpr int smem = GqaSmem<C>::BYTES;
+  static int configured_device = -1;  // the shared-memory opt-in is per device
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(gqa_split_kernel<D, MQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(C::THREADS), smem, stream, attr);
+  return cudaLaunchKernelEx(&cfg, gqa_split_kernel<D, MQ>, tm_k, tm_v, tm_q, a);
+}
+
+// Q == 1 (decode) runs the kernel compiled without the per-position row logic.
+template <int D>
+cudaError_t launch_split_any(int grid, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const CUtensorMap &tm_q,
+                             const GqaArgs &a, cudaStream_t stream) {
+  return a.Q > 1 ? launch_split<D, true>(grid, tm_k, tm_v, tm_q, a, stream)
+                 : launch_split<D, false>(grid, tm_k, tm_v, tm_q, a, stream);
+}
+
+template <int D>
+cudaError_t launch_combine(const CombineArgs &a, cudaStream_t stream) {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pdl_config(dim3(a.nparts), dim3(128), 0, stream, attr);
+  return cudaLaunchKernelEx(&cfg, gqa_combine_kernel<D>, a);
+}
+
+}  // namespace pa

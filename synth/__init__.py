@@ -143,9 +143,12 @@ def context_lengths(seed: int, batch: int, dist: str, lo: int = 0, hi: int = 0,
     return np.clip(lens, lo, hi).astype(np.int32)
 
 
-def visible_range(L: int, window: int) -> tuple:
-    """Token range [lo, L) a query row attends to: the W most recent keys when window W > 0."""
-    lo = max(0, L - window) if window > 0 else 0
+def visible_range(L: int, window: int, num_query: int = 1) -> tuple:
+    """Token range [lo, L) some query of a row attends to.  A row of length L holding Q new
+    tokens has query positions i < Q at logical positions L - Q + i; position i attends to the
+    keys up to and including its own, the W most recent of them when window W > 0.  The union
+    over positions is [max(0, L - Q + 1 - W), L) (Q = 1: the W most recent keys)."""
+    lo = max(0, L - num_query + 1 - window) if window > 0 else 0
     return lo, L
 
 
@@ -189,7 +192,7 @@ def make_layout(seed: int, context_lens: np.ndarray, page_size: int, pool_factor
 
 
 def _fill_pool(state: int, layout: PagedLayout, row_width: int, std: float, window: int,
-               visible_only: bool) -> np.ndarray:
+               visible_only: bool, num_query: int = 1) -> np.ndarray:
     """Pool [num_pages, P, row_width] bf16 bits; values drawn per logical (page, slot, element)."""
     P = layout.page_size
     pool = np.full((layout.num_pages, P, row_width), BF16_NAN, dtype=np.uint16)
@@ -198,7 +201,7 @@ def _fill_pool(state: int, layout: PagedLayout, row_width: int, std: float, wind
         L = int(layout.context_lens[b])
         if L == 0:
             continue
-        lo, hi = visible_range(L, window) if visible_only else (0, L)
+        lo, hi = visible_range(L, window, num_query) if visible_only else (0, L)
         p0, p1 = lo // P, (hi + P - 1) // P
         g0 = int(layout.logical_page_of_row[b])
         vals = _normal_bf16_range(state, (g0 + p0) * per_page, (p1 - p0) * per_page, std)
@@ -215,7 +218,7 @@ def _fill_pool(state: int, layout: PagedLayout, row_width: int, std: float, wind
 class GQAWorkload:
     name: str
     seed: int
-    q: np.ndarray            # [B, Hq, D] bf16 bits
+    q: np.ndarray            # [B, Hq, D] bf16 bits ([B, Q, Hq, D] when num_query > 1)
     k_pool: np.ndarray       # [num_pages, P, Hkv, D] bf16 bits
     v_pool: np.ndarray       # [num_pages, P, Hkv, D] bf16 bits
     layout: PagedLayout
@@ -225,41 +228,44 @@ class GQAWorkload:
     scale: float
     window: int
     k_std: float = 1.0
+    num_query: int = 1
 
     @property
     def batch(self):
         return self.layout.batch
 
     def visible_tokens(self) -> int:
-        return int(sum(visible_range(int(L), self.window)[1] - visible_range(int(L), self.window)[0]
-                       for L in self.layout.context_lens))
+        r = [visible_range(int(L), self.window, self.num_query) for L in self.layout.context_lens]
+        return int(sum(hi - lo for lo, hi in r))
 
     def algorithmic_bytes(self) -> int:
-        """Bytes the method must move: every visible K and V row of each kv head, all of q, and the output."""
+        """Bytes the method must move: every visible K and V row of each kv head once, all of q, and
+        the output (every query position of a row shares the one walk over its keys)."""
         kv = self.visible_tokens() * self.num_kv_heads * self.head_dim * 2 * 2
-        qb = self.batch * self.num_q_heads * self.head_dim * 2
-        ob = self.batch * self.num_q_heads * (self.head_dim * 2 + 4)
+        qb = self.batch * self.num_query * self.num_q_heads * self.head_dim * 2
+        ob = self.batch * self.num_query * self.num_q_heads * (self.head_dim * 2 + 4)
         return kv + qb + ob
 
 
 def make_gqa(seed: int, context_lens, num_q_heads: int, num_kv_heads: int, head_dim: int,
              page_size: int, window: int = 0, k_std: float = 1.0, pool_factor: int = 1,
              scale: Optional[float] = None, scramble: bool = True, name: str = "gqa",
-             visible_only: bool = True, extra_table_cols: int = 0) -> GQAWorkload:
+             visible_only: bool = True, extra_table_cols: int = 0, num_query: int = 1) -> GQAWorkload:
     lens = np.asarray(context_lens, dtype=np.int32)
     layout = make_layout(seed, lens, page_size, pool_factor, scramble, extra_table_cols)
     B = lens.shape[0]
-    q = _normal_bf16_dense(stream_seed(seed, TAG_Q), B * num_q_heads * head_dim, 1.0)
-    q = q.reshape(B, num_q_heads, head_dim)
+    Q = num_query
+    q = _normal_bf16_dense(stream_seed(seed, TAG_Q), B * Q * num_q_heads * head_dim, 1.0)
+    q = q.reshape(B, num_q_heads, head_dim) if Q == 1 else q.reshape(B, Q, num_q_heads, head_dim)
     w = num_kv_heads * head_dim
-    k = _fill_pool(stream_seed(seed, TAG_K), layout, w, k_std, window, visible_only)
-    v = _fill_pool(stream_seed(seed, TAG_V), layout, w, 1.0, window, visible_only)
+    k = _fill_pool(stream_seed(seed, TAG_K), layout, w, k_std, window, visible_only, Q)
+    v = _fill_pool(stream_seed(seed, TAG_V), layout, w, 1.0, window, visible_only, Q)
     k = k.reshape(layout.num_pages, page_size, num_kv_heads, head_dim)
     v = v.reshape(layout.num_pages, page_size, num_kv_heads, head_dim)
     if scale is None:
         scale = 1.0 / math.sqrt(head_dim)
     return GQAWorkload(name, seed, q, k, v, layout, num_q_heads, num_kv_heads, head_dim,
-                       float(scale), int(window), float(k_std))
+                       float(scale), int(window), float(k_std), int(Q))
 
 
 MLA_NOPE, MLA_ROPE, MLA_LATENT, MLA_VDIM = 128, 64, 512, 128
@@ -369,7 +375,7 @@ def make_kv_write(seed: int, num_tokens: int, num_kv_heads: int, head_dim: int, 
     return KVWriteWorkload(name, seed, k, v, slots.astype(np.int64), num_pages, page_size, mla)
 
 
-WORKLOADS = ("tiny", "llama3-8b", "qwen3-32b", "hd256-window", "mla", "kv-write")
+WORKLOADS = ("tiny", "llama3-8b", "qwen3-32b", "hd256-window", "mla", "kv-write", "qwen3-32b-verify4")
 
 
 def workload(name: str, seed: Optional[int] = None, scramble: bool = True):
@@ -391,6 +397,10 @@ def workload(name: str, seed: Optional[int] = None, scramble: bool = True):
     if name == "mla":
         lens = context_lengths(seed, 16, "uniform", 1024, 8192)
         return make_mla(seed, lens, 128, 64, name=name, scramble=scramble)
+    if name == "qwen3-32b-verify4":
+        # speculative verify: the qwen3-32b rows (same lengths) with 4 query positions each
+        lens = context_lengths(20262 if seed == 20266 else seed, 32, "loguniform", 128, 16384)
+        return make_gqa(seed, lens, 64, 8, 128, 32, name=name, scramble=scramble, num_query=4)
     if name == "kv-write":
         # a 16384-token prefill chunk into a Qwen3-32B-shaped cache (8 KV heads, D 128, page 32)
         return make_kv_write(seed, 16384, 8, 128, 32, 1024, name=name)

@@ -53,6 +53,38 @@ def dense_gqa(w: synth.GQAWorkload, window=None):
     return o.numpy(), lse.numpy()
 
 
+def dense_verify(w: synth.GQAWorkload):
+    """Causal multi-query attention in dense torch float64: the row's Q newest tokens are the
+    queries; a [Q, T] mask lets query i see key t when t <= L - Q + i (and t > L - Q + i - W
+    under a window).  Returns o [B, Q, Hq, D], lse [B, Q, Hq]."""
+    B, Q, Hq, D = w.q.shape
+    Hkv = w.num_kv_heads
+    G = Hq // Hkv
+    q = torch.from_numpy(synth.bf16_bits_to_f32(w.q).astype(np.float64))
+    o = torch.zeros(B, Q, Hq, D, dtype=torch.float64)
+    lse = torch.full((B, Q, Hq), -math.inf, dtype=torch.float64)
+    for b in range(B):
+        L = int(w.layout.context_lens[b])
+        if L == 0:
+            continue
+        K = torch.from_numpy(_logical_pool_rows(w.seed, synth.TAG_K, w.layout, b, Hkv * D, w.k_std)[:L])
+        V = torch.from_numpy(_logical_pool_rows(w.seed, synth.TAG_V, w.layout, b, Hkv * D, 1.0)[:L])
+        K, V = K.reshape(L, Hkv, D), V.reshape(L, Hkv, D)
+        t = torch.arange(L)
+        pos = L - Q + torch.arange(Q)                       # logical position of each query
+        see = t[None, :] <= pos[:, None]
+        if w.window > 0:
+            see &= t[None, :] > pos[:, None] - w.window
+        for h in range(Hq):
+            s = (q[b, :, h, :] @ K[:, h // G, :].T) * w.scale  # [Q, L]
+            s = s.masked_fill(~see, -math.inf)
+            for i in range(Q):
+                if see[i].any():
+                    o[b, i, h] = torch.softmax(s[i], dim=0) @ V[:, h // G, :]
+                    lse[b, i, h] = torch.logsumexp(s[i], dim=0)
+    return o.numpy(), lse.numpy()
+
+
 def logical_cache(w: synth.MLAWorkload, b: int) -> np.ndarray:
     L = int(w.layout.context_lens[b])
     return _logical_pool_rows(w.seed, synth.TAG_CACHE, w.layout, b, synth.MLA_CDIM, 1.0)[:L]
