@@ -47,8 +47,8 @@ CLEAN_BYTES = 512 << 20
 DEFAULT_WORKLOAD = "qwen3-32b"
 WORKLOADS = ["tiny", "llama3-8b", "qwen3-32b", "hd256-window", "mla", "kv-write", "qwen3-32b-verify4"]
 # sources of the kernel each roofline line profiles (a change voids its committed ncu traffic)
-KERNEL_SOURCES = {"gqa": ("pa_gqa.cuh", "pa_common.cuh"),
-                  "mla": ("pa_mla.cu", "pa_plan.cu", "pa_plan.cuh", "pa_common.cuh")}
+KERNEL_SOURCES = {"gqa": ("pa_gqa.cuh", "pa_partition.cuh", "pa_common.cuh"),
+                  "mla": ("pa_mla_tc.cuh", "pa_mla.cu", "pa_partition.cuh", "pa_common.cuh")}
 
 
 def parse():
@@ -87,6 +87,15 @@ def measured_peaks():
         return float(p["hbm_gbs"]), "measured"
     except Exception:
         return 6800.0, "fallback"
+
+
+def measured_bf16_tflops():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
 
 
 def kernel_hash(kind: str = "gqa") -> str:
@@ -417,7 +426,7 @@ def run_ours(args, rank, local_rank, world):
         "config": dict(cfg, num_splits=args.num_splits or "auto", parallelism=f"replicas x{world}",
                        l2="between timed calls, outside the timed events: a 512 MB buffer written, then another 512 MB read"),
         "roofline": {"bound": "alu" if is_mla else "hbm",
-                     "kernel": "kv_write_kernel" if is_write else "mla_split_kernel" if is_mla else "gqa_split_kernel",
+                     "kernel": "kv_write_kernel" if is_write else "mla_tc_split_kernel" if is_mla else "gqa_split_kernel",
                      "achieved": round(kernel_gbs, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(kernel_gbs / peak, 4), "peak_source": f"hbm_gbs of {peak_kind}",
                      "kernel_us": round(kms * 1000, 2), "traffic": ncu_traffic(args.workload)},
@@ -428,14 +437,16 @@ def run_ours(args, rank, local_rank, world):
         "clocks": clocks.summary(),
     }
     if is_mla:
-        # the MLA attention core runs on the CUDA cores: report it against the FP32 FMA peak too
+        # the MLA attention core is a tensor-core contraction: its roofline is the bf16 tensor peak
+        # (the algorithmic flops: 2 x (576 + 512) per (head, visible token); the kernel also spends
+        # 2 x 512 more on the low half of q_lat, not counted)
         flops = 2.0 * w.visible_tokens() * w.num_heads * (576 + 512)
-        sm_clock = line["clocks"]["sm_mhz"] or 1900.0
-        fp32_peak = 152 * 128 * 2 * sm_clock * 1e6 / 1e12
-        line["roofline"].update({"alu_tflops": round(flops / (kms * 1e-3) / 1e12, 2),
-                                 "alu_peak_tflops": round(fp32_peak, 1),
-                                 "alu_frac": round(flops / (kms * 1e-3) / 1e12 / fp32_peak, 4),
-                                 "alu_peak_source": "152 SMs x 128 FP32 lanes x 2 x median SM clock"})
+        tf_peak, tf_kind = measured_bf16_tflops()
+        achieved = flops / (kms * 1e-3) / 1e12
+        line["roofline"].update({"bound": "tensor", "achieved": round(achieved, 2), "peak": tf_peak,
+                                 "unit": "TFLOP/s", "frac": round(achieved / tf_peak, 4),
+                                 "peak_source": f"bf16_tflops of {tf_kind} (cuBLAS bf16 burst)",
+                                 "hbm_gbs": round(kernel_gbs, 2), "hbm_frac": round(kernel_gbs / peak, 4)})
     if not args.no_cpu_baseline:
         v, desc, cores = cpu_oracle_time(w, args.workload)
         line["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",

@@ -57,9 +57,8 @@
  *     flattened row by row, are cut into that many equal contiguous shares,
  *     each handled by one CTA and merged in ascending order where a sequence
  *     spans several shares; 0 = automatic (one share per SM, at most 256),
- *     n in [1, 4096] = n shares.  MLA: 0 = automatic (page-aligned chunks
- *     balanced over the SMs); n > 0 = every row is cut into n page-aligned
- *     chunks of ceil(pages / n) pages, trailing chunks possibly empty.  For a
+ *     n in [1, 4096] = n shares; MLA the same, its sequences being (row, 16-head
+ *     tile) over the one latent cache row.  For a
  *     fixed num_splits (and fixed inputs) results are bitwise reproducible
  *     from run to run and independent of the physical page order; different
  *     split counts agree within rounding.
@@ -69,7 +68,8 @@
  *     calls sharing one workspace must be ordered on one stream.  The GQA
  *     workspace depends on head_dim and num_splits only (two fp32 partial
  *     results of 16 heads per share: 16 KB per share at head_dim 128, about
- *     4.2 MB in automatic mode); the MLA one grows with batch and context.
+ *     4.2 MB in automatic mode); the MLA one adds q_abs and o_lat in bf16
+ *     (2.2 KB per (row, head)) to its 64 KB per share.
  */
 #ifndef PA_DECODE_H
 #define PA_DECODE_H
@@ -165,7 +165,7 @@ int pa_verify_gqa(const void *q, const void *k_pool, const void *v_pool,
  *   block_table, context_lens as for GQA (one latent head shared by all heads)
  *   out          [batch, num_heads, 128] bf16 (written)
  *   lse          [batch, num_heads] fp32 (written), or NULL
- * page_size a power of two in [1, 256]; num_splits in [0, 1024] (chunks per row, see above).
+ * page_size a power of two in [8, 256]; num_splits as for GQA (shares, in [0, 4096]).
  */
 int pa_decode_mla_absorbed(const void *q, const void *cache, const void *w_uk, const void *w_uv,
                            const int32_t *block_table, const int32_t *context_lens, void *out,

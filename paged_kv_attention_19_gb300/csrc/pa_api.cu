@@ -15,7 +15,6 @@
 #include "pa_gqa.cuh"
 #include "pa_launch.h"
 #include "pa_mla.h"
-#include "pa_plan.cuh"
 
 namespace {
 

@@ -18,28 +18,10 @@ namespace pa {
 
 // Workspace header, at offset 0 of every workspace.
 struct WsHeader {
-  uint32_t status;        // PA_DEV_* bits, OR-ed by kernels
-  uint32_t item_counter;  // dynamic work queue cursor (reset by the plan kernel)
-  uint32_t n_items;       // items emitted by the plan kernel
-  uint32_t chunk_pages;   // chunk length chosen by the plan (auto mode)
-  uint32_t pad[60];
+  uint32_t status;  // PA_DEV_* bits of the last call (written by its combine kernel)
+  uint32_t pad[63];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
-
-// Work item of the split-KV kernels: one (row, head subgroup) and a
-// page-aligned chunk [page_begin, page_end) of the row's visible pages, with
-// the row facts the kernels need (so fetching an item is a single load).
-struct WorkItem {
-  int32_t b;
-  int32_t sub;        // KV head x head subgroup (GQA) / head group (MLA)
-  int32_t split;      // chunk index within the row
-  int32_t page_begin;
-  int32_t page_end;
-  int32_t tok_lo;     // attended tokens of the chunk: [tok_lo, tok_hi)
-  int32_t tok_hi;
-  int32_t splits;     // (row's split count << 16) | row's non-empty split count
-};
-static_assert(sizeof(WorkItem) == 32, "work item is 32 bytes");
 
 constexpr unsigned FULL = 0xffffffffu;
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;  // 1 s: far beyond any legal wait

@@ -48,6 +48,7 @@
 #pragma once
 
 #include "pa_common.cuh"
+#include "pa_partition.cuh"
 
 namespace pa {
 
@@ -118,10 +119,9 @@ static_assert(sizeof(StageMeta) == 64, "stage meta is 64 bytes");
 // Small shared state of a CTA outside the ring.
 struct GqaMisc {
   uint32_t status;
-  int32_t found_b;
-  long long found_off;
+  int32_t pad[3];
   GqaPartDesc desc;
-  long long warp_part[10];
+  PartitionState part;
 };
 
 template <class C>
@@ -144,16 +144,6 @@ __device__ __forceinline__ uint32_t kv_off(int tok, int chunk) {
   return (uint32_t)((chunk >> 3) * C::PLANE + tok * 128 + (((chunk & 7) ^ (tok & 7)) << 4));
 }
 
-// Units of a row of length L that some of its Q query positions attend to:
-// [*u_lo, u_lo + return value), the union of the positions' key ranges.
-__device__ __forceinline__ int row_units(int L, int Q, int window, int log2_bh, int *u_lo) {
-  const int lo = window > 0 ? max(L - Q + 1 - window, 0) : 0;
-  *u_lo = lo >> log2_bh;
-  return L > 0 ? ((L + (1 << log2_bh) - 1) >> log2_bh) - *u_lo : 0;
-}
-
-__device__ __forceinline__ int clamp_len(int L, int max_len) { return min(max(L, 0), max_len); }
-
 // Tile t of a KV head's query rows: positions [i0, i0 + nq), heads [h0, h0 + nh) of the
 // group (h0 relative to the group's first head).  MMA row r is position i0 + r / gt, head
 // h0 + r % gt; it is a real row when r / gt < nq and r % gt < nh.
@@ -175,52 +165,6 @@ __device__ __forceinline__ Tile tile_of(int t, int G, int nsub, int Q, int qt) {
   }
   return x;
 }
-
-// Keys of query position i of a row of length L holding Q new tokens: [lo, hi) with
-// hi = L - Q + 1 + i (the position itself included) and lo = max(0, hi - window) under a window.
-__device__ __forceinline__ int pos_hi(int L, int Q, int i) { return max(L - Q + 1 + i, 0); }
-__device__ __forceinline__ int pos_lo(int L, int Q, int i, int window) {
-  return window > 0 ? max(pos_hi(L, Q, i) - window, 0) : 0;
-}
-
-// Block-wide sum / exclusive scan of 64-bit values (all threads of the CTA take part).
-__device__ __forceinline__ long long block_sum64(long long v, long long *warp_part) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
-  if (lane == 0) warp_part[warp] = v;
-  __syncthreads();
-  long long t = 0;
-  for (int w = 0; w < nw; ++w) t += warp_part[w];
-  __syncthreads();
-  return t;
-}
-
-__device__ __forceinline__ long long block_scan64(long long v, long long *excl, long long *warp_part) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  long long x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const long long y = __shfl_up_sync(FULL, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) warp_part[warp] = x;
-  __syncthreads();
-  long long before = 0, t = 0;
-  for (int w = 0; w < nw; ++w) {
-    if (w < warp) before += warp_part[w];
-    t += warp_part[w];
-  }
-  __syncthreads();
-  *excl = before + x - v;
-  return t;
-}
-
-// One piece: units [ub, ue) of sequence (b, hs); lo / L: the row's visible token range.
-struct Piece {
-  int b, hs, ub, ue, lo, L;
-  bool starts, ends;
-};
 
 // MQ: several query positions per row (verify); false compiles the decode-only row logic.
 template <int D, bool MQ>
@@ -247,7 +191,6 @@ __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
     }
     fence_mbar_init();
     misc->status = 0;
-    misc->found_b = -1;
   }
   if (warp == C::NCW && lane == 0) {
     prefetch_tensormap(&tm_k);
@@ -260,82 +203,19 @@ __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
   uint32_t *status = &misc->status;
 
   // ---------------------------------------------- prologue: this CTA's range
-  // The CTAs form NG groups of HG = min(HS, nparts) consecutive CTAs; CTA r of a group
-  // serves KV-head subgroups r, r + HG, ... .  A row's column cost is w_b = n_b +
-  // piece_cost units (0 when n_b == 0); the column axis (rows in order) is cut into NG
-  // equal ranges, one per group, so the HG CTAs of a group stream the same pages (each
-  // its own head) at about the same time and every CTA streams the same cost.  A position
-  // inside the first piece_cost units of a row maps to no key: those units stand for the
-  // fixed cost of a piece (its query stage, the merge at its end).  With NG >= 2 each CTA
-  // serves exactly one subgroup (HG == HS); with NG == 1 every piece is a whole sequence.
-  auto seq_cost = [&](int L, int *n_out) {
-    int ul;
-    const int n = row_units(L, a.Q, a.window, a.log2_bh, &ul);
-    *n_out = n;
-    return n > 0 ? n + a.piece_cost : 0;
-  };
-  const int HG = a.hg, NG = a.nparts / a.hg;
-  const int grp = (int)blockIdx.x / HG, hr = (int)blockIdx.x % HG;
-  const bool member = grp < NG;  // CTAs past the last full group get no work
-  long long W = 0;  // total column cost
-  if (a.batch <= C::THREADS) {
-    // one pass: every row in one thread
-    long long v = 0;
-    if (tid < a.batch) {
-      const int L0 = a.context_lens[tid];
-      if (L0 < 0 || L0 > a.max_context_len) atomicOr(status, PA_DEV_BAD_LEN);
-      int n;
-      v = seq_cost(clamp_len(L0, a.max_context_len), &n);
-    }
-    long long ex;
-    W = block_scan64(v, &ex, misc->warp_part);
-    const long long xb = (long long)grp * W / NG, xe = ((long long)grp + 1) * W / NG;
-    if (member && v > 0 && xb >= ex && xb < ex + v && xb < xe) {
-      misc->found_b = tid;
-      misc->found_off = xb - ex;
-    }
-  } else {
-    long long local = 0;
-    for (int b = tid; b < a.batch; b += C::THREADS) {
-      const int L0 = a.context_lens[b];
-      if (L0 < 0 || L0 > a.max_context_len) atomicOr(status, PA_DEV_BAD_LEN);
-      int n;
-      local += seq_cost(clamp_len(L0, a.max_context_len), &n);
-    }
-    W = block_sum64(local, misc->warp_part);
-    const long long xb = (long long)grp * W / NG, xe = ((long long)grp + 1) * W / NG;
-    if (member && xb < xe) {
-      long long base = 0;
-      for (int b0 = 0; b0 < a.batch; b0 += C::THREADS) {
-        const int b = b0 + tid;
-        long long v = 0;
-        if (b < a.batch) {
-          int n;
-          v = seq_cost(clamp_len(a.context_lens[b], a.max_context_len), &n);
-        }
-        long long ex;
-        const long long tot = block_scan64(v, &ex, misc->warp_part);
-        if (v > 0 && xb >= base + ex && xb < base + ex + v) {
-          misc->found_b = b;
-          misc->found_off = xb - base - ex;
-        }
-        base += tot;
-        __syncthreads();
-        if (misc->found_b >= 0) break;
-      }
-    }
-  }
-  const long long x_begin = member ? (long long)grp * W / NG : 0;
-  const long long x_end = member ? ((long long)grp + 1) * W / NG : 0;
-  // rows without a visible key: out = 0, lse = -inf (rows b = blockIdx.x mod nparts)
-  for (int b = blockIdx.x; b < a.batch; b += a.nparts) {
-    int ul;
-    if (row_units(clamp_len(a.context_lens[b], a.max_context_len), a.Q, a.window, a.log2_bh, &ul) != 0) continue;
-    uint4 *o = reinterpret_cast<uint4 *>(a.out + (size_t)b * a.Q * a.Hq * D);
-    for (int e = tid; e < a.Q * a.Hq * D / 8; e += C::THREADS) o[e] = make_uint4(0, 0, 0, 0);
-    if (a.lse)
-      for (int h = tid; h < a.Q * a.Hq; h += C::THREADS) a.lse[(size_t)b * a.Q * a.Hq + h] = -INFINITY;
-  }
+  PartitionArgs pargs;
+  pargs.context_lens = a.context_lens;
+  pargs.batch = a.batch;
+  pargs.max_context_len = a.max_context_len;
+  pargs.Q = a.Q;
+  pargs.window = a.window;
+  pargs.log2_bh = a.log2_bh;
+  pargs.piece_cost = a.piece_cost;
+  pargs.nparts = a.nparts;
+  pargs.hg = a.hg;
+  pargs.hs = HS;
+  partition_prologue<C::THREADS>(pargs, &misc->part, status);
+  zero_empty_rows<C::THREADS>(pargs, a.out, a.lse, a.Q * a.Hq * D, a.Q * a.Hq);
   __syncthreads();
 
   if (warp == C::NCW) {
@@ -344,65 +224,11 @@ __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
     const int nbox = C::ST >> a.log2_bh;  // boxes (units) per stage
     uint32_t j = 0;
     bool ok = true;
-    const int b_first = max(misc->found_b, 0);
-    const int in_first = misc->found_b >= 0 ? (int)misc->found_off : 0;
-    long long R = misc->found_b >= 0 ? x_end - x_begin : 0;  // column cost still to walk for it_hs
     int npieces = 0;
     Piece last_piece = {};
     bool first_ends = false;
-    // lens window: lane l holds the clamped length of row rb + l
-    int rb = b_first;
-    int lwin = rb + lane < a.batch ? clamp_len(a.context_lens[rb + lane], a.max_context_len) : 0;
-    auto len_of = [&](int row) {
-      if (row < rb || row >= rb + 32) {
-        rb = row;
-        lwin = rb + lane < a.batch ? clamp_len(a.context_lens[rb + lane], a.max_context_len) : 0;
-      }
-      return __shfl_sync(FULL, lwin, row - rb);
-    };
-    // walk position: subgroup it_hs, row it_b, `it_in` cost units into the row
-    int it_hs = hr, it_b = b_first, it_in = in_first;
-    // the next piece that holds at least one key; false once the range is walked for every
-    // subgroup of this CTA
-    auto take_piece = [&](Piece &p) {
-      while (true) {
-        if (R == 0) {
-          it_hs += HG;
-          if (misc->found_b < 0 || it_hs >= HS) return false;
-          R = x_end - x_begin;
-          it_b = b_first;
-          it_in = in_first;
-        }
-        const int L = len_of(it_b);
-        int n;
-        const int w = seq_cost(L, &n);
-        const int take = (int)min((long long)(w - it_in), R);
-        const int u0 = max(0, it_in - a.piece_cost), u1 = max(0, it_in + take - a.piece_cost);
-        const int b = it_b;
-        R -= take;
-        it_in += take;
-        if (it_in == w && R > 0) {
-          it_in = 0;
-          int nn;
-          do {
-            ++it_b;
-          } while (it_b < a.batch - 1 && seq_cost(len_of(it_b), &nn) == 0);
-        }
-        if (u1 > u0) {
-          int ul;
-          row_units(L, a.Q, a.window, a.log2_bh, &ul);
-          p.b = b;
-          p.hs = it_hs;
-          p.L = L;
-          p.lo = pos_lo(L, a.Q, 0, a.window);
-          p.ub = ul + u0;
-          p.ue = ul + u1;
-          p.starts = u0 == 0;
-          p.ends = u1 == n;
-          return true;
-        }
-      }
-    };
+    PieceWalker walker(pargs, &misc->part, lane);
+    auto take_piece = [&](Piece &pc) { return walker.take(pc); };
     auto tile = [&](const Piece &p) { return tile_of(p.hs % a.ntile, a.G, a.nsub, a.Q, a.qt); };
     // block-table window 0 of a piece (lane l: entry l of its first page)
     auto piece_window = [&](const Piece &p) {

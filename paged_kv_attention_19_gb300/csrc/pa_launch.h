@@ -10,10 +10,8 @@ void note_launches(int n);
 cudaError_t profile_mark(bool before, cudaStream_t stream);
 
 struct GqaArgs;
-struct PlanArgs;
 struct CombineArgs;
 
-cudaError_t launch_plan(const PlanArgs &a, cudaStream_t stream);
 cudaError_t launch_gqa_split_d64(int grid, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const CUtensorMap &tm_q,
                                   const GqaArgs &a,
                                  cudaStream_t stream);

@@ -121,6 +121,7 @@ def test_mla_host_validation(pa):
     assert _mla(pa, batch=0) == pa.PA_OK
     assert _mla(pa, h=0) == pa.PA_ERR_INVALID_ARGUMENT
     assert _mla(pa, p=48) == pa.PA_ERR_UNSUPPORTED
+    assert _mla(pa, p=4) == pa.PA_ERR_UNSUPPORTED
     assert _mla(pa, wk=None) == pa.PA_ERR_INVALID_ARGUMENT
     assert _mla(pa, maxp=4) == pa.PA_ERR_INVALID_ARGUMENT
     assert _mla(pa, c=0x20004) == pa.PA_ERR_MISALIGNED

@@ -16,7 +16,7 @@ def test_small_all_rows(H):
     gu.check_mla(w, o, l)
 
 
-@pytest.mark.parametrize("P", [8, 16, 32, 64, 128])
+@pytest.mark.parametrize("P", [8, 16, 32, 64, 128, 256])
 def test_page_sizes(P):
     w = synth.make_mla(1100 + P, [1, 31, 33, 200, 700], 8, P)
     o, l = gu.MlaDev(w).run()
