@@ -4,16 +4,18 @@
 // decode kernel" (Schedule section, steps 1-7) and the vllm.cpp kernel-matrix row
 // KERNEL-ATTN-MLA-SPARSE (absorption = two batched contractions around a split-KV decode
 // with a fixed ascending merge):
-//   1. q_abs = (q_nope . W_UK) || q_rope, q_lat as a bf16 hi + lo pair  [q_absorb_kernel]
+//   1. q_abs = bf16(q_nope . W_UK) || q_rope, and the rounding remainder q_lo  [q_absorb_kernel]
 //   2-6. scores over the 576-wide latent || rope cache, online softmax,
 //        o_lat = sum_t p_t c_t[0:512], per piece of the balanced partition
 //                                                                   [mla_tc_split_kernel]
 //   merge of split sequences, ascending, o_lat rounded to bf16      [gqa_combine_kernel<512>]
-//   7. o = W_UV . o_lat                                             [mla_uv_kernel]
+//   7. o = W_UV . o_lat; lse += scale * q_lo . o_lat                [mla_uv_kernel]
 // Differences from the pages' kernel, all deliberate: scores, probabilities and the
 // softmax state stay fp32; the context is walked once with an online max instead of
-// twice.  q_lat enters the tensor-core scores as hi + lo bf16 parts (about 16 significant
-// bits); o_lat is rounded to bf16 as the operand of step 7.
+// twice.  q_lat enters the tensor-core scores rounded to bf16; the rounding's first-order
+// effect on the LSE (scale * q_lo . o_lat, up to ~1e-3 for short rows) is added back in step
+// 7, its effect on o_lat stays within the output tolerance.  o_lat is rounded to bf16 as the
+// operand of step 7.
 #include <cudaTypedefs.h>
 
 #include <cmath>
@@ -26,17 +28,17 @@
 namespace pa {
 
 constexpr int MLA_NOPE = 128, MLA_QD = 192, MLA_LAT = 512, MLA_C = 576, MLA_V = 128;
-constexpr int MLA_QA = 1088;  // q_abs row: q_lat hi (512) | q_lat lo (512) | q_rope (64)
 
 __device__ __forceinline__ uint32_t pack_u16(uint16_t lo, uint16_t hi) {
   return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
-// q_lat[b][h][j] = sum_d q_nope[b][h][d] * W_UK[h][d][j] (fp32), stored in q_abs as
-// hi = bf16(q_lat) at [0:512] and lo = bf16(q_lat - hi) at [512:1024]; q_rope at [1024:1088].
+// q_lat[b][h][j] = sum_d q_nope[b][h][d] * W_UK[h][d][j] (fp32): q_abs[b][h] = bf16(q_lat) ||
+// q_rope (576) and q_lo[b][h] = bf16(q_lat - bf16(q_lat)) (512, for the LSE term of the
+// projection kernel).
 // Grid (H, 4 chunks of 128 j), 4 warps; the batch rows are the M dimension of the MMAs.
 __global__ void __launch_bounds__(128) q_absorb_kernel(const uint16_t *q, const uint16_t *w_uk, uint16_t *q_abs,
-                                                       int B, int H) {
+                                                       uint16_t *q_lo, int B, int H) {
   __shared__ __align__(16) uint16_t w[MLA_NOPE][128];
   pdl_launch_dependents();  // the split kernel may start its prologue; it waits for q_abs
   const int h = blockIdx.x, j0 = blockIdx.y * 128;
@@ -50,7 +52,7 @@ __global__ void __launch_bounds__(128) q_absorb_kernel(const uint16_t *q, const 
     // the rope part is copied as it is (8 vectors of 16 bytes per row)
     for (int i = tid; i < B * 8; i += 128) {
       const int b = i >> 3, c = i & 7;
-      *reinterpret_cast<uint4 *>(q_abs + ((size_t)b * H + h) * MLA_QA + 2 * MLA_LAT + c * 8) =
+      *reinterpret_cast<uint4 *>(q_abs + ((size_t)b * H + h) * MLA_C + MLA_LAT + c * 8) =
           *reinterpret_cast<const uint4 *>(q + ((size_t)b * H + h) * MLA_QD + MLA_NOPE + c * 8);
     }
   }
@@ -88,23 +90,22 @@ __global__ void __launch_bounds__(128) q_absorb_kernel(const uint16_t *q, const 
       const uint32_t l0 = pack_bf16x2(acc[nt][0] - __uint_as_float(h0 << 16), acc[nt][1] - __uint_as_float(h0 & 0xffff0000u));
       const uint32_t l1 = pack_bf16x2(acc[nt][2] - __uint_as_float(h1 << 16), acc[nt][3] - __uint_as_float(h1 & 0xffff0000u));
       if (r0 < B) {
-        uint16_t *row = q_abs + ((size_t)r0 * H + h) * MLA_QA;
-        *reinterpret_cast<uint32_t *>(row + col) = h0;
-        *reinterpret_cast<uint32_t *>(row + MLA_LAT + col) = l0;
+        *reinterpret_cast<uint32_t *>(q_abs + ((size_t)r0 * H + h) * MLA_C + col) = h0;
+        *reinterpret_cast<uint32_t *>(q_lo + ((size_t)r0 * H + h) * MLA_LAT + col) = l0;
       }
       if (r1 < B) {
-        uint16_t *row = q_abs + ((size_t)r1 * H + h) * MLA_QA;
-        *reinterpret_cast<uint32_t *>(row + col) = h1;
-        *reinterpret_cast<uint32_t *>(row + MLA_LAT + col) = l1;
+        *reinterpret_cast<uint32_t *>(q_abs + ((size_t)r1 * H + h) * MLA_C + col) = h1;
+        *reinterpret_cast<uint32_t *>(q_lo + ((size_t)r1 * H + h) * MLA_LAT + col) = l1;
       }
     }
   }
 }
 
 // o[b][h][v] = sum_j W_UV[h][v][j] o_lat[b][h][j] on the tensor cores.  One block per head,
-// 4 warps (warp w: v in [32 w, 32 w + 32)); 16 batch rows per MMA tile.
+// 4 warps (warp w: v in [32 w, 32 w + 32)); 16 batch rows per MMA tile.  With lse, it also adds
+// the first-order LSE term of q_lat's bf16 rounding: lse += scale * (q_lo . o_lat).
 __global__ void __launch_bounds__(128) mla_uv_kernel(const uint16_t *o_lat, const uint16_t *w_uv, uint16_t *out,
-                                                     int B, int H) {
+                                                     const uint16_t *q_lo, float *lse, float scale, int B, int H) {
   __shared__ __align__(16) uint16_t ol[16][MLA_LAT + 8];
   pdl_wait();  // o_lat (split and combine kernels) is visible from here on
   const int h = blockIdx.x;
@@ -120,6 +121,33 @@ __global__ void __launch_bounds__(128) mla_uv_kernel(const uint16_t *o_lat, cons
       *reinterpret_cast<uint4 *>(&ol[r][c * 8]) = v;
     }
     __syncthreads();
+    if (lse) {
+      // warp w: rows 4 w .. 4 w + 3; lane l: dims [16 l, 16 l + 16)
+      for (int r = warp * 4; r < warp * 4 + 4; ++r) {
+        const int b = m0 + r;
+        if (b >= B) break;
+        const uint16_t *ql = q_lo + ((size_t)b * H + h) * MLA_LAT + lane * 16;
+        float d = 0.f;
+#pragma unroll
+        for (int e = 0; e < 16; e += 8) {
+          const uint4 qv = *reinterpret_cast<const uint4 *>(ql + e);
+          const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t ow = *reinterpret_cast<const uint32_t *>(&ol[r][lane * 16 + e + 2 * i]);
+            d += __uint_as_float(qw[i] << 16) * __uint_as_float(ow << 16) +
+                 __uint_as_float(qw[i] & 0xffff0000u) * __uint_as_float(ow & 0xffff0000u);
+          }
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) d += __shfl_xor_sync(FULL, d, o);
+        if (lane == 0) {
+          const size_t bh = (size_t)b * H + h;
+          const float l = lse[bh];
+          if (l != -INFINITY) lse[bh] = l + scale * d;
+        }
+      }
+    }
     float acc[4][4];
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
@@ -172,11 +200,11 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 struct MlaPlan {
   int ntile, nparts_max;
-  size_t off_desc, off_part_lse, off_part_o, off_qabs, off_olat, total;
+  size_t off_desc, off_part_lse, off_part_o, off_qabs, off_qlo, off_olat, total;
 };
 
 // The workspace: header, one descriptor per share, two fp32 partial slots (16 heads x 512)
-// per share, q_abs [B, H, 1088] bf16 and o_lat [B, H, 512] bf16.
+// per share, q_abs [B, H, 576], q_lo [B, H, 512] and o_lat [B, H, 512], all bf16.
 int mla_shape(int batch, int H, int max_ctx, int P, int num_splits, MlaPlan *pl) {
   if (batch < 0 || H <= 0 || max_ctx < 0 || num_splits < 0) return PA_ERR_INVALID_ARGUMENT;
   if (num_splits > kMaxSplits) return PA_ERR_UNSUPPORTED;
@@ -192,7 +220,9 @@ int mla_shape(int batch, int H, int max_ctx, int P, int num_splits, MlaPlan *pl)
   pl->off_part_o = off;
   off = round_up(off + np * 2 * PART_HEADS * (size_t)MLA_LAT * sizeof(float), 256);
   pl->off_qabs = off;
-  off = round_up(off + B * (size_t)H * MLA_QA * 2, 256);
+  off = round_up(off + B * (size_t)H * MLA_C * 2, 256);
+  pl->off_qlo = off;
+  off = round_up(off + B * (size_t)H * MLA_LAT * 2, 256);
   pl->off_olat = off;
   off = round_up(off + B * (size_t)H * MLA_LAT * 2, 256);
   pl->total = off;
@@ -226,12 +256,12 @@ bool encode_cache_map(CUtensorMap *m, const void *base, int num_pages, int P, in
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D map over q_abs [rows, 1088] bf16; box = (64 dims, 16 rows), 128-byte swizzle.
+// 2-D map over q_abs [rows, 576] bf16; box = (64 dims, 16 rows), 128-byte swizzle.
 bool encode_qabs_map(CUtensorMap *m, const void *base, long long rows) {
   auto fn = mla_encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)MLA_QA, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)MLA_QA * 2};
+  cuuint64_t dims[2] = {(cuuint64_t)MLA_C, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)MLA_C * 2};
   cuuint32_t box[2] = {64u, (cuuint32_t)PART_HEADS};
   cuuint32_t estr[2] = {1u, 1u};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
@@ -278,6 +308,7 @@ int mla_decode(const void *q, const void *cache, const void *w_uk, const void *w
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   uint16_t *q_abs = reinterpret_cast<uint16_t *>(ws + pl.off_qabs);
   uint16_t *o_lat = reinterpret_cast<uint16_t *>(ws + pl.off_olat);
+  uint16_t *q_lo = reinterpret_cast<uint16_t *>(ws + pl.off_qlo);
   CUtensorMap tm_c, tm_q;
   if (!encode_cache_map(&tm_c, cache, num_pages, P, BH) || !encode_qabs_map(&tm_q, q_abs, (long long)batch * H))
     return PA_ERR_UNSUPPORTED;
@@ -292,7 +323,8 @@ int mla_decode(const void *q, const void *cache, const void *w_uk, const void *w
 
   // 1. q_abs
   q_absorb_kernel<<<dim3(H, MLA_LAT / 128), 128, 0, stream>>>(static_cast<const uint16_t *>(q),
-                                                               static_cast<const uint16_t *>(w_uk), q_abs, batch, H);
+                                                               static_cast<const uint16_t *>(w_uk), q_abs, q_lo, batch,
+                                                               H);
   if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
   ++*launches;
 
@@ -363,7 +395,7 @@ int mla_decode(const void *q, const void *cache, const void *w_uk, const void *w
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = pdl_config(dim3(H), dim3(128), 0, stream, attr);
     if (cudaLaunchKernelEx(&cfg, mla_uv_kernel, (const uint16_t *)o_lat, static_cast<const uint16_t *>(w_uv),
-                           static_cast<uint16_t *>(out), batch, H) != cudaSuccess)
+                           static_cast<uint16_t *>(out), (const uint16_t *)q_lo, lse, scale, batch, H) != cudaSuccess)
       return PA_ERR_CUDA;
   }
   ++*launches;

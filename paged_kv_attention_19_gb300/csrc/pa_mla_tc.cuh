@@ -3,10 +3,10 @@
 // What is computed follows pegainfer PR #938 "warp-cooperative two-pass MLA absorbed
 // decode kernel" (Schedule section, steps 2-6): for each head, scores over the 576-wide
 // latent || rope cache row of every visible token, softmax, and o_lat = sum_t p_t c_t[0:512].
-// The query arrives from the absorb kernel as 1088 bf16 values per head: q_lat split into a
-// high and a low bf16 part (q_lat = hi + lo to about 16 significant bits, so a score is as
-// exact as from an fp32 q_lat: one bf16 rounding of q_lat alone moves the LSE of a short row
-// by ~1e-3) and q_rope; the scores contract [hi | lo | rope] with [latent | latent | rope].
+// The query arrives from the absorb kernel as q_abs = bf16(q_lat) || q_rope (576 values per
+// head).  The rounding of q_lat moves each score by scale * lo . c_t (lo = q_lat - bf16(q_lat)),
+// which shifts the LSE by scale * lo . o_lat to first order (up to ~1e-3 for a short row); the
+// projection kernel adds that term back, which leaves ~1e-6.
 //
 // GB300 mapping: the absorbed core is multi-query attention with one 576-wide KV row per
 // token shared by all heads, so it runs on the split-KV machinery of the GQA kernel
@@ -14,10 +14,10 @@
 // CTA group that streams the same cache pages at about the same time (DRAM once, L2 for
 // the others), and the per-piece partials are merged by the GQA combine kernel (D = 512).
 //   * producer warp: TMA copies of 32-token stages (9 planes of 64 dims x 32 tokens, 128-byte
-//     swizzle, 36 KB) into a 4-stage ring, plus one query stage per piece (17 planes of 16
+//     swizzle, 36 KB) into a 5-stage ring, plus one query stage per piece (9 planes of 16
 //     heads), which the consumers copy into a query area;
 //   * 8 consumer warps = 2 token groups (16 tokens each) x 4 quarters: for the scores each
-//     warp of a group contracts its quarter of the 1088 query dims (17 k-steps of m16n8k16,
+//     warp of a group contracts its quarter of the 576 dims (9 k-steps of m16n8k16,
 //     the 16 heads as M rows, query fragments read from the piece's query area); the four
 //     partial score tiles meet in shared memory and every warp of the group sums them in
 //     the same order, so all four hold identical scores and softmax state.  For P.V each warp
@@ -47,23 +47,21 @@ struct MlaTcArgs {
 struct MlaTcCfg {
   static constexpr int M = PART_HEADS;        // heads per tile (MMA rows)
   static constexpr int DQK = 576, DV = 512;
-  static constexpr int DQ = 1088;             // query dims: q_lat hi (512) | lo (512) | rope (64)
   static constexpr int NQK = DQK / 64;        // 9 swizzle planes per cache row
-  static constexpr int NQQ = DQ / 64;         // 17 planes per query row
   static constexpr int ST = 32;               // tokens per stage
   static constexpr int TW = 16;               // tokens per token group
   static constexpr int TG = ST / TW;          // 2
   static constexpr int DSPLIT = 4;            // warps per token group
   static constexpr int NCW = TG * DSPLIT;     // 8 consumer warps
   static constexpr int THREADS = (NCW + 1) * 32;
-  static constexpr int KSW = DQ / 16 / DSPLIT;   // score k-steps per warp: 17
+  static constexpr int KSW = DQK / 16 / DSPLIT;  // score k-steps per warp: 9
   static constexpr int NT_PV = DV / 8 / DSPLIT;  // P.V n-tiles per warp: 16
   static constexpr int PLANE = ST * 128;         // 4 KB
   static constexpr int STAGE_BYTES = NQK * PLANE;  // 36 KB
   static constexpr int QPLANE = M * 128;         // 2 KB
-  static constexpr int NS = 4;
+  static constexpr int NS = 5;
   static constexpr int SPART = TG * DSPLIT * 32 * 8 * 4;  // partial scores: per warp 32 lanes x 8 floats
-  static_assert(QPLANE * NQQ <= STAGE_BYTES, "the query stage fits a ring slot");
+  static_assert(QPLANE * NQK <= STAGE_BYTES, "the query stage fits a ring slot");
   static_assert(DSPLIT * M * (DV / DSPLIT) * 4 <= STAGE_BYTES, "pairwise merge area fits a stage");
 };
 
@@ -78,7 +76,7 @@ struct MlaTcSmem {
   using C = MlaTcCfg;
   static constexpr int OFF_STAGE = 0;
   static constexpr int OFF_Q = OFF_STAGE + C::NS * C::STAGE_BYTES;   // the piece's query rows
-  static constexpr int OFF_SP = OFF_Q + C::NQQ * C::QPLANE;           // 2 buffers of partial scores
+  static constexpr int OFF_SP = OFF_Q + C::NQK * C::QPLANE;           // 2 buffers of partial scores
   static constexpr int OFF_ML = OFF_SP + 2 * C::SPART;
   static constexpr int OFF_META = OFF_ML + C::M * 2 * 4 * 2;
   static constexpr int OFF_BAR = OFF_META + C::NS * (int)sizeof(StageMeta);
@@ -175,7 +173,7 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
       int cwin = cwin0, wi = 0;
       int fwin = (lane + 32 < npages) ? bt_piece[32 + lane] : 0;
       {
-        // the query stage: q_abs rows b * H + h0 .. + 16, 1088 dims (rows past H are masked)
+        // the query stage: q_abs rows b * H + h0 .. + 16 (rows past H are masked)
         const int s = j % C::NS;
         const uint32_t u = j / C::NS;
         if (u > 0) ok = mbar_wait(&empty[s], (u - 1) & 1, status);
@@ -188,10 +186,10 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
           m.b = cur.b;
           m.hq0 = h0;
           m.ghead = nh;
-          mbar_arrive_expect_tx(&full[s], (uint32_t)(C::NQQ * C::QPLANE));
+          mbar_arrive_expect_tx(&full[s], (uint32_t)(C::NQK * C::QPLANE));
           uint8_t *qdst = smem + S::OFF_STAGE + s * C::STAGE_BYTES;
 #pragma unroll
-          for (int dq = 0; dq < C::NQQ; ++dq)
+          for (int dq = 0; dq < C::NQK; ++dq)
             tma_load_2d(qdst + dq * C::QPLANE, &tm_q, dq * 64, cur.b * a.H + h0, &full[s]);
         }
         __syncwarp();
@@ -287,7 +285,7 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
     const int g8 = lane >> 2, tq = lane & 3;
     const int lm_mat = lane >> 3, lm_row = lane & 7;
     const int tgrp = warp % C::TG;           // token group
-    const int dq4 = warp / C::TG;            // quarter: query k-steps [17 dq4, +17), P.V columns [128 dq4, +128)
+    const int dq4 = warp / C::TG;            // quarter: score dims [144 dq4, +144), P.V columns [128 dq4, +128)
     const int wbase = tgrp * C::TW;
     const int nd0 = dq4 * C::NT_PV;
     float *sm_ml = reinterpret_cast<float *>(smem + S::OFF_ML);
@@ -314,7 +312,7 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
         {
           const uint4 *src = reinterpret_cast<const uint4 *>(smem + S::OFF_STAGE + s * C::STAGE_BYTES);
           uint4 *dst = reinterpret_cast<uint4 *>(smem + S::OFF_Q);
-          for (int e = tid; e < C::NQQ * C::QPLANE / 16; e += C::NCW * 32) dst[e] = src[e];
+          for (int e = tid; e < C::NQK * C::QPLANE / 16; e += C::NCW * 32) dst[e] = src[e];
         }
         named_bar(1, C::NCW * 32);
 #pragma unroll
@@ -325,8 +323,7 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
         if (lane == 0) mbar_arrive(&empty[s]);
         continue;
       }
-      // ---- partial scores over this warp's 272 query dims, for the group's 16 tokens (2 n-tiles);
-      // query k-step ks pairs with cache k-step ks (hi), ks - 32 (lo) or ks - 32 (rope)
+      // ---- partial scores over this warp's 144 dims, for the group's 16 tokens (2 n-tiles)
       float sp[2][4];
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) sp[nt][0] = sp[nt][1] = sp[nt][2] = sp[nt][3] = 0.f;
@@ -337,8 +334,7 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
         ldmatrix_x4(qa, qarea + mla_off(C::QPLANE, (lm_mat & 1) * 8 + lm_row, 2 * ks + (lm_mat >> 1)));
         // matrices: (tokens 0-7, dims 0-7), (tokens 0-7, dims 8-15), (tokens 8-15, ...) of the k-step
         uint32_t b[4];
-        const int cks = ks < 32 ? ks : ks - 32;
-        const int tok = wbase + (lm_mat >> 1) * 8 + lm_row, chunk = 2 * cks + (lm_mat & 1);
+        const int tok = wbase + (lm_mat >> 1) * 8 + lm_row, chunk = 2 * ks + (lm_mat & 1);
         ldmatrix_x4(b, cbase + mla_off(C::PLANE, tok, chunk));
         mma_bf16_16816(sp[0], qa, b[0], b[1]);
         mma_bf16_16816(sp[1], qa, b[2], b[3]);
