@@ -664,7 +664,8 @@ struct CombineArgs {
 // o = sum_k w_k o_k / sum_k w_k in ascending k, each lane owning D/32 dims.
 template <int D>
 __global__ void __launch_bounds__(128) gqa_combine_kernel(const CombineArgs a) {
-  pdl_wait();  // the split kernel's partials and descriptors are visible from here on
+  pdl_wait();               // the split kernel's partials and descriptors are visible from here on
+  pdl_launch_dependents();  // a following kernel (MLA: the W_UV projection) may stage its inputs
   const int c = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (c == 0 && warp == 0) {
     uint32_t s = 0;

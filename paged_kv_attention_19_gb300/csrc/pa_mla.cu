@@ -33,59 +33,88 @@ __device__ __forceinline__ uint32_t pack_u16(uint16_t lo, uint16_t hi) {
   return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
-// q_lat[b][h][j] = sum_d q_nope[b][h][d] * W_UK[h][d][j] (fp32): q_abs[b][h] = bf16(q_lat) ||
-// q_rope (576) and q_lo[b][h] = bf16(q_lat - bf16(q_lat)) (512, for the LSE term of the
-// projection kernel).
-// Grid (H, 4 chunks of 128 j), 4 warps; the batch rows are the M dimension of the MMAs.
-__global__ void __launch_bounds__(128) q_absorb_kernel(const uint16_t *q, const uint16_t *w_uk, uint16_t *q_abs,
-                                                       uint16_t *q_lo, int B, int H) {
-  __shared__ __align__(16) uint16_t w[MLA_NOPE][128];
-  pdl_launch_dependents();  // the split kernel may start its prologue; it waits for q_abs
-  const int h = blockIdx.x, j0 = blockIdx.y * 128;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint16_t *wsrc = w_uk + (size_t)h * MLA_NOPE * MLA_LAT + j0;
-  for (int i = tid; i < MLA_NOPE * 16; i += 128) {
-    const int d = i >> 4, c = i & 15;
-    *reinterpret_cast<uint4 *>(&w[d][c * 8]) = *reinterpret_cast<const uint4 *>(wsrc + (size_t)d * MLA_LAT + c * 8);
-  }
-  if (blockIdx.y == 0) {
-    // the rope part is copied as it is (8 vectors of 16 bytes per row)
-    for (int i = tid; i < B * 8; i += 128) {
-      const int b = i >> 3, c = i & 7;
-      *reinterpret_cast<uint4 *>(q_abs + ((size_t)b * H + h) * MLA_C + MLA_LAT + c * 8) =
-          *reinterpret_cast<const uint4 *>(q + ((size_t)b * H + h) * MLA_QD + MLA_NOPE + c * 8);
-    }
+// Shared-memory rows of the projection weights are padded to 520 bf16 (1040 bytes): the
+// 16-byte offset between consecutive rows keeps fragment loads free of bank conflicts.
+constexpr int WROW = MLA_LAT + 8;
+constexpr int PROJ_SMEM = 128 * WROW * 2 + 16 * WROW * 2 + 16;  // one head's weights, 16 activation rows, a barrier
+
+// Stage 128 rows of 512 bf16 (one head's weights) into padded shared-memory rows with TMA bulk
+// copies (warp 0 issues them, completion counted on *bar).
+__device__ __forceinline__ void stage_weights_issue(uint16_t *w, const uint16_t *src, uint64_t *bar) {
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
   }
   __syncthreads();
+  if (threadIdx.x < 32) {
+    if (threadIdx.x == 0) mbar_arrive_expect_tx(bar, 128u * MLA_LAT * 2);
+    __syncwarp();
+    for (int r = threadIdx.x; r < 128; r += 32) bulk_load(w + r * WROW, src + (size_t)r * MLA_LAT, MLA_LAT * 2, bar);
+  }
+}
+
+// q_lat[b][h][j] = sum_d q_nope[b][h][d] * W_UK[h][d][j] (fp32): q_abs[b][h] = bf16(q_lat) ||
+// q_rope (576) and q_lo[b][h] = bf16(q_lat - bf16(q_lat)) (512, for the LSE term of the
+// projection kernel).  One block of 8 warps per head: W_UK[h] (128 x 512) is staged in shared
+// memory with coalesced 16-byte loads; the batch rows (16 per tile) are the M dimension of
+// m16n8k16 MMAs, warp w producing latent columns [64 w, 64 w + 64).
+__global__ void __launch_bounds__(256) q_absorb_kernel(const uint16_t *q, const uint16_t *w_uk, uint16_t *q_abs,
+                                                       uint16_t *q_lo, int B, int H) {
+  extern __shared__ __align__(16) uint8_t psmem[];
+  uint16_t *w = reinterpret_cast<uint16_t *>(psmem);        // [128 d][WROW]
+  uint16_t *qn = w + 128 * WROW;                            // [16 rows][WROW] (first 128 used)
+  pdl_launch_dependents();  // the split kernel may start its prologue; it waits for q_abs
+  const int h = blockIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, tq = lane & 3;
+  const int lm_mat = lane >> 3, lm_row = lane & 7;
+  {
+    const uint16_t *wsrc = w_uk + (size_t)h * MLA_NOPE * MLA_LAT;
+    for (int i = tid; i < MLA_NOPE * (MLA_LAT / 8); i += 256) {
+      const int d = i / (MLA_LAT / 8), c = i % (MLA_LAT / 8);
+      *reinterpret_cast<uint4 *>(w + d * WROW + c * 8) = *reinterpret_cast<const uint4 *>(wsrc + (size_t)d * MLA_LAT + c * 8);
+    }
+  }
+  // the rope part is copied as it is (8 vectors of 16 bytes per row)
+  for (int i = tid; i < B * 8; i += 256) {
+    const int b = i >> 3, c = i & 7;
+    *reinterpret_cast<uint4 *>(q_abs + ((size_t)b * H + h) * MLA_C + MLA_LAT + c * 8) =
+        *reinterpret_cast<const uint4 *>(q + ((size_t)b * H + h) * MLA_QD + MLA_NOPE + c * 8);
+  }
   for (int m0 = 0; m0 < B; m0 += 16) {
-    float acc[4][4];
+    for (int i = tid; i < 16 * (MLA_NOPE / 8); i += 256) {
+      const int r = i / (MLA_NOPE / 8), c = i % (MLA_NOPE / 8);
+      const int b = m0 + r;
+      *reinterpret_cast<uint4 *>(qn + r * WROW + c * 8) =
+          b < B ? *reinterpret_cast<const uint4 *>(q + ((size_t)b * H + h) * MLA_QD + c * 8) : make_uint4(0, 0, 0, 0);
+    }
+    __syncthreads();
+    float acc[8][4];
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+    for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
-    const int r0 = m0 + g, r1 = m0 + g + 8;
-    const uint16_t *q0 = q + ((size_t)r0 * H + h) * MLA_QD;
-    const uint16_t *q1 = q + ((size_t)r1 * H + h) * MLA_QD;
 #pragma unroll
     for (int k0 = 0; k0 < MLA_NOPE; k0 += 16) {
       uint32_t af[4];
-      af[0] = r0 < B ? *reinterpret_cast<const uint32_t *>(q0 + k0 + 2 * tq) : 0u;
-      af[1] = r1 < B ? *reinterpret_cast<const uint32_t *>(q1 + k0 + 2 * tq) : 0u;
-      af[2] = r0 < B ? *reinterpret_cast<const uint32_t *>(q0 + k0 + 8 + 2 * tq) : 0u;
-      af[3] = r1 < B ? *reinterpret_cast<const uint32_t *>(q1 + k0 + 8 + 2 * tq) : 0u;
+      {
+        const int row = (lm_mat & 1) * 8 + lm_row, col = k0 + (lm_mat >> 1) * 8;
+        ldmatrix_x4(af, smem_u32(qn + row * WROW + col));
+      }
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        const int n = warp * 32 + nt * 8 + g;
-        uint32_t bf[2];
-        bf[0] = pack_u16(w[k0 + 2 * tq][n], w[k0 + 2 * tq + 1][n]);
-        bf[1] = pack_u16(w[k0 + 8 + 2 * tq][n], w[k0 + 9 + 2 * tq][n]);
+      for (int nt = 0; nt < 8; nt += 2) {
+        // W rows k0..k0+15 (k), columns 64 warp + 8 nt .. + 16 (two n-tiles), transposed
+        uint32_t bf[4];
+        const int krow = k0 + (lm_mat & 1) * 8 + lm_row, col = warp * 64 + nt * 8 + (lm_mat >> 1) * 8;
+        ldmatrix_x4_trans(bf, smem_u32(w + krow * WROW + col));
         mma_bf16_16816(acc[nt], af, bf[0], bf[1]);
+        mma_bf16_16816(acc[nt + 1], af, bf[2], bf[3]);
       }
     }
+    const int r0 = m0 + g, r1 = m0 + g + 8;
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      const int col = j0 + warp * 32 + nt * 8 + 2 * tq;
+    for (int nt = 0; nt < 8; ++nt) {
+      const int col = warp * 64 + nt * 8 + 2 * tq;
       const uint32_t h0 = pack_bf16x2(acc[nt][0], acc[nt][1]), h1 = pack_bf16x2(acc[nt][2], acc[nt][3]);
       const uint32_t l0 = pack_bf16x2(acc[nt][0] - __uint_as_float(h0 << 16), acc[nt][1] - __uint_as_float(h0 & 0xffff0000u));
       const uint32_t l1 = pack_bf16x2(acc[nt][2] - __uint_as_float(h1 << 16), acc[nt][3] - __uint_as_float(h1 & 0xffff0000u));
@@ -98,32 +127,39 @@ __global__ void __launch_bounds__(128) q_absorb_kernel(const uint16_t *q, const 
         *reinterpret_cast<uint32_t *>(q_lo + ((size_t)r1 * H + h) * MLA_LAT + col) = l1;
       }
     }
+    __syncthreads();
   }
 }
 
-// o[b][h][v] = sum_j W_UV[h][v][j] o_lat[b][h][j] on the tensor cores.  One block per head,
-// 4 warps (warp w: v in [32 w, 32 w + 32)); 16 batch rows per MMA tile.  With lse, it also adds
-// the first-order LSE term of q_lat's bf16 rounding: lse += scale * (q_lo . o_lat).
-__global__ void __launch_bounds__(128) mla_uv_kernel(const uint16_t *o_lat, const uint16_t *w_uv, uint16_t *out,
-                                                     const uint16_t *q_lo, float *lse, float scale, int B, int H) {
-  __shared__ __align__(16) uint16_t ol[16][MLA_LAT + 8];
-  pdl_wait();  // o_lat (split and combine kernels) is visible from here on
+// o[b][h][v] = sum_j W_UV[h][v][j] o_lat[b][h][j] on the tensor cores.  One block of 8 warps
+// per head: W_UV[h] (128 x 512) is staged in shared memory with coalesced 16-byte loads; warp
+// w produces v in [16 w, 16 w + 16) for 16 batch rows per tile.  With lse, it also adds the
+// first-order LSE term of q_lat's bf16 rounding: lse += scale * (q_lo . o_lat).
+__global__ void __launch_bounds__(256) mla_uv_kernel(const uint16_t *o_lat, const uint16_t *w_uv, uint16_t *out,
+                                                     const uint16_t *q_lo, float *lse, float scale, int B, int H,
+                                                     uint32_t *status) {
+  extern __shared__ __align__(16) uint8_t psmem[];
+  uint16_t *w = reinterpret_cast<uint16_t *>(psmem);  // [128 v][WROW]
+  uint16_t *ol = w + 128 * WROW;                      // [16 rows][WROW]
+  uint64_t *bar = reinterpret_cast<uint64_t *>(ol + 16 * WROW);
   const int h = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, tq = lane & 3;
-  const uint16_t *wv = w_uv + (size_t)h * MLA_V * MLA_LAT;
+  const int lm_mat = lane >> 3, lm_row = lane & 7;
+  stage_weights_issue(w, w_uv + (size_t)h * MLA_V * MLA_LAT, bar);
+  pdl_wait();  // o_lat, lse and the status word (split and combine kernels) are final from here on
+  mbar_wait(bar, 0, status);
   for (int m0 = 0; m0 < B; m0 += 16) {
-    for (int i = tid; i < 16 * (MLA_LAT / 8); i += 128) {
+    for (int i = tid; i < 16 * (MLA_LAT / 8); i += 256) {
       const int r = i / (MLA_LAT / 8), c = i % (MLA_LAT / 8);
       const int b = m0 + r;
-      const uint4 v = b < B ? *reinterpret_cast<const uint4 *>(o_lat + ((size_t)b * H + h) * MLA_LAT + c * 8)
-                            : make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4 *>(&ol[r][c * 8]) = v;
+      *reinterpret_cast<uint4 *>(ol + r * WROW + c * 8) =
+          b < B ? *reinterpret_cast<const uint4 *>(o_lat + ((size_t)b * H + h) * MLA_LAT + c * 8) : make_uint4(0, 0, 0, 0);
     }
     __syncthreads();
     if (lse) {
-      // warp w: rows 4 w .. 4 w + 3; lane l: dims [16 l, 16 l + 16)
-      for (int r = warp * 4; r < warp * 4 + 4; ++r) {
+      // warp w: rows 2 w, 2 w + 1; lane l: dims [16 l, 16 l + 16)
+      for (int r = warp * 2; r < warp * 2 + 2; ++r) {
         const int b = m0 + r;
         if (b >= B) break;
         const uint16_t *ql = q_lo + ((size_t)b * H + h) * MLA_LAT + lane * 16;
@@ -134,7 +170,7 @@ __global__ void __launch_bounds__(128) mla_uv_kernel(const uint16_t *o_lat, cons
           const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const uint32_t ow = *reinterpret_cast<const uint32_t *>(&ol[r][lane * 16 + e + 2 * i]);
+            const uint32_t ow = *reinterpret_cast<const uint32_t *>(ol + r * WROW + lane * 16 + e + 2 * i);
             d += __uint_as_float(qw[i] << 16) * __uint_as_float(ow << 16) +
                  __uint_as_float(qw[i] & 0xffff0000u) * __uint_as_float(ow & 0xffff0000u);
           }
@@ -148,31 +184,30 @@ __global__ void __launch_bounds__(128) mla_uv_kernel(const uint16_t *o_lat, cons
         }
       }
     }
-    float acc[4][4];
+    float acc[2][4];
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
-#pragma unroll 4
+#pragma unroll 8
     for (int k0 = 0; k0 < MLA_LAT; k0 += 16) {
-      uint32_t af[4];
-      af[0] = *reinterpret_cast<const uint32_t *>(&ol[g][k0 + 2 * tq]);
-      af[1] = *reinterpret_cast<const uint32_t *>(&ol[g + 8][k0 + 2 * tq]);
-      af[2] = *reinterpret_cast<const uint32_t *>(&ol[g][k0 + 8 + 2 * tq]);
-      af[3] = *reinterpret_cast<const uint32_t *>(&ol[g + 8][k0 + 8 + 2 * tq]);
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        const int v = warp * 32 + nt * 8 + g;
-        uint32_t bf[2];
-        bf[0] = *reinterpret_cast<const uint32_t *>(wv + (size_t)v * MLA_LAT + k0 + 2 * tq);
-        bf[1] = *reinterpret_cast<const uint32_t *>(wv + (size_t)v * MLA_LAT + k0 + 8 + 2 * tq);
-        mma_bf16_16816(acc[nt], af, bf[0], bf[1]);
+      uint32_t af[4], bf[4];
+      {
+        const int row = (lm_mat & 1) * 8 + lm_row, col = k0 + (lm_mat >> 1) * 8;
+        ldmatrix_x4(af, smem_u32(ol + row * WROW + col));
       }
+      {
+        // B = W_UV^T: W rows v (the n index), columns k0.. (the k index), not transposed
+        const int vrow = warp * 16 + (lm_mat >> 1) * 8 + lm_row, col = k0 + (lm_mat & 1) * 8;
+        ldmatrix_x4(bf, smem_u32(w + vrow * WROW + col));
+      }
+      mma_bf16_16816(acc[0], af, bf[0], bf[1]);
+      mma_bf16_16816(acc[1], af, bf[2], bf[3]);
     }
     const int r0 = m0 + g, r1 = m0 + g + 8;
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      const int col = warp * 32 + nt * 8 + 2 * tq;
+    for (int nt = 0; nt < 2; ++nt) {
+      const int col = warp * 16 + nt * 8 + 2 * tq;
       if (r0 < B)
         *reinterpret_cast<uint32_t *>(out + ((size_t)r0 * H + h) * MLA_V + col) = pack_bf16x2(acc[nt][0], acc[nt][1]);
       if (r1 < B)
@@ -321,10 +356,21 @@ int mla_decode(const void *q, const void *cache, const void *w_uk, const void *w
   float *part_lse = reinterpret_cast<float *>(ws + pl.off_part_lse);
   float *part_o = reinterpret_cast<float *>(ws + pl.off_part_o);
 
+  static int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    if (cudaFuncSetAttribute(mla_tc_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, MlaTcSmem::BYTES) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(q_absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PROJ_SMEM) != cudaSuccess ||
+        cudaFuncSetAttribute(mla_uv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PROJ_SMEM) != cudaSuccess)
+      return PA_ERR_CUDA;
+    configured_device = dev;
+  }
+
   // 1. q_abs
-  q_absorb_kernel<<<dim3(H, MLA_LAT / 128), 128, 0, stream>>>(static_cast<const uint16_t *>(q),
-                                                               static_cast<const uint16_t *>(w_uk), q_abs, q_lo, batch,
-                                                               H);
+  q_absorb_kernel<<<H, 256, PROJ_SMEM, stream>>>(static_cast<const uint16_t *>(q), static_cast<const uint16_t *>(w_uk),
+                                                  q_abs, q_lo, batch, H);
   if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
   ++*launches;
 
@@ -352,15 +398,6 @@ int mla_decode(const void *q, const void *cache, const void *w_uk, const void *w
   ma.nparts = nparts;
   ma.hg = pl.ntile < nparts ? pl.ntile : nparts;
   ma.qscale = scale * LOG2E;
-  static int configured_device = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_device != dev) {
-    if (cudaFuncSetAttribute(mla_tc_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, MlaTcSmem::BYTES) !=
-        cudaSuccess)
-      return PA_ERR_CUDA;
-    configured_device = dev;
-  }
   if (ev_before && cudaEventRecord(ev_before, stream) != cudaSuccess) return PA_ERR_CUDA;
   {
     cudaLaunchAttribute attr[1];
@@ -393,9 +430,10 @@ int mla_decode(const void *q, const void *cache, const void *w_uk, const void *w
   // 7. o = W_UV . o_lat
   {
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = pdl_config(dim3(H), dim3(128), 0, stream, attr);
+    cudaLaunchConfig_t cfg = pdl_config(dim3(H), dim3(256), PROJ_SMEM, stream, attr);
     if (cudaLaunchKernelEx(&cfg, mla_uv_kernel, (const uint16_t *)o_lat, static_cast<const uint16_t *>(w_uv),
-                           static_cast<uint16_t *>(out), (const uint16_t *)q_lo, lse, scale, batch, H) != cudaSuccess)
+                           static_cast<uint16_t *>(out), (const uint16_t *)q_lo, lse, scale, batch, H,
+                           &hdr->status) != cudaSuccess)
       return PA_ERR_CUDA;
   }
   ++*launches;
