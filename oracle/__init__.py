@@ -220,3 +220,95 @@ def mla_cache_write(c_lat, k_rope, slots, cache):
         out[s // P, s % P, :512] = c_lat[t]
         out[s // P, s % P, 512:] = k_rope[t]
     return out
+
+
+# ----------------------------------------------------------------------------- FP8 (E4M3) KV cache
+# The quantized KV cache of the vllm.cpp kernel-matrix row KERNEL-KV-QUANT ("FP8"), read as: the
+# pools hold FP8 E4M3 codes (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; no
+# infinities; S.1111.111 is NaN; largest finite magnitude 448), and one float scale per pool
+# turns a code into its value: K = decode(code) * k_scale, V = decode(code) * v_scale.
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Value of each E4M3 code (float64), from the format's definition."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    s = np.where(c >> 7, -1.0, 1.0)
+    e = (c >> 3) & 15
+    m = (c & 7).astype(np.float64)
+    val = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7))
+    val = np.where((e == 15) & ((c & 7) == 7), np.nan, val)
+    return s * val
+
+
+_E4M3_POS = e4m3_decode(np.arange(127, dtype=np.uint8))  # finite non-negative codes 0..126, ascending
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """Nearest E4M3 code of each value: round to nearest, ties to the code with an even
+    mantissa, magnitudes above 448 saturate to 448, NaN maps to the NaN code (the saturating
+    conversion of the write step)."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    idx = np.searchsorted(_E4M3_POS, np.minimum(a, 448.0))      # first code >= a
+    hi = np.minimum(idx, 126)
+    lo = np.maximum(hi - 1, 0)
+    d_hi = _E4M3_POS[hi] - np.minimum(a, 448.0)
+    d_lo = np.minimum(a, 448.0) - _E4M3_POS[lo]
+    pick_lo = (d_lo < d_hi) | ((d_lo == d_hi) & ((lo & 1) == 0))
+    code = np.where(pick_lo, lo, hi)
+    code = np.where(a >= 448.0, 126, code)
+    code = code | np.where(np.signbit(x), 0x80, 0)
+    code = np.where(np.isnan(x), 0x7F, code)
+    return code.astype(np.uint8)
+
+
+def kv_write_fp8(k, v, slots, k_pool, v_pool, k_scale: float, v_scale: float):
+    """FP8 paged KV write: token t's bf16 rows k[t], v[t] are divided by the pool's scale in
+    float32 and stored as E4M3 codes at slot slots[t] (negative: padding).  Returns new pools."""
+    kf = synth_bf16_to_f32(k) / np.float32(k_scale)
+    vf = synth_bf16_to_f32(v) / np.float32(v_scale)
+    return kv_write(e4m3_encode(kf.astype(np.float64)), e4m3_encode(vf.astype(np.float64)), slots, k_pool, v_pool)
+
+
+def synth_bf16_to_f32(bits) -> np.ndarray:
+    """bf16 bit patterns (uint16) to float32 values (exact)."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def gqa_fp8(q, k_codes, v_codes, block_table, context_lens, scale: float, k_scale: float, v_scale: float,
+            window: int = 0, rows=None, num_query: int = 1):
+    """GQA decode (or multi-query verify with num_query > 1, q [B, Q, Hq, D]) over an FP8 cache,
+    in float64: the attention of the decode oracle with keys decode(K code) * k_scale and values
+    decode(V code) * v_scale.  Written out per (row, head) with numpy: scores over the row's
+    visible keys, max, exp, sum, weighted values.  Returns (o [n, D], lse [n])."""
+    q = np.asarray(q, dtype=np.uint16)
+    if num_query == 1 and q.ndim == 3:
+        q = q[:, None]
+    B, Q, Hq, D = q.shape
+    npg, P, Hkv, _ = k_codes.shape
+    G = Hq // Hkv
+    qf = synth_bf16_to_f32(q).astype(np.float64)
+    K = e4m3_decode(k_codes) * float(np.float32(k_scale))
+    V = e4m3_decode(v_codes) * float(np.float32(v_scale))
+    bt = np.asarray(block_table, dtype=np.int64)
+    lens = np.asarray(context_lens, dtype=np.int64)
+    if rows is None:
+        rows = [(b, i, h) for b in range(B) for i in range(Q) for h in range(Hq)]
+    elif len(rows) and len(rows[0]) == 2:
+        rows = [(b, 0, h) for b, h in rows]
+    o = np.zeros((len(rows), D))
+    lse = np.full(len(rows), -np.inf)
+    for n, (b, i, h) in enumerate(rows):
+        hi = max(int(lens[b]) - Q + 1 + i, 0)
+        lo = max(hi - window, 0) if window > 0 else 0
+        if hi <= lo:
+            continue
+        t = np.arange(lo, hi)
+        pages = bt[b, t // P]
+        k = K[pages, t % P, h // G]
+        v = V[pages, t % P, h // G]
+        s = float(scale) * (k @ qf[b, i, h])
+        m = s.max()
+        p = np.exp(s - m)
+        o[n] = (p / p.sum()) @ v
+        lse[n] = m + np.log(p.sum())
+    return o, lse
