@@ -45,7 +45,8 @@ METRIC = "µs/call and achieved HBM GB/s (frac of ~8 TB/s) for paged decode atte
 FLUSH_BYTES = 512 << 20
 CLEAN_BYTES = 512 << 20
 DEFAULT_WORKLOAD = "qwen3-32b"
-WORKLOADS = ["tiny", "llama3-8b", "qwen3-32b", "hd256-window", "mla", "kv-write", "qwen3-32b-verify4"]
+WORKLOADS = ["tiny", "llama3-8b", "qwen3-32b", "hd256-window", "mla", "kv-write", "qwen3-32b-verify4",
+             "qwen3-32b-fp8"]
 # sources of the kernel each roofline line profiles (a change voids its committed ncu traffic)
 KERNEL_SOURCES = {"gqa": ("pa_gqa.cuh", "pa_partition.cuh", "pa_common.cuh"),
                   "mla": ("pa_mla_tc.cuh", "pa_mla.cu", "pa_partition.cuh", "pa_common.cuh")}
@@ -133,11 +134,14 @@ def describe(w, name):
     ctx = {"tiny": "fixed{1,31,32,33,64,100}", "llama3-8b": "uniform[512,4096]",
            "qwen3-32b": "loguniform[128,16384]", "hd256-window": "uniform[2048,32768], window 4096",
            "qwen3-32b-verify4": "loguniform[128,16384] (the qwen3-32b lengths), 4 query positions per row, "
-                                "causal among them"}[name]
+                                "causal among them",
+           "qwen3-32b-fp8": "loguniform[128,16384] (the qwen3-32b lengths)"}[name]
     return {"workload": name, "batch": w.batch, "query_positions": w.num_query, "q_heads": w.num_q_heads,
             "kv_heads": w.num_kv_heads,
             "head_dim": w.head_dim, "page_size": w.layout.page_size, "context": ctx, "window": w.window,
-            "visible_tokens": w.visible_tokens(), "algorithmic_bytes": w.algorithmic_bytes(), "seed": w.seed}
+            "visible_tokens": w.visible_tokens(), "algorithmic_bytes": w.algorithmic_bytes(), "seed": w.seed,
+            **({"kv_cache": "fp8 e4m3 codes, per-pool scales", "k_scale": w.k_scale, "v_scale": w.v_scale}
+               if w.fp8 else {"kv_cache": "bf16"})}
 
 
 class ClockSampler:
@@ -220,7 +224,12 @@ class OracleSample:
         win = 0 if is_mla else w.window
         vis = [synth.visible_range(int(L), win, Q) for L in w.layout.context_lens]
         total_work = sum(hi - lo for lo, hi in vis) * H
-        if Q > 1:
+        if not is_mla and w.fp8:
+            self.fn = lambda rows: oracle.gqa_fp8(w.q, w.k_pool, w.v_pool, w.layout.block_table,
+                                                  w.layout.context_lens, w.scale, w.k_scale, w.v_scale, w.window,
+                                                  rows=[(b, i, h) for b, h in rows for i in range(Q)],
+                                                  num_query=Q)
+        elif Q > 1:
             # every query position of a sampled (row, head)
             self.fn = lambda rows: oracle.verify_gqa(w.q, w.k_pool, w.v_pool, w.layout.block_table,
                                                      w.layout.context_lens, w.scale, w.window,
@@ -330,11 +339,16 @@ def run_ours(args, rank, local_rank, world):
         lse = torch.empty(w.q.shape[:-1], dtype=torch.float32, device="cuda")
         ws = pa.workspace_for_gqa(d.q, d.k, d.bt, args.num_splits)
         ins, outs = [d.q, d.bt, d.lens], [out, lse]
-        entry = pa.pa_verify_gqa if w.num_query > 1 else pa.pa_decode_gqa
+        if w.fp8:
+            def call(q, bt, lens):
+                pa.pa_decode_gqa_fp8(q, d.k, d.v, bt, lens, out, lse, scale=w.scale, k_scale=w.k_scale,
+                                     v_scale=w.v_scale, window=w.window, workspace=ws, num_splits=args.num_splits)
+        else:
+            entry = pa.pa_verify_gqa if w.num_query > 1 else pa.pa_decode_gqa
 
-        def call(q, bt, lens):
-            entry(q, d.k, d.v, bt, lens, out, lse, scale=w.scale, window=w.window, workspace=ws,
-                  num_splits=args.num_splits)
+            def call(q, bt, lens):
+                entry(q, d.k, d.v, bt, lens, out, lse, scale=w.scale, window=w.window, workspace=ws,
+                      num_splits=args.num_splits)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     clean = torch.zeros(CLEAN_BYTES // 4, dtype=torch.float32, device="cuda")
 
@@ -421,7 +435,8 @@ def run_ours(args, rank, local_rank, world):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "us_per_call": round(ms * 1000, 2),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16 mma over e4m3 codes, f32 softmax" if getattr(w, "fp8", False) else "bf16",
         "data": "synthetic", "impl": "ours",
         "config": dict(cfg, num_splits=args.num_splits or "auto", parallelism=f"replicas x{world}",
                        l2="between timed calls, outside the timed events: a 512 MB buffer written, then another 512 MB read"),

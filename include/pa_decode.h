@@ -156,6 +156,30 @@ int pa_verify_gqa(const void *q, const void *k_pool, const void *v_pool,
                   cudaStream_t stream);
 
 /*
+ * GQA decode and multi-query verify over an FP8 KV cache (vllm.cpp
+ * kernel-matrix, row KERNEL-KV-QUANT, "FP8": the quantized form of the paged
+ * cache).  The pools hold FP8 E4M3 codes, one byte per value (1 sign bit, 4
+ * exponent bits with bias 7, 3 mantissa bits, no infinities, S.1111.111 NaN,
+ * largest finite 448), and one float scale per pool turns a code into its
+ * value: key = E4M3(code) * k_scale, value = E4M3(code) * v_scale.
+ *   k_pool, v_pool [num_pages, page_size, num_kv_heads, head_dim] uint8 codes
+ *   k_scale, v_scale finite and > 0 (else PA_ERR_INVALID_ARGUMENT)
+ *   num_query    query positions per row as for pa_verify_gqa (1: decode, q of
+ *                shape [batch, num_q_heads, head_dim])
+ * Every other argument, the workspace (pa_workspace_size(PA_KIND_GQA, ...)),
+ * the window and the error codes are those of pa_verify_gqa; head_dim in
+ * {128, 256} (64: PA_ERR_UNSUPPORTED).  The codes widen exactly to f16 for the
+ * tensor cores, q is rounded from bf16 to f16 (|q| must stay below 65504) and
+ * the weights P to f16 as the MMA operand; the softmax stays fp32.
+ */
+int pa_decode_gqa_fp8(const void *q, const void *k_pool, const void *v_pool,
+                      const int32_t *block_table, const int32_t *context_lens, void *out,
+                      float *lse, int batch, int num_query, int num_q_heads, int num_kv_heads,
+                      int head_dim, int page_size, int num_pages, int max_pages_per_seq,
+                      int max_context_len, float scale, float k_scale, float v_scale, int window,
+                      int num_splits, void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * MLA absorbed decode (DeepSeek-V2-style geometry: 128 nope + 64 rope query
  * dims, 512 latent + 64 rope cache dims, 128 value dims per head).
  *   q            [batch, num_heads, 192] bf16: q_nope (128) || q_rope (64)
@@ -226,6 +250,22 @@ int pa_decode_gqa_noalloc(const void *q, const void *k_pool, const void *v_pool,
 int pa_kv_write(const void *k, const void *v, const int64_t *slot_mapping, void *k_pool, void *v_pool,
                 int num_tokens, int num_kv_heads, int head_dim, int page_size, int num_pages,
                 uint32_t *status, cudaStream_t stream);
+
+/*
+ * FP8 paged KV write: as pa_kv_write into FP8 E4M3 pools (the layout of
+ * pa_decode_gqa_fp8): every bf16 value x of k (v) is stored as the E4M3 code
+ * nearest to the fp32 quotient x / k_scale (x / v_scale), rounded to nearest
+ * with ties to even, magnitudes above 448 saturating to 448 (NaN stays NaN).
+ *   k_pool, v_pool [num_pages, page_size, num_kv_heads, head_dim] uint8 codes
+ *   k_scale, v_scale finite and > 0 (else PA_ERR_INVALID_ARGUMENT)
+ * head_dim a multiple of 16 up to 1024; k_pool and v_pool 16-byte aligned, k
+ * and v 16-byte aligned.  slot_mapping, status and num_tokens as for
+ * pa_kv_write.
+ */
+int pa_kv_write_fp8(const void *k, const void *v, const int64_t *slot_mapping, void *k_pool,
+                    void *v_pool, int num_tokens, int num_kv_heads, int head_dim, int page_size,
+                    int num_pages, float k_scale, float v_scale, uint32_t *status,
+                    cudaStream_t stream);
 
 /*
  * MLA cache write: the 576-wide cache row of each new token is its latent

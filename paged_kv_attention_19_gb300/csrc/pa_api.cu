@@ -40,8 +40,8 @@ int ilog2(int x) {
 }
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Tokens per stage of the split kernel for a head_dim (must match GqaCfg<D>::ST).
-int gqa_stage_tokens(int D) { return D <= 128 ? 64 : 32; }
+// Tokens per stage of the split kernel (must match GqaCfg<D, fp8>::ST).
+int gqa_stage_tokens(int D, bool fp8) { return fp8 ? (D <= 128 ? 128 : 64) : (D <= 128 ? 64 : 32); }
 
 struct GqaPlan {
   int nsub, nparts_max;
@@ -87,16 +87,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 4-D map over a [num_pages, P, H, D] bf16 pool; box = (64 dims, 1 head, BH tokens, 1 page),
-// written to shared memory with the 128-byte swizzle (one box row is 128 bytes).
-bool encode_pool_map(CUtensorMap *m, const void *base, int num_pages, int P, int H, int D, int BH) {
+// 4-D map over a [num_pages, P, H, D] pool of bf16 (esz 2) or FP8 (esz 1) values; box = (one
+// 128-byte row fragment: 64 or 128 dims, 1 head, BH tokens, 1 page), written to shared memory
+// with the 128-byte swizzle.
+bool encode_pool_map(CUtensorMap *m, const void *base, int num_pages, int P, int H, int D, int BH, int esz = 2) {
   auto fn = encode_fn();
   if (!fn) return false;
+  const cuuint64_t e = (cuuint64_t)esz;
   cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)P, (cuuint64_t)num_pages};
-  cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)P * H * D * 2};
-  cuuint32_t box[4] = {64u, 1u, (cuuint32_t)BH, 1u};
+  cuuint64_t strides[3] = {(cuuint64_t)D * e, (cuuint64_t)H * D * e, (cuuint64_t)P * H * D * e};
+  cuuint32_t box[4] = {128u / (cuuint32_t)esz, 1u, (cuuint32_t)BH, 1u};
   cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
+  CUresult r = fn(m, esz == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -162,18 +164,28 @@ size_t pa_workspace_size(int kind, int batch, int num_q_heads, int num_kv_heads,
 
 namespace {
 
-// GQA decode (Q == 1) and verify (Q > 1 query positions per row, causal among them).
+// FP8 pool scales: one float per pool, each finite and positive.
+struct Fp8Scales {
+  bool on;
+  float k, v;
+};
+
+// GQA decode (Q == 1) and verify (Q > 1 query positions per row, causal among them), over
+// bf16 pools or (f8.on) FP8 E4M3 pools with per-pool scales.
 int gqa_call(const void *q, const void *k_pool, const void *v_pool, const int32_t *block_table,
              const int32_t *context_lens, void *out, float *lse, int batch, int Q, int num_q_heads,
              int num_kv_heads, int head_dim, int page_size, int num_pages, int max_pages_per_seq,
              int max_context_len, float scale, int window, int num_splits, void *workspace,
-             size_t workspace_bytes, cudaStream_t stream) {
+             size_t workspace_bytes, cudaStream_t stream, Fp8Scales f8 = {false, 1.f, 1.f}) {
   t_last_launches = 0;
   if (Q <= 0 || Q > kMaxQueryPositions) return Q <= 0 ? PA_ERR_INVALID_ARGUMENT : PA_ERR_UNSUPPORTED;
+  if (f8.on && !(std::isfinite(f8.k) && f8.k > 0.f && std::isfinite(f8.v) && f8.v > 0.f))
+    return PA_ERR_INVALID_ARGUMENT;
   if (batch == 0) return PA_OK;
   GqaPlan pl;
   int rc = gqa_shape(batch, num_q_heads, num_kv_heads, head_dim, max_context_len, page_size, num_splits, &pl);
   if (rc != PA_OK) return rc;
+  if (f8.on && head_dim != 128 && head_dim != 256) return PA_ERR_UNSUPPORTED;
   if (!q || !k_pool || !v_pool || !block_table || !context_lens || !out || !workspace)
     return PA_ERR_INVALID_ARGUMENT;
   if (num_pages <= 0 || max_pages_per_seq <= 0 || !std::isfinite(scale)) return PA_ERR_INVALID_ARGUMENT;
@@ -185,7 +197,7 @@ int gqa_call(const void *q, const void *k_pool, const void *v_pool, const int32_
   if (workspace_bytes < pl.total) return PA_ERR_WORKSPACE_TOO_SMALL;
 
   const int D = head_dim, P = page_size;
-  const int ST = gqa_stage_tokens(D);
+  const int ST = gqa_stage_tokens(D, f8.on);
   const int BH = P < ST ? P : ST;  // tokens per TMA box = per work unit
   // query tiles of at most 16 MMA rows: qt positions x gt heads of one KV head's group
   const int G = num_q_heads / num_kv_heads;
@@ -193,8 +205,9 @@ int gqa_call(const void *q, const void *k_pool, const void *v_pool, const int32_
   const int qt = G < PART_HEADS ? (Q < PART_HEADS / G ? Q : PART_HEADS / G) : 1;
   const int ntile = G < PART_HEADS ? (Q + qt - 1) / qt : Q * pl.nsub;
   CUtensorMap tm_k, tm_v, tm_q;
-  if (!encode_pool_map(&tm_k, k_pool, num_pages, P, num_kv_heads, D, BH) ||
-      !encode_pool_map(&tm_v, v_pool, num_pages, P, num_kv_heads, D, BH) ||
+  const int esz = f8.on ? 1 : 2;
+  if (!encode_pool_map(&tm_k, k_pool, num_pages, P, num_kv_heads, D, BH, esz) ||
+      !encode_pool_map(&tm_v, v_pool, num_pages, P, num_kv_heads, D, BH, esz) ||
       !encode_q_map(&tm_q, q, (long long)batch * Q, num_q_heads, D, gt, qt))
     return PA_ERR_UNSUPPORTED;
   const int sms = sm_count();
@@ -237,10 +250,11 @@ int gqa_call(const void *q, const void *k_pool, const void *v_pool, const int32_
     ga.hg = hs < nparts ? hs : nparts;
   }
   {
-    const long long unit_bytes = (long long)BH * D * 4;  // K and V of one unit of one KV head
+    const long long unit_bytes = (long long)BH * D * 2 * esz;  // K and V of one unit of one KV head
     ga.piece_cost = (int)((kPieceCostBytes + unit_bytes - 1) / unit_bytes);
   }
-  ga.qscale = scale * LOG2E;
+  ga.qscale = scale * LOG2E * (f8.on ? f8.k : 1.f);
+  ga.vscale = f8.on ? f8.v : 1.f;
 
   CombineArgs ca;
   ca.out = static_cast<uint16_t *>(out);
@@ -261,10 +275,15 @@ int gqa_call(const void *q, const void *k_pool, const void *v_pool, const int32_
 
   cudaError_t e;
   if (t_ev_before && cudaEventRecord(t_ev_before, stream) != cudaSuccess) return PA_ERR_CUDA;
-  switch (D) {
-    case 64: e = launch_gqa_split_d64(nparts, tm_k, tm_v, tm_q, ga, stream); break;
-    case 128: e = launch_gqa_split_d128(nparts, tm_k, tm_v, tm_q, ga, stream); break;
-    default: e = launch_gqa_split_d256(nparts, tm_k, tm_v, tm_q, ga, stream); break;
+  if (f8.on) {
+    e = D == 128 ? launch_gqa_split_fp8_d128(nparts, tm_k, tm_v, tm_q, ga, stream)
+                 : launch_gqa_split_fp8_d256(nparts, tm_k, tm_v, tm_q, ga, stream);
+  } else {
+    switch (D) {
+      case 64: e = launch_gqa_split_d64(nparts, tm_k, tm_v, tm_q, ga, stream); break;
+      case 128: e = launch_gqa_split_d128(nparts, tm_k, tm_v, tm_q, ga, stream); break;
+      default: e = launch_gqa_split_d256(nparts, tm_k, tm_v, tm_q, ga, stream); break;
+    }
   }
   if (e != cudaSuccess) return PA_ERR_CUDA;
   ++t_last_launches;
@@ -301,6 +320,17 @@ int pa_verify_gqa(const void *q, const void *k_pool, const void *v_pool, const i
   return gqa_call(q, k_pool, v_pool, block_table, context_lens, out, lse, batch, num_query, num_q_heads,
                   num_kv_heads, head_dim, page_size, num_pages, max_pages_per_seq, max_context_len, scale, window,
                   num_splits, workspace, workspace_bytes, stream);
+}
+
+int pa_decode_gqa_fp8(const void *q, const void *k_pool, const void *v_pool, const int32_t *block_table,
+                      const int32_t *context_lens, void *out, float *lse, int batch, int num_query,
+                      int num_q_heads, int num_kv_heads, int head_dim, int page_size, int num_pages,
+                      int max_pages_per_seq, int max_context_len, float scale, float k_scale, float v_scale,
+                      int window, int num_splits, void *workspace, size_t workspace_bytes,
+                      cudaStream_t stream) {
+  return gqa_call(q, k_pool, v_pool, block_table, context_lens, out, lse, batch, num_query, num_q_heads,
+                  num_kv_heads, head_dim, page_size, num_pages, max_pages_per_seq, max_context_len, scale, window,
+                  num_splits, workspace, workspace_bytes, stream, Fp8Scales{true, k_scale, v_scale});
 }
 
 int pa_decode_mla_absorbed(const void *q, const void *cache, const void *w_uk, const void *w_uv,

@@ -1,5 +1,6 @@
 // pa_gqa_launch.cuh -- host launchers of the GQA split-KV and combine kernels, instantiated
-// once per head_dim by pa_gqa_d{64,128,256}.cu (one translation unit each, built in parallel).
+// once per head_dim by pa_gqa_d{64,128,256}.cu and, for FP8 pools, by pa_gqa_fp8.cu (one
+// translation unit each, built in parallel).
 #pragma once
 
 #include "pa_gqa.cuh"
@@ -24,30 +25,30 @@ inline cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, int smem, cudaStream
   return cfg;
 }
 
-template <int D, bool MQ>
+template <int D, bool MQ, bool F8>
 cudaError_t launch_split(int grid, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const CUtensorMap &tm_q,
                          const GqaArgs &a, cudaStream_t stream) {
-  using C = GqaCfg<D>;
+  using C = GqaCfg<D, F8>;
   constexpr int smem = GqaSmem<C>::BYTES;
   static int configured_device = -1;  // the shared-memory opt-in is per device
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(gqa_split_kernel<D, MQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(gqa_split_kernel<D, MQ, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(C::THREADS), smem, stream, attr);
-  return cudaLaunchKernelEx(&cfg, gqa_split_kernel<D, MQ>, tm_k, tm_v, tm_q, a);
+  return cudaLaunchKernelEx(&cfg, gqa_split_kernel<D, MQ, F8>, tm_k, tm_v, tm_q, a);
 }
 
 // Q == 1 (decode) runs the kernel compiled without the per-position row logic.
-template <int D>
+template <int D, bool F8 = false>
 cudaError_t launch_split_any(int grid, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const CUtensorMap &tm_q,
                              const GqaArgs &a, cudaStream_t stream) {
-  return a.Q > 1 ? launch_split<D, true>(grid, tm_k, tm_v, tm_q, a, stream)
-                 : launch_split<D, false>(grid, tm_k, tm_v, tm_q, a, stream);
+  return a.Q > 1 ? launch_split<D, true, F8>(grid, tm_k, tm_v, tm_q, a, stream)
+                 : launch_split<D, false, F8>(grid, tm_k, tm_v, tm_q, a, stream);
 }
 
 template <int D>

@@ -21,6 +21,11 @@ cudaError_t launch_gqa_split_d128(int grid, const CUtensorMap &tm_k, const CUten
 cudaError_t launch_gqa_split_d256(int grid, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const CUtensorMap &tm_q,
                                   const GqaArgs &a,
                                   cudaStream_t stream);
+// FP8 E4M3 pools (head_dim 128 and 256)
+cudaError_t launch_gqa_split_fp8_d128(int grid, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                                      const CUtensorMap &tm_q, const GqaArgs &a, cudaStream_t stream);
+cudaError_t launch_gqa_split_fp8_d256(int grid, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                                      const CUtensorMap &tm_q, const GqaArgs &a, cudaStream_t stream);
 cudaError_t launch_gqa_combine_d64(const CombineArgs &a, cudaStream_t stream);
 cudaError_t launch_gqa_combine_d128(const CombineArgs &a, cudaStream_t stream);
 cudaError_t launch_gqa_combine_d256(const CombineArgs &a, cudaStream_t stream);

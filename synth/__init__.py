@@ -23,6 +23,12 @@ Recipe (all counter-based, so any element can be regenerated on its own):
   bf16 NaN, so a stray read poisons the result.
 * Data is drawn per *logical* (row, token, head, dim) coordinate, so the same
   seed gives the same logical cache under any physical page permutation.
+* FP8 (E4M3) pools hold codes drawn directly (no conversion from values):
+  output ``x`` of the element's stream gives the sign (bit 0) and, with
+  probability 1/32 (bits 1-5 all zero), a 7-bit magnitude code uniform over all
+  127 finite ones (zeros, subnormals, 448 included), else one uniform over
+  0x28..0x6F (values 0.25 .. 120, log-uniform).  Slots that must not be read
+  hold the NaN code 0x7F.
 
 The workloads mirror the decode shapes of the pages: the Llama-3-8B / Qwen3-32B
 GQA geometries and the 576-wide (512 latent + 64 rope) MLA cache of
@@ -41,6 +47,7 @@ GOLDEN = np.uint64(0x9E3779B97F4A7C15)
 _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 BF16_NAN = np.uint16(0x7FC0)
+E4M3_NAN = np.uint8(0x7F)
 
 # stream tags: one independent splitmix64 stream per drawn quantity
 TAG_Q, TAG_K, TAG_V, TAG_LENS, TAG_PERM, TAG_CACHE, TAG_WUK, TAG_WUV, TAG_SLOT = range(1, 10)
@@ -113,6 +120,24 @@ def _normal_bf16_range(state: int, start: int, n: int, std: float, chunk: int = 
 
 def _normal_bf16_dense(state: int, n: int, std: float) -> np.ndarray:
     return _normal_bf16_range(state, 0, n, std)
+
+
+def e4m3_codes(state: int, index: np.ndarray) -> np.ndarray:
+    """FP8 E4M3 codes (uint8), one per ``index``, by the recipe in the module docstring."""
+    x = splitmix64(state, index)
+    sign = (x & np.uint64(1)).astype(np.uint8) << np.uint8(7)
+    wide = ((x >> np.uint64(1)) & np.uint64(31)) == 0
+    r = x >> np.uint64(8)
+    mag = np.where(wide, r % np.uint64(127), np.uint64(0x28) + r % np.uint64(0x48)).astype(np.uint8)
+    return sign | mag
+
+
+def _codes_range(state: int, start: int, n: int, chunk: int = 1 << 18) -> np.ndarray:
+    out = np.empty(n, dtype=np.uint8)
+    for s in range(0, n, chunk):
+        e = min(n, s + chunk)
+        out[s:e] = e4m3_codes(state, np.arange(start + s, start + e, dtype=np.uint64))
+    return out
 
 
 def permutation(state: int, n: int) -> np.ndarray:
@@ -192,10 +217,12 @@ def make_layout(seed: int, context_lens: np.ndarray, page_size: int, pool_factor
 
 
 def _fill_pool(state: int, layout: PagedLayout, row_width: int, std: float, window: int,
-               visible_only: bool, num_query: int = 1) -> np.ndarray:
-    """Pool [num_pages, P, row_width] bf16 bits; values drawn per logical (page, slot, element)."""
+               visible_only: bool, num_query: int = 1, fp8: bool = False) -> np.ndarray:
+    """Pool [num_pages, P, row_width] bf16 bits (fp8: E4M3 codes); values drawn per logical
+    (page, slot, element)."""
     P = layout.page_size
-    pool = np.full((layout.num_pages, P, row_width), BF16_NAN, dtype=np.uint16)
+    poison = E4M3_NAN if fp8 else BF16_NAN
+    pool = np.full((layout.num_pages, P, row_width), poison, dtype=np.uint8 if fp8 else np.uint16)
     per_page = P * row_width
     for b in range(layout.batch):
         L = int(layout.context_lens[b])
@@ -204,12 +231,15 @@ def _fill_pool(state: int, layout: PagedLayout, row_width: int, std: float, wind
         lo, hi = visible_range(L, window, num_query) if visible_only else (0, L)
         p0, p1 = lo // P, (hi + P - 1) // P
         g0 = int(layout.logical_page_of_row[b])
-        vals = _normal_bf16_range(state, (g0 + p0) * per_page, (p1 - p0) * per_page, std)
+        if fp8:
+            vals = _codes_range(state, (g0 + p0) * per_page, (p1 - p0) * per_page)
+        else:
+            vals = _normal_bf16_range(state, (g0 + p0) * per_page, (p1 - p0) * per_page, std)
         vals = vals.reshape(p1 - p0, P, row_width)
         flat = vals.reshape((p1 - p0) * P, row_width)
         # poison the slots of the visited pages that lie outside [lo, hi)
-        flat[: lo - p0 * P] = BF16_NAN
-        flat[hi - p0 * P:] = BF16_NAN
+        flat[: lo - p0 * P] = poison
+        flat[hi - p0 * P:] = poison
         pool[layout.block_table[b, p0:p1]] = vals
     return pool
 
@@ -219,8 +249,8 @@ class GQAWorkload:
     name: str
     seed: int
     q: np.ndarray            # [B, Hq, D] bf16 bits ([B, Q, Hq, D] when num_query > 1)
-    k_pool: np.ndarray       # [num_pages, P, Hkv, D] bf16 bits
-    v_pool: np.ndarray       # [num_pages, P, Hkv, D] bf16 bits
+    k_pool: np.ndarray       # [num_pages, P, Hkv, D] bf16 bits (fp8: uint8 E4M3 codes)
+    v_pool: np.ndarray       # [num_pages, P, Hkv, D] bf16 bits (fp8: uint8 E4M3 codes)
     layout: PagedLayout
     num_q_heads: int
     num_kv_heads: int
@@ -229,6 +259,9 @@ class GQAWorkload:
     window: int
     k_std: float = 1.0
     num_query: int = 1
+    fp8: bool = False
+    k_scale: float = 1.0     # fp8: key = E4M3(code) * k_scale
+    v_scale: float = 1.0     # fp8: value = E4M3(code) * v_scale
 
     @property
     def batch(self):
@@ -241,7 +274,7 @@ class GQAWorkload:
     def algorithmic_bytes(self) -> int:
         """Bytes the method must move: every visible K and V row of each kv head once, all of q, and
         the output (every query position of a row shares the one walk over its keys)."""
-        kv = self.visible_tokens() * self.num_kv_heads * self.head_dim * 2 * 2
+        kv = self.visible_tokens() * self.num_kv_heads * self.head_dim * 2 * (1 if self.fp8 else 2)
         qb = self.batch * self.num_query * self.num_q_heads * self.head_dim * 2
         ob = self.batch * self.num_query * self.num_q_heads * (self.head_dim * 2 + 4)
         return kv + qb + ob
@@ -250,7 +283,10 @@ class GQAWorkload:
 def make_gqa(seed: int, context_lens, num_q_heads: int, num_kv_heads: int, head_dim: int,
              page_size: int, window: int = 0, k_std: float = 1.0, pool_factor: int = 1,
              scale: Optional[float] = None, scramble: bool = True, name: str = "gqa",
-             visible_only: bool = True, extra_table_cols: int = 0, num_query: int = 1) -> GQAWorkload:
+             visible_only: bool = True, extra_table_cols: int = 0, num_query: int = 1,
+             fp8: bool = False, k_scale: float = 1.0 / 64, v_scale: float = 1.0 / 128) -> GQAWorkload:
+    """GQA decode / verify inputs; fp8: E4M3 code pools with the given per-pool scales (k_std
+    does not apply to them)."""
     lens = np.asarray(context_lens, dtype=np.int32)
     layout = make_layout(seed, lens, page_size, pool_factor, scramble, extra_table_cols)
     B = lens.shape[0]
@@ -258,14 +294,15 @@ def make_gqa(seed: int, context_lens, num_q_heads: int, num_kv_heads: int, head_
     q = _normal_bf16_dense(stream_seed(seed, TAG_Q), B * Q * num_q_heads * head_dim, 1.0)
     q = q.reshape(B, num_q_heads, head_dim) if Q == 1 else q.reshape(B, Q, num_q_heads, head_dim)
     w = num_kv_heads * head_dim
-    k = _fill_pool(stream_seed(seed, TAG_K), layout, w, k_std, window, visible_only, Q)
-    v = _fill_pool(stream_seed(seed, TAG_V), layout, w, 1.0, window, visible_only, Q)
+    k = _fill_pool(stream_seed(seed, TAG_K), layout, w, k_std, window, visible_only, Q, fp8)
+    v = _fill_pool(stream_seed(seed, TAG_V), layout, w, 1.0, window, visible_only, Q, fp8)
     k = k.reshape(layout.num_pages, page_size, num_kv_heads, head_dim)
     v = v.reshape(layout.num_pages, page_size, num_kv_heads, head_dim)
     if scale is None:
         scale = 1.0 / math.sqrt(head_dim)
     return GQAWorkload(name, seed, q, k, v, layout, num_q_heads, num_kv_heads, head_dim,
-                       float(scale), int(window), float(k_std), int(Q))
+                       float(scale), int(window), float(k_std), int(Q), bool(fp8),
+                       float(np.float32(k_scale)) if fp8 else 1.0, float(np.float32(v_scale)) if fp8 else 1.0)
 
 
 MLA_NOPE, MLA_ROPE, MLA_LATENT, MLA_VDIM = 128, 64, 512, 128
@@ -375,7 +412,8 @@ def make_kv_write(seed: int, num_tokens: int, num_kv_heads: int, head_dim: int, 
     return KVWriteWorkload(name, seed, k, v, slots.astype(np.int64), num_pages, page_size, mla)
 
 
-WORKLOADS = ("tiny", "llama3-8b", "qwen3-32b", "hd256-window", "mla", "kv-write", "qwen3-32b-verify4")
+WORKLOADS = ("tiny", "llama3-8b", "qwen3-32b", "hd256-window", "mla", "kv-write", "qwen3-32b-verify4",
+             "qwen3-32b-fp8")
 
 
 def workload(name: str, seed: Optional[int] = None, scramble: bool = True):
@@ -401,6 +439,10 @@ def workload(name: str, seed: Optional[int] = None, scramble: bool = True):
         # speculative verify: the qwen3-32b rows (same lengths) with 4 query positions each
         lens = context_lengths(20262 if seed == 20266 else seed, 32, "loguniform", 128, 16384)
         return make_gqa(seed, lens, 64, 8, 128, 32, name=name, scramble=scramble, num_query=4)
+    if name == "qwen3-32b-fp8":
+        # the qwen3-32b rows (same lengths) over an FP8 E4M3 cache
+        lens = context_lengths(20262 if seed == 20267 else seed, 32, "loguniform", 128, 16384)
+        return make_gqa(seed, lens, 64, 8, 128, 32, name=name, scramble=scramble, fp8=True)
     if name == "kv-write":
         # a 16384-token prefill chunk into a Qwen3-32B-shaped cache (8 KV heads, D 128, page 32)
         return make_kv_write(seed, 16384, 8, 128, 32, 1024, name=name)

@@ -154,3 +154,43 @@ def test_kv_write_host_validation(pa):
     assert mw(P=0) == pa.PA_ERR_INVALID_ARGUMENT
     assert mw(cache=None) == pa.PA_ERR_INVALID_ARGUMENT
     assert mw(r=0x20008) == pa.PA_ERR_MISALIGNED
+
+
+def _gqa_fp8(pa, **kw):
+    a = dict(q=0x10000, k=0x20000, v=0x30000, bt=0x40000, lens=0x50000, out=0x60000, lse=None, batch=2, nq=1,
+             hq=8, hkv=2, d=128, p=16, pages=10, maxp=5, maxctx=80, scale=0.1, ks=0.02, vs=0.03, window=0,
+             splits=0, ws=0x70000, wsb=1 << 30)
+    a.update(kw)
+    return pa.lib.pa_decode_gqa_fp8(a["q"], a["k"], a["v"], a["bt"], a["lens"], a["out"], a["lse"], a["batch"],
+                                    a["nq"], a["hq"], a["hkv"], a["d"], a["p"], a["pages"], a["maxp"], a["maxctx"],
+                                    a["scale"], a["ks"], a["vs"], a["window"], a["splits"], a["ws"], a["wsb"], None)
+
+
+def test_gqa_fp8_host_validation(pa):
+    assert _gqa_fp8(pa, batch=0) == pa.PA_OK
+    assert _gqa_fp8(pa, ks=0.0) == pa.PA_ERR_INVALID_ARGUMENT
+    assert _gqa_fp8(pa, vs=-1.0) == pa.PA_ERR_INVALID_ARGUMENT
+    assert _gqa_fp8(pa, ks=float("inf")) == pa.PA_ERR_INVALID_ARGUMENT
+    assert _gqa_fp8(pa, vs=float("nan"), batch=0) == pa.PA_ERR_INVALID_ARGUMENT  # scales checked first
+    assert _gqa_fp8(pa, d=64) == pa.PA_ERR_UNSUPPORTED                          # bf16 pools only
+    assert _gqa_fp8(pa, d=96) == pa.PA_ERR_UNSUPPORTED
+    assert _gqa_fp8(pa, nq=0) == pa.PA_ERR_INVALID_ARGUMENT
+    assert _gqa_fp8(pa, nq=65) == pa.PA_ERR_UNSUPPORTED
+    assert _gqa_fp8(pa, k=None) == pa.PA_ERR_INVALID_ARGUMENT
+    assert _gqa_fp8(pa, v=0x30008) == pa.PA_ERR_MISALIGNED
+    assert _gqa_fp8(pa, wsb=1024) == pa.PA_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_kv_write_fp8_host_validation(pa):
+    kw = lambda **a: pa.lib.pa_kv_write_fp8(a.get("k", 0x10000), a.get("v", 0x20000), a.get("s", 0x30000),
+                                            a.get("kp", 0x40000), a.get("vp", 0x50000), a.get("T", 4),
+                                            a.get("H", 2), a.get("D", 64), a.get("P", 16), a.get("pages", 4),
+                                            a.get("ks", 0.5), a.get("vs", 0.5), a.get("st", None), None)
+    assert kw(T=0) == pa.PA_OK
+    assert kw(T=-1) == pa.PA_ERR_INVALID_ARGUMENT
+    assert kw(ks=0.0) == pa.PA_ERR_INVALID_ARGUMENT
+    assert kw(vs=float("nan")) == pa.PA_ERR_INVALID_ARGUMENT
+    assert kw(D=40) == pa.PA_ERR_UNSUPPORTED          # rows of whole 16-byte code vectors
+    assert kw(kp=None) == pa.PA_ERR_INVALID_ARGUMENT
+    assert kw(vp=0x50008) == pa.PA_ERR_MISALIGNED
+    assert kw(s=0x30004) == pa.PA_ERR_MISALIGNED
