@@ -40,7 +40,7 @@ int ilog2(int x) {
 }
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Tokens per stage of the split kernel (must match GqaCfg<D, fp8>::ST).
+// Tokens per stage of the split kernel (must match GqaCfg<D>::ST and GqaF8Cfg<D, *>::ST).
 int gqa_stage_tokens(int D, bool fp8) { return fp8 ? (D <= 128 ? 128 : 64) : (D <= 128 ? 64 : 32); }
 
 struct GqaPlan {

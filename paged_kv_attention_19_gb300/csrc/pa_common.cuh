@@ -192,17 +192,6 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// D += A(16x32, row) * B(32x8, col), FP8 E4M3 inputs (4 per register), fp32 accumulation;
-// fragment layout of the 8-bit m16n8k32 shape: a0 / a1 rows g and g + 8, k = 4 t .. 4 t + 3,
-// a2 / a3 the same rows at k + 16; b0 column g, k = 4 t .. 4 t + 3, b1 at k + 16.
-__device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
 // Byte permute: byte i of the result is byte ((sel >> 4 i) & 7) of the pair {hi:lo}.
 __device__ __forceinline__ uint32_t prmt(uint32_t lo, uint32_t hi, uint32_t sel) {
   uint32_t r;
@@ -214,30 +203,6 @@ __device__ __forceinline__ uint2 lds_u2(uint32_t addr) {
   uint2 r;
   asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(addr));
   return r;
-}
-
-// Largest magnitude of the two bf16 values of a pair.
-__device__ __forceinline__ float bf16x2_absmax(uint32_t v) {
-  return fmaxf(fabsf(__uint_as_float(v << 16)), fabsf(__uint_as_float(v & 0xffff0000u)));
-}
-
-// 2^s as a float, s in [-126, 127].
-__device__ __forceinline__ float pow2f(int s) { return __uint_as_float((uint32_t)(s + 127) << 23); }
-
-// Two-term E4M3 split of an f16 pair: x = hi + lo + e with |e| <= 2^-8 |x| (hi the nearest code,
-// lo the nearest code of the exact f16 remainder; exact when x has at most 8 significant bits
-// and lies in the normal range of both terms).  Each result holds 2 codes, x.lo's first.
-__device__ __forceinline__ void split_e4m3x2(__half2_raw x, uint32_t &hi, uint32_t &lo) {
-  const __nv_fp8x2_storage_t h = __nv_cvt_halfraw2_to_fp8x2(x, __NV_SATFINITE, __NV_E4M3);
-  const __half2_raw hb = __nv_cvt_fp8x2_to_halfraw2(h, __NV_E4M3);
-  const __half2 r = __hsub2(*reinterpret_cast<const __half2 *>(&x), *reinterpret_cast<const __half2 *>(&hb));
-  hi = (uint32_t)h;
-  lo = (uint32_t)__nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw *>(&r), __NV_SATFINITE, __NV_E4M3);
-}
-
-__device__ __forceinline__ __half2_raw f32x2_to_f16x2_raw(float lo, float hi) {
-  const __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const __half2_raw *>(&h);
 }
 
 // Two fp32 -> one bf16x2 (round to nearest even); `lo` lands in the low half.

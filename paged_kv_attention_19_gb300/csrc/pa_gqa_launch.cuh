@@ -4,6 +4,7 @@
 #pragma once
 
 #include "pa_gqa.cuh"
+#include "pa_gqa_f8.cuh"
 #include "pa_launch.h"
 
 namespace pa {
@@ -25,30 +26,48 @@ inline cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, int smem, cudaStream
   return cfg;
 }
 
-template <int D, bool MQ, bool F8>
-cudaError_t launch_split(int grid, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const CUtensorMap &tm_q,
-                         const GqaArgs &a, cudaStream_t stream) {
-  using C = GqaCfg<D, F8>;
+// One launch of split kernel `kernel` with configuration C (the shared-memory opt-in is made
+// once per device and kernel: one static per instantiation).
+template <class C, auto kernel>
+cudaError_t launch_split_kernel(int grid, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const CUtensorMap &tm_q,
+                                const GqaArgs &a, cudaStream_t stream) {
   constexpr int smem = GqaSmem<C>::BYTES;
-  static int configured_device = -1;  // the shared-memory opt-in is per device
+  static int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(gqa_split_kernel<D, MQ, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(C::THREADS), smem, stream, attr);
-  return cudaLaunchKernelEx(&cfg, gqa_split_kernel<D, MQ, F8>, tm_k, tm_v, tm_q, a);
+  return cudaLaunchKernelEx(&cfg, kernel, tm_k, tm_v, tm_q, a);
 }
 
 // Q == 1 (decode) runs the kernel compiled without the per-position row logic.
-template <int D, bool F8 = false>
+template <int D>
 cudaError_t launch_split_any(int grid, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const CUtensorMap &tm_q,
                              const GqaArgs &a, cudaStream_t stream) {
-  return a.Q > 1 ? launch_split<D, true, F8>(grid, tm_k, tm_v, tm_q, a, stream)
-                 : launch_split<D, false, F8>(grid, tm_k, tm_v, tm_q, a, stream);
+  using C = GqaCfg<D>;
+  return a.Q > 1 ? launch_split_kernel<C, gqa_split_kernel<D, true>>(grid, tm_k, tm_v, tm_q, a, stream)
+                 : launch_split_kernel<C, gqa_split_kernel<D, false>>(grid, tm_k, tm_v, tm_q, a, stream);
+}
+
+// FP8 pools: NH8 = 1 when a tile has at most 8 (head, position) columns, else 2.
+template <int D, int NH8>
+cudaError_t launch_f8_split(int grid, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const CUtensorMap &tm_q,
+                            const GqaArgs &a, cudaStream_t stream) {
+  using C = GqaF8Cfg<D, NH8>;
+  return a.Q > 1 ? launch_split_kernel<C, gqa_f8_split_kernel<D, true, NH8>>(grid, tm_k, tm_v, tm_q, a, stream)
+                 : launch_split_kernel<C, gqa_f8_split_kernel<D, false, NH8>>(grid, tm_k, tm_v, tm_q, a, stream);
+}
+
+template <int D>
+cudaError_t launch_f8_split_any(int grid, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const CUtensorMap &tm_q,
+                                const GqaArgs &a, cudaStream_t stream) {
+  return a.gt * a.qt <= 8 ? launch_f8_split<D, 1>(grid, tm_k, tm_v, tm_q, a, stream)
+                          : launch_f8_split<D, 2>(grid, tm_k, tm_v, tm_q, a, stream);
 }
 
 template <int D>
