@@ -98,6 +98,7 @@ struct GqaCfg {
   static constexpr int ST = D <= 128 ? 64 : 32;    // tokens per stage
   static constexpr int TW = 16;                    // tokens per token group per stage
   static constexpr int TG = ST / TW;               // token groups per stage
+  static constexpr int MG = TG;                    // groups merged at the end of a piece
   static constexpr int DSPLIT = 2;                 // warps sharing a token group (each: D / 2 of P.V)
   static constexpr int NCW = TG * DSPLIT;          // consumer warps
   static constexpr int THREADS = (NCW + 1) * 32;   // + producer warp
@@ -109,7 +110,7 @@ struct GqaCfg {
   static constexpr int STAGE_BYTES = 2 * KV_BYTES;
   static constexpr int NS = (229376 / STAGE_BYTES) < 16 ? (229376 / STAGE_BYTES) : 16;  // 224 KB ring
   static constexpr int NACC = 2;                   // independent QK accumulators
-  static_assert(MR * D * 4 * TG <= STAGE_BYTES, "the end-of-piece merge fits the consumed stage");
+  static_assert(MR * D * 4 * MG <= STAGE_BYTES, "the end-of-piece merge fits the consumed stage");
 };
 
 struct alignas(16) StageMeta {
@@ -133,7 +134,7 @@ template <class C>
 struct GqaSmem {
   static constexpr int OFF_STAGE = 0;
   static constexpr int OFF_ML = OFF_STAGE + C::NS * C::STAGE_BYTES;
-  static constexpr int OFF_META = OFF_ML + C::TG * C::M * 2 * 4;
+  static constexpr int OFF_META = OFF_ML + C::MG * C::M * 2 * 4;
   static constexpr int OFF_BAR = OFF_META + C::NS * (int)sizeof(StageMeta);
   static constexpr int OFF_MISC = OFF_BAR + 2 * C::NS * 8;
   static constexpr int USED = OFF_MISC + (int)sizeof(GqaMisc);
@@ -396,7 +397,7 @@ __device__ __forceinline__ void gqa_produce(uint8_t *smem, const CUtensorMap *tm
   }
 }
 
-// End of a piece, after every token group has put its (m, l) in sm_ml and its unnormalised
+// End of a piece, after each of the C::MG groups has put its (m, l) in sm_ml and its unnormalised
 // output rows in the merge area mg ([group][row][D] fp32, column of (row h, dim d) at
 // d ^ (4 (h & 7))): each thread takes 4 consecutive dims of one row and merges the groups
 // with weights exp2(m_w - M) / sum_w l_w exp2(m_w - M); a piece that covers its sequence writes
@@ -411,16 +412,16 @@ __device__ __forceinline__ void gqa_merge_out(const float *mg, const float *sm_m
   for (int e = ct; e < nrows * (D / 4); e += C::NCW * 32) {
     const int h = e / (D / 4), d4 = (e % (D / 4)) * 4;  // h: the MMA row
     if (MQ && h % a.gt >= mt.ghead) continue;          // not a head of this tile
-    float mw[C::TG], M = -INFINITY;
+    float mw[C::MG], M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < C::TG; ++w) {
+    for (int w = 0; w < C::MG; ++w) {
       mw[w] = sm_ml[(w * C::MR + h) * 2];
       M = fmaxf(M, mw[w]);
     }
     float L = 0.f;
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int w = 0; w < C::TG; ++w) {
+    for (int w = 0; w < C::MG; ++w) {
       const float wt = (mw[w] == -INFINITY) ? 0.f : fast_exp2(mw[w] - M);
       L += sm_ml[(w * C::MR + h) * 2 + 1] * wt;
       const float4 x = *reinterpret_cast<const float4 *>(mg + (w * C::MR + h) * D + (d4 ^ (4 * (h & 7))));
