@@ -49,7 +49,12 @@ WORKLOADS = ["tiny", "llama3-8b", "qwen3-32b", "hd256-window", "mla", "kv-write"
              "qwen3-32b-fp8"]
 # sources of the kernel each roofline line profiles (a change voids its committed ncu traffic)
 KERNEL_SOURCES = {"gqa": ("pa_gqa.cuh", "pa_partition.cuh", "pa_common.cuh"),
-                  "mla": ("pa_mla_tc.cuh", "pa_mla.cu", "pa_partition.cuh", "pa_common.cuh")}
+                  "gqa_f8": ("pa_gqa_f8.cuh", "pa_gqa.cuh", "pa_partition.cuh", "pa_common.cuh"),
+                  "mla": ("pa_mla_tc.cuh", "pa_mla.cu", "pa_gqa.cuh", "pa_partition.cuh", "pa_common.cuh")}
+
+
+def kernel_kind(workload: str) -> str:
+    return "mla" if workload == "mla" else "gqa_f8" if workload.endswith("-fp8") else "gqa"
 
 
 def parse():
@@ -113,8 +118,7 @@ def ncu_traffic(workload: str):
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             e = json.load(f)[workload]
-        kind = "mla" if workload == "mla" else "gqa"
-        return float(e["dram_bytes"]) if e["kernel_hash"] == kernel_hash(kind) else None
+        return float(e["dram_bytes"]) if e["kernel_hash"] == kernel_hash(kernel_kind(workload)) else None
     except Exception:
         return None
 
@@ -441,7 +445,8 @@ def run_ours(args, rank, local_rank, world):
         "config": dict(cfg, num_splits=args.num_splits or "auto", parallelism=f"replicas x{world}",
                        l2="between timed calls, outside the timed events: a 512 MB buffer written, then another 512 MB read"),
         "roofline": {"bound": "alu" if is_mla else "hbm",
-                     "kernel": "kv_write_kernel" if is_write else "mla_tc_split_kernel" if is_mla else "gqa_split_kernel",
+                     "kernel": ("kv_write_kernel" if is_write else "mla_tc_split_kernel" if is_mla
+                                else "gqa_f8_split_kernel" if getattr(w, "fp8", False) else "gqa_split_kernel"),
                      "achieved": round(kernel_gbs, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(kernel_gbs / peak, 4), "peak_source": f"hbm_gbs of {peak_kind}",
                      "kernel_us": round(kms * 1000, 2), "traffic": ncu_traffic(args.workload)},
