@@ -26,6 +26,9 @@ constexpr int kMaxQueryPositions = 64;  // verify: query positions per row
 // Fixed cost of one piece of work in the GQA partition (the Q load and the end-of-piece
 // merge, about 0.8 us of one SM), expressed as the KV bytes the SM streams meanwhile.
 constexpr long long kPieceCostBytes = 32 << 10;
+// The same for FP8 pools, whose pieces cost more (the query split and a merge over twice
+// the token groups) while each byte carries twice the tokens.
+constexpr long long kPieceCostBytesF8 = 128 << 10;
 
 thread_local cudaEvent_t t_ev_before = nullptr;
 thread_local cudaEvent_t t_ev_after = nullptr;
@@ -251,7 +254,8 @@ int gqa_call(const void *q, const void *k_pool, const void *v_pool, const int32_
   }
   {
     const long long unit_bytes = (long long)BH * D * 2 * esz;  // K and V of one unit of one KV head
-    ga.piece_cost = (int)((kPieceCostBytes + unit_bytes - 1) / unit_bytes);
+    const long long piece_bytes = f8.on ? kPieceCostBytesF8 : kPieceCostBytes;
+    ga.piece_cost = (int)((piece_bytes + unit_bytes - 1) / unit_bytes);
   }
   ga.qscale = scale * LOG2E * (f8.on ? f8.k : 1.f);
   ga.vscale = f8.on ? f8.v : 1.f;

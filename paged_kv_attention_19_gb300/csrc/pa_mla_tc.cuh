@@ -323,22 +323,33 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
         if (lane == 0) mbar_arrive(&empty[s]);
         continue;
       }
-      // ---- partial scores over this warp's 144 dims, for the group's 16 tokens (2 n-tiles)
-      float sp[2][4];
+      // ---- partial scores over this warp's 144 dims, for the group's 16 tokens (2 n-tiles);
+      // even and odd k-steps go to separate accumulators (two independent chains per n-tile)
+      float sp[2][4], sq[2][4];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) sp[nt][0] = sp[nt][1] = sp[nt][2] = sp[nt][3] = 0.f;
-#pragma unroll 4
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sp[nt][e] = sq[nt][e] = 0.f;
+#pragma unroll
       for (int k = 0; k < C::KSW; ++k) {
         const int ks = dq4 * C::KSW + k;
-        uint32_t qa[4];
-        ldmatrix_x4(qa, qarea + mla_off(C::QPLANE, (lm_mat & 1) * 8 + lm_row, 2 * ks + (lm_mat >> 1)));
         // matrices: (tokens 0-7, dims 0-7), (tokens 0-7, dims 8-15), (tokens 8-15, ...) of the k-step
-        uint32_t b[4];
+        uint32_t qa[4], b[4];
+        ldmatrix_x4(qa, qarea + mla_off(C::QPLANE, (lm_mat & 1) * 8 + lm_row, 2 * ks + (lm_mat >> 1)));
         const int tok = wbase + (lm_mat >> 1) * 8 + lm_row, chunk = 2 * ks + (lm_mat & 1);
         ldmatrix_x4(b, cbase + mla_off(C::PLANE, tok, chunk));
-        mma_bf16_16816(sp[0], qa, b[0], b[1]);
-        mma_bf16_16816(sp[1], qa, b[2], b[3]);
+        if (k & 1) {
+          mma_bf16_16816(sq[0], qa, b[0], b[1]);
+          mma_bf16_16816(sq[1], qa, b[2], b[3]);
+        } else {
+          mma_bf16_16816(sp[0], qa, b[0], b[1]);
+          mma_bf16_16816(sp[1], qa, b[2], b[3]);
+        }
       }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sp[nt][e] += sq[nt][e];
       float *myp = spart + (j & 1) * (C::SPART / 4) + (size_t)(tgrp * C::DSPLIT + dq4) * 32 * 8;
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
