@@ -191,3 +191,49 @@ def test_decode_over_gpu_written_fp8_pools():
     st = compare.compare(gu.bits(out).reshape(-1, D), ro)
     assert st.max_abs <= compare.MAX_ABS and st.max_rel <= compare.MAX_REL, str(st)
     assert compare.lse_max_abs(lse.cpu().numpy().reshape(-1), rl) <= compare.LSE_ABS
+
+
+def test_fp8_empty_rows_and_batch_zero():
+    """Rows with no key give out = 0 and lse = -inf; batch 0 is a no-op."""
+    import paged_kv_attention_19_gb300 as pa
+    w = synth.make_gqa(670, [0, 5, 0, 300], 16, 2, 128, 16, fp8=True)
+    o, l = _run(w)
+    _check(w, o, l)
+    assert np.all(o.reshape(4, 16, 128)[[0, 2]] == 0) and np.all(np.isneginf(l.reshape(4, 16)[[0, 2]]))
+    q = torch.empty(0, 16, 128, dtype=torch.bfloat16, device="cuda")
+    k = gu.dev(w.k_pool)
+    bt = torch.empty(0, 4, dtype=torch.int32, device="cuda")
+    lens = torch.empty(0, dtype=torch.int32, device="cuda")
+    out = torch.empty(0, 16, 128, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    pa.pa_decode_gqa_fp8(q, k, k, bt, lens, out, None, scale=0.1, k_scale=1.0, v_scale=1.0, workspace=ws)
+    torch.cuda.synchronize()
+
+
+def test_fp8_bad_page_is_reported_not_trapped():
+    import paged_kv_attention_19_gb300 as pa
+    w = synth.make_gqa(680, [40, 70], 8, 2, 128, 16, fp8=True)
+    q, k, v = gu.dev(w.q), gu.dev(w.k_pool), gu.dev(w.v_pool)
+    lens = gu.dev(w.layout.context_lens)
+    bt = w.layout.block_table.copy()
+    bt[1, 2] = w.layout.num_pages + 5          # out of the pool
+    out = torch.empty(w.q.shape, dtype=torch.bfloat16, device="cuda")
+    ws = pa.workspace_for_gqa(q, k, gu.dev(bt))
+    pa.pa_decode_gqa_fp8(q, k, v, gu.dev(bt), lens, out, None, scale=w.scale, k_scale=w.k_scale,
+                         v_scale=w.v_scale, workspace=ws)
+    assert pa.pa_read_device_status(ws) & pa.PA_DEV_BAD_PAGE
+    # row 0 is unaffected by row 1's bad entry
+    ro, _ = oracle.gqa_fp8(w.q, w.k_pool, w.v_pool, w.layout.block_table, w.layout.context_lens, w.scale,
+                           w.k_scale, w.v_scale, rows=[(0, h) for h in range(8)])
+    assert compare.compare(gu.bits(out)[0], ro).ok()
+    # a clean call clears the status word
+    pa.pa_decode_gqa_fp8(q, k, v, gu.dev(w.layout.block_table), lens, out, None, scale=w.scale,
+                         k_scale=w.k_scale, v_scale=w.v_scale, workspace=ws)
+    assert pa.pa_read_device_status(ws) == 0
+
+
+def test_fp8_run_to_run_bitwise():
+    w = synth.make_gqa(690, LADDER, 64, 8, 128, 32, fp8=True)
+    a = _run(w, num_splits=300)
+    b = _run(w, num_splits=300)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1].view(np.uint32), b[1].view(np.uint32))
