@@ -62,3 +62,28 @@ def test_workload_shapes():
     assert lens.min() >= 2048 and lens.max() <= 32768
     lens = synth.context_lengths(20262, 32, "loguniform", 128, 16384)
     assert lens.min() >= 128 and lens.max() <= 16384
+
+
+def test_fp8_codes_recipe():
+    """FP8 pools: visible slots hold finite E4M3 codes (never S.1111.111), drawn per the recipe
+    (about 1/32 from all 127 magnitudes, the rest from 0x28..0x6F), and every slot no row may
+    read holds the NaN code 0x7F; the same logical codes under any page order."""
+    codes = synth.e4m3_codes(synth.stream_seed(5, synth.TAG_K), np.arange(200000, dtype=np.uint64))
+    mag = codes & 0x7F
+    assert not np.any(mag == 0x7F)
+    wide = (mag < 0x28) | (mag > 0x6F)
+    assert 0.01 < wide.mean() < 0.03                      # the 1/32 arm, outside the narrow range
+    assert {0x00, 0x01, 0x7E} <= set(np.unique(mag).tolist())  # zero, smallest subnormal, 448
+    assert 0.45 < (codes >> 7).mean() < 0.55               # signs balanced
+    w = synth.make_gqa(9, [1, 31, 40], 8, 2, 128, 16, fp8=True, window=20)
+    wi = synth.make_gqa(9, [1, 31, 40], 8, 2, 128, 16, fp8=True, window=20, scramble=False)
+    bt, P = w.layout.block_table, w.layout.page_size
+    seen = np.zeros(w.k_pool.shape[:2], dtype=bool)
+    for b, L in enumerate(w.layout.context_lens):
+        lo, hi = synth.visible_range(int(L), w.window)
+        t = np.arange(lo, hi)
+        pk = w.k_pool[bt[b, t // P], t % P]
+        assert not np.any((pk & 0x7F) == 0x7F)
+        assert np.array_equal(pk, wi.k_pool[wi.layout.block_table[b, t // P], t % P])
+        seen[bt[b, t // P], t % P] = True
+    assert np.all(w.k_pool[~seen] == synth.E4M3_NAN) and np.all(w.v_pool[~seen] == synth.E4M3_NAN)
