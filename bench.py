@@ -46,7 +46,7 @@ FLUSH_BYTES = 512 << 20
 CLEAN_BYTES = 512 << 20
 DEFAULT_WORKLOAD = "qwen3-32b"
 WORKLOADS = ["tiny", "llama3-8b", "qwen3-32b", "hd256-window", "mla", "kv-write", "qwen3-32b-verify4",
-             "qwen3-32b-fp8"]
+             "qwen3-32b-fp8", "kv-write-fp8"]
 # sources of the kernel each roofline line profiles (a change voids its committed ncu traffic)
 KERNEL_SOURCES = {"gqa": ("pa_gqa.cuh", "pa_partition.cuh", "pa_common.cuh"),
                   "gqa_f8": ("pa_gqa_f8.cuh", "pa_gqa.cuh", "pa_partition.cuh", "pa_common.cuh"),
@@ -129,7 +129,8 @@ def describe(w, name):
         return {"workload": name, "tokens": w.num_tokens, "kv_heads": int(w.k.shape[1]),
                 "head_dim": int(w.k.shape[2]), "page_size": w.page_size, "pool_pages": w.num_pages,
                 "slots": "prefill order: token t at position t % P of page perm[t // P]",
-                "algorithmic_bytes": w.algorithmic_bytes(), "seed": w.seed}
+                "algorithmic_bytes": w.algorithmic_bytes(), "seed": w.seed,
+                **({"pools": "fp8 e4m3 codes", "k_scale": w.k_scale, "v_scale": w.v_scale} if w.fp8 else {})}
     if isinstance(w, synth.MLAWorkload):
         return {"workload": name, "batch": w.batch, "heads": w.num_heads, "q_dim": 192, "cache_dim": 576,
                 "v_dim": 128, "page_size": w.layout.page_size, "context": "uniform[1024,8192]",
@@ -216,7 +217,10 @@ class OracleSample:
         if isinstance(w, synth.KVWriteWorkload):
             # the oracle writes token by token into copies of the pools: time it on all tokens
             kp, vp = w.empty_pool(), w.empty_pool()
-            self.fn = lambda rows: oracle.kv_write(w.k, w.v, w.slots, kp, vp)
+            if w.fp8:
+                self.fn = lambda rows: oracle.kv_write_fp8(w.k, w.v, w.slots, kp, vp, w.k_scale, w.v_scale)
+            else:
+                self.fn = lambda rows: oracle.kv_write(w.k, w.v, w.slots, kp, vp)
             self.rows, self.bytes = None, w.algorithmic_bytes()
             self.desc = f"all {w.num_tokens} tokens of the {name} workload"
             self.cores = 1
@@ -323,6 +327,9 @@ def run_ours(args, rank, local_rank, world):
         if w.mla:
             def call(c, r, s):
                 pa.pa_mla_cache_write(c, r, s, kp, status=status)
+        elif w.fp8:
+            def call(k, v, s):
+                pa.pa_kv_write_fp8(k, v, s, kp, vp, k_scale=w.k_scale, v_scale=w.v_scale, status=status)
         else:
             def call(k, v, s):
                 pa.pa_kv_write(k, v, s, kp, vp, status=status)
@@ -445,7 +452,8 @@ def run_ours(args, rank, local_rank, world):
         "config": dict(cfg, num_splits=args.num_splits or "auto", parallelism=f"replicas x{world}",
                        l2="between timed calls, outside the timed events: a 512 MB buffer written, then another 512 MB read"),
         "roofline": {"bound": "alu" if is_mla else "hbm",
-                     "kernel": ("kv_write_kernel" if is_write else "mla_tc_split_kernel" if is_mla
+                     "kernel": (("kv_write_fp8_kernel" if w.fp8 else "kv_write_kernel") if is_write
+                                else "mla_tc_split_kernel" if is_mla
                                 else "gqa_f8_split_kernel" if getattr(w, "fp8", False) else "gqa_split_kernel"),
                      "achieved": round(kernel_gbs, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(kernel_gbs / peak, 4), "peak_source": f"hbm_gbs of {peak_kind}",

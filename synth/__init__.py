@@ -374,6 +374,9 @@ class KVWriteWorkload:
     num_pages: int
     page_size: int
     mla: bool = False
+    fp8: bool = False          # quantizing write into E4M3 pools
+    k_scale: float = 1.0
+    v_scale: float = 1.0
 
     @property
     def num_tokens(self) -> int:
@@ -385,13 +388,17 @@ class KVWriteWorkload:
         return (self.num_pages, self.page_size) + tuple(self.k.shape[1:])
 
     def empty_pool(self) -> np.ndarray:
+        if self.fp8:
+            return np.full(self.pool_shape(), E4M3_NAN, dtype=np.uint8)
         return np.full(self.pool_shape(), BF16_NAN, dtype=np.uint16)
 
     def algorithmic_bytes(self) -> int:
-        """Bytes read (new rows of the written tokens) plus bytes written (the same rows)."""
+        """Bytes read (the bf16 new rows of the written tokens) plus bytes written (the same rows
+        in the pools: one byte per value for FP8 pools)."""
         written = int((self.slots >= 0).sum())
-        row = (576 * 2) if self.mla else 2 * int(np.prod(self.k.shape[1:])) * 2
-        return 2 * written * row
+        row_in = (576 * 2) if self.mla else 2 * int(np.prod(self.k.shape[1:])) * 2
+        row_out = row_in // 2 if self.fp8 else row_in
+        return written * (row_in + row_out)
 
 
 def make_kv_write(seed: int, num_tokens: int, num_kv_heads: int, head_dim: int, page_size: int,
@@ -413,7 +420,7 @@ def make_kv_write(seed: int, num_tokens: int, num_kv_heads: int, head_dim: int, 
 
 
 WORKLOADS = ("tiny", "llama3-8b", "qwen3-32b", "hd256-window", "mla", "kv-write", "qwen3-32b-verify4",
-             "qwen3-32b-fp8")
+             "qwen3-32b-fp8", "kv-write-fp8")
 
 
 def workload(name: str, seed: Optional[int] = None, scramble: bool = True):
@@ -443,6 +450,10 @@ def workload(name: str, seed: Optional[int] = None, scramble: bool = True):
         # the qwen3-32b rows (same lengths) over an FP8 E4M3 cache
         lens = context_lengths(20262 if seed == 20267 else seed, 32, "loguniform", 128, 16384)
         return make_gqa(seed, lens, 64, 8, 128, 32, name=name, scramble=scramble, fp8=True)
+    if name == "kv-write-fp8":
+        # the kv-write prefill chunk quantized into E4M3 pools (scales 1/64, 1/128)
+        w = make_kv_write(20265 if seed == 20268 else seed, 16384, 8, 128, 32, 1024, name=name)
+        return dataclasses.replace(w, fp8=True, k_scale=float(np.float32(1 / 64)), v_scale=float(np.float32(1 / 128)))
     if name == "kv-write":
         # a 16384-token prefill chunk into a Qwen3-32B-shaped cache (8 KV heads, D 128, page 32)
         return make_kv_write(seed, 16384, 8, 128, 32, 1024, name=name)
