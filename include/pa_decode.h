@@ -168,9 +168,11 @@ int pa_verify_gqa(const void *q, const void *k_pool, const void *v_pool,
  *                shape [batch, num_q_heads, head_dim])
  * Every other argument, the workspace (pa_workspace_size(PA_KIND_GQA, ...)),
  * the window and the error codes are those of pa_verify_gqa; head_dim in
- * {128, 256} (64: PA_ERR_UNSUPPORTED).  The codes widen exactly to f16 for the
- * tensor cores, q is rounded from bf16 to f16 (|q| must stay below 65504) and
- * the weights P to f16 as the MMA operand; the softmax stays fp32.
+ * {128, 256} (64: PA_ERR_UNSUPPORTED).  The codes enter FP8 tensor-core MMAs
+ * unchanged.  Each query column (one head at one position) is scaled by a
+ * power of two and split into two E4M3 terms, exact for every element above
+ * 2^-10 of the column's largest magnitude.  The softmax weights are split into
+ * two terms within 2^-8 relative.  Scores, softmax and accumulation are fp32.
  */
 int pa_decode_gqa_fp8(const void *q, const void *k_pool, const void *v_pool,
                       const int32_t *block_table, const int32_t *context_lens, void *out,
