@@ -53,6 +53,16 @@ KERNEL_SOURCES = {"gqa": ("pa_gqa.cuh", "pa_partition.cuh", "pa_common.cuh"),
                   "mla": ("pa_mla_tc.cuh", "pa_mla.cu", "pa_gqa.cuh", "pa_partition.cuh", "pa_common.cuh")}
 
 
+def compute_dtype(w):
+    """(dtype, description) of the arithmetic the timed path computes in."""
+    import synth
+    if isinstance(w, synth.KVWriteWorkload):
+        return ("f32", "fp32 divide by the scale, e4m3 encode") if w.fp8 else ("bf16", "bf16 copy")
+    if getattr(w, "fp8", False):
+        return "e4m3", "e4m3 tensor-core mma (two-term q and p), f32 softmax and accumulation"
+    return "bf16", "bf16 tensor-core mma, f32 softmax and accumulation"
+
+
 def kernel_kind(workload: str) -> str:
     return "mla" if workload == "mla" else "gqa_f8" if workload.endswith("-fp8") else "gqa"
 
@@ -447,7 +457,7 @@ def run_ours(args, rank, local_rank, world):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "us_per_call": round(ms * 1000, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f16 mma over e4m3 codes, f32 softmax" if getattr(w, "fp8", False) else "bf16",
+        "dtype": compute_dtype(w)[0], "arithmetic": compute_dtype(w)[1],
         "data": "synthetic", "impl": "ours",
         "config": dict(cfg, num_splits=args.num_splits or "auto", parallelism=f"replicas x{world}",
                        l2="between timed calls, outside the timed events: a 512 MB buffer written, then another 512 MB read"),
