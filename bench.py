@@ -1,14 +1,17 @@
 """Benchmark of the paged decode attention hot path on GB300.
 
-One step = one decode call through the C ABI (plan + split-KV attention +
-combine for GQA; plan + q_absorb + attention + merge/W_UV for MLA) over one
-batch of seeded synthetic input of the chosen workload.
+One step = one call through the C ABI over one batch of seeded synthetic
+input of the chosen workload: for GQA (bf16 or FP8 pools, decode or verify)
+the split-KV attention kernel and the combine; for MLA the absorb, the
+attention core, the combine and the W_UV projection; for the KV writes the
+write kernel.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
 Prints ONE JSON line (rank 0).  ``value`` is the achieved HBM bandwidth of the
 whole call: algorithmic bytes (visible K/V rows of every KV head, or latent
-rows for MLA, plus q and the outputs; weights too for MLA) divided by the
+rows for MLA, plus q and the outputs; weights too for MLA; rows read and
+written for the KV writes) divided by the
 device time per call, with the inputs resident in HBM and a 512 MB buffer
 written between timed calls (outside the timed events) so no call reads a
 warm L2.  ``roofline`` reports the dominant kernel (the split-KV attention
@@ -23,8 +26,8 @@ on its GPU (decode attention exchanges nothing between GPUs: replicas / weak
 scaling); the time is the max over ranks and value the sum of all ranks'
 bytes over it.
 
---impl reference times the fp64 CPU oracle (the reference arm of this build)
-on the host cores, on the same workload, metric and unit.
+--impl reference times the fp64 CPU oracle (the reference arm) on the host
+cores, on the same workload, metric and unit.
 """
 from __future__ import annotations
 

@@ -220,8 +220,9 @@ int pa_decode_mla_absorbed(const void *q, const void *cache, const void *w_uk, c
  *     (current) device and caches it; make that first call before starting
  *     any stream capture on the device.
  *   - All calls on a device share the one array.  Nothing in it has to start
- *     at zero (each call's planner rewrites the parts the kernels read before
- *     they read them), but two calls that may overlap on the GPU race on it:
+ *     at zero (each call's split kernel writes every descriptor and partial
+ *     slot the combine kernel then reads), but two calls that may overlap on
+ *     the GPU race on it:
  *     order them on one stream, or use pa_decode_gqa with separate workspaces.
  *   - The array keeps the last call's contents; pa_read_device_status cannot
  *     reach it, so this entry point offers no device status word.

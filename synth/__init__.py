@@ -355,8 +355,8 @@ def make_mla(seed: int, context_lens, num_heads: int, page_size: int, w_std: flo
 
 
 # ---------------------------------------------------------------------------
-# The five workloads of the build (seed = 20260 + index).  Shapes follow the
-# decode geometries the pages discuss; see the design doc for the recipe table.
+# The named workloads (seed = 20260 + index in WORKLOADS).  Shapes follow the
+# decode geometries the pages discuss.
 # ---------------------------------------------------------------------------
 @dataclasses.dataclass
 class KVWriteWorkload:
