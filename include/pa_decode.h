@@ -303,6 +303,16 @@ int pa_set_profile_events(cudaEvent_t before_main, cudaEvent_t after_main);
 /* Number of kernel launches the last decode call on this host thread issued. */
 int pa_last_launch_count(void);
 
+/*
+ * The CUDA runtime error (a cudaError_t value) behind the most recent
+ * PA_ERR_CUDA returned by any entry point on the calling thread, and its
+ * text; cudaSuccess (0) and "no error" if no call on this thread has returned
+ * PA_ERR_CUDA.  Calls that succeed leave it unchanged.  The pages describe no
+ * counterpart: it is diagnostics for the boundary's PA_ERR_CUDA code.
+ */
+int pa_last_cuda_error(void);
+const char *pa_last_cuda_error_string(void);
+
 #ifdef __cplusplus
 }
 #endif

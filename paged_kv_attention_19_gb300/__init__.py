@@ -8,7 +8,8 @@ library has not been built (``python paged_kv_attention_19_gb300/build.py``).
 Names follow the C ABI: ``pa_workspace_size``, ``pa_decode_gqa``,
 ``pa_decode_mla_absorbed``, ``pa_verify_gqa``, ``pa_decode_gqa_fp8``, ``pa_decode_gqa_noalloc``,
 ``pa_kv_write``, ``pa_kv_write_fp8``, ``pa_mla_cache_write``, ``pa_status_string``, ``pa_read_device_status``,
-``pa_set_profile_events``, ``pa_last_launch_count``.  The tensor-taking
+``pa_set_profile_events``, ``pa_last_launch_count``, ``pa_last_cuda_error``,
+``pa_last_cuda_error_string``.  The tensor-taking
 functions accept torch tensors (device memory, the layouts of the header) and
 infer every size from their shapes.
 """
@@ -51,6 +52,8 @@ SIGNATURES = {
     "pa_read_device_status": (_I, [_P, _P, _U32P]),
     "pa_set_profile_events": (_I, [_P, _P]),
     "pa_last_launch_count": (_I, []),
+    "pa_last_cuda_error": (_I, []),
+    "pa_last_cuda_error_string": (ctypes.c_char_p, []),
 }
 
 
@@ -72,7 +75,8 @@ lib = _load()
 class PaError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
-        super().__init__(f"{what}: {pa_status_string(status)} ({status})")
+        detail = f"; {lib.pa_last_cuda_error_string().decode()}" if status == PA_ERR_CUDA else ""
+        super().__init__(f"{what}: {pa_status_string(status)} ({status}){detail}")
 
 
 def pa_status_string(status: int) -> str:
@@ -229,6 +233,14 @@ def pa_set_profile_events(before=None, after=None) -> None:
 
 def pa_last_launch_count() -> int:
     return int(lib.pa_last_launch_count())
+
+
+def pa_last_cuda_error() -> int:
+    return int(lib.pa_last_cuda_error())
+
+
+def pa_last_cuda_error_string() -> str:
+    return lib.pa_last_cuda_error_string().decode()
 
 
 def workspace_for_gqa(q, k_pool, block_table, num_splits: int = 0, max_context_len=None, device=None):

@@ -33,6 +33,7 @@ constexpr long long kPieceCostBytesF8 = 128 << 10;
 thread_local cudaEvent_t t_ev_before = nullptr;
 thread_local cudaEvent_t t_ev_after = nullptr;
 thread_local int t_last_launches = 0;
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
@@ -140,6 +141,11 @@ int sm_count() {
 
 namespace pa {
 void note_launches(int n) { t_last_launches = n; }
+int cuda_fail(cudaError_t e) {
+  if (e == cudaSuccess) e = cudaGetLastError();
+  t_last_cuda_error = e == cudaSuccess ? cudaErrorUnknown : e;
+  return PA_ERR_CUDA;
+}
 cudaError_t profile_mark(bool before, cudaStream_t stream) {
   cudaEvent_t e = before ? t_ev_before : t_ev_after;
   return e ? cudaEventRecord(e, stream) : cudaSuccess;
@@ -214,7 +220,7 @@ int gqa_call(const void *q, const void *k_pool, const void *v_pool, const int32_
       !encode_q_map(&tm_q, q, (long long)batch * Q, num_q_heads, D, gt, qt))
     return PA_ERR_UNSUPPORTED;
   const int sms = sm_count();
-  if (sms <= 0) return PA_ERR_CUDA;
+  if (sms <= 0) return pa::cuda_fail(cudaSuccess);
   const int nparts = num_splits > 0 ? num_splits : (sms < kAutoPartsMax ? sms : kAutoPartsMax);
 
   uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -278,7 +284,9 @@ int gqa_call(const void *q, const void *k_pool, const void *v_pool, const int32_
   ca.ntile = ntile;
 
   cudaError_t e;
-  if (t_ev_before && cudaEventRecord(t_ev_before, stream) != cudaSuccess) return PA_ERR_CUDA;
+  if (t_ev_before) {
+    if (const cudaError_t ce = cudaEventRecord(t_ev_before, stream); ce != cudaSuccess) return pa::cuda_fail(ce);
+  }
   if (f8.on) {
     e = D == 128 ? launch_gqa_split_fp8_d128(nparts, tm_k, tm_v, tm_q, ga, stream)
                  : launch_gqa_split_fp8_d256(nparts, tm_k, tm_v, tm_q, ga, stream);
@@ -289,15 +297,17 @@ int gqa_call(const void *q, const void *k_pool, const void *v_pool, const int32_
       default: e = launch_gqa_split_d256(nparts, tm_k, tm_v, tm_q, ga, stream); break;
     }
   }
-  if (e != cudaSuccess) return PA_ERR_CUDA;
+  if (e != cudaSuccess) return pa::cuda_fail(e);
   ++t_last_launches;
-  if (t_ev_after && cudaEventRecord(t_ev_after, stream) != cudaSuccess) return PA_ERR_CUDA;
+  if (t_ev_after) {
+    if (const cudaError_t ce = cudaEventRecord(t_ev_after, stream); ce != cudaSuccess) return pa::cuda_fail(ce);
+  }
   switch (D) {
     case 64: e = launch_gqa_combine_d64(ca, stream); break;
     case 128: e = launch_gqa_combine_d128(ca, stream); break;
     default: e = launch_gqa_combine_d256(ca, stream); break;
   }
-  if (e != cudaSuccess) return PA_ERR_CUDA;
+  if (e != cudaSuccess) return pa::cuda_fail(e);
   ++t_last_launches;
   return PA_OK;
 }
@@ -367,8 +377,8 @@ int pa_read_device_status(const void *workspace, cudaStream_t stream, uint32_t *
   if (!workspace || !out_bits) return PA_ERR_INVALID_ARGUMENT;
   if (!aligned(workspace, 16)) return PA_ERR_MISALIGNED;
   uint32_t v = 0;
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return PA_ERR_CUDA;
-  if (cudaMemcpy(&v, workspace, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return PA_ERR_CUDA;
+  if (const cudaError_t ce = cudaStreamSynchronize(stream); ce != cudaSuccess) return pa::cuda_fail(ce);
+  if (const cudaError_t ce = cudaMemcpy(&v, workspace, sizeof v, cudaMemcpyDeviceToHost); ce != cudaSuccess) return pa::cuda_fail(ce);
   *out_bits = v;
   return PA_OK;
 }
@@ -381,5 +391,9 @@ int pa_set_profile_events(cudaEvent_t before_main, cudaEvent_t after_main) {
 }
 
 int pa_last_launch_count(void) { return t_last_launches; }
+
+int pa_last_cuda_error(void) { return (int)t_last_cuda_error; }
+
+const char *pa_last_cuda_error_string(void) { return cudaGetErrorString(t_last_cuda_error); }
 
 }  // extern "C"

@@ -131,15 +131,16 @@ extern "C" int pa_kv_write(const void *k, const void *v, const int64_t *slot_map
   const int vec_per_token = num_kv_heads * head_dim / 8;
   const long long n_vec = (long long)num_tokens * vec_per_token;
   const int grid = pa::grid_for(n_vec);
-  if (grid <= 0) return PA_ERR_CUDA;
+  if (grid <= 0) return pa::cuda_fail(cudaSuccess);
   pa::note_launches(0);
-  if (pa::profile_mark(true, stream) != cudaSuccess) return PA_ERR_CUDA;
+  if (const cudaError_t ce = pa::profile_mark(true, stream); ce != cudaSuccess) return pa::cuda_fail(ce);
   pa::kv_write_kernel<<<grid, 256, 0, stream>>>(
       static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping, static_cast<uint4 *>(k_pool),
       static_cast<uint4 *>(v_pool), n_vec, vec_per_token, (long long)num_pages * page_size, status);
-  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  if (const cudaError_t ce = cudaGetLastError(); ce != cudaSuccess) return pa::cuda_fail(ce);
   pa::note_launches(1);
-  return pa::profile_mark(false, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  if (const cudaError_t ce = pa::profile_mark(false, stream); ce != cudaSuccess) return pa::cuda_fail(ce);
+  return PA_OK;
 }
 
 extern "C" int pa_kv_write_fp8(const void *k, const void *v, const int64_t *slot_mapping, void *k_pool,
@@ -159,16 +160,17 @@ extern "C" int pa_kv_write_fp8(const void *k, const void *v, const int64_t *slot
   const int vec_per_token = num_kv_heads * head_dim / 16;  // 16-byte vectors of codes
   const long long n_vec = (long long)num_tokens * vec_per_token;
   const int grid = pa::grid_for(n_vec);
-  if (grid <= 0) return PA_ERR_CUDA;
+  if (grid <= 0) return pa::cuda_fail(cudaSuccess);
   pa::note_launches(0);
-  if (pa::profile_mark(true, stream) != cudaSuccess) return PA_ERR_CUDA;
+  if (const cudaError_t ce = pa::profile_mark(true, stream); ce != cudaSuccess) return pa::cuda_fail(ce);
   pa::kv_write_fp8_kernel<<<grid, 256, 0, stream>>>(
       static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping, static_cast<uint4 *>(k_pool),
       static_cast<uint4 *>(v_pool), n_vec, vec_per_token, (long long)num_pages * page_size, k_scale, v_scale,
       status);
-  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  if (const cudaError_t ce = cudaGetLastError(); ce != cudaSuccess) return pa::cuda_fail(ce);
   pa::note_launches(1);
-  return pa::profile_mark(false, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  if (const cudaError_t ce = pa::profile_mark(false, stream); ce != cudaSuccess) return pa::cuda_fail(ce);
+  return PA_OK;
 }
 
 extern "C" int pa_mla_cache_write(const void *c_lat, const void *k_rope, const int64_t *slot_mapping, void *cache,
@@ -182,13 +184,14 @@ extern "C" int pa_mla_cache_write(const void *c_lat, const void *k_rope, const i
     return PA_ERR_MISALIGNED;
   const long long n_vec = (long long)num_tokens * 72;
   const int grid = pa::grid_for(n_vec);
-  if (grid <= 0) return PA_ERR_CUDA;
+  if (grid <= 0) return pa::cuda_fail(cudaSuccess);
   pa::note_launches(0);
-  if (pa::profile_mark(true, stream) != cudaSuccess) return PA_ERR_CUDA;
+  if (const cudaError_t ce = pa::profile_mark(true, stream); ce != cudaSuccess) return pa::cuda_fail(ce);
   pa::mla_cache_write_kernel<<<grid, 256, 0, stream>>>(
       static_cast<const uint4 *>(c_lat), static_cast<const uint4 *>(k_rope), slot_mapping,
       static_cast<uint4 *>(cache), n_vec, (long long)num_pages * page_size, status);
-  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  if (const cudaError_t ce = cudaGetLastError(); ce != cudaSuccess) return pa::cuda_fail(ce);
   pa::note_launches(1);
-  return pa::profile_mark(false, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  if (const cudaError_t ce = pa::profile_mark(false, stream); ce != cudaSuccess) return pa::cuda_fail(ce);
+  return PA_OK;
 }

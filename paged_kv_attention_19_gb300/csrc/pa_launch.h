@@ -8,6 +8,9 @@ namespace pa {
 // Bookkeeping of the profiling hook and launch counter of the C ABI (pa_api.cu).
 void note_launches(int n);
 cudaError_t profile_mark(bool before, cudaStream_t stream);
+// Records e (or the thread's last CUDA error, if e is cudaSuccess) as the CUDA error behind
+// a PA_ERR_CUDA return, and returns PA_ERR_CUDA.
+int cuda_fail(cudaError_t e);
 
 struct GqaArgs;
 struct CombineArgs;

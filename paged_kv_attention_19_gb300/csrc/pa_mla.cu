@@ -348,7 +348,7 @@ int mla_decode(const void *q, const void *cache, const void *w_uk, const void *w
   if (!encode_cache_map(&tm_c, cache, num_pages, P, BH) || !encode_qabs_map(&tm_q, q_abs, (long long)batch * H))
     return PA_ERR_UNSUPPORTED;
   const int sms = sm_count_mla();
-  if (sms <= 0) return PA_ERR_CUDA;
+  if (sms <= 0) return pa::cuda_fail(cudaSuccess);
   const int nparts = num_splits > 0 ? num_splits : (sms < kAutoPartsMax ? sms : kAutoPartsMax);
 
   WsHeader *hdr = reinterpret_cast<WsHeader *>(ws);
@@ -360,18 +360,19 @@ int mla_decode(const void *q, const void *cache, const void *w_uk, const void *w
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    if (cudaFuncSetAttribute(mla_tc_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, MlaTcSmem::BYTES) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(q_absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PROJ_SMEM) != cudaSuccess ||
-        cudaFuncSetAttribute(mla_uv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PROJ_SMEM) != cudaSuccess)
-      return PA_ERR_CUDA;
+    for (const void *k : {(const void *)mla_tc_split_kernel, (const void *)q_absorb_kernel, (const void *)mla_uv_kernel}) {
+      const int bytes = k == (const void *)mla_tc_split_kernel ? MlaTcSmem::BYTES : PROJ_SMEM;
+      if (const cudaError_t ce = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+          ce != cudaSuccess)
+        return pa::cuda_fail(ce);
+    }
     configured_device = dev;
   }
 
   // 1. q_abs
   q_absorb_kernel<<<H, 256, PROJ_SMEM, stream>>>(static_cast<const uint16_t *>(q), static_cast<const uint16_t *>(w_uk),
                                                   q_abs, q_lo, batch, H);
-  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  if (const cudaError_t ce = cudaGetLastError(); ce != cudaSuccess) return pa::cuda_fail(ce);
   ++*launches;
 
   // 2-6. the attention core
@@ -398,14 +399,18 @@ int mla_decode(const void *q, const void *cache, const void *w_uk, const void *w
   ma.nparts = nparts;
   ma.hg = pl.ntile < nparts ? pl.ntile : nparts;
   ma.qscale = scale * LOG2E;
-  if (ev_before && cudaEventRecord(ev_before, stream) != cudaSuccess) return PA_ERR_CUDA;
+  if (ev_before) {
+    if (const cudaError_t ce = cudaEventRecord(ev_before, stream); ce != cudaSuccess) return pa::cuda_fail(ce);
+  }
   {
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = pdl_config(dim3(nparts), dim3(C::THREADS), MlaTcSmem::BYTES, stream, attr);
-    if (cudaLaunchKernelEx(&cfg, mla_tc_split_kernel, tm_c, tm_q, ma) != cudaSuccess) return PA_ERR_CUDA;
+    if (const cudaError_t ce = cudaLaunchKernelEx(&cfg, mla_tc_split_kernel, tm_c, tm_q, ma); ce != cudaSuccess) return pa::cuda_fail(ce);
   }
   ++*launches;
-  if (ev_after && cudaEventRecord(ev_after, stream) != cudaSuccess) return PA_ERR_CUDA;
+  if (ev_after) {
+    if (const cudaError_t ce = cudaEventRecord(ev_after, stream); ce != cudaSuccess) return pa::cuda_fail(ce);
+  }
 
   // merge of split sequences into o_lat (and lse)
   CombineArgs ca;
@@ -424,17 +429,18 @@ int mla_decode(const void *q, const void *cache, const void *w_uk, const void *w
   ca.gt = PART_HEADS;
   ca.qt = 1;
   ca.ntile = pl.ntile;
-  if (launch_combine<MLA_LAT>(ca, stream) != cudaSuccess) return PA_ERR_CUDA;
+  if (const cudaError_t ce = launch_combine<MLA_LAT>(ca, stream); ce != cudaSuccess) return pa::cuda_fail(ce);
   ++*launches;
 
   // 7. o = W_UV . o_lat
   {
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = pdl_config(dim3(H), dim3(256), PROJ_SMEM, stream, attr);
-    if (cudaLaunchKernelEx(&cfg, mla_uv_kernel, (const uint16_t *)o_lat, static_cast<const uint16_t *>(w_uv),
-                           static_cast<uint16_t *>(out), (const uint16_t *)q_lo, lse, scale, batch, H,
-                           &hdr->status) != cudaSuccess)
-      return PA_ERR_CUDA;
+    if (const cudaError_t ce = cudaLaunchKernelEx(&cfg, mla_uv_kernel, (const uint16_t *)o_lat,
+                                                  static_cast<const uint16_t *>(w_uv), static_cast<uint16_t *>(out),
+                                                  (const uint16_t *)q_lo, lse, scale, batch, H, &hdr->status);
+        ce != cudaSuccess)
+      return pa::cuda_fail(ce);
   }
   ++*launches;
   return PA_OK;

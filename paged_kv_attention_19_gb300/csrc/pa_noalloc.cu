@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "pa_decode.h"
+#include "pa_launch.h"
 
 namespace {
 
@@ -26,12 +27,13 @@ void *g_scratch_ptr[kMaxDevices] = {};
 // Device address of the scratch on the current device, looked up once per device.
 int scratch_address(void **out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+  if (const cudaError_t ce = cudaGetDevice(&dev); ce != cudaSuccess) return pa::cuda_fail(ce);
   if (dev < 0 || dev >= kMaxDevices) return PA_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_mu);
   if (!g_scratch_ptr[dev]) {
     void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_pa_scratch) != cudaSuccess || p == nullptr) return PA_ERR_CUDA;
+    if (const cudaError_t ce = cudaGetSymbolAddress(&p, g_pa_scratch); ce != cudaSuccess || p == nullptr)
+      return pa::cuda_fail(ce);
     g_scratch_ptr[dev] = p;
   }
   *out = g_scratch_ptr[dev];

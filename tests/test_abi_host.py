@@ -194,3 +194,9 @@ def test_kv_write_fp8_host_validation(pa):
     assert kw(kp=None) == pa.PA_ERR_INVALID_ARGUMENT
     assert kw(vp=0x50008) == pa.PA_ERR_MISALIGNED
     assert kw(s=0x30004) == pa.PA_ERR_MISALIGNED
+
+
+def test_last_cuda_error_starts_clean(pa):
+    # no call on this thread has returned PA_ERR_CUDA: no error recorded
+    assert pa.pa_last_cuda_error() == 0
+    assert isinstance(pa.pa_last_cuda_error_string(), str)
