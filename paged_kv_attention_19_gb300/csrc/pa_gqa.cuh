@@ -714,10 +714,12 @@ struct CombineArgs {
 // CTA c's slot (1 if the CTA has several pieces, else 0) and slot 0 of CTAs
 // c + hg, c + 2 hg, ... (the same head in the following groups) up to the
 // first one whose first piece ends the sequence.
-// Warp w handles heads w, w + 4, ...: weights exp2(lse_k - M), then
+// Warp w handles MMA row w (one warp per row, so the rows' few dependent
+// loads from L2 overlap instead of queueing): weights exp2(lse_k - M), then
 // o = sum_k w_k o_k / sum_k w_k in ascending k, each lane owning D/32 dims.
+constexpr int COMBINE_THREADS = PART_HEADS * 32;
 template <int D>
-__global__ void __launch_bounds__(128) gqa_combine_kernel(const CombineArgs a) {
+__global__ void __launch_bounds__(COMBINE_THREADS) gqa_combine_kernel(const CombineArgs a) {
   pdl_wait();               // the split kernel's partials and descriptors are visible from here on
   pdl_launch_dependents();  // a following kernel (MLA: the W_UV projection) may stage its inputs
   const int c = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -749,8 +751,9 @@ __global__ void __launch_bounds__(128) gqa_combine_kernel(const CombineArgs a) {
   const Tile tl = tile_of(d0.last_hs % a.ntile, a.G, a.nsub, a.Q, a.qt);
   const int hq0 = g * a.G + tl.h0;
   constexpr int PER = D / 32;  // 2, 4 or 8 consecutive dims per lane
-  for (int h = warp; h < tl.nq * a.gt; h += 4) {  // h: the MMA row
-    if (h % a.gt >= tl.nh) continue;
+  {
+    const int h = warp;  // the MMA row
+    if (h >= tl.nq * a.gt || h % a.gt >= tl.nh) return;
     float M = -INFINITY;
     for (int i = lane; i < k; i += 32) {
       const size_t pi = i == 0 ? (size_t)c * 2 + first_slot : (size_t)(c + i * a.hg) * 2;
