@@ -33,53 +33,69 @@ __device__ __forceinline__ uint32_t pack_u16(uint16_t lo, uint16_t hi) {
   return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
-// Shared-memory rows of the projection weights are padded to 520 bf16 (1040 bytes): the
-// 16-byte offset between consecutive rows keeps fragment loads free of bank conflicts.
+// Activation rows in shared memory are padded to 520 bf16 (1040 bytes): the 16-byte offset
+// between consecutive rows keeps fragment loads free of bank conflicts.
 constexpr int WROW = MLA_LAT + 8;
-constexpr int PROJ_SMEM = 128 * WROW * 2 + 16 * WROW * 2 + 16;  // one head's weights, 16 activation rows, a barrier
+// Projection weights arrive by TMA in boxes of 64 columns (128 bytes) with the 128-byte swizzle:
+// a plane holds one box, rows of 128 bytes, the 16-byte chunk c of row r at c ^ (r & 7).
+// q_absorb stages a head's W_UK column quarter (128 rows x 128 columns: 2 planes of 16 KB),
+// mla_uv a head's W_UV row half (64 rows x 512 columns: 8 planes of 8 KB).
+constexpr int ABS_PARTS = 4, UV_PARTS = 2;
+constexpr int ABS_COLS = MLA_LAT / ABS_PARTS;  // 128 latent columns per absorb block
+constexpr int UV_ROWS = MLA_V / UV_PARTS;      // 64 output dims per projection block
+constexpr int ABS_PLANE = 128 * 128, UV_PLANE = UV_ROWS * 128;
+constexpr int ABS_W = (ABS_COLS / 64) * ABS_PLANE;  // 32 KB
+constexpr int UV_W = (MLA_LAT / 64) * UV_PLANE;      // 64 KB
+constexpr int PROJ_SMEM = 1024 + (ABS_W > UV_W ? ABS_W : UV_W) + 16 * WROW * 2 + 16;  // alignment, weights, rows, barrier
 
-// Stage 128 rows of 512 bf16 (one head's weights) into padded shared-memory rows with TMA bulk
-// copies (warp 0 issues them, completion counted on *bar).
-__device__ __forceinline__ void stage_weights_issue(uint16_t *w, const uint16_t *src, uint64_t *bar) {
+// Byte offset of (row, col) in staged weights with planes of `plane` bytes (col a multiple of 8).
+__device__ __forceinline__ uint32_t wsw(int plane, int row, int col) {
+  return (uint32_t)((col >> 6) * plane + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4));
+}
+
+// The projection kernels' weight planes start on a 1024-byte boundary (the swizzle pattern
+// repeats every 1024 bytes).
+__device__ __forceinline__ uint8_t *proj_weights(uint8_t *raw) {
+  return raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
+}
+
+// Thread 0 initialises *bar and issues n_box copies of the box at (x0 + 64 i, y) into planes of
+// `plane` bytes at w; completion counted on *bar.
+__device__ __forceinline__ void stage_weights_issue(uint8_t *w, const CUtensorMap *map, int x0, int y, int n_box,
+                                                    int plane, uint64_t *bar) {
   if (threadIdx.x == 0) {
     mbar_init(bar, 1);
     fence_mbar_init();
-  }
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    if (threadIdx.x == 0) mbar_arrive_expect_tx(bar, 128u * MLA_LAT * 2);
-    __syncwarp();
-    for (int r = threadIdx.x; r < 128; r += 32) bulk_load(w + r * WROW, src + (size_t)r * MLA_LAT, MLA_LAT * 2, bar);
+    mbar_arrive_expect_tx(bar, (uint32_t)(n_box * plane));
+    for (int i = 0; i < n_box; ++i) tma_load_2d(w + i * plane, map, x0 + 64 * i, y, bar);
   }
 }
 
 // q_lat[b][h][j] = sum_d q_nope[b][h][d] * W_UK[h][d][j] (fp32): q_abs[b][h] = bf16(q_lat) ||
 // q_rope (576) and q_lo[b][h] = bf16(q_lat - bf16(q_lat)) (512, for the LSE term of the
-// projection kernel).  One block of 8 warps per head: W_UK[h] (128 x 512) is staged in shared
-// memory with coalesced 16-byte loads; the batch rows (16 per tile) are the M dimension of
-// m16n8k16 MMAs, warp w producing latent columns [64 w, 64 w + 64).
-__global__ void __launch_bounds__(256) q_absorb_kernel(const uint16_t *q, const uint16_t *w_uk, uint16_t *q_abs,
-                                                       uint16_t *q_lo, int B, int H) {
-  extern __shared__ __align__(16) uint8_t psmem[];
-  uint16_t *w = reinterpret_cast<uint16_t *>(psmem);        // [128 d][WROW]
-  uint16_t *qn = w + 128 * WROW;                            // [16 rows][WROW] (first 128 used)
+// projection kernel).  Block (h, part) of 8 warps computes latent columns [128 part, +128) of
+// head h from its W_UK quarter (128 x 128, staged by TMA); the batch rows (16 per tile) are the
+// M dimension of m16n8k16 MMAs, warp w producing columns [16 w, 16 w + 16) of the quarter.
+__global__ void __launch_bounds__(256) q_absorb_kernel(const __grid_constant__ CUtensorMap tm_w, const uint16_t *q,
+                                                       uint16_t *q_abs, uint16_t *q_lo, int B, int H,
+                                                       uint32_t *status) {
+  extern __shared__ __align__(1024) uint8_t psmem[];
+  uint8_t *w = proj_weights(psmem);                                  // W_UK[h][:, quarter]
+  uint16_t *qn = reinterpret_cast<uint16_t *>(w + ABS_W);            // [16 rows][WROW] (first 128 used)
+  uint64_t *bar = reinterpret_cast<uint64_t *>(qn + 16 * WROW);
   pdl_launch_dependents();  // the split kernel may start its prologue; it waits for q_abs
-  const int h = blockIdx.x;
+  const int h = blockIdx.x / ABS_PARTS, part = blockIdx.x % ABS_PARTS;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, tq = lane & 3;
   const int lm_mat = lane >> 3, lm_row = lane & 7;
-  {
-    const uint16_t *wsrc = w_uk + (size_t)h * MLA_NOPE * MLA_LAT;
-    for (int i = tid; i < MLA_NOPE * (MLA_LAT / 8); i += 256) {
-      const int d = i / (MLA_LAT / 8), c = i % (MLA_LAT / 8);
-      *reinterpret_cast<uint4 *>(w + d * WROW + c * 8) = *reinterpret_cast<const uint4 *>(wsrc + (size_t)d * MLA_LAT + c * 8);
+  stage_weights_issue(w, &tm_w, part * ABS_COLS, h * MLA_NOPE, ABS_COLS / 64, ABS_PLANE, bar);
+  if (part == 0) {
+    // the rope part is copied as it is (8 vectors of 16 bytes per row)
+    for (int i = tid; i < B * 8; i += 256) {
+      const int b = i >> 3, c = i & 7;
+      *reinterpret_cast<uint4 *>(q_abs + ((size_t)b * H + h) * MLA_C + MLA_LAT + c * 8) =
+          *reinterpret_cast<const uint4 *>(q + ((size_t)b * H + h) * MLA_QD + MLA_NOPE + c * 8);
     }
-  }
-  // the rope part is copied as it is (8 vectors of 16 bytes per row)
-  for (int i = tid; i < B * 8; i += 256) {
-    const int b = i >> 3, c = i & 7;
-    *reinterpret_cast<uint4 *>(q_abs + ((size_t)b * H + h) * MLA_C + MLA_LAT + c * 8) =
-        *reinterpret_cast<const uint4 *>(q + ((size_t)b * H + h) * MLA_QD + MLA_NOPE + c * 8);
   }
   for (int m0 = 0; m0 < B; m0 += 16) {
     for (int i = tid; i < 16 * (MLA_NOPE / 8); i += 256) {
@@ -89,32 +105,31 @@ __global__ void __launch_bounds__(256) q_absorb_kernel(const uint16_t *q, const 
           b < B ? *reinterpret_cast<const uint4 *>(q + ((size_t)b * H + h) * MLA_QD + c * 8) : make_uint4(0, 0, 0, 0);
     }
     __syncthreads();
-    float acc[8][4];
+    if (m0 == 0 && !mbar_wait(bar, 0, status)) return;  // the weights have landed
+    float acc[2][4];
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
 #pragma unroll
     for (int k0 = 0; k0 < MLA_NOPE; k0 += 16) {
-      uint32_t af[4];
+      uint32_t af[4], bf[4];
       {
         const int row = (lm_mat & 1) * 8 + lm_row, col = k0 + (lm_mat >> 1) * 8;
         ldmatrix_x4(af, smem_u32(qn + row * WROW + col));
       }
-#pragma unroll
-      for (int nt = 0; nt < 8; nt += 2) {
-        // W rows k0..k0+15 (k), columns 64 warp + 8 nt .. + 16 (two n-tiles), transposed
-        uint32_t bf[4];
-        const int krow = k0 + (lm_mat & 1) * 8 + lm_row, col = warp * 64 + nt * 8 + (lm_mat >> 1) * 8;
-        ldmatrix_x4_trans(bf, smem_u32(w + krow * WROW + col));
-        mma_bf16_16816(acc[nt], af, bf[0], bf[1]);
-        mma_bf16_16816(acc[nt + 1], af, bf[2], bf[3]);
+      {
+        // W rows k0..k0+15 (k), columns 16 warp .. + 16 of the quarter (two n-tiles), transposed
+        const int krow = k0 + (lm_mat & 1) * 8 + lm_row, col = warp * 16 + (lm_mat >> 1) * 8;
+        ldmatrix_x4_trans(bf, smem_u32(w) + wsw(ABS_PLANE, krow, col));
       }
+      mma_bf16_16816(acc[0], af, bf[0], bf[1]);
+      mma_bf16_16816(acc[1], af, bf[2], bf[3]);
     }
     const int r0 = m0 + g, r1 = m0 + g + 8;
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      const int col = warp * 64 + nt * 8 + 2 * tq;
+    for (int nt = 0; nt < 2; ++nt) {
+      const int col = part * ABS_COLS + warp * 16 + nt * 8 + 2 * tq;
       const uint32_t h0 = pack_bf16x2(acc[nt][0], acc[nt][1]), h1 = pack_bf16x2(acc[nt][2], acc[nt][3]);
       const uint32_t l0 = pack_bf16x2(acc[nt][0] - __uint_as_float(h0 << 16), acc[nt][1] - __uint_as_float(h0 & 0xffff0000u));
       const uint32_t l1 = pack_bf16x2(acc[nt][2] - __uint_as_float(h1 << 16), acc[nt][3] - __uint_as_float(h1 & 0xffff0000u));
@@ -131,24 +146,26 @@ __global__ void __launch_bounds__(256) q_absorb_kernel(const uint16_t *q, const 
   }
 }
 
-// o[b][h][v] = sum_j W_UV[h][v][j] o_lat[b][h][j] on the tensor cores.  One block of 8 warps
-// per head: W_UV[h] (128 x 512) is staged in shared memory with coalesced 16-byte loads; warp
-// w produces v in [16 w, 16 w + 16) for 16 batch rows per tile.  With lse, it also adds the
-// first-order LSE term of q_lat's bf16 rounding: lse += scale * (q_lo . o_lat).
-__global__ void __launch_bounds__(256) mla_uv_kernel(const uint16_t *o_lat, const uint16_t *w_uv, uint16_t *out,
-                                                     const uint16_t *q_lo, float *lse, float scale, int B, int H,
-                                                     uint32_t *status) {
-  extern __shared__ __align__(16) uint8_t psmem[];
-  uint16_t *w = reinterpret_cast<uint16_t *>(psmem);  // [128 v][WROW]
-  uint16_t *ol = w + 128 * WROW;                      // [16 rows][WROW]
+// o[b][h][v] = sum_j W_UV[h][v][j] o_lat[b][h][j] on the tensor cores.  Block (h, part) of 8
+// warps computes v in [64 part, +64) from its W_UV half (64 x 512, staged by TMA before the wait
+// for the previous kernels); warp w produces v in [8 w, 8 w + 8) of the half for 16 batch rows
+// per tile.  Part 0 also adds, with lse, the first-order LSE term of q_lat's bf16 rounding:
+// lse += scale * (q_lo . o_lat).
+__global__ void __launch_bounds__(256) mla_uv_kernel(const __grid_constant__ CUtensorMap tm_w, const uint16_t *o_lat,
+                                                     uint16_t *out, const uint16_t *q_lo, float *lse, float scale,
+                                                     int B, int H, uint32_t *status) {
+  extern __shared__ __align__(1024) uint8_t psmem[];
+  uint8_t *w = proj_weights(psmem);                                    // W_UV[h][half, :]
+  uint16_t *ol = reinterpret_cast<uint16_t *>(w + UV_W);               // [16 rows][WROW]
   uint64_t *bar = reinterpret_cast<uint64_t *>(ol + 16 * WROW);
-  const int h = blockIdx.x;
+  const int h = blockIdx.x / UV_PARTS, part = blockIdx.x % UV_PARTS;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, tq = lane & 3;
   const int lm_mat = lane >> 3, lm_row = lane & 7;
-  stage_weights_issue(w, w_uv + (size_t)h * MLA_V * MLA_LAT, bar);
+  stage_weights_issue(w, &tm_w, 0, h * MLA_V + part * UV_ROWS, MLA_LAT / 64, UV_PLANE, bar);
+  __syncthreads();  // the barrier is initialised before any thread waits on it
   pdl_wait();  // o_lat, lse and the status word (split and combine kernels) are final from here on
-  mbar_wait(bar, 0, status);
+  if (!mbar_wait(bar, 0, status)) return;
   for (int m0 = 0; m0 < B; m0 += 16) {
     for (int i = tid; i < 16 * (MLA_LAT / 8); i += 256) {
       const int r = i / (MLA_LAT / 8), c = i % (MLA_LAT / 8);
@@ -157,7 +174,7 @@ __global__ void __launch_bounds__(256) mla_uv_kernel(const uint16_t *o_lat, cons
           b < B ? *reinterpret_cast<const uint4 *>(o_lat + ((size_t)b * H + h) * MLA_LAT + c * 8) : make_uint4(0, 0, 0, 0);
     }
     __syncthreads();
-    if (lse) {
+    if (lse && part == 0) {
       // warp w: rows 2 w, 2 w + 1; lane l: dims [16 l, 16 l + 16)
       for (int r = warp * 2; r < warp * 2 + 2; ++r) {
         const int b = m0 + r;
@@ -184,35 +201,36 @@ __global__ void __launch_bounds__(256) mla_uv_kernel(const uint16_t *o_lat, cons
         }
       }
     }
+    // two accumulators (even and odd k-steps): two independent MMA chains
     float acc[2][4];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+    for (int q2 = 0; q2 < 2; ++q2)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
-#pragma unroll 8
-    for (int k0 = 0; k0 < MLA_LAT; k0 += 16) {
-      uint32_t af[4], bf[4];
+      for (int e = 0; e < 4; ++e) acc[q2][e] = 0.f;
+#pragma unroll 4
+    for (int k0 = 0; k0 < MLA_LAT; k0 += 32) {
+      uint32_t af0[4], af1[4], bf[4];
       {
         const int row = (lm_mat & 1) * 8 + lm_row, col = k0 + (lm_mat >> 1) * 8;
-        ldmatrix_x4(af, smem_u32(ol + row * WROW + col));
+        ldmatrix_x4(af0, smem_u32(ol + row * WROW + col));
+        ldmatrix_x4(af1, smem_u32(ol + row * WROW + col + 16));
       }
       {
-        // B = W_UV^T: W rows v (the n index), columns k0.. (the k index), not transposed
-        const int vrow = warp * 16 + (lm_mat >> 1) * 8 + lm_row, col = k0 + (lm_mat & 1) * 8;
-        ldmatrix_x4(bf, smem_u32(w + vrow * WROW + col));
+        // B = W_UV^T: W rows v (the n index, 8 of them), columns k0 .. k0 + 31 (two k-steps)
+        const int vrow = warp * 8 + lm_row, col = k0 + lm_mat * 8;
+        ldmatrix_x4(bf, smem_u32(w) + wsw(UV_PLANE, vrow, col));
       }
-      mma_bf16_16816(acc[0], af, bf[0], bf[1]);
-      mma_bf16_16816(acc[1], af, bf[2], bf[3]);
+      mma_bf16_16816(acc[0], af0, bf[0], bf[1]);
+      mma_bf16_16816(acc[1], af1, bf[2], bf[3]);
     }
     const int r0 = m0 + g, r1 = m0 + g + 8;
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      const int col = warp * 16 + nt * 8 + 2 * tq;
-      if (r0 < B)
-        *reinterpret_cast<uint32_t *>(out + ((size_t)r0 * H + h) * MLA_V + col) = pack_bf16x2(acc[nt][0], acc[nt][1]);
-      if (r1 < B)
-        *reinterpret_cast<uint32_t *>(out + ((size_t)r1 * H + h) * MLA_V + col) = pack_bf16x2(acc[nt][2], acc[nt][3]);
-    }
+    const int col = part * UV_ROWS + warp * 8 + 2 * tq;
+    if (r0 < B)
+      *reinterpret_cast<uint32_t *>(out + ((size_t)r0 * H + h) * MLA_V + col) =
+          pack_bf16x2(acc[0][0] + acc[1][0], acc[0][1] + acc[1][1]);
+    if (r1 < B)
+      *reinterpret_cast<uint32_t *>(out + ((size_t)r1 * H + h) * MLA_V + col) =
+          pack_bf16x2(acc[0][2] + acc[1][2], acc[0][3] + acc[1][3]);
     __syncthreads();
   }
 }
@@ -291,6 +309,20 @@ bool encode_cache_map(CUtensorMap *m, const void *base, int num_pages, int P, in
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D map over projection weights viewed as [H * 128 rows, 512] bf16; box = (64 columns,
+// box_rows rows), 128-byte swizzle.
+bool encode_weight_map(CUtensorMap *m, const void *base, int H, int box_rows) {
+  auto fn = mla_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)MLA_LAT, (cuuint64_t)H * 128};
+  cuuint64_t strides[1] = {(cuuint64_t)MLA_LAT * 2};
+  cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2-D map over q_abs [rows, 576] bf16; box = (64 dims, 16 rows), 128-byte swizzle.
 bool encode_qabs_map(CUtensorMap *m, const void *base, long long rows) {
   auto fn = mla_encode_fn();
@@ -344,8 +376,9 @@ int mla_decode(const void *q, const void *cache, const void *w_uk, const void *w
   uint16_t *q_abs = reinterpret_cast<uint16_t *>(ws + pl.off_qabs);
   uint16_t *o_lat = reinterpret_cast<uint16_t *>(ws + pl.off_olat);
   uint16_t *q_lo = reinterpret_cast<uint16_t *>(ws + pl.off_qlo);
-  CUtensorMap tm_c, tm_q;
-  if (!encode_cache_map(&tm_c, cache, num_pages, P, BH) || !encode_qabs_map(&tm_q, q_abs, (long long)batch * H))
+  CUtensorMap tm_c, tm_q, tm_wuk, tm_wuv;
+  if (!encode_cache_map(&tm_c, cache, num_pages, P, BH) || !encode_qabs_map(&tm_q, q_abs, (long long)batch * H) ||
+      !encode_weight_map(&tm_wuk, w_uk, H, MLA_NOPE) || !encode_weight_map(&tm_wuv, w_uv, H, UV_ROWS))
     return PA_ERR_UNSUPPORTED;
   const int sms = sm_count_mla();
   if (sms <= 0) return pa::cuda_fail(cudaSuccess);
@@ -370,8 +403,8 @@ int mla_decode(const void *q, const void *cache, const void *w_uk, const void *w
   }
 
   // 1. q_abs
-  q_absorb_kernel<<<H, 256, PROJ_SMEM, stream>>>(static_cast<const uint16_t *>(q), static_cast<const uint16_t *>(w_uk),
-                                                  q_abs, q_lo, batch, H);
+  q_absorb_kernel<<<H * ABS_PARTS, 256, PROJ_SMEM, stream>>>(tm_wuk, static_cast<const uint16_t *>(q), q_abs, q_lo, batch, H,
+                                                  &hdr->status);
   if (const cudaError_t ce = cudaGetLastError(); ce != cudaSuccess) return pa::cuda_fail(ce);
   ++*launches;
 
@@ -435,10 +468,10 @@ int mla_decode(const void *q, const void *cache, const void *w_uk, const void *w
   // 7. o = W_UV . o_lat
   {
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = pdl_config(dim3(H), dim3(256), PROJ_SMEM, stream, attr);
-    if (const cudaError_t ce = cudaLaunchKernelEx(&cfg, mla_uv_kernel, (const uint16_t *)o_lat,
-                                                  static_cast<const uint16_t *>(w_uv), static_cast<uint16_t *>(out),
-                                                  (const uint16_t *)q_lo, lse, scale, batch, H, &hdr->status);
+    cudaLaunchConfig_t cfg = pdl_config(dim3(H * UV_PARTS), dim3(256), PROJ_SMEM, stream, attr);
+    if (const cudaError_t ce = cudaLaunchKernelEx(&cfg, mla_uv_kernel, tm_wuv, (const uint16_t *)o_lat,
+                                                  static_cast<uint16_t *>(out), (const uint16_t *)q_lo, lse, scale,
+                                                  batch, H, &hdr->status);
         ce != cudaSuccess)
       return pa::cuda_fail(ce);
   }
