@@ -29,10 +29,6 @@ namespace pa {
 
 constexpr int MLA_NOPE = 128, MLA_QD = 192, MLA_LAT = 512, MLA_C = 576, MLA_V = 128;
 
-__device__ __forceinline__ uint32_t pack_u16(uint16_t lo, uint16_t hi) {
-  return (uint32_t)lo | ((uint32_t)hi << 16);
-}
-
 // Activation rows in shared memory are padded to 520 bf16 (1040 bytes): the 16-byte offset
 // between consecutive rows keeps fragment loads free of bank conflicts.
 constexpr int WROW = MLA_LAT + 8;
