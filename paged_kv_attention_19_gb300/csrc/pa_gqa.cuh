@@ -12,39 +12,44 @@
 // data (vllm.cpp kernel-matrix, rows KERNEL-ATTN-FA2 and KERNEL-ATTN-MLA-SPARSE).
 //
 // GB300 design (how):
-//   * static, balanced partition.  The visible keys of every (row, KV head,
-//     16-head subgroup) sequence are cut into units of one TMA box (min(page,
-//     stage) tokens).  All units, flattened row by row, are divided into
-//     `nparts` equal contiguous ranges, one per CTA (one CTA per SM by
-//     default), so every SM streams the same number of KV bytes.  Each CTA
-//     finds its range from the context lengths in a short prologue: no
-//     planner launch, no work queue, no atomics, identical from run to run.
-//     A range is a list of pieces (maximal runs of one sequence); only its
-//     first and last piece can be part of a sequence that another CTA also
-//     touches, so a CTA leaves at most two partial results;
+//   * static, balanced partition.  A sequence is (row, KV head, tile), a tile
+//     being up to 16 query rows of the KV head (a 16-head subgroup, or
+//     positions x heads for verify); its visible keys are cut into units of
+//     one TMA box (min(page, stage) tokens).  The CTAs (one per SM by
+//     default) form groups of HG = KV heads x tiles per KV head; each group
+//     takes an equal share of the rows' total cost (units plus a fixed cost
+//     per piece) and CTA r of a group serves sequence r of those rows, so the
+//     group's CTAs stream the same pages at about the same time (DRAM once,
+//     L2 for the rest).  Each CTA finds its range from the context lengths in
+//     a short prologue: no planner launch, no work queue, no atomics,
+//     identical from run to run.  A range is a list of pieces (maximal runs of
+//     one sequence); only its first and last piece can be part of a sequence
+//     that another CTA also touches, so a CTA leaves at most two partials;
 //   * the last warp is a TMA producer: it walks the CTA's pieces, keeps 32
 //     block-table entries in a register window (the next window and the next
-//     piece's first window already in flight), and issues 4-D tensor-map
+//     piece's first window already in flight), and issues a stage of the
+//     piece's query rows (a 3-D tensor-map box) and then 4-D tensor-map
 //     copies of page fragments into a ring of shared-memory stages (K and V
 //     of 64 tokens, 32 for head_dim 256) with the 128-byte swizzle, so the
 //     tensor-core fragment loads are bank-conflict free.  The ring takes all
 //     of shared memory (224 KB) to keep ~200 KB of copies in flight per SM;
 //   * the consumer warps take 16 tokens of every stage per token group; two
 //     warps share a group, both computing its scores and each accumulating
-//     half of the P.V columns.  The group's (up to 16) query heads are the M
-//     rows of mma.sync m16n8k16 bf16 tiles, so S = Q K^T and O += P V cost one
-//     tensor-core instruction per 8 tokens x 16 dims.  The online softmax
-//     (running max with a lazy rescale, fp32 denominator) runs on the CUDA
-//     cores; P is rounded to bf16 only as the MMA operand.  Q is read from
-//     global memory into registers at the start of a piece (the producer has
-//     prefetched it to L2), so no shared memory is spent on it;
+//     half of the P.V columns.  The tile's (up to 16) query rows are the M
+//     rows of mma.sync m16n8k16 bf16 tiles, read with ldmatrix from the query
+//     stage into registers at the start of a piece, so S = Q K^T and
+//     O += P V cost one tensor-core instruction per 8 tokens x 16 dims.  The
+//     online softmax (running max with a lazy rescale, fp32 denominator) runs
+//     on the CUDA cores; P is rounded to bf16 only as the MMA operand;
 //   * at the end of a piece the token groups merge through the consumed stage
 //     buffer; a piece that covers its whole sequence writes the final bf16
 //     output and LSE, any other writes an fp32 partial (normalised output +
 //     LSE) to one of the CTA's two slots;
+//   * the setup, the producer, the end-of-piece merge and the epilogue are
+//     device functions shared with the FP8 kernel (pa_gqa_f8.cuh);
 //   * the combine kernel (a programmatic dependent launch, so its launch hides
 //     under the split kernel's tail) merges every split sequence over the
-//     CTAs that hold its pieces, in ascending order.
+//     CTAs that hold its pieces, in ascending order, one warp per row.
 #pragma once
 
 #include "pa_common.cuh"

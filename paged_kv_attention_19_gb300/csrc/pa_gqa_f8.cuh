@@ -27,6 +27,10 @@
 //     (at most 256, the lazy-rescale bound being 2) are hi + lo within 2^-8
 //     relative; each product therefore takes two MMAs.  The 2^-s, k_scale,
 //     v_scale and 1/128 factors are applied to the fp32 scores and outputs;
+//   * each warp owns 32 tokens of a stage (one k32 of the P.V MMA); for
+//     tiles of at most 8 columns two warp sets take turns on a piece's K/V
+//     stages, each with its own softmax state, merged with the token groups
+//     at the end of the piece: twice the warps in flight, no duplicated work;
 //   * scores, softmax and accumulation are fp32.
 #pragma once
 
