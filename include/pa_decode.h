@@ -2,10 +2,13 @@
  * pa_decode.h -- C ABI of the paged decode attention library (GB300, sm_103a).
  *
  * Single-token decode (and speculative-verify) attention of a batch of query
- * rows against a paged bf16 KV cache, in two variants:
+ * rows against a paged KV cache, and the write of new tokens into the cache:
  *
  *   pa_decode_gqa           grouped-query attention, optional sliding window
+ *   pa_verify_gqa           the same for several query positions per row
+ *   pa_decode_gqa_fp8       both over an FP8 (E4M3) cache with per-pool scales
  *   pa_decode_mla_absorbed  multi-head latent attention in the absorbed form
+ *   pa_kv_write, pa_kv_write_fp8, pa_mla_cache_write   the paged writes
  *
  * The operations are the ones the following pages describe:
  *   - paged cache: K/V pools [pages, block_size, Hkv, D], per-request
@@ -25,13 +28,17 @@
  *     PR #938 "warp-cooperative two-pass MLA absorbed decode kernel",
  *     Schedule section, steps 1-7; kernel-matrix row KERNEL-ATTN-MLA-SPARSE,
  *     weight absorption as two batched contractions);
+ *   - the paged writes and the FP8 form of the cache (kernel-matrix rows
+ *     KERNEL-KV-CACHE and KERNEL-KV-QUANT);
  *   - the raw pointer / shape / scalar / workspace / stream calling
  *     convention of the planned drop-in kernel ABI (kernel-matrix preamble).
  *
  * Conventions shared by every entry point
  *   - Every data pointer is DEVICE memory owned by the caller; the library
- *     allocates nothing and keeps no state between calls (re-entrant).  The
- *     only library state is the optional per-host-thread profiling hook.
+ *     allocates nothing at call time and keeps no state between calls
+ *     (re-entrant).  The only library state is per host thread (the optional
+ *     profiling hook, the launch count, the last CUDA error) and the fixed
+ *     scratch array of pa_decode_gqa_noalloc.
  *   - Tensors are dense, row-major, in the layouts written beside each
  *     argument.  bf16 means IEEE bfloat16 bit patterns.  q, pools, cache,
  *     weights, out and workspace must be 16-byte aligned; block_table,
