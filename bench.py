@@ -53,7 +53,8 @@ WORKLOADS = ["tiny", "llama3-8b", "qwen3-32b", "hd256-window", "mla", "kv-write"
 # sources of the kernel each roofline line profiles (a change voids its committed ncu traffic)
 KERNEL_SOURCES = {"gqa": ("pa_gqa.cuh", "pa_partition.cuh", "pa_common.cuh"),
                   "gqa_f8": ("pa_gqa_f8.cuh", "pa_gqa.cuh", "pa_partition.cuh", "pa_common.cuh"),
-                  "mla": ("pa_mla_tc.cuh", "pa_mla.cu", "pa_gqa.cuh", "pa_partition.cuh", "pa_common.cuh")}
+                  "mla": ("pa_mla_tc.cuh", "pa_tcgen05.cuh", "pa_mla.cu", "pa_gqa.cuh", "pa_partition.cuh",
+                          "pa_common.cuh")}
 
 
 def compute_dtype(w):

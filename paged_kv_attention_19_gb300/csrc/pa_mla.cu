@@ -8,7 +8,7 @@
 //   2-6. scores over the 576-wide latent || rope cache, online softmax,
 //        o_lat = sum_t p_t c_t[0:512], per piece of the balanced partition
 //                                                                   [mla_tc_split_kernel]
-//   merge of split sequences, ascending, o_lat rounded to bf16      [gqa_combine_kernel<512>]
+//   merge of split sequences, ascending, o_lat rounded to bf16      [mla_combine_kernel]
 //   7. o = W_UV . o_lat; lse += scale * q_lo . o_lat                [mla_uv_kernel]
 // Differences from the pages' kernel, all deliberate: scores, probabilities and the
 // softmax state stay fp32; the context is walked once with an online max instead of
@@ -142,7 +142,8 @@ __global__ void __launch_bounds__(256) q_absorb_kernel(const __grid_constant__ C
   }
 }
 
-// o[b][h][v] = sum_j W_UV[h][v][j] o_lat[b][h][j] on the tensor cores.  Block (h, part) of 8
+// o[b][h][v] = sum_j W_UV[h][v][j] o_lat[b][h][j] on the tensor cores (o_lat stored as its two
+// column halves, [B, 2, H, 256]).  Block (h, part) of 8
 // warps computes v in [64 part, +64) from its W_UV half (64 x 512, staged by TMA before the wait
 // for the previous kernels); warp w produces v in [8 w, 8 w + 8) of the half for 16 batch rows
 // per tile.  Part 0 also adds, with lse, the first-order LSE term of q_lat's bf16 rounding:
@@ -167,7 +168,8 @@ __global__ void __launch_bounds__(256) mla_uv_kernel(const __grid_constant__ CUt
       const int r = i / (MLA_LAT / 8), c = i % (MLA_LAT / 8);
       const int b = m0 + r;
       *reinterpret_cast<uint4 *>(ol + r * WROW + c * 8) =
-          b < B ? *reinterpret_cast<const uint4 *>(o_lat + ((size_t)b * H + h) * MLA_LAT + c * 8) : make_uint4(0, 0, 0, 0);
+          b < B ? *reinterpret_cast<const uint4 *>(o_lat + (((size_t)b * 2 + c / 32) * H + h) * (MLA_LAT / 2) + (c % 32) * 8)
+                : make_uint4(0, 0, 0, 0);
     }
     __syncthreads();
     if (lse && part == 0) {
@@ -248,26 +250,27 @@ int ilog2(int x) {
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 struct MlaPlan {
-  int ntile, nparts_max;
+  int ntile, rs, nparts_max;
   size_t off_desc, off_part_lse, off_part_o, off_qabs, off_qlo, off_olat, total;
 };
 
-// The workspace: header, one descriptor per share, two fp32 partial slots (16 heads x 512)
-// per share, q_abs [B, H, 576], q_lo [B, H, 512] and o_lat [B, H, 512], all bf16.
+// The workspace: header, one descriptor per share, two fp32 partial slots (min(H, 128) heads x 256
+// columns) per share, q_abs [B, H, 576], q_lo [B, H, 512] and o_lat [B, 2, H, 256], all bf16.
 int mla_shape(int batch, int H, int max_ctx, int P, int num_splits, MlaPlan *pl) {
   if (batch < 0 || H <= 0 || max_ctx < 0 || num_splits < 0) return PA_ERR_INVALID_ARGUMENT;
   if (num_splits > kMaxSplits) return PA_ERR_UNSUPPORTED;
   if (!is_pow2(P) || P < 8 || P > 256) return PA_ERR_UNSUPPORTED;  // a TMA box starts on 1024 bytes
-  pl->ntile = (H + PART_HEADS - 1) / PART_HEADS;
+  pl->ntile = 2 * ((H + MlaTcCfg::M - 1) / MlaTcCfg::M);  // (head tile, column half) per row
+  pl->rs = H < MlaTcCfg::M ? H : MlaTcCfg::M;
   pl->nparts_max = num_splits > 0 ? num_splits : kAutoPartsMax;
   const size_t np = (size_t)pl->nparts_max, B = (size_t)(batch > 0 ? batch : 1);
   size_t off = sizeof(WsHeader);
   pl->off_desc = off;
   off = round_up(off + np * sizeof(GqaPartDesc), 256);
   pl->off_part_lse = off;
-  off = round_up(off + np * 2 * PART_HEADS * sizeof(float), 256);
+  off = round_up(off + np * 2 * pl->rs * sizeof(float), 256);
   pl->off_part_o = off;
-  off = round_up(off + np * 2 * PART_HEADS * (size_t)MLA_LAT * sizeof(float), 256);
+  off = round_up(off + np * 2 * pl->rs * (size_t)MlaTcCfg::DVH * sizeof(float), 256);
   pl->off_qabs = off;
   off = round_up(off + B * (size_t)H * MLA_C * 2, 256);
   pl->off_qlo = off;
@@ -319,13 +322,13 @@ bool encode_weight_map(CUtensorMap *m, const void *base, int H, int box_rows) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D map over q_abs [rows, 576] bf16; box = (64 dims, 16 rows), 128-byte swizzle.
+// 2-D map over q_abs [rows, 576] bf16; box = (64 dims, 128 rows: one head tile), 128-byte swizzle.
 bool encode_qabs_map(CUtensorMap *m, const void *base, long long rows) {
   auto fn = mla_encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)MLA_C, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)MLA_C * 2};
-  cuuint32_t box[2] = {64u, (cuuint32_t)PART_HEADS};
+  cuuint32_t box[2] = {64u, (cuuint32_t)MlaTcCfg::M};
   cuuint32_t estr[2] = {1u, 1u};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -389,7 +392,8 @@ int mla_decode(const void *q, const void *cache, const void *w_uk, const void *w
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    for (const void *k : {(const void *)mla_tc_split_kernel, (const void *)q_absorb_kernel, (const void *)mla_uv_kernel}) {
+    for (const void *k :
+         {(const void *)mla_tc_split_kernel, (const void *)q_absorb_kernel, (const void *)mla_uv_kernel}) {
       const int bytes = k == (const void *)mla_tc_split_kernel ? MlaTcSmem::BYTES : PROJ_SMEM;
       if (const cudaError_t ce = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
           ce != cudaSuccess)
@@ -419,6 +423,7 @@ int mla_decode(const void *q, const void *cache, const void *w_uk, const void *w
   ma.max_context_len = max_context_len;
   ma.H = H;
   ma.ntile = pl.ntile;
+  ma.rs = pl.rs;
   ma.log2_page = ilog2(P);
   ma.log2_bh = ilog2(BH);
   {
@@ -442,23 +447,24 @@ int mla_decode(const void *q, const void *cache, const void *w_uk, const void *w
   }
 
   // merge of split sequences into o_lat (and lse)
-  CombineArgs ca;
-  ca.out = o_lat;
-  ca.lse = lse;
-  ca.part_o = part_o;
-  ca.part_lse = part_lse;
-  ca.desc = desc;
-  ca.status = &hdr->status;
-  ca.Hq = H;
-  ca.G = H;
-  ca.nsub = pl.ntile;
-  ca.nparts = nparts;
-  ca.hg = ma.hg;
-  ca.Q = 1;
-  ca.gt = PART_HEADS;
-  ca.qt = 1;
-  ca.ntile = pl.ntile;
-  if (const cudaError_t ce = launch_combine<MLA_LAT>(ca, stream); ce != cudaSuccess) return pa::cuda_fail(ce);
+  {
+    MlaCombineArgs ca;
+    ca.o_lat = o_lat;
+    ca.lse = lse;
+    ca.part_o = part_o;
+    ca.part_lse = part_lse;
+    ca.desc = desc;
+    ca.status = &hdr->status;
+    ca.H = H;
+    ca.rs = pl.rs;
+    ca.nparts = nparts;
+    ca.hg = ma.hg;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg =
+        pdl_config(dim3(nparts, MlaTcCfg::M / MLA_COMBINE_ROWS), dim3(MLA_COMBINE_THREADS), 0, stream, attr);
+    if (const cudaError_t ce = cudaLaunchKernelEx(&cfg, mla_combine_kernel, ca); ce != cudaSuccess)
+      return pa::cuda_fail(ce);
+  }
   ++*launches;
 
   // 7. o = W_UV . o_lat

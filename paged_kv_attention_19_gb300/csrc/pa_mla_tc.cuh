@@ -1,4 +1,4 @@
-// pa_mla_tc.cuh -- MLA absorbed decode, attention core on the tensor cores (sm_103a).
+// pa_mla_tc.cuh -- MLA absorbed decode, attention core on the 5th-generation tensor cores (sm_103a).
 //
 // What is computed follows pegainfer PR #938 "warp-cooperative two-pass MLA absorbed
 // decode kernel" (Schedule section, steps 2-6): for each head, scores over the 576-wide
@@ -8,87 +8,88 @@
 // which shifts the LSE by scale * lo . o_lat to first order (up to ~1e-3 for a short row); the
 // projection kernel adds that term back, which leaves ~1e-6.
 //
-// GB300 mapping: the absorbed core is multi-query attention with one 576-wide KV row per
-// token shared by all heads, so it runs on the split-KV machinery of the GQA kernel
-// (pa_partition.cuh): a sequence is (row, tile of 16 heads), the 8 tiles of a row form a
-// CTA group that streams the same cache pages at about the same time (DRAM once, L2 for
-// the others), and the per-piece partials are merged by the GQA combine kernel (D = 512).
-//   * producer warp: TMA copies of 32-token stages (9 planes of 64 dims x 32 tokens, 128-byte
-//     swizzle, 36 KB) into a 5-stage ring, plus one query stage per piece (9 planes of 16
-//     heads), which the consumers copy into a query area;
-//   * 8 consumer warps = 2 token groups (16 tokens each) x 4 quarters: for the scores each
-//     warp of a group contracts its quarter of the 576 dims (9 k-steps of m16n8k16,
-//     the 16 heads as M rows, query fragments read from the piece's query area); the four
-//     partial score tiles meet in shared memory and every warp of the group sums them in
-//     the same order, so all four hold identical scores and softmax state.  For P.V each warp
-//     owns 128 of the 512 latent columns (V is the first 512 dims of the same cache row);
-//   * end of a piece: the two token groups merge pairwise through the consumed stage buffer.
+// GB300 mapping.  The absorbed core is multi-query attention: one 576-wide cache row per token,
+// shared by all heads.  A tile of 128 heads is the M dimension of tcgen05 MMAs (one head per
+// tensor-memory lane), so every cache row a CTA stages serves all the tile's heads at once.  The
+// fp32 o_lat of 128 heads x 512 columns would fill the whole tensor memory, so a sequence is
+// (row, head tile, half of the 512 latent columns): the two halves of a tile are the CTA group
+// of the split-KV partition (pa_partition.cuh), stream the same cache pages at about the same
+// time (DRAM once, L2 for the other) and each compute the full scores.  Per CTA:
+//   * warp 0, producer: TMA copies of 32-token stages (9 planes of 64 dims x 32 tokens, 128-byte
+//     swizzle, 36 KB) into a 2-stage ring, and per piece the tile's 128 query rows (9 planes,
+//     144 KB) into the query area once the previous piece's score MMAs have read it;
+//   * warp 1, one thread issues the MMAs: S = Q C^T (M = 128 heads, N = 32 tokens, K = 576, both
+//     operands K-major in shared memory) into one of two score buffers in tensor memory, then
+//     O += P V for the previous stage (P: 128 x 32 bf16 from tensor memory, V: the stage's
+//     latent columns of this half, MN-major in shared memory, N = 256) into the O columns;
+//     completions go to mbarriers by tcgen05.commit;
+//   * warps 2-5, softmax: one thread per head row reads its 32 scores from tensor memory, keeps
+//     the fp32 running max and sum (rescaling its O row in tensor memory only when the max grows
+//     by more than 2^8), writes the probabilities as bf16 back to tensor memory, and at the end of
+//     a piece reads O, divides by the sum and stores o_lat (or an fp32 partial) and the LSE.
+// Tensor-memory columns: scores 0-63 (two buffers of 32), P 64-79, O 256-511.
 #pragma once
 
 #include "pa_gqa.cuh"
 #include "pa_partition.cuh"
+#include "pa_tcgen05.cuh"
 
 namespace pa {
 
 struct MlaTcArgs {
   const int32_t *block_table;   // [B, max_pages_per_seq]
   const int32_t *context_lens;  // [B]
-  uint16_t *o_lat;              // [B, H, 512] bf16: o_lat of whole-sequence pieces
+  uint16_t *o_lat;              // [B, 2, H, 256] bf16: the two column halves of o_lat, whole-sequence pieces
   float *lse;                   // [B, H] or null
-  float *part_o;                // [nparts, 2, 16, 512] fp32
-  float *part_lse;              // [nparts, 2, 16] fp32, log2 units
+  float *part_o;                // [nparts, 2, RS, 256] fp32
+  float *part_lse;              // [nparts, 2, RS] fp32, log2 units
   GqaPartDesc *desc;            // [nparts]
   int batch, max_pages_per_seq, num_pages, max_context_len;
-  int H, ntile;                 // heads, tiles of 16 heads
+  int H, ntile, rs;             // heads; sequences per row (2 x head tiles); rows per partial slot
   int log2_page, log2_bh, piece_cost, nparts, hg;
   float qscale;                 // scale * log2(e)
 };
 
 struct MlaTcCfg {
-  static constexpr int M = PART_HEADS;        // heads per tile (MMA rows)
-  static constexpr int DQK = 576, DV = 512;
-  static constexpr int NQK = DQK / 64;        // 9 swizzle planes per cache row
-  static constexpr int ST = 32;               // tokens per stage
-  static constexpr int TW = 16;               // tokens per token group
-  static constexpr int TG = ST / TW;          // 2
-  static constexpr int DSPLIT = 4;            // warps per token group
-  static constexpr int NCW = TG * DSPLIT;     // 8 consumer warps
-  static constexpr int THREADS = (NCW + 1) * 32;
-  static constexpr int KSW = DQK / 16 / DSPLIT;  // score k-steps per warp: 9
-  static constexpr int NT_PV = DV / 8 / DSPLIT;  // P.V n-tiles per warp: 16
-  static constexpr int PLANE = ST * 128;         // 4 KB
-  static constexpr int STAGE_BYTES = NQK * PLANE;  // 36 KB
-  static constexpr int QPLANE = M * 128;         // 2 KB
-  static constexpr int NS = 5;
-  static constexpr int SPART = TG * DSPLIT * 32 * 8 * 4;  // partial scores: per warp 32 lanes x 8 floats
-  static_assert(QPLANE * NQK <= STAGE_BYTES, "the query stage fits a ring slot");
-  static_assert(DSPLIT * M * (DV / DSPLIT) * 4 <= STAGE_BYTES, "pairwise merge area fits a stage");
+  static constexpr int M = 128;                   // heads per tile: MMA rows, tensor-memory lanes
+  static constexpr int DQK = 576, DV = 512, DVH = DV / 2;
+  static constexpr int NQK = DQK / 64;            // 9 swizzle planes per cache row
+  static constexpr int ST = 32;                   // tokens per stage: N of the score MMA, K of P.V
+  static constexpr int NS = 2;                    // stages in the ring
+  static constexpr int PLANE = ST * 128;          // 4 KB
+  static constexpr int STAGE_BYTES = NQK * PLANE; // 36 KB
+  static constexpr int QPLANE = M * 128;          // 16 KB
+  static constexpr int Q_BYTES = NQK * QPLANE;    // 144 KB
+  static constexpr int SOFTMAX_WARPS = 4;
+  static constexpr int THREADS = (2 + SOFTMAX_WARPS) * 32;
+  static constexpr uint32_t TM_S = 0, TM_P = 64, TM_O = 256, TM_COLS = 512;
+  static constexpr float TAU = 8.f;               // lazy rescale threshold (log2 units)
+  static constexpr uint32_t IDESC_S = tc_idesc_bf16(M, ST, false);
+  static constexpr uint32_t IDESC_PV = tc_idesc_bf16(M, DVH, true);
+  static_assert(NQK % 3 == 0, "the scores are issued in chunks of 3 planes");
 };
 
 struct MlaTcMisc {
   uint32_t status;
-  int32_t pad[3];
+  uint32_t tmem;   // base address of the tensor-memory allocation
+  int32_t pad[2];
   GqaPartDesc desc;
   PartitionState part;
 };
 
 struct MlaTcSmem {
   using C = MlaTcCfg;
-  static constexpr int OFF_STAGE = 0;
-  static constexpr int OFF_Q = OFF_STAGE + C::NS * C::STAGE_BYTES;   // the piece's query rows
-  static constexpr int OFF_SP = OFF_Q + C::NQK * C::QPLANE;           // 2 buffers of partial scores
-  static constexpr int OFF_ML = OFF_SP + 2 * C::SPART;
-  static constexpr int OFF_META = OFF_ML + C::M * 2 * 4 * 2;
+  static constexpr int OFF_Q = 0;                                      // the piece's query rows
+  static constexpr int OFF_STAGE = OFF_Q + C::Q_BYTES;
+  static constexpr int OFF_META = OFF_STAGE + C::NS * C::STAGE_BYTES;
   static constexpr int OFF_BAR = OFF_META + C::NS * (int)sizeof(StageMeta);
-  static constexpr int OFF_MISC = OFF_BAR + 2 * C::NS * 8;
+  // full[NS], empty[NS], q_full, q_empty, s_full[2], s_free[2], p_full, pv_done, o_free, drain
+  static constexpr int NBAR = 2 * C::NS + 10;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int USED = OFF_MISC + (int)sizeof(MlaTcMisc);
   static constexpr int BYTES = USED + 1024;
   static_assert(BYTES <= 232448, "fits the 227 KB opt-in shared memory of one CTA");
 };
-
-__device__ __forceinline__ uint32_t mla_off(int plane_bytes, int row, int chunk) {
-  return (uint32_t)((chunk >> 3) * plane_bytes + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
-}
 
 __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
     mla_tc_split_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_q,
@@ -97,8 +98,11 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
   using S = MlaTcSmem;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::OFF_BAR);
-  uint64_t *empty = full + C::NS;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::OFF_BAR);
+  uint64_t *full = bars, *empty = bars + C::NS;
+  uint64_t *q_full = bars + 2 * C::NS, *q_empty = q_full + 1;
+  uint64_t *s_full = q_full + 2, *s_free = s_full + 2;
+  uint64_t *p_full = s_free + 2, *pv_done = p_full + 1, *o_free = p_full + 2, *drain = p_full + 3;
   StageMeta *meta = reinterpret_cast<StageMeta *>(smem + S::OFF_META);
   MlaTcMisc *misc = reinterpret_cast<MlaTcMisc *>(smem + S::OFF_MISC);
 
@@ -107,16 +111,30 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
   if (tid == 0) {
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], C::NCW);
+      mbar_init(&empty[s], 1);
     }
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], C::SOFTMAX_WARPS);
+    }
+    mbar_init(p_full, C::SOFTMAX_WARPS);
+    mbar_init(pv_done, 1);
+    mbar_init(o_free, C::SOFTMAX_WARPS);
+    mbar_init(drain, 1);
     fence_mbar_init();
     misc->status = 0;
   }
-  if (warp == C::NCW && lane == 0) {
+  if (warp == 0 && lane == 0) {
     prefetch_tensormap(&tm_c);
     prefetch_tensormap(&tm_q);
   }
+  if (warp == 1) tc_alloc(&misc->tmem, C::TM_COLS);
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc->tmem;
   pdl_wait();               // q_abs, written by the absorb kernel, is visible from here on
   pdl_launch_dependents();  // the combine kernel may be scheduled; it waits for this grid to finish
   uint32_t *status = &misc->status;
@@ -136,11 +154,12 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
   zero_empty_rows<C::THREADS>(pargs, a.o_lat, a.lse, a.H * C::DV, a.H);
   __syncthreads();
 
-  if (warp == C::NCW) {
+  if (warp == 0) {
     // ------------------------------------------------------------ producer
     const int P = 1 << a.log2_page;
     const int nbox = C::ST >> a.log2_bh;
-    uint32_t j = 0;
+    uint32_t j = 0;   // stages issued
+    uint32_t kq = 0;  // query tiles issued
     bool ok = true;
     int npieces = 0;
     Piece last_piece = {};
@@ -161,7 +180,7 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
       if (has_next) nwin0 = piece_window(nxt);
     }
     while (has_cur && ok) {
-      const int h0 = cur.hs * C::M;
+      const int h0 = (cur.hs >> 1) * C::M, hv = cur.hs & 1;
       const int nh = min(C::M, a.H - h0);
       const int slot = (cur.starts && cur.ends) ? -1 : (npieces == 0 ? 0 : 1);
       const int T0 = cur.ub << a.log2_bh;
@@ -172,30 +191,7 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
       const int32_t *bt_piece = a.block_table + (size_t)cur.b * a.max_pages_per_seq + pb;
       int cwin = cwin0, wi = 0;
       int fwin = (lane + 32 < npages) ? bt_piece[32 + lane] : 0;
-      {
-        // the query stage: q_abs rows b * H + h0 .. + 16 (rows past H are masked)
-        const int s = j % C::NS;
-        const uint32_t u = j / C::NS;
-        if (u > 0) ok = mbar_wait(&empty[s], (u - 1) & 1, status);
-        if (!ok) break;
-        if (lane == 0) {
-          StageMeta &m = meta[s];
-          m.end = 0;
-          m.first = 1;
-          m.last = 0;
-          m.b = cur.b;
-          m.hq0 = h0;
-          m.ghead = nh;
-          mbar_arrive_expect_tx(&full[s], (uint32_t)(C::NQK * C::QPLANE));
-          uint8_t *qdst = smem + S::OFF_STAGE + s * C::STAGE_BYTES;
-#pragma unroll
-          for (int dq = 0; dq < C::NQK; ++dq)
-            tma_load_2d(qdst + dq * C::QPLANE, &tm_q, dq * 64, cur.b * a.H + h0, &full[s]);
-        }
-        __syncwarp();
-        ++j;
-      }
-      for (int t = 0; t < n_stages && ok; ++t, ++j) {
+      for (int t = 0; t < n_stages && ok; ++t) {
         const int s = j % C::NS;
         const uint32_t u = j / C::NS;
         if (u > 0) ok = mbar_wait(&empty[s], (u - 1) & 1, status);
@@ -229,11 +225,12 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
         if (lane == 0) {
           StageMeta &m = meta[s];
           m.end = 0;
-          m.first = 0;
+          m.first = t == 0;
           m.last = last;
           m.b = cur.b;
           m.hq0 = h0;
           m.ghead = nh;
+          m.i0 = hv;
           m.slot = slot;
           m.tok0 = tok0;
           m.tok_lo = tok_lo;
@@ -248,6 +245,21 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
           uint8_t *dst = kdst + (lane << a.log2_bh) * 128;
 #pragma unroll
           for (int dq = 0; dq < C::NQK; ++dq) tma_load_3d(dst + dq * C::PLANE, &tm_c, dq * 64, pslot, phys, &full[s]);
+        }
+        ++j;
+        if (t == 0) {
+          // the tile's query rows, after the first stage is under way: the area is free once the
+          // previous piece's score MMAs have completed
+          if (kq > 0) ok = mbar_wait(q_empty, (kq - 1) & 1, status);
+          if (!ok) break;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(q_full, (uint32_t)C::Q_BYTES);
+#pragma unroll
+            for (int dq = 0; dq < C::NQK; ++dq)
+              tma_load_2d(smem + S::OFF_Q + dq * C::QPLANE, &tm_q, dq * 64, cur.b * a.H + h0, q_full);
+          }
+          __syncwarp();
+          ++kq;
         }
       }
       if (!ok) break;
@@ -271,8 +283,10 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
       }
     }
     if (!ok) {
+      // copies still in flight land before the CTA exits
       const uint32_t first = j > (uint32_t)C::NS ? j - C::NS : 0u;
       for (uint32_t i = first; i < j; ++i) mbar_wait(&full[i % C::NS], (i / C::NS) & 1, status);
+      if (kq > 0) mbar_wait(q_full, (kq - 1) & 1, status);
     }
     if (lane == 0) {
       misc->desc.last_b = last_piece.b;
@@ -280,256 +294,335 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
       misc->desc.flags = (uint32_t)npieces | (last_piece.starts ? DESC_LAST_STARTS : 0u) |
                          (last_piece.ends ? DESC_LAST_ENDS : 0u) | (first_ends ? DESC_FIRST_ENDS : 0u);
     }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issue (one thread)
+    // A polling loop over the events the MMAs wait for.  P.V of the oldest stage goes first (it
+    // frees a ring slot); the 36 score MMAs of a stage go out in chunks of 3 planes, so a P.V
+    // whose probabilities are ready waits for at most one chunk.
+    if (lane == 0) {
+      const uint64_t qd0 = tc_sdesc_sw128(smem_u32(smem + S::OFF_Q), 16, 1024);
+      const uint32_t stage0 = smem_u32(smem + S::OFF_STAGE);
+      uint32_t js = 0;    // stage whose scores are issued next
+      uint32_t jp = 0;    // stage whose P.V is issued next (jp <= js)
+      uint32_t kq = 0;    // query tiles consumed (q_full phases)
+      uint32_t npp = 0;   // pieces whose first P.V was issued (o_free phases: one per earlier piece)
+      int plane = -1;     // >= 0: the scores of stage js are being issued, next plane
+      bool last_js = false, ended = false;
+      uint64_t idle_since = 0;
+      while (!(ended && jp == js)) {
+        bool progress = false;
+        if (jp < js && mbar_test(p_full, jp & 1)) {
+          const StageMeta &mp = meta[jp % C::NS];
+          const bool first = mp.first;
+          if (!first || npp == 0 || mbar_test(o_free, (npp - 1) & 1)) {
+            tc_fence_after();
+            if (first) ++npp;
+            const int sp = jp % C::NS;
+            const uint64_t vd = tc_sdesc_sw128(stage0 + sp * C::STAGE_BYTES + mp.i0 * 4 * C::PLANE, C::PLANE, 1024);
+#pragma unroll
+            for (int kk = 0; kk < C::ST / 16; ++kk)
+              tc_mma_ts(tmem + C::TM_O, tmem + C::TM_P + 8 * kk, vd + (uint64_t)((kk * 16 * 128) >> 4), C::IDESC_PV,
+                        (first && kk == 0) ? 0u : 1u);
+            tc_commit(&empty[sp]);
+            tc_commit(pv_done);
+            ++jp;
+            progress = true;
+          }
+        }
+        if (!progress && plane >= 0) {
+          const int s = js % C::NS, sb = js & 1;
+          const uint64_t cd0 = tc_sdesc_sw128(stage0 + s * C::STAGE_BYTES, 16, 1024);
+#pragma unroll
+          for (int pp = 0; pp < 3; ++pp) {
+            const int p = plane + pp;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              tc_mma_ss(tmem + C::TM_S + sb * C::ST, qd0 + (uint64_t)((p * C::QPLANE + 32 * kk) >> 4),
+                        cd0 + (uint64_t)((p * C::PLANE + 32 * kk) >> 4), C::IDESC_S, (p | kk) != 0 ? 1u : 0u);
+          }
+          plane += 3;
+          if (plane == C::NQK) {
+            tc_commit(&s_full[sb]);
+            if (last_js) tc_commit(q_empty);  // the query area may take the next piece's rows
+            plane = -1;
+            ++js;
+          }
+          progress = true;
+        }
+        if (!progress && plane < 0 && !ended && mbar_test(&full[js % C::NS], (js / C::NS) & 1) &&
+            (js < 2 || mbar_test(&s_free[js & 1], ((js >> 1) - 1) & 1))) {
+          const StageMeta &mt = meta[js % C::NS];
+          if (mt.end) {
+            tc_fence_after();
+            mbar_arrive(&s_full[js & 1]);  // the softmax warps stop at this stage
+            ended = true;
+            progress = true;
+          } else if (!mt.first || mbar_test(q_full, kq & 1)) {
+            tc_fence_after();
+            if (mt.first) ++kq;
+            last_js = mt.last;
+            plane = 0;
+            progress = true;
+          }
+        }
+        if (progress) {
+          idle_since = 0;
+        } else {
+          const uint64_t now = global_timer_ns();
+          if (idle_since == 0) {
+            idle_since = now;
+          } else if (now - idle_since > WAIT_LIMIT_NS) {
+            atomicOr(status, PA_DEV_TIMEOUT);
+            break;
+          }
+        }
+      }
+      // every MMA this thread issued has completed before the tensor memory is released
+      tc_commit(drain);
+      mbar_wait(drain, 0, status);
+    }
+    __syncwarp();
   } else {
-    // ------------------------------------------------------------ consumers
-    const int g8 = lane >> 2, tq = lane & 3;
-    const int lm_mat = lane >> 3, lm_row = lane & 7;
-    const int tgrp = warp % C::TG;           // token group
-    const int dq4 = warp / C::TG;            // quarter: score dims [144 dq4, +144), P.V columns [128 dq4, +128)
-    const int wbase = tgrp * C::TW;
-    const int nd0 = dq4 * C::NT_PV;
-    float *sm_ml = reinterpret_cast<float *>(smem + S::OFF_ML);
-    float *spart = reinterpret_cast<float *>(smem + S::OFF_SP);
-    const float TAU = 8.f;
+    // ------------------------------------------------------------ softmax and output
+    const int q4 = warp & 3;                      // lanes [32 q4, +32) of the tensor memory
+    const int row = 32 * q4 + lane;               // head row of the tile
+    const int ts = tid - 64;                      // 0 .. 127
+    const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
     const int bh_tokens = 1 << a.log2_bh;
-
-    const uint32_t qarea = smem_u32(smem + S::OFF_Q);
-    float acc[C::NT_PV][4];
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    bool rv0 = false, rv1 = false;
-
+    float m = -INFINITY, l = 0.f;
     for (uint32_t j = 0;; ++j) {
-      const int s = j % C::NS;
-      if (!mbar_wait(&full[s], (j / C::NS) & 1, status)) break;
+      const int sb = j & 1, s = j % C::NS;
+      if (!mbar_wait(&s_full[sb], (j >> 1) & 1, status)) break;
+      tc_fence_after();
       const StageMeta &mt = meta[s];
       if (mt.end) break;
-      const uint32_t cbase = smem_u32(smem + S::OFF_STAGE + s * C::STAGE_BYTES);
-      if (mt.first) {
-        // a new piece: its query rows into the query area (every warp finished the previous
-        // piece's scores before the merge barrier of its last stage)
-        rv0 = g8 < mt.ghead;
-        rv1 = g8 + 8 < mt.ghead;
-        {
-          const uint4 *src = reinterpret_cast<const uint4 *>(smem + S::OFF_STAGE + s * C::STAGE_BYTES);
-          uint4 *dst = reinterpret_cast<uint4 *>(smem + S::OFF_Q);
-          for (int e = tid; e < C::NQK * C::QPLANE / 16; e += C::NCW * 32) dst[e] = src[e];
-        }
-        named_bar(1, C::NCW * 32);
-#pragma unroll
-        for (int n = 0; n < C::NT_PV; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-        m0 = m1 = -INFINITY;
-        l0 = l1 = 0.f;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-        continue;
+      const bool first = mt.first, last = mt.last, masked = mt.masked;
+      const int tok0 = mt.tok0, tok_lo = mt.tok_lo, tok_hi = mt.tok_hi;
+      const uint32_t badmask = mt.badmask;
+      const int b = mt.b, h0 = mt.hq0, nh = mt.ghead, hv = mt.i0, slot = mt.slot;
+      if (first) {
+        m = -INFINITY;
+        l = 0.f;
       }
-      // ---- partial scores over this warp's 144 dims, for the group's 16 tokens (2 n-tiles);
-      // even and odd k-steps go to separate accumulators (two independent chains per n-tile)
-      float sp[2][4], sq[2][4];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sp[nt][e] = sq[nt][e] = 0.f;
-#pragma unroll
-      for (int k = 0; k < C::KSW; ++k) {
-        const int ks = dq4 * C::KSW + k;
-        // matrices: (tokens 0-7, dims 0-7), (tokens 0-7, dims 8-15), (tokens 8-15, ...) of the k-step
-        uint32_t qa[4], b[4];
-        ldmatrix_x4(qa, qarea + mla_off(C::QPLANE, (lm_mat & 1) * 8 + lm_row, 2 * ks + (lm_mat >> 1)));
-        const int tok = wbase + (lm_mat >> 1) * 8 + lm_row, chunk = 2 * ks + (lm_mat & 1);
-        ldmatrix_x4(b, cbase + mla_off(C::PLANE, tok, chunk));
-        if (k & 1) {
-          mma_bf16_16816(sq[0], qa, b[0], b[1]);
-          mma_bf16_16816(sq[1], qa, b[2], b[3]);
-        } else {
-          mma_bf16_16816(sp[0], qa, b[0], b[1]);
-          mma_bf16_16816(sp[1], qa, b[2], b[3]);
-        }
-      }
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sp[nt][e] += sq[nt][e];
-      float *myp = spart + (j & 1) * (C::SPART / 4) + (size_t)(tgrp * C::DSPLIT + dq4) * 32 * 8;
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) myp[(nt * 4 + e) * 32 + lane] = sp[nt][e];
-      named_bar(2 + tgrp, C::DSPLIT * 32);  // the group's four partials are written
-      float sv[2][4];
-      {
-        const float *gp = spart + (j & 1) * (C::SPART / 4) + (size_t)(tgrp * C::DSPLIT) * 32 * 8;
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float x = 0.f;
-#pragma unroll
-            for (int w = 0; w < C::DSPLIT; ++w) x += gp[(size_t)w * 32 * 8 + (nt * 4 + e) * 32 + lane];
-            sv[nt][e] = x;
-          }
-      }
-      const bool masked = mt.masked;
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float v = sv[nt][e] * a.qscale;
-          bool valid = (e < 2) ? rv0 : rv1;
-          if (masked) {
-            const int stok = wbase + nt * 8 + 2 * tq + (e & 1);
-            const int ltok = mt.tok0 + stok;
-            valid = valid && ltok >= mt.tok_lo && ltok < mt.tok_hi && !((mt.badmask >> (stok / bh_tokens)) & 1u);
-          }
-          sv[nt][e] = valid ? v : -INFINITY;
-        }
-      float x0 = fmaxf(fmaxf(sv[0][0], sv[0][1]), fmaxf(sv[1][0], sv[1][1]));
-      float x1 = fmaxf(fmaxf(sv[0][2], sv[0][3]), fmaxf(sv[1][2], sv[1][3]));
-      x0 = fmaxf(x0, __shfl_xor_sync(FULL, x0, 1));
-      x0 = fmaxf(x0, __shfl_xor_sync(FULL, x0, 2));
-      x1 = fmaxf(x1, __shfl_xor_sync(FULL, x1, 1));
-      x1 = fmaxf(x1, __shfl_xor_sync(FULL, x1, 2));
-      if (__any_sync(FULL, (x0 > m0 + TAU) || (x1 > m1 + TAU))) {
-        const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
-        const float a0 = (n0 == -INFINITY) ? 1.f : fast_exp2(m0 - n0);
-        const float a1 = (n1 == -INFINITY) ? 1.f : fast_exp2(m1 - n1);
-        m0 = n0;
-        m1 = n1;
-        l0 *= a0;
-        l1 *= a1;
-#pragma unroll
-        for (int n = 0; n < C::NT_PV; ++n) {
-          acc[n][0] *= a0;
-          acc[n][1] *= a0;
-          acc[n][2] *= a1;
-          acc[n][3] *= a1;
-        }
-      }
-      uint32_t pa[4];
-      {
-        float p[2][4];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float mr = (e < 2) ? m0 : m1;
-            p[nt][e] = (sv[nt][e] == -INFINITY) ? 0.f : fast_exp2(sv[nt][e] - mr);
-          }
-        pa[0] = pack_bf16x2(p[0][0], p[0][1]);
-        pa[1] = pack_bf16x2(p[0][2], p[0][3]);
-        pa[2] = pack_bf16x2(p[1][0], p[1][1]);
-        pa[3] = pack_bf16x2(p[1][2], p[1][3]);
-        l0 += (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
-        l1 += (p[0][2] + p[0][3]) + (p[1][2] + p[1][3]);
-      }
-      if (masked) {
-        // cache rows of keys that are not attended may hold anything (NaN included): zero this
-        // warp's latent columns of them (every warp of the group has read its score dims)
-        uint8_t *vgen = smem + S::OFF_STAGE + s * C::STAGE_BYTES;
-        constexpr int CPW = C::DV / 8 / C::DSPLIT;  // 16-byte chunks of a row owned by this warp: 16
-        for (int e = lane; e < C::TW * CPW; e += 32) {
-          const int stok = wbase + e / CPW;
-          const int chunk = dq4 * CPW + e % CPW;
-          const int ltok = mt.tok0 + stok;
-          if (ltok < mt.tok_lo || ltok >= mt.tok_hi || ((mt.badmask >> (stok / bh_tokens)) & 1u))
-            *reinterpret_cast<uint4 *>(vgen + mla_off(C::PLANE, stok, chunk)) = make_uint4(0, 0, 0, 0);
-        }
-        __syncwarp();
-      }
-      // ---- O += P V over this warp's 128 latent columns
-      {
-        const int tok = wbase + (lm_mat & 1) * 8 + lm_row;
-#pragma unroll
-        for (int nd = 0; nd < C::NT_PV; nd += 2) {
-          uint32_t b[4];
-          ldmatrix_x4_trans(b, cbase + mla_off(C::PLANE, tok, nd0 + nd + (lm_mat >> 1)));
-          mma_bf16_16816(acc[nd], pa, b[0], b[1]);
-          mma_bf16_16816(acc[nd + 1], pa, b[2], b[3]);
-        }
-      }
-
-      if (mt.last) {
-        // ---- end of a piece: token group 1 hands (acc, m, l) to group 0 through this stage
-        l0 += __shfl_xor_sync(FULL, l0, 1);
-        l0 += __shfl_xor_sync(FULL, l0, 2);
-        l1 += __shfl_xor_sync(FULL, l1, 1);
-        l1 += __shfl_xor_sync(FULL, l1, 2);
-        named_bar(1, C::NCW * 32);  // all warps are done reading this stage
-        float *mg = reinterpret_cast<float *>(smem + S::OFF_STAGE + s * C::STAGE_BYTES);
-        // area of quarter dq4: 16 rows x 128 columns; column c of row r at c ^ (4 (r & 7))
-        float *mq = mg + dq4 * C::M * (C::DV / C::DSPLIT);
-        if (tgrp == 1) {
-#pragma unroll
-          for (int n = 0; n < C::NT_PV; ++n) {
-            const int c = (n * 8 + 2 * tq) ^ (4 * g8);
-            *reinterpret_cast<float2 *>(mq + g8 * (C::DV / C::DSPLIT) + c) = make_float2(acc[n][0], acc[n][1]);
-            *reinterpret_cast<float2 *>(mq + (g8 + 8) * (C::DV / C::DSPLIT) + c) = make_float2(acc[n][2], acc[n][3]);
-          }
-          if (tq == 0 && dq4 == 0) {
-            sm_ml[g8 * 2] = m0;
-            sm_ml[g8 * 2 + 1] = l0;
-            sm_ml[(g8 + 8) * 2] = m1;
-            sm_ml[(g8 + 8) * 2 + 1] = l1;
-          }
-        }
-        named_bar(1, C::NCW * 32);
-        if (tgrp == 0) {
-          const float om0 = sm_ml[g8 * 2], ol0 = sm_ml[g8 * 2 + 1];
-          const float om1 = sm_ml[(g8 + 8) * 2], ol1 = sm_ml[(g8 + 8) * 2 + 1];
-          const float M0 = fmaxf(m0, om0), M1 = fmaxf(m1, om1);
-          const float wa0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - M0), wb0 = om0 == -INFINITY ? 0.f : fast_exp2(om0 - M0);
-          const float wa1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - M1), wb1 = om1 == -INFINITY ? 0.f : fast_exp2(om1 - M1);
-          const float L0 = l0 * wa0 + ol0 * wb0, L1 = l1 * wa1 + ol1 * wb1;
-          const float i0 = L0 > 0.f ? 1.f / L0 : 0.f, i1 = L1 > 0.f ? 1.f / L1 : 0.f;
-          const int slot = mt.slot;
-          const size_t pi = (size_t)blockIdx.x * 2 + (slot > 0 ? 1 : 0);
-          const size_t bh0 = (size_t)mt.b * a.H + mt.hq0 + g8, bh1 = bh0 + 8;
-#pragma unroll
-          for (int n = 0; n < C::NT_PV; ++n) {
-            const int c = (n * 8 + 2 * tq) ^ (4 * g8);
-            const float2 x0v = *reinterpret_cast<const float2 *>(mq + g8 * (C::DV / C::DSPLIT) + c);
-            const float2 x1v = *reinterpret_cast<const float2 *>(mq + (g8 + 8) * (C::DV / C::DSPLIT) + c);
-            const float o00 = (acc[n][0] * wa0 + x0v.x * wb0) * i0, o01 = (acc[n][1] * wa0 + x0v.y * wb0) * i0;
-            const float o10 = (acc[n][2] * wa1 + x1v.x * wb1) * i1, o11 = (acc[n][3] * wa1 + x1v.y * wb1) * i1;
-            const int col = (nd0 + n) * 8 + 2 * tq;
-            if (slot < 0) {
-              if (rv0) *reinterpret_cast<uint32_t *>(a.o_lat + bh0 * C::DV + col) = pack_bf16x2(o00, o01);
-              if (rv1) *reinterpret_cast<uint32_t *>(a.o_lat + bh1 * C::DV + col) = pack_bf16x2(o10, o11);
-            } else {
-              *reinterpret_cast<float2 *>(a.part_o + (pi * C::M + g8) * C::DV + col) = make_float2(o00, o01);
-              *reinterpret_cast<float2 *>(a.part_o + (pi * C::M + g8 + 8) * C::DV + col) = make_float2(o10, o11);
-            }
-          }
-          if (tq == 0 && dq4 == 0) {
-            const float s0 = (M0 == -INFINITY || L0 == 0.f) ? -INFINITY : M0 + __log2f(L0);
-            const float s1 = (M1 == -INFINITY || L1 == 0.f) ? -INFINITY : M1 + __log2f(L1);
-            if (slot < 0) {
-              if (a.lse && rv0) a.lse[bh0] = s0 * LN2;
-              if (a.lse && rv1) a.lse[bh1] = s1 * LN2;
-            } else {
-              a.part_lse[pi * C::M + g8] = s0;
-              a.part_lse[pi * C::M + g8 + 8] = s1;
-            }
-          }
-        }
-        fence_proxy_async_smem();
-      } else if (masked) {
-        fence_proxy_async_smem();
-      }
+      auto visible = [&](int t) {
+        const int lt = tok0 + t;
+        return lt >= tok_lo && lt < tok_hi && !((badmask >> (t / bh_tokens)) & 1u);
+      };
+      float x[32];
+      tc_ld32(tl + C::TM_S + sb * C::ST, x);
+      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
+      if (lane == 0) mbar_arrive(&s_free[sb]);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float v = x[i] * a.qscale;
+        x[i] = (!masked || visible(i)) ? v : -INFINITY;
+        mx = fmaxf(mx, x[i]);
+      }
+      // the previous stage's P.V has completed: P may be rewritten and O rescaled
+      if (j > 0 && !mbar_wait(pv_done, (j - 1) & 1, status)) break;
+      tc_fence_after();
+      if (__any_sync(FULL, m != -INFINITY && mx > m + C::TAU)) {
+        const float mn = fmaxf(m, mx);
+        const float alpha = m == -INFINITY ? 0.f : fast_exp2(m - mn);
+        m = mn;
+        l *= alpha;
+#pragma unroll 1
+        for (int c = 0; c < C::DVH; c += 32) {
+          float o[32];
+          tc_ld32(tl + C::TM_O + c, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= alpha;
+          tc_st32(tl + C::TM_O + c, o);
+        }
+        tc_wait_st();
+      } else if (m == -INFINITY) {
+        m = mx;  // nothing attended yet in this piece: O is zero or is overwritten by the first P.V
+      }
+      uint32_t w[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const float p0 = x[2 * c] == -INFINITY ? 0.f : fast_exp2(x[2 * c] - m);
+        const float p1 = x[2 * c + 1] == -INFINITY ? 0.f : fast_exp2(x[2 * c + 1] - m);
+        l += p0 + p1;
+        w[c] = pack_bf16x2(p0, p1);
+      }
+      tc_st16(tl + C::TM_P, w);
+      tc_wait_st();
+      if (masked) {
+        // cache rows of keys that are not attended may hold anything (NaN included): zero their
+        // latent columns of this half before P.V reads them
+        uint8_t *st = smem + S::OFF_STAGE + s * C::STAGE_BYTES + hv * 4 * C::PLANE;
+        for (int e = ts; e < C::ST * 32; e += C::SOFTMAX_WARPS * 32) {
+          const int t = e >> 5, ch = e & 31;
+          if (!visible(t))
+            *reinterpret_cast<uint4 *>(st + (ch >> 3) * C::PLANE + t * 128 + (((ch & 7) ^ (t & 7)) << 4)) =
+                make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+      if (last) {
+        // ---- end of a piece: O / l of this row, and the LSE
+        if (!mbar_wait(pv_done, j & 1, status)) break;
+        tc_fence_after();
+        const bool rv = row < nh;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const float lse2 = (m == -INFINITY || l == 0.f) ? -INFINITY : m + __log2f(l);
+        const size_t pi = (size_t)blockIdx.x * 2 + (slot > 0 ? 1 : 0);
+        uint16_t *orow = a.o_lat + (((size_t)b * 2 + hv) * a.H + h0 + row) * C::DVH;
+        float *prow = a.part_o + (pi * a.rs + row) * C::DVH;
+#pragma unroll 1
+        for (int c = 0; c < C::DVH; c += 32) {
+          float o[32];
+          tc_ld32(tl + C::TM_O + c, o);
+          if (rv) {
+            if (slot < 0) {
+#pragma unroll
+              for (int i = 0; i < 32; i += 8) {
+                uint4 v;
+                v.x = pack_bf16x2(o[i] * inv, o[i + 1] * inv);
+                v.y = pack_bf16x2(o[i + 2] * inv, o[i + 3] * inv);
+                v.z = pack_bf16x2(o[i + 4] * inv, o[i + 5] * inv);
+                v.w = pack_bf16x2(o[i + 6] * inv, o[i + 7] * inv);
+                *reinterpret_cast<uint4 *>(orow + c + i) = v;
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; i += 4)
+                *reinterpret_cast<float4 *>(prow + c + i) =
+                    make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(o_free);
+        if (rv) {
+          if (slot < 0) {
+            if (a.lse && hv == 0) a.lse[(size_t)b * a.H + h0 + row] = lse2 * LN2;
+          } else {
+            a.part_lse[pi * a.rs + row] = lse2;
+          }
+        }
+      }
     }
   }
 
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tc_dealloc(tmem, C::TM_COLS);
   if (tid == 0) {
     GqaPartDesc d = misc->desc;
     d.status = misc->status;
     a.desc[blockIdx.x] = d;
   }
   if ((misc->desc.flags & DESC_PIECES) == 0) {
-    for (int e = tid; e < C::M * C::DV; e += C::THREADS) a.part_o[(size_t)blockIdx.x * 2 * C::M * C::DV + e] = 0.f;
-    for (int h = tid; h < C::M; h += C::THREADS) a.part_lse[(size_t)blockIdx.x * 2 * C::M + h] = -INFINITY;
+    // a CTA whose range held no visible key can still lie between two pieces of a sequence: the
+    // merge walks over its slot 0, which must weigh nothing
+    float *po = a.part_o + (size_t)blockIdx.x * 2 * a.rs * C::DVH;
+    for (int e = tid; e < a.rs * C::DVH; e += C::THREADS) po[e] = 0.f;
+    for (int h = tid; h < a.rs; h += C::THREADS) a.part_lse[(size_t)blockIdx.x * 2 * a.rs + h] = -INFINITY;
+  }
+}
+
+// Merge of the pieces of split sequences: the CTA c whose last piece starts a sequence and does
+// not end it finds the sequence's later pieces in CTAs c + hg, c + 2 hg, ... (the same position
+// in the next groups) and merges them in that order.  Block (c, y) handles rows [8 y, 8 y + 8) of
+// the tile, one warp per row (the rows' dependent loads from L2 overlap instead of queueing); a
+// row's weights are exp2(lse_k - max), o = sum_k w_k o_k / sum_k w_k, each lane owning 8 of the
+// half's 256 columns.  The half-0 sequence writes the merged LSE.
+struct MlaCombineArgs {
+  uint16_t *o_lat;
+  float *lse;
+  const float *part_o, *part_lse;
+  const GqaPartDesc *desc;
+  uint32_t *status;
+  int H, rs, nparts, hg;
+};
+
+constexpr int MLA_COMBINE_THREADS = 256;
+constexpr int MLA_COMBINE_ROWS = MLA_COMBINE_THREADS / 32;  // rows per block: gridDim.y = 128 / 8
+
+__global__ void __launch_bounds__(MLA_COMBINE_THREADS) mla_combine_kernel(const MlaCombineArgs a) {
+  constexpr int DVH = MlaTcCfg::DVH, PER = DVH / 32;
+  pdl_wait();               // the split kernel's partials and descriptors are visible from here on
+  pdl_launch_dependents();  // the W_UV projection may stage its weights
+  const int c = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (c == 0 && blockIdx.y == 0 && warp == 0) {
+    uint32_t s = 0;
+    for (int i = lane; i < a.nparts; i += 32) s |= a.desc[i].status;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) s |= __shfl_xor_sync(FULL, s, o);
+    if (lane == 0) *a.status = s;
+  }
+  const GqaPartDesc d0 = a.desc[c];
+  const uint32_t np = d0.flags & DESC_PIECES;
+  if (np == 0 || !(d0.flags & DESC_LAST_STARTS) || (d0.flags & DESC_LAST_ENDS)) return;
+  int k = -1;  // pieces: CTA c + i hg holds piece i, i < k
+  for (int base = 1; c + base * a.hg < a.nparts && k < 0; base += 32) {
+    const int i = c + (base + lane) * a.hg;
+    bool hit = false;
+    if (i < a.nparts) {
+      const uint32_t f = a.desc[i].flags;
+      hit = (f & DESC_PIECES) != 0 && (f & DESC_FIRST_ENDS) != 0;
+    }
+    const uint32_t msk = __ballot_sync(FULL, hit);
+    if (msk) k = base + __ffs(msk);
+  }
+  if (k < 0) return;  // not reachable for a consistent partition
+  const int first_slot = np >= 2 ? 1 : 0;
+  const int h0 = (d0.last_hs >> 1) * MlaTcCfg::M, hv = d0.last_hs & 1;
+  const int nh = min(MlaTcCfg::M, a.H - h0);
+  {
+    const int r = blockIdx.y * MLA_COMBINE_ROWS + warp;
+    if (r >= nh) return;
+    float M = -INFINITY;
+    for (int i = lane; i < k; i += 32) {
+      const size_t pi = i == 0 ? (size_t)c * 2 + first_slot : (size_t)(c + i * a.hg) * 2;
+      M = fmaxf(M, a.part_lse[pi * a.rs + r]);
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, o));
+    float Z = 0.f;
+    for (int i = lane; i < k; i += 32) {
+      const size_t pi = i == 0 ? (size_t)c * 2 + first_slot : (size_t)(c + i * a.hg) * 2;
+      const float l = a.part_lse[pi * a.rs + r];
+      Z += (l == -INFINITY || M == -INFINITY) ? 0.f : fast_exp2(l - M);
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) Z += __shfl_xor_sync(FULL, Z, o);
+    float acc[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+#pragma unroll 4
+    for (int i = 0; i < k; ++i) {
+      const size_t pi = i == 0 ? (size_t)c * 2 + first_slot : (size_t)(c + i * a.hg) * 2;
+      const float l = a.part_lse[pi * a.rs + r];
+      const float wc = (l == -INFINITY || M == -INFINITY) ? 0.f : fast_exp2(l - M);
+      const float *po = a.part_o + (pi * a.rs + r) * DVH + lane * PER;
+#pragma unroll
+      for (int e = 0; e < PER; e += 4) {
+        const float4 x = *reinterpret_cast<const float4 *>(po + e);
+        acc[e] += wc * x.x;
+        acc[e + 1] += wc * x.y;
+        acc[e + 2] += wc * x.z;
+        acc[e + 3] += wc * x.w;
+      }
+    }
+    const float inv = Z > 0.f ? 1.f / Z : 0.f;
+    uint4 v;
+    v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+    v.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+    v.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+    *reinterpret_cast<uint4 *>(a.o_lat + (((size_t)d0.last_b * 2 + hv) * a.H + h0 + r) * DVH + lane * PER) = v;
+    if (lane == 0 && hv == 0 && a.lse)
+      a.lse[(size_t)d0.last_b * a.H + h0 + r] = (M == -INFINITY || Z == 0.f) ? -INFINITY : (M + __log2f(Z)) * LN2;
   }
 }
 
