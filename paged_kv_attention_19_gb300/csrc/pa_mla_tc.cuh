@@ -14,21 +14,29 @@
 // fp32 o_lat of 128 heads x 512 columns would fill the whole tensor memory, so a sequence is
 // (row, head tile, half of the 512 latent columns): the two halves of a tile are the CTA group
 // of the split-KV partition (pa_partition.cuh), stream the same cache pages at about the same
-// time (DRAM once, L2 for the other) and each compute the full scores.  Per CTA:
-//   * warp 0, producer: TMA copies of 32-token stages (9 planes of 64 dims x 32 tokens, 128-byte
-//     swizzle, 36 KB) into a 2-stage ring, and per piece the tile's 128 query rows (9 planes,
-//     144 KB) into the query area once the previous piece's score MMAs have read it;
-//   * warp 1, one thread issues the MMAs: S = Q C^T (M = 128 heads, N = 32 tokens, K = 576, both
-//     operands K-major in shared memory) into one of two score buffers in tensor memory, then
-//     O += P V for the previous stage (P: 128 x 32 bf16 from tensor memory, V: the stage's
-//     latent columns of this half, MN-major in shared memory, N = 256) into the O columns;
-//     completions go to mbarriers by tcgen05.commit;
-//   * warps 2-5, softmax: one thread per head row reads its 32 scores from tensor memory, keeps
-//     the fp32 running max and sum (rescaling its O row in tensor memory only when the max grows
-//     by more than 2^8), writes the probabilities as bf16 back to tensor memory, and at the end of
-//     a piece reads O, divides by the sum and stores o_lat (or an fp32 partial) and the LSE.
-// Tensor-memory columns: scores 0-63 (two buffers of 32), P 64-79, O 256-511.
+// time (DRAM once, L2 for the other) and each compute the full scores.
+//
+// An MMA instruction costs about the same issue time for N = 32 as for N = 128, so the score MMAs
+// take 64 tokens at once (N = 64).  Shared memory cannot hold the tile's 144 KB of query rows next
+// to a ring of 72 KB stages, so the query is split: its first 5 planes of 64 dims stay in shared
+// memory (A operand from shared memory), the last 4 are copied into tensor memory by tcgen05.cp
+// once per piece (A operand from tensor memory).  Per CTA:
+//   * warp 0, producer: per piece the query planes 0-4 into the query area and planes 5-8 into a
+//     ring slot (a "query stage"), then TMA copies of 64-token stages (9 planes of 64 dims x 64
+//     tokens, 128-byte swizzle, 72 KB) into the 2-slot ring;
+//   * warp 1, one thread issues the tensor-core work from a polling loop: the tcgen05.cp of a query
+//     stage, the 36 score MMAs of a stage (S = Q C^T, M = 128 heads, N = 64 tokens, K = 576) into
+//     one of two score buffers, in chunks of 3 planes, and, as soon as a stage's probabilities are
+//     in tensor memory, its P.V (P: 128 x 64 bf16 written over the stage's own scores, V: the
+//     stage's latent columns of this half, MN-major, N = 256) into the O columns;
+//   * warps 2-5, softmax: one thread per head row reads its 64 scores, keeps the fp32 running max
+//     and sum (rescaling its O row in tensor memory only when the max grows by more than 2^8),
+//     writes the probabilities as bf16 over the scores, and at the end of a piece reads O, divides
+//     by the sum and stores o_lat (or an fp32 partial) and the LSE.
+// Tensor-memory columns: scores (then P) 0-127 (two buffers of 64), query planes 5-8 128-255, O 256-511.
 #pragma once
+
+#include <type_traits>
 
 #include "pa_gqa.cuh"
 #include "pa_partition.cuh"
@@ -54,19 +62,23 @@ struct MlaTcCfg {
   static constexpr int M = 128;                   // heads per tile: MMA rows, tensor-memory lanes
   static constexpr int DQK = 576, DV = 512, DVH = DV / 2;
   static constexpr int NQK = DQK / 64;            // 9 swizzle planes per cache row
-  static constexpr int ST = 32;                   // tokens per stage: N of the score MMA, K of P.V
-  static constexpr int NS = 2;                    // stages in the ring
-  static constexpr int PLANE = ST * 128;          // 4 KB
-  static constexpr int STAGE_BYTES = NQK * PLANE; // 36 KB
+  static constexpr int NQS = 5;                   // query planes in shared memory; the rest in tensor memory
+  static constexpr int ST = 64;                   // tokens per stage: N of the score MMA, K of P.V
+  static constexpr int NS = 2;                    // slots in the ring
+  static constexpr int PLANE = ST * 128;          // 8 KB
+  static constexpr int STAGE_BYTES = NQK * PLANE; // 72 KB
   static constexpr int QPLANE = M * 128;          // 16 KB
-  static constexpr int Q_BYTES = NQK * QPLANE;    // 144 KB
+  static constexpr int QS_BYTES = NQS * QPLANE;   // 80 KB: planes 0-4
+  static constexpr int QT_BYTES = (NQK - NQS) * QPLANE;  // 64 KB: planes 5-8, through a ring slot
   static constexpr int SOFTMAX_WARPS = 4;
   static constexpr int THREADS = (2 + SOFTMAX_WARPS) * 32;
-  static constexpr uint32_t TM_S = 0, TM_P = 64, TM_O = 256, TM_COLS = 512;
+  static constexpr uint32_t TM_S = 0, TM_QT = 128, TM_O = 256, TM_COLS = 512;
   static constexpr float TAU = 8.f;               // lazy rescale threshold (log2 units)
   static constexpr uint32_t IDESC_S = tc_idesc_bf16(M, ST, false);
   static constexpr uint32_t IDESC_PV = tc_idesc_bf16(M, DVH, true);
   static_assert(NQK % 3 == 0, "the scores are issued in chunks of 3 planes");
+  static_assert(QT_BYTES <= STAGE_BYTES, "the query planes 5-8 fit a ring slot");
+  static_assert(2 * ST + (NQK - NQS) * 4 * 8 + DVH <= (int)TM_COLS, "tensor-memory budget");
 };
 
 struct MlaTcMisc {
@@ -79,11 +91,12 @@ struct MlaTcMisc {
 
 struct MlaTcSmem {
   using C = MlaTcCfg;
-  static constexpr int OFF_Q = 0;                                      // the piece's query rows
-  static constexpr int OFF_STAGE = OFF_Q + C::Q_BYTES;
-  static constexpr int OFF_META = OFF_STAGE + C::NS * C::STAGE_BYTES;
-  static constexpr int OFF_BAR = OFF_META + C::NS * (int)sizeof(StageMeta);
-  // full[NS], empty[NS], q_full, q_empty, s_full[2], s_free[2], p_full, pv_done, o_free, drain
+  static constexpr int OFF_Q = 0;                                      // the piece's query planes 0-4
+  static constexpr int OFF_STAGE = OFF_Q + C::QS_BYTES;
+  static constexpr int OFF_META = OFF_STAGE + C::NS * C::STAGE_BYTES;  // per ring slot
+  static constexpr int OFF_SINFO = OFF_META + C::NS * (int)sizeof(StageMeta);  // per score buffer
+  // full[NS], empty[NS], q_full, q_empty, s_full[2], sbuf_free[2], p_full, pv_done, o_free, drain
+  static constexpr int OFF_BAR = OFF_SINFO + 2 * (int)sizeof(StageMeta);
   static constexpr int NBAR = 2 * C::NS + 10;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int USED = OFF_MISC + (int)sizeof(MlaTcMisc);
@@ -91,6 +104,8 @@ struct MlaTcSmem {
   static_assert(BYTES <= 232448, "fits the 227 KB opt-in shared memory of one CTA");
 };
 
+// StageMeta fields as used here: nq = 1 marks a query stage; pad0 (score buffers) = the ring slot
+// holding the stage's cache rows.
 __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
     mla_tc_split_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_q,
                         const MlaTcArgs a) {
@@ -101,9 +116,10 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::OFF_BAR);
   uint64_t *full = bars, *empty = bars + C::NS;
   uint64_t *q_full = bars + 2 * C::NS, *q_empty = q_full + 1;
-  uint64_t *s_full = q_full + 2, *s_free = s_full + 2;
-  uint64_t *p_full = s_free + 2, *pv_done = p_full + 1, *o_free = p_full + 2, *drain = p_full + 3;
+  uint64_t *s_full = q_full + 2, *sbuf_free = s_full + 2;
+  uint64_t *p_full = sbuf_free + 2, *pv_done = p_full + 1, *o_free = p_full + 2, *drain = p_full + 3;
   StageMeta *meta = reinterpret_cast<StageMeta *>(smem + S::OFF_META);
+  StageMeta *sinfo = reinterpret_cast<StageMeta *>(smem + S::OFF_SINFO);
   MlaTcMisc *misc = reinterpret_cast<MlaTcMisc *>(smem + S::OFF_MISC);
 
   const int tid = threadIdx.x;
@@ -116,8 +132,8 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], C::SOFTMAX_WARPS);
+      mbar_init(&s_full[i], 2);  // the scores' commit and the issuing thread's arrive (after sinfo)
+      mbar_init(&sbuf_free[i], 1);
     }
     mbar_init(p_full, C::SOFTMAX_WARPS);
     mbar_init(pv_done, 1);
@@ -135,7 +151,8 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc->tmem;
-  pdl_wait();               // q_abs, written by the absorb kernel, is visible from here on
+  // Only the query rows come from the absorb kernel: the producer waits for it (griddepcontrol)
+  // just before their first copy, so the partition and the first cache stage overlap its tail.
   pdl_launch_dependents();  // the combine kernel may be scheduled; it waits for this grid to finish
   uint32_t *status = &misc->status;
 
@@ -158,9 +175,10 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
     // ------------------------------------------------------------ producer
     const int P = 1 << a.log2_page;
     const int nbox = C::ST >> a.log2_bh;
-    uint32_t j = 0;   // stages issued
-    uint32_t kq = 0;  // query tiles issued
+    uint32_t j = 0;   // ring slots issued
+    uint32_t kq = 0;  // pieces whose query was issued
     bool ok = true;
+    bool pre_pending = false;  // ring index 1 was issued ahead of ring index 0
     int npieces = 0;
     Piece last_piece = {};
     bool first_ends = false;
@@ -191,11 +209,11 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
       const int32_t *bt_piece = a.block_table + (size_t)cur.b * a.max_pages_per_seq + pb;
       int cwin = cwin0, wi = 0;
       int fwin = (lane + 32 < npages) ? bt_piece[32 + lane] : 0;
-      for (int t = 0; t < n_stages && ok; ++t) {
-        const int s = j % C::NS;
-        const uint32_t u = j / C::NS;
-        if (u > 0) ok = mbar_wait(&empty[s], (u - 1) & 1, status);
-        if (!ok) break;
+      // cache stage t of the piece into ring index jj
+      auto issue_stage = [&](int t, uint32_t jj) -> bool {
+        const int s = jj % C::NS;
+        const uint32_t u = jj / C::NS;
+        if (u > 0 && !mbar_wait(&empty[s], (u - 1) & 1, status)) return false;
         const int unit0 = cur.ub + t * nbox;
         const int tok0 = unit0 << a.log2_bh;
         const int pwin = ((tok0 >> a.log2_page) - pb) >> 5;
@@ -220,13 +238,13 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
         }
         const uint32_t bad = __ballot_sync(FULL, isbad);
         const int nvalid = __popc(__ballot_sync(FULL, load));
-        const bool last = (t == n_stages - 1);
         uint8_t *kdst = smem + S::OFF_STAGE + s * C::STAGE_BYTES;
         if (lane == 0) {
           StageMeta &m = meta[s];
           m.end = 0;
+          m.nq = 0;
           m.first = t == 0;
-          m.last = last;
+          m.last = t == n_stages - 1;
           m.b = cur.b;
           m.hq0 = h0;
           m.ghead = nh;
@@ -246,21 +264,47 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
 #pragma unroll
           for (int dq = 0; dq < C::NQK; ++dq) tma_load_3d(dst + dq * C::PLANE, &tm_c, dq * 64, pslot, phys, &full[s]);
         }
-        ++j;
-        if (t == 0) {
-          // the tile's query rows, after the first stage is under way: the area is free once the
-          // previous piece's score MMAs have completed
-          if (kq > 0) ok = mbar_wait(q_empty, (kq - 1) & 1, status);
-          if (!ok) break;
-          if (lane == 0) {
-            mbar_arrive_expect_tx(q_full, (uint32_t)C::Q_BYTES);
+        return true;
+      };
+      // The ring holds the piece's query stage, then its cache stages.  The first piece's first
+      // cache stage (ring index 1) is issued before the wait for the absorb kernel.
+      const bool early = kq == 0;
+      if (early) {
+        ok = issue_stage(0, j + 1);
+        pre_pending = ok;
+        pdl_wait();  // q_abs is visible from here on
+      }
+      if (ok) {
+        // the tile's query: planes 0-4 into the query area, planes 5-8 into ring index j; both are
+        // free once the previous piece's score MMAs have completed
+        if (kq > 0) ok = mbar_wait(q_empty, (kq - 1) & 1, status);
+        const int s = j % C::NS;
+        const uint32_t u = j / C::NS;
+        if (ok && u > 0) ok = mbar_wait(&empty[s], (u - 1) & 1, status);
+        if (ok && lane == 0) {
+          StageMeta &m = meta[s];
+          m.end = 0;
+          m.nq = 1;
+          mbar_arrive_expect_tx(q_full, (uint32_t)C::QS_BYTES);
 #pragma unroll
-            for (int dq = 0; dq < C::NQK; ++dq)
-              tma_load_2d(smem + S::OFF_Q + dq * C::QPLANE, &tm_q, dq * 64, cur.b * a.H + h0, q_full);
-          }
-          __syncwarp();
-          ++kq;
+          for (int dq = 0; dq < C::NQS; ++dq)
+            tma_load_2d(smem + S::OFF_Q + dq * C::QPLANE, &tm_q, dq * 64, cur.b * a.H + h0, q_full);
+          mbar_arrive_expect_tx(&full[s], (uint32_t)C::QT_BYTES);
+          uint8_t *qt = smem + S::OFF_STAGE + s * C::STAGE_BYTES;
+#pragma unroll
+          for (int dq = C::NQS; dq < C::NQK; ++dq)
+            tma_load_2d(qt + (dq - C::NQS) * C::QPLANE, &tm_q, dq * 64, cur.b * a.H + h0, &full[s]);
         }
+        __syncwarp();
+        if (ok) {
+          ++kq;
+          j += early ? 2 : 1;
+          pre_pending = false;
+        }
+      }
+      for (int t = early ? 1 : 0; t < n_stages && ok; ++t) {
+        ok = issue_stage(t, j);
+        if (ok) ++j;
       }
       if (!ok) break;
       if (npieces == 0) first_ends = cur.ends;
@@ -279,6 +323,7 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
       if (u > 0) ok = mbar_wait(&empty[s], (u - 1) & 1, status);
       if (ok && lane == 0) {
         meta[s].end = 1;
+        meta[s].nq = 0;
         mbar_arrive(&full[s]);
       }
     }
@@ -286,6 +331,7 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
       // copies still in flight land before the CTA exits
       const uint32_t first = j > (uint32_t)C::NS ? j - C::NS : 0u;
       for (uint32_t i = first; i < j; ++i) mbar_wait(&full[i % C::NS], (i / C::NS) & 1, status);
+      if (pre_pending) mbar_wait(&full[1 % C::NS], 0, status);
       if (kq > 0) mbar_wait(q_full, (kq - 1) & 1, status);
     }
     if (lane == 0) {
@@ -295,73 +341,122 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
                          (last_piece.ends ? DESC_LAST_ENDS : 0u) | (first_ends ? DESC_FIRST_ENDS : 0u);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issue (one thread)
-    // A polling loop over the events the MMAs wait for.  P.V of the oldest stage goes first (it
-    // frees a ring slot); the 36 score MMAs of a stage go out in chunks of 3 planes, so a P.V
-    // whose probabilities are ready waits for at most one chunk.
+    // ------------------------------------------------------------ tensor-core issue (one thread)
+    // A polling loop over the events the tensor-core work waits for.  P.V of the oldest stage goes
+    // first (it frees a ring slot and a score buffer); the 36 score MMAs of a stage go out in
+    // chunks of 3 planes, so a P.V whose probabilities are ready waits for at most one chunk.
     if (lane == 0) {
       const uint64_t qd0 = tc_sdesc_sw128(smem_u32(smem + S::OFF_Q), 16, 1024);
       const uint32_t stage0 = smem_u32(smem + S::OFF_STAGE);
+      uint32_t r = 0;     // ring slot consumed next
       uint32_t js = 0;    // stage whose scores are issued next
       uint32_t jp = 0;    // stage whose P.V is issued next (jp <= js)
-      uint32_t kq = 0;    // query tiles consumed (q_full phases)
+      uint32_t kq = 0;    // query stages copied (q_empty phases awaited: one per earlier piece)
+      uint32_t kf = 0;    // pieces whose first scores were issued (q_full phases)
       uint32_t npp = 0;   // pieces whose first P.V was issued (o_free phases: one per earlier piece)
+      uint32_t rs0 = 0, rs1 = 0;  // ring slots of the stages in score buffers 0 and 1
       int plane = -1;     // >= 0: the scores of stage js are being issued, next plane
       bool last_js = false, ended = false;
       uint64_t idle_since = 0;
       while (!(ended && jp == js)) {
         bool progress = false;
         if (jp < js && mbar_test(p_full, jp & 1)) {
-          const StageMeta &mp = meta[jp % C::NS];
-          const bool first = mp.first;
+          const int bp = jp & 1;
+          const StageMeta &ip = sinfo[bp];
+          const bool first = ip.first;
           if (!first || npp == 0 || mbar_test(o_free, (npp - 1) & 1)) {
             tc_fence_after();
             if (first) ++npp;
-            const int sp = jp % C::NS;
-            const uint64_t vd = tc_sdesc_sw128(stage0 + sp * C::STAGE_BYTES + mp.i0 * 4 * C::PLANE, C::PLANE, 1024);
+            const uint32_t sp = bp ? rs1 : rs0;
+            const uint64_t vd = tc_sdesc_sw128(stage0 + sp * C::STAGE_BYTES + ip.i0 * 4 * C::PLANE, C::PLANE, 1024);
 #pragma unroll
             for (int kk = 0; kk < C::ST / 16; ++kk)
-              tc_mma_ts(tmem + C::TM_O, tmem + C::TM_P + 8 * kk, vd + (uint64_t)((kk * 16 * 128) >> 4), C::IDESC_PV,
-                        (first && kk == 0) ? 0u : 1u);
+              tc_mma_ts(tmem + C::TM_O, tmem + C::TM_S + bp * C::ST + 8 * kk, vd + (uint64_t)((kk * 16 * 128) >> 4),
+                        C::IDESC_PV, (first && kk == 0) ? 0u : 1u);
             tc_commit(&empty[sp]);
             tc_commit(pv_done);
+            tc_commit(&sbuf_free[bp]);
             ++jp;
             progress = true;
           }
         }
         if (!progress && plane >= 0) {
-          const int s = js % C::NS, sb = js & 1;
-          const uint64_t cd0 = tc_sdesc_sw128(stage0 + s * C::STAGE_BYTES, 16, 1024);
+          const int sb = js & 1;
+          const uint64_t cd0 = tc_sdesc_sw128(stage0 + (sb ? rs1 : rs0) * C::STAGE_BYTES, 16, 1024);
+          const uint32_t dS = tmem + C::TM_S + sb * C::ST;
+          // planes [P0, P0 + 3) with compile-time operand offsets
+          auto chunk = [&](auto p0c) {
+            constexpr int P0 = decltype(p0c)::value;
 #pragma unroll
-          for (int pp = 0; pp < 3; ++pp) {
-            const int p = plane + pp;
+            for (int pp = 0; pp < 3; ++pp) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              tc_mma_ss(tmem + C::TM_S + sb * C::ST, qd0 + (uint64_t)((p * C::QPLANE + 32 * kk) >> 4),
-                        cd0 + (uint64_t)((p * C::PLANE + 32 * kk) >> 4), C::IDESC_S, (p | kk) != 0 ? 1u : 0u);
-          }
+              for (int kk = 0; kk < 4; ++kk) {
+                const int p = P0 + pp;
+                const uint64_t bd = cd0 + (uint64_t)((p * C::PLANE + 32 * kk) >> 4);
+                if (p < C::NQS)
+                  tc_mma_ss(dS, qd0 + (uint64_t)((p * C::QPLANE + 32 * kk) >> 4), bd, C::IDESC_S,
+                            (p | kk) != 0 ? 1u : 0u);
+                else
+                  tc_mma_ts(dS, tmem + C::TM_QT + ((p - C::NQS) * 4 + kk) * 8, bd, C::IDESC_S, 1u);
+              }
+            }
+          };
+          if (plane == 0)
+            chunk(std::integral_constant<int, 0>{});
+          else if (plane == 3)
+            chunk(std::integral_constant<int, 3>{});
+          else
+            chunk(std::integral_constant<int, 6>{});
           plane += 3;
           if (plane == C::NQK) {
             tc_commit(&s_full[sb]);
-            if (last_js) tc_commit(q_empty);  // the query area may take the next piece's rows
+            if (last_js) tc_commit(q_empty);  // the query may be replaced by the next piece's
             plane = -1;
             ++js;
           }
           progress = true;
         }
-        if (!progress && plane < 0 && !ended && mbar_test(&full[js % C::NS], (js / C::NS) & 1) &&
-            (js < 2 || mbar_test(&s_free[js & 1], ((js >> 1) - 1) & 1))) {
-          const StageMeta &mt = meta[js % C::NS];
-          if (mt.end) {
+        if (!progress && plane < 0 && !ended && mbar_test(&full[r % C::NS], (r / C::NS) & 1)) {
+          const int s = r % C::NS;
+          const StageMeta &mt = meta[s];
+          const int sb = js & 1;
+          const bool buf_free = js < 2 || mbar_test(&sbuf_free[sb], ((js >> 1) - 1) & 1);
+          if (mt.nq) {
+            // a query stage: planes 5-8 into tensor memory once the previous piece's scores are done
+            if (kq == 0 || mbar_test(q_empty, (kq - 1) & 1)) {
+              tc_fence_after();
+              const uint64_t td0 = tc_sdesc_sw128(stage0 + s * C::STAGE_BYTES, 16, 1024);
+#pragma unroll
+              for (int p = 0; p < C::NQK - C::NQS; ++p)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                  tc_cp_128x256b(tmem + C::TM_QT + (p * 4 + kk) * 8, td0 + (uint64_t)((p * C::QPLANE + 32 * kk) >> 4));
+              tc_commit(&empty[s]);
+              ++kq;
+              ++r;
+              progress = true;
+            }
+          } else if (mt.end) {
+            if (buf_free) {
+              tc_fence_after();
+              sinfo[sb].end = 1;
+              mbar_arrive(&s_full[sb]);  // the softmax warps stop at this stage
+              mbar_arrive(&s_full[sb]);
+              ended = true;
+              progress = true;
+            }
+          } else if (buf_free && (!mt.first || mbar_test(q_full, kf & 1))) {
             tc_fence_after();
-            mbar_arrive(&s_full[js & 1]);  // the softmax warps stop at this stage
-            ended = true;
-            progress = true;
-          } else if (!mt.first || mbar_test(q_full, kq & 1)) {
-            tc_fence_after();
-            if (mt.first) ++kq;
+            if (mt.first) ++kf;
+            StageMeta &si = sinfo[sb];
+            si = mt;
+            si.end = 0;
+            si.pad0 = s;
+            if (sb) rs1 = s; else rs0 = s;
+            mbar_arrive(&s_full[sb]);  // releases sinfo; the phase completes with the scores' commit
             last_js = mt.last;
             plane = 0;
+            ++r;
             progress = true;
           }
         }
@@ -377,7 +472,7 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
           }
         }
       }
-      // every MMA this thread issued has completed before the tensor memory is released
+      // every operation this thread issued has completed before the tensor memory is released
       tc_commit(drain);
       mbar_wait(drain, 0, status);
     }
@@ -391,15 +486,15 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
     const int bh_tokens = 1 << a.log2_bh;
     float m = -INFINITY, l = 0.f;
     for (uint32_t j = 0;; ++j) {
-      const int sb = j & 1, s = j % C::NS;
+      const int sb = j & 1;
       if (!mbar_wait(&s_full[sb], (j >> 1) & 1, status)) break;
       tc_fence_after();
-      const StageMeta &mt = meta[s];
+      const StageMeta &mt = sinfo[sb];
       if (mt.end) break;
       const bool first = mt.first, last = mt.last, masked = mt.masked;
       const int tok0 = mt.tok0, tok_lo = mt.tok_lo, tok_hi = mt.tok_hi;
       const uint32_t badmask = mt.badmask;
-      const int b = mt.b, h0 = mt.hq0, nh = mt.ghead, hv = mt.i0, slot = mt.slot;
+      const int b = mt.b, h0 = mt.hq0, nh = mt.ghead, hv = mt.i0, slot = mt.slot, rslot = mt.pad0;
       if (first) {
         m = -INFINITY;
         l = 0.f;
@@ -408,19 +503,18 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
         const int lt = tok0 + t;
         return lt >= tok_lo && lt < tok_hi && !((badmask >> (t / bh_tokens)) & 1u);
       };
-      float x[32];
-      tc_ld32(tl + C::TM_S + sb * C::ST, x);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[sb]);
+      const uint32_t tS = tl + C::TM_S + sb * C::ST;
+      float x[C::ST];
+      tc_ld32(tS, *reinterpret_cast<float(*)[32]>(&x[0]));
+      tc_ld32(tS + 32, *reinterpret_cast<float(*)[32]>(&x[32]));
       float mx = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
+      for (int i = 0; i < C::ST; ++i) {
         const float v = x[i] * a.qscale;
         x[i] = (!masked || visible(i)) ? v : -INFINITY;
         mx = fmaxf(mx, x[i]);
       }
-      // the previous stage's P.V has completed: P may be rewritten and O rescaled
+      // the previous stage's P.V has completed: O may be rescaled
       if (j > 0 && !mbar_wait(pv_done, (j - 1) & 1, status)) break;
       tc_fence_after();
       if (__any_sync(FULL, m != -INFINITY && mx > m + C::TAU)) {
@@ -440,20 +534,25 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
       } else if (m == -INFINITY) {
         m = mx;  // nothing attended yet in this piece: O is zero or is overwritten by the first P.V
       }
-      uint32_t w[16];
+      // the probabilities, as bf16 pairs (even token in the low half), over the stage's scores
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const float p0 = x[2 * c] == -INFINITY ? 0.f : fast_exp2(x[2 * c] - m);
-        const float p1 = x[2 * c + 1] == -INFINITY ? 0.f : fast_exp2(x[2 * c + 1] - m);
-        l += p0 + p1;
-        w[c] = pack_bf16x2(p0, p1);
+      for (int h = 0; h < 2; ++h) {
+        uint32_t w[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float x0 = x[32 * h + 2 * c], x1 = x[32 * h + 2 * c + 1];
+          const float p0 = x0 == -INFINITY ? 0.f : fast_exp2(x0 - m);
+          const float p1 = x1 == -INFINITY ? 0.f : fast_exp2(x1 - m);
+          l += p0 + p1;
+          w[c] = pack_bf16x2(p0, p1);
+        }
+        tc_st16(tS + 16 * h, w);
       }
-      tc_st16(tl + C::TM_P, w);
       tc_wait_st();
       if (masked) {
         // cache rows of keys that are not attended may hold anything (NaN included): zero their
         // latent columns of this half before P.V reads them
-        uint8_t *st = smem + S::OFF_STAGE + s * C::STAGE_BYTES + hv * 4 * C::PLANE;
+        uint8_t *st = smem + S::OFF_STAGE + rslot * C::STAGE_BYTES + hv * 4 * C::PLANE;
         for (int e = ts; e < C::ST * 32; e += C::SOFTMAX_WARPS * 32) {
           const int t = e >> 5, ch = e & 31;
           if (!visible(t))

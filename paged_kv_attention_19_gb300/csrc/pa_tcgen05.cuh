@@ -21,8 +21,8 @@
 // the even K index in the low half.  Warp w of the CTA reaches lanes [32 (w % 4), +32).
 //
 // These encodings were checked on a GB300 against an fp64 product: a 128 x 576 by 576 x 32 score
-// MMA with both operands K-major, and a 128 x 32 by 32 x 256 product with B MN-major and A from
-// shared memory or from tensor memory.
+// MMA with both operands K-major, a 128 x 32 by 32 x 256 product with B MN-major and A from
+// shared memory or from tensor memory, and an A operand copied into tensor memory by tcgen05.cp.
 #pragma once
 
 #include <cstdint>
@@ -71,6 +71,13 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d, uint32_t a_tmem, uint64_t 
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// Copy of a 128-row x 32-byte matrix from shared memory (described like an MMA operand) into 8
+// columns of all 128 lanes; a K-major bf16 operand lands in the layout an A operand read from
+// tensor memory has (row i in lane i, two bf16 per column).  One thread issues.
+__device__ __forceinline__ void tc_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 // One arrival on *bar once every tcgen05 operation this thread issued before has completed.
