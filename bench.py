@@ -480,15 +480,18 @@ def run_ours(args, rank, local_rank, world):
     }
     if is_mla:
         # the MLA attention core is a tensor-core contraction: its roofline is the bf16 tensor peak
-        # (the algorithmic flops: 2 x (576 + 512) per (head, visible token); the kernel also spends
-        # 2 x 512 more on the low half of q_lat, not counted)
+        # (the algorithmic flops: 2 x (576 + 512) per (head, visible token); the two column-half
+        # CTAs of a head tile each compute the full scores, 2 x 576 more per (head, token) that is
+        # executed but not counted).  Its HBM rate counts the bytes the core itself reads: the
+        # visible cache rows and q_abs, not the projection weights.
         flops = 2.0 * w.visible_tokens() * w.num_heads * (576 + 512)
         tf_peak, tf_kind = measured_bf16_tflops()
         achieved = flops / (kms * 1e-3) / 1e12
+        core_gbs = w.algorithmic_bytes(with_weights=False) / (kms * 1e-3) / 1e9
         line["roofline"].update({"bound": "tensor", "achieved": round(achieved, 2), "peak": tf_peak,
                                  "unit": "TFLOP/s", "frac": round(achieved / tf_peak, 4),
                                  "peak_source": f"bf16_tflops of {tf_kind} (cuBLAS bf16 burst)",
-                                 "hbm_gbs": round(kernel_gbs, 2), "hbm_frac": round(kernel_gbs / peak, 4)})
+                                 "hbm_gbs": round(core_gbs, 2), "hbm_frac": round(core_gbs / peak, 4)})
     if not args.no_cpu_baseline:
         v, desc, cores = cpu_oracle_time(w, args.workload)
         line["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",

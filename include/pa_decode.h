@@ -64,8 +64,9 @@
  *     flattened row by row, are cut into that many equal contiguous shares,
  *     each handled by one CTA and merged in ascending order where a sequence
  *     spans several shares; 0 = automatic (one share per SM, at most 256),
- *     n in [1, 4096] = n shares; MLA the same, its sequences being (row, 16-head
- *     tile) over the one latent cache row.  For a
+ *     n in [1, 4096] = n shares; MLA the same, its sequences being (row, tile
+ *     of 128 heads, half of the 512 latent columns) over the one latent cache
+ *     row.  For a
  *     fixed num_splits (and fixed inputs) results are bitwise reproducible
  *     from run to run and independent of the physical page order; different
  *     split counts agree within rounding.
@@ -75,8 +76,10 @@
  *     calls sharing one workspace must be ordered on one stream.  The GQA
  *     workspace depends on head_dim and num_splits only (two fp32 partial
  *     results of 16 heads per share: 16 KB per share at head_dim 128, about
- *     4.2 MB in automatic mode); the MLA one adds q_abs and o_lat in bf16
- *     (2.2 KB per (row, head)) to its 64 KB per share.
+ *     4.2 MB in automatic mode).  The MLA workspace holds two fp32 partial
+ *     results of min(num_heads, 128) heads x 256 columns per share (256 KB
+ *     per share for 128 heads, 64 MB in automatic mode), plus q_abs, q_lo and
+ *     o_lat in bf16 (3.1 KB per (row, head)).
  */
 #ifndef PA_DECODE_H
 #define PA_DECODE_H
