@@ -58,3 +58,33 @@ def test_full_size_workload_sampled():
     B, H, _ = w.q.shape
     rows = gu.sample_rows(B, H, 24, 99)
     gu.check_mla(w, o, l, rows=rows)
+
+
+@pytest.mark.parametrize("H", [200, 256])
+def test_several_head_tiles(H):
+    """More than 128 heads: two tiles of the tensor-core core (the second one partial for H = 200),
+    automatic and explicit split counts."""
+    w = synth.make_mla(1500 + H, [1, 65, 300, 700], H, 64)
+    g = gu.MlaDev(w)
+    for n in [0, 3]:
+        o, l = g.run(num_splits=n)
+        gu.check_mla(w, o, l)
+
+
+def test_bad_page_is_reported_not_trapped():
+    import paged_kv_attention_19_gb300 as pa
+    w = synth.make_mla(1600, [70, 200], 16, 64)
+    g = gu.MlaDev(w)
+    bt = w.layout.block_table.copy()
+    bt[1, 2] = w.layout.num_pages + 5          # out of the pool
+    g.bt = gu.dev(bt)
+    ws = pa.workspace_for_mla(g.q, g.cache, g.bt, 0)
+    o, l = g.run(workspace=ws)
+    assert pa.pa_read_device_status(ws) & pa.PA_DEV_BAD_PAGE
+    # row 0 is unaffected by row 1's bad entry
+    gu.check_mla(w, o, l, rows=[(0, h) for h in range(16)])
+    # a clean call clears the status word
+    g.bt = gu.dev(w.layout.block_table)
+    o, l = g.run(workspace=ws)
+    assert pa.pa_read_device_status(ws) == 0
+    gu.check_mla(w, o, l)
