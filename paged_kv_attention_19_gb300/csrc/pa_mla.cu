@@ -42,7 +42,10 @@ constexpr int UV_ROWS = MLA_V / UV_PARTS;      // 64 output dims per projection 
 constexpr int ABS_PLANE = 128 * 128, UV_PLANE = UV_ROWS * 128;
 constexpr int ABS_W = (ABS_COLS / 64) * ABS_PLANE;  // 32 KB
 constexpr int UV_W = (MLA_LAT / 64) * UV_PLANE;      // 64 KB
-constexpr int PROJ_SMEM = 1024 + (ABS_W > UV_W ? ABS_W : UV_W) + 16 * WROW * 2 + 16;  // alignment, weights, rows, barrier
+// alignment, weights, rows, barrier: each projection kernel asks for its own size, so that the
+// absorb kernel's 512 blocks fit 4 to an SM (one wave)
+constexpr int ABS_SMEM = 1024 + ABS_W + 16 * WROW * 2 + 16;
+constexpr int UV_SMEM = 1024 + UV_W + 16 * WROW * 2 + 16;
 
 // Byte offset of (row, col) in staged weights with planes of `plane` bytes (col a multiple of 8).
 __device__ __forceinline__ uint32_t wsw(int plane, int row, int col) {
@@ -394,7 +397,9 @@ int mla_decode(const void *q, const void *cache, const void *w_uk, const void *w
   if (configured_device != dev) {
     for (const void *k :
          {(const void *)mla_tc_split_kernel, (const void *)q_absorb_kernel, (const void *)mla_uv_kernel}) {
-      const int bytes = k == (const void *)mla_tc_split_kernel ? MlaTcSmem::BYTES : PROJ_SMEM;
+      const int bytes = k == (const void *)mla_tc_split_kernel ? MlaTcSmem::BYTES
+                        : k == (const void *)q_absorb_kernel  ? ABS_SMEM
+                                                               : UV_SMEM;
       if (const cudaError_t ce = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
           ce != cudaSuccess)
         return pa::cuda_fail(ce);
@@ -403,7 +408,7 @@ int mla_decode(const void *q, const void *cache, const void *w_uk, const void *w
   }
 
   // 1. q_abs
-  q_absorb_kernel<<<H * ABS_PARTS, 256, PROJ_SMEM, stream>>>(tm_wuk, static_cast<const uint16_t *>(q), q_abs, q_lo, batch, H,
+  q_absorb_kernel<<<H * ABS_PARTS, 256, ABS_SMEM, stream>>>(tm_wuk, static_cast<const uint16_t *>(q), q_abs, q_lo, batch, H,
                                                   &hdr->status);
   if (const cudaError_t ce = cudaGetLastError(); ce != cudaSuccess) return pa::cuda_fail(ce);
   ++*launches;
@@ -470,7 +475,7 @@ int mla_decode(const void *q, const void *cache, const void *w_uk, const void *w
   // 7. o = W_UV . o_lat
   {
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = pdl_config(dim3(H * UV_PARTS), dim3(256), PROJ_SMEM, stream, attr);
+    cudaLaunchConfig_t cfg = pdl_config(dim3(H * UV_PARTS), dim3(256), UV_SMEM, stream, attr);
     if (const cudaError_t ce = cudaLaunchKernelEx(&cfg, mla_uv_kernel, tm_wuv, (const uint16_t *)o_lat,
                                                   static_cast<uint16_t *>(out), (const uint16_t *)q_lo, lse, scale,
                                                   batch, H, &hdr->status);
