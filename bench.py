@@ -323,8 +323,7 @@ def run_ours(args, rank, local_rank, world):
         dist.init_process_group("gloo")
     import paged_kv_attention_19_gb300 as pa
     import synth
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    import gpu_util as gu
+    import synth.device as gu
 
     w = synth.workload(args.workload)
     cfg = describe(w, args.workload)

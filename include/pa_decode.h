@@ -226,9 +226,12 @@ int pa_decode_mla_absorbed(const void *q, const void *cache, const void *w_uk, c
  *     PA_NOALLOC_SCRATCH_BYTES returns PA_ERR_WORKSPACE_TOO_SMALL before any
  *     device work.  Automatic mode (num_splits 0) always fits; an explicit
  *     num_splits fits up to about 2000 shares at head_dim 128 (1000 at 256).
- *   - The first call on a device looks up the array's device address on that
- *     (current) device and caches it; make that first call before starting
- *     any stream capture on the device.
+ *   - The first call in a CUDA context (normally the device's primary
+ *     context) looks up the array's device address in that context and
+ *     caches it under the context's unique ID; make that first call before
+ *     starting any stream capture on the device.  A context created later
+ *     (after cudaDeviceReset, or one the caller makes current) has a new ID,
+ *     so its first call looks the address up again.
  *   - All calls on a device share the one array.  Nothing in it has to start
  *     at zero (each call's split kernel writes every descriptor and partial
  *     slot the combine kernel then reads), but two calls that may overlap on

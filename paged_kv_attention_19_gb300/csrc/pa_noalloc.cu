@@ -8,6 +8,8 @@
 // them, pa_decode_gqa_noalloc runs the same decode with the workspace placed
 // in the fixed-size device array below, which every GPU that loads this
 // library holds until the process exits.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "pa_decode.h"
@@ -17,26 +19,80 @@ namespace {
 
 // The built-in scratch.  In host code this name is only a stand-in for the
 // device array, never a device address: host code must use the address that
-// cudaGetSymbolAddress returns for the current device.
+// cudaGetSymbolAddress returns in the current context.
 static __device__ __align__(256) unsigned char g_pa_scratch[PA_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
+// The array's address is looked up once per CUDA context and cached under the
+// context's unique ID (cuCtxGetId: never reused within a process), so a
+// context created later on the same device -- after cudaDeviceReset, or a
+// caller's own non-primary context -- gets a fresh lookup, never a stale address.
+constexpr int kCacheSlots = 64;
+struct ScratchSlot {
+  unsigned long long ctx_id;
+  void *ptr;
+};
 std::mutex g_mu;
-void *g_scratch_ptr[kMaxDevices] = {};
+ScratchSlot g_cache[kCacheSlots] = {};
+int g_next_slot = 0;
 
-// Device address of the scratch on the current device, looked up once per device.
-int scratch_address(void **out) {
-  int dev = 0;
-  if (const cudaError_t ce = cudaGetDevice(&dev); ce != cudaSuccess) return pa::cuda_fail(ce);
-  if (dev < 0 || dev >= kMaxDevices) return PA_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_ptr[dev]) {
+struct CtxFns {
+  PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  PFN_cuCtxGetId_v12000 get_id = nullptr;
+};
+
+const CtxFns &ctx_fns() {
+  static CtxFns fns;
+  static std::once_flag once;
+  std::call_once(once, [] {
     void *p = nullptr;
-    if (const cudaError_t ce = cudaGetSymbolAddress(&p, g_pa_scratch); ce != cudaSuccess || p == nullptr)
-      return pa::cuda_fail(ce);
-    g_scratch_ptr[dev] = p;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fns.get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fns.get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  return fns;
+}
+
+// Unique ID of the calling thread's current context; 0 if none is current yet.
+int current_ctx_id(unsigned long long *id) {
+  const CtxFns &f = ctx_fns();
+  if (!f.get_current || !f.get_id) return pa::cuda_fail(cudaErrorNotSupported);
+  CUcontext ctx = nullptr;
+  if (f.get_current(&ctx) != CUDA_SUCCESS) return pa::cuda_fail(cudaErrorContextIsDestroyed);
+  *id = 0;
+  if (ctx && f.get_id(ctx, id) != CUDA_SUCCESS) return pa::cuda_fail(cudaErrorContextIsDestroyed);
+  return PA_OK;
+}
+
+// Device address of the scratch in the current context (looked up on the first call in a
+// context, then cached).
+int scratch_address(void **out) {
+  unsigned long long id = 0;
+  int rc = current_ctx_id(&id);
+  if (rc != PA_OK) return rc;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (id != 0) {
+    for (const ScratchSlot &e : g_cache)
+      if (e.ctx_id == id) {
+        *out = e.ptr;
+        return PA_OK;
+      }
   }
-  *out = g_scratch_ptr[dev];
+  void *p = nullptr;
+  if (const cudaError_t ce = cudaGetSymbolAddress(&p, g_pa_scratch); ce != cudaSuccess || p == nullptr)
+    return pa::cuda_fail(ce);
+  if (id == 0) {  // no context was current: the lookup made the device's primary context current
+    rc = current_ctx_id(&id);
+    if (rc != PA_OK) return rc;
+  }
+  if (id != 0) {
+    g_cache[g_next_slot] = {id, p};
+    g_next_slot = (g_next_slot + 1) % kCacheSlots;
+  }
+  *out = p;
   return PA_OK;
 }
 

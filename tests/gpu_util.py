@@ -1,57 +1,16 @@
-"""Helpers of the GPU parity tests: upload a seeded workload, run the CUDA path
-through the C ABI binding, and compare with the fp64 oracle (imported only by
-the comparison helpers, so the benchmark can reuse the upload helpers)."""
+"""Helpers of the GPU parity tests: compare what the CUDA path returned (through
+the C ABI binding) with the fp64 oracle.  The upload helpers live in
+synth.device (the benchmark and smoke() use them too) and are re-exported
+here for the tests."""
 from __future__ import annotations
 
+import json
+
 import numpy as np
-import torch
 
 import compare
 import synth
-
-
-def dev(a: np.ndarray, dtype=None):
-    a = np.ascontiguousarray(a)
-    if a.dtype == np.uint16:
-        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
-    else:
-        t = torch.from_numpy(a)
-    return t.to("cuda") if dtype is None else t.to("cuda", dtype)
-
-
-def bits(t: torch.Tensor) -> np.ndarray:
-    return t.detach().view(torch.int16).cpu().numpy().view(np.uint16)
-
-
-class GqaDev:
-    """A GQA workload resident on the GPU."""
-
-    def __init__(self, w: synth.GQAWorkload):
-        self.w = w
-        self.q = dev(w.q)
-        self.k = dev(w.k_pool)
-        self.v = dev(w.v_pool)
-        self.bt = dev(w.layout.block_table)
-        self.lens = dev(w.layout.context_lens)
-
-    def run(self, num_splits=0, window=None, out=None, lse=None, poison=True, workspace=None,
-            max_context_len=None):
-        import paged_kv_attention_19_gb300 as pa
-        w = self.w
-        B, Hq, D = w.q.shape
-        if out is None:
-            out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device="cuda")
-            if poison:
-                out.fill_(float("nan"))
-        if lse is None:
-            lse = torch.full((B, Hq), float("nan"), dtype=torch.float32, device="cuda")
-        if workspace is None:
-            workspace = pa.workspace_for_gqa(self.q, self.k, self.bt, num_splits, max_context_len)
-        pa.pa_decode_gqa(self.q, self.k, self.v, self.bt, self.lens, out, lse, scale=w.scale,
-                         window=w.window if window is None else window, num_splits=num_splits,
-                         workspace=workspace, max_context_len=max_context_len)
-        torch.cuda.synchronize()
-        return bits(out), lse.cpu().numpy()
+from synth.device import GqaDev, MlaDev, bits, dev  # noqa: F401  (re-exported for the tests)
 
 
 def gqa_oracle(w: synth.GQAWorkload, rows=None, window=None):
@@ -78,32 +37,6 @@ def check_gqa(w, out_bits, lse, rows=None, window=None, tol_abs=compare.MAX_ABS,
     return st, dl
 
 
-class MlaDev:
-    def __init__(self, w: synth.MLAWorkload):
-        self.w = w
-        self.q = dev(w.q)
-        self.cache = dev(w.cache)
-        self.wuk = dev(w.w_uk)
-        self.wuv = dev(w.w_uv)
-        self.bt = dev(w.layout.block_table)
-        self.lens = dev(w.layout.context_lens)
-
-    def run(self, num_splits=0, poison=True, workspace=None):
-        import paged_kv_attention_19_gb300 as pa
-        w = self.w
-        B, H, _ = w.q.shape
-        out = torch.empty(B, H, 128, dtype=torch.bfloat16, device="cuda")
-        if poison:
-            out.fill_(float("nan"))
-        lse = torch.full((B, H), float("nan"), dtype=torch.float32, device="cuda")
-        if workspace is None:
-            workspace = pa.workspace_for_mla(self.q, self.cache, self.bt, num_splits)
-        pa.pa_decode_mla_absorbed(self.q, self.cache, self.wuk, self.wuv, self.bt, self.lens, out, lse,
-                                  scale=w.scale, num_splits=num_splits, workspace=workspace)
-        torch.cuda.synchronize()
-        return bits(out), lse.cpu().numpy()
-
-
 def check_mla(w, out_bits, lse, rows=None):
     import oracle
     B, H, _ = w.q.shape
@@ -121,6 +54,19 @@ def check_mla(w, out_bits, lse, rows=None):
     assert st.max_abs <= compare.MAX_ABS and st.max_rel <= compare.MAX_REL, f"{w.name}: {st}"
     assert dl <= compare.LSE_ABS, f"{w.name}: lse max abs err {dl:.3e}"
     return st, dl
+
+
+def report(name: str, shape, st: compare.Stats, lse_err: float) -> dict:
+    """One line of the whole-tensor numerics table (the statistics of the kernel-numerics table
+    of vllm.cpp PR #425, EVIDENCE section), printed with a NUMERICS prefix so a run with -s
+    can collect the table; the worst element's index is unravelled over the output shape."""
+    worst = tuple(int(x) for x in np.unravel_index(st.worst_index, shape)) if st.worst_index >= 0 else None
+    rec = {"workload": name, "outputs": int(np.prod(shape[:-1])), "elements": st.n,
+           "max_abs": float(f"{st.max_abs:.4g}"), "max_rel": float(f"{st.max_rel:.4g}"),
+           "max_rel_elem": float(f"{st.max_rel_elem:.4g}"), "bitwise_pct": round(st.bitwise_pct, 3),
+           "worst_index": worst, "lse_max_abs": float(f"{lse_err:.4g}")}
+    print("NUMERICS " + json.dumps(rec), flush=True)
+    return rec
 
 
 def sample_rows(B, H, n, seed):
