@@ -3,7 +3,7 @@
 One step = one call through the C ABI over one batch of seeded synthetic
 input of the chosen workload: for GQA (bf16 or FP8 pools, decode or verify)
 the split-KV attention kernel and the combine; for MLA the absorb, the
-attention core, the combine and the W_UV projection; for the KV writes the
+attention core and the merge fused with the W_UV projection; for the KV writes the
 write kernel.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]

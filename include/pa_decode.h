@@ -22,7 +22,8 @@
  *     kernel", description and limitations list);
  *   - split-KV over the sequence with a separate combine step that merges
  *     splits in a fixed ascending order, no atomics on the data, empty splits
- *     skipped (kernel-matrix rows KERNEL-ATTN-FA2 and KERNEL-ATTN-MLA-SPARSE);
+ *     skipped (kernel-matrix rows KERNEL-ATTN-FA2 and KERNEL-ATTN-MLA-SPARSE;
+ *     for MLA the combine runs inside the W_UV projection's launch);
  *   - the absorbed MLA schedule q_lat = q_nope.W_UK || q_rope, scores over
  *     the 576-wide latent cache, o_lat = sum p c, o = W_UV.o_lat (pegainfer
  *     PR #938 "warp-cooperative two-pass MLA absorbed decode kernel",
@@ -79,7 +80,9 @@
  *     4.2 MB in automatic mode).  The MLA workspace holds two fp32 partial
  *     results of min(num_heads, 128) heads x 256 columns per share (256 KB
  *     per share for 128 heads, 64 MB in automatic mode), plus q_abs, q_lo and
- *     o_lat in bf16 (3.1 KB per (row, head)).
+ *     o_lat in bf16 (3.1 KB per (row, head)) and two int32 tables of where
+ *     each (row, head tile, column half) sequence's pieces are (16 bytes per
+ *     (row, tile of 128 heads)).
  */
 #ifndef PA_DECODE_H
 #define PA_DECODE_H

@@ -8,7 +8,7 @@
 //   2-6. scores over the 576-wide latent || rope cache, online softmax,
 //        o_lat = sum_t p_t c_t[0:512], per piece of the balanced partition
 //                                                                   [mla_tc_split_kernel]
-//   merge of split sequences, ascending, o_lat rounded to bf16      [mla_combine_kernel]
+//   merge of split sequences, ascending, o_lat rounded to bf16, and
 //   7. o = W_UV . o_lat; lse += scale * q_lo . o_lat                [mla_uv_kernel]
 // Differences from the pages' kernel, all deliberate: scores, probabilities and the
 // softmax state stay fp32; the context is walked once with an online max instead of
@@ -104,7 +104,8 @@ __global__ void __launch_bounds__(256) q_absorb_kernel(const __grid_constant__ C
           b < B ? *reinterpret_cast<const uint4 *>(q + ((size_t)b * H + h) * MLA_QD + c * 8) : make_uint4(0, 0, 0, 0);
     }
     __syncthreads();
-    if (m0 == 0 && !mbar_wait(bar, 0, status)) return;  // the weights have landed
+    // the weights have landed (a wait that gave up ends every thread of the block together)
+    if (m0 == 0 && !__syncthreads_and(mbar_wait(bar, 0, status))) return;
     float acc[2][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
@@ -145,94 +146,258 @@ __global__ void __launch_bounds__(256) q_absorb_kernel(const __grid_constant__ C
   }
 }
 
-// o[b][h][v] = sum_j W_UV[h][v][j] o_lat[b][h][j] on the tensor cores (o_lat stored as its two
-// column halves, [B, 2, H, 256]).  Block (h, part) of 8
-// warps computes v in [64 part, +64) from its W_UV half (64 x 512, staged by TMA before the wait
-// for the previous kernels); warp w produces v in [8 w, 8 w + 8) of the half for 16 batch rows
-// per tile.  Part 0 also adds, with lse, the first-order LSE term of q_lat's bf16 rounding:
-// lse += scale * (q_lo . o_lat).
-__global__ void __launch_bounds__(256) mla_uv_kernel(const __grid_constant__ CUtensorMap tm_w, const uint16_t *o_lat,
-                                                     uint16_t *out, const uint16_t *q_lo, float *lse, float scale,
-                                                     int B, int H, uint32_t *status) {
+// Arguments of the merge + projection kernel.
+struct MlaUvArgs {
+  const uint16_t *o_lat;       // [B, 2, H, 256] bf16: halves of o_lat written whole by the split kernel
+  const float *part_o;         // [nparts, 2, rs, 256] fp32 partials (normalised) of split sequences
+  const float *part_lse;       // [nparts, 2, rs] fp32, log2 units
+  const int32_t *seq_first;    // [B, ntile]: -1 whole; else 2 x CTA + slot of the sequence's first piece
+  const int32_t *seq_last;     // [B, ntile]: CTA holding its last piece
+  const GqaPartDesc *desc;     // [nparts]: status bits of every split CTA
+  const int32_t *context_lens;  // [B]
+  const uint16_t *q_lo;        // [B, H, 512] bf16: q_lat - bf16(q_lat)
+  uint16_t *out;               // [B, H, 128] bf16
+  float *lse;                  // [B, H] or null
+  uint32_t *status;            // the workspace status word: OR of every CTA's bits
+  float scale;
+  int B, H, ntile, rs, nparts, hg, max_context_len;
+};
+
+// Distributed shared memory of the 2-CTA cluster of the projection kernel.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address of this CTA's shared-memory location `local` in the shared memory of cluster CTA `rank`.
+__device__ __forceinline__ uint32_t dsmem_addr(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void dsmem_st_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+// All threads of both CTAs: writes before it (shared memory of either CTA) are visible after it.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Merge of split sequences fused with step 7.  The two blocks (h, part 0) and (h, part 1) of head
+// h form a 2-CTA cluster; block part computes o[b][h][v] = sum_j W_UV[h][v][j] o_lat[b][h][j] for
+// v in [64 part, +64), 16 batch rows per tile:
+//   * before the wait for the split kernel, its W_UV half (64 x 512) is requested by TMA;
+//   * o_lat of the tile's 16 rows is assembled as bf16 in both blocks' shared memory, each block
+//     producing column half `part` (the sequence (row, tile, half)) and storing it into its own
+//     and its partner's shared memory.  A half that one piece covered whole is copied from the
+//     split kernel's output; a split one is merged from its fp32 partials (slots of CTAs first,
+//     first + hg, ..., last: the sequence's pieces in ascending token order) as an online
+//     log-sum-exp merge.  Lane l of warp w owns columns [8 l, +8) of rows w and w + 8, and the
+//     loop over partials is outermost, so both rows' loads of a partial (its LSE and values
+//     together) are in flight at once;
+//   * warp w produces v in [8 w, 8 w + 8) of the half on m16n8k16 MMAs (batch rows as M);
+//   * part 0 (which merges column half 0) writes the LSE: the merged one (or the split kernel's,
+//     for a whole sequence) plus the first-order term of q_lat's bf16 rounding,
+//     scale * (q_lo . o_lat); q_lo and the split kernel's LSE are loaded beside the table lookup.
+// Every path through the tile loop passes the same two cluster barriers per tile, so neither block
+// waits for one that has left.  Sequence indices from the workspace are range-checked, so a stale
+// or partial table never makes a load leave the partial slots.
+__global__ void __launch_bounds__(256) mla_uv_kernel(const __grid_constant__ CUtensorMap tm_w, const MlaUvArgs a) {
   extern __shared__ __align__(1024) uint8_t psmem[];
   uint8_t *w = proj_weights(psmem);                                    // W_UV[h][half, :]
   uint16_t *ol = reinterpret_cast<uint16_t *>(w + UV_W);               // [16 rows][WROW]
   uint64_t *bar = reinterpret_cast<uint64_t *>(ol + 16 * WROW);
+  __shared__ int32_t s_first[16], s_k[16];  // -1: whole (copy); else 2 x CTA + slot, piece count
+  __shared__ float s_lse[16];               // merged LSE (natural log) of split rows; NaN: whole
   const int h = blockIdx.x / UV_PARTS, part = blockIdx.x % UV_PARTS;
+  const uint32_t peer = cluster_ctarank() ^ 1u;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, tq = lane & 3;
   const int lm_mat = lane >> 3, lm_row = lane & 7;
+  const int H = a.H;
+  const int rh_head = h % MlaTcCfg::M;         // row of head h in its tile's partial slots
+  const int hs = (h / MlaTcCfg::M) * 2 + part;  // the sequence index of column half `part` of head h
   stage_weights_issue(w, &tm_w, 0, h * MLA_V + part * UV_ROWS, MLA_LAT / 64, UV_PLANE, bar);
   __syncthreads();  // the barrier is initialised before any thread waits on it
-  pdl_wait();  // o_lat, lse and the status word (split and combine kernels) are final from here on
-  if (!mbar_wait(bar, 0, status)) return;
-  for (int m0 = 0; m0 < B; m0 += 16) {
-    for (int i = tid; i < 16 * (MLA_LAT / 8); i += 256) {
-      const int r = i / (MLA_LAT / 8), c = i % (MLA_LAT / 8);
-      const int b = m0 + r;
-      *reinterpret_cast<uint4 *>(ol + r * WROW + c * 8) =
-          b < B ? *reinterpret_cast<const uint4 *>(o_lat + (((size_t)b * 2 + c / 32) * H + h) * (MLA_LAT / 2) + (c % 32) * 8)
-                : make_uint4(0, 0, 0, 0);
+  pdl_wait();  // the split kernel's outputs, partials, tables and status are final from here on
+  if (blockIdx.x == 0 && warp == 0) {
+    uint32_t st = 0;
+    for (int i = lane; i < a.nparts; i += 32) st |= a.desc[i].status;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) st |= __shfl_xor_sync(FULL, st, o);
+    if (lane == 0) *a.status = st;
+  }
+  const bool do_lse = a.lse && part == 0;
+  bool weights_ready = false, ok = true;
+  for (int m0 = 0; m0 < a.B; m0 += 16) {
+    // ---- where each row's sequence is (one thread per row; the three table loads are
+    // independent).  Meanwhile part 0 loads q_lo and the split kernel's LSE of its two rows.
+    if (tid < 16) {
+      const int b = m0 + tid;
+      int first = -1, k = 0;
+      if (b < a.B) {
+        const size_t si = (size_t)b * a.ntile + hs;
+        const int L = a.context_lens[b], f = a.seq_first[si], cl = a.seq_last[si];
+        const int c0 = f >> 1;
+        if (clamp_len(L, a.max_context_len) > 0 && f >= 0 && c0 < a.nparts && cl >= c0 && cl < a.nparts &&
+            (cl - c0) % a.hg == 0) {
+          first = f;
+          k = (cl - c0) / a.hg + 1;
+        }
+      }
+      s_first[tid] = first;
+      s_k[tid] = k;
+    }
+    uint4 qlo[2][2];  // part 0, warp w: rows 2 w, 2 w + 1; lane l: dims [16 l, 16 l + 16)
+    float lse_split[2];
+    if (do_lse) {
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int b = m0 + warp * 2 + q;
+        lse_split[q] = -INFINITY;
+        qlo[q][0] = qlo[q][1] = make_uint4(0, 0, 0, 0);
+        if (b < a.B) {
+          const uint16_t *ql = a.q_lo + ((size_t)b * H + h) * MLA_LAT + lane * 16;
+          qlo[q][0] = *reinterpret_cast<const uint4 *>(ql);
+          qlo[q][1] = *reinterpret_cast<const uint4 *>(ql + 8);
+          if (lane == 0) lse_split[q] = a.lse[(size_t)b * H + h];
+        }
+      }
     }
     __syncthreads();
-    if (lse && part == 0) {
-      // warp w: rows 2 w, 2 w + 1; lane l: dims [16 l, 16 l + 16)
-      for (int r = warp * 2; r < warp * 2 + 2; ++r) {
-        const int b = m0 + r;
-        if (b >= B) break;
-        const uint16_t *ql = q_lo + ((size_t)b * H + h) * MLA_LAT + lane * 16;
+    // ---- column half `part` of o_lat of the tile, into both blocks' shared memory
+    {
+      constexpr int NI = 2;
+      int fi[NI], ki[NI];
+      float mi[NI], zi[NI], acc[NI][8];
+      int kmax = 0;
+#pragma unroll
+      for (int n = 0; n < NI; ++n) {
+        const int r = warp + 8 * n;
+        fi[n] = m0 + r < a.B ? s_first[r] : -1;
+        ki[n] = fi[n] >= 0 ? s_k[r] : 0;
+        kmax = max(kmax, ki[n]);
+        mi[n] = -INFINITY;
+        zi[n] = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[n][e] = 0.f;
+      }
+#pragma unroll 2
+      for (int i = 0; i < kmax; ++i) {
+#pragma unroll
+        for (int n = 0; n < NI; ++n) {
+          if (i < ki[n]) {
+            const int f = fi[n];
+            const size_t pi = i == 0 ? (size_t)f : (size_t)((f >> 1) + i * a.hg) * 2;
+            const float l = a.part_lse[pi * a.rs + rh_head];
+            const float *po = a.part_o + (pi * a.rs + rh_head) * MlaTcCfg::DVH + lane * 8;
+            const float4 x0 = *reinterpret_cast<const float4 *>(po);
+            const float4 x1 = *reinterpret_cast<const float4 *>(po + 4);
+            if (l != -INFINITY) {  // a partial with no attended key weighs nothing
+              const float mn = fmaxf(mi[n], l);
+              const float sc = mi[n] == -INFINITY ? 0.f : fast_exp2(mi[n] - mn);
+              const float wc = fast_exp2(l - mn);
+              mi[n] = mn;
+              zi[n] = zi[n] * sc + wc;
+              acc[n][0] = acc[n][0] * sc + wc * x0.x;
+              acc[n][1] = acc[n][1] * sc + wc * x0.y;
+              acc[n][2] = acc[n][2] * sc + wc * x0.z;
+              acc[n][3] = acc[n][3] * sc + wc * x0.w;
+              acc[n][4] = acc[n][4] * sc + wc * x1.x;
+              acc[n][5] = acc[n][5] * sc + wc * x1.y;
+              acc[n][6] = acc[n][6] * sc + wc * x1.z;
+              acc[n][7] = acc[n][7] * sc + wc * x1.w;
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int n = 0; n < NI; ++n) {
+        const int r = warp + 8 * n, b = m0 + r;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (b < a.B) {
+          if (fi[n] < 0) {
+            v = *reinterpret_cast<const uint4 *>(a.o_lat + (((size_t)b * 2 + part) * H + h) * MlaTcCfg::DVH + lane * 8);
+            if (lane == 0) s_lse[r] = NAN;
+          } else {
+            const float inv = zi[n] > 0.f ? 1.f / zi[n] : 0.f;
+            v.x = pack_bf16x2(acc[n][0] * inv, acc[n][1] * inv);
+            v.y = pack_bf16x2(acc[n][2] * inv, acc[n][3] * inv);
+            v.z = pack_bf16x2(acc[n][4] * inv, acc[n][5] * inv);
+            v.w = pack_bf16x2(acc[n][6] * inv, acc[n][7] * inv);
+            if (lane == 0)
+              s_lse[r] = (mi[n] == -INFINITY || zi[n] == 0.f) ? -INFINITY : (mi[n] + __log2f(zi[n])) * LN2;
+          }
+        }
+        uint16_t *dst = ol + r * WROW + part * MlaTcCfg::DVH + lane * 8;
+        *reinterpret_cast<uint4 *>(dst) = v;
+        dsmem_st_v4(dsmem_addr(smem_u32(dst), peer), v);
+      }
+    }
+    cluster_sync();  // both column halves of the tile are in both blocks' shared memory
+    if (!weights_ready) {
+      // the weights have landed (a wait that gave up makes the whole block skip its output)
+      ok = __syncthreads_and(mbar_wait(bar, 0, a.status));
+      weights_ready = true;
+    }
+    if (ok && do_lse) {
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int r = warp * 2 + q, b = m0 + r;
+        if (b >= a.B) break;
+        const uint32_t qw[8] = {qlo[q][0].x, qlo[q][0].y, qlo[q][0].z, qlo[q][0].w,
+                                qlo[q][1].x, qlo[q][1].y, qlo[q][1].z, qlo[q][1].w};
         float d = 0.f;
 #pragma unroll
-        for (int e = 0; e < 16; e += 8) {
-          const uint4 qv = *reinterpret_cast<const uint4 *>(ql + e);
-          const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint32_t ow = *reinterpret_cast<const uint32_t *>(ol + r * WROW + lane * 16 + e + 2 * i);
-            d += __uint_as_float(qw[i] << 16) * __uint_as_float(ow << 16) +
-                 __uint_as_float(qw[i] & 0xffff0000u) * __uint_as_float(ow & 0xffff0000u);
-          }
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t ow = *reinterpret_cast<const uint32_t *>(ol + r * WROW + lane * 16 + 2 * i);
+          d += __uint_as_float(qw[i] << 16) * __uint_as_float(ow << 16) +
+               __uint_as_float(qw[i] & 0xffff0000u) * __uint_as_float(ow & 0xffff0000u);
         }
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) d += __shfl_xor_sync(FULL, d, o);
         if (lane == 0) {
-          const size_t bh = (size_t)b * H + h;
-          const float l = lse[bh];
-          if (l != -INFINITY) lse[bh] = l + scale * d;
+          const float merged = s_lse[r];
+          const float l = isnan(merged) ? lse_split[q] : merged;  // a whole sequence's LSE is the split kernel's
+          a.lse[(size_t)b * H + h] = l == -INFINITY ? l : l + a.scale * d;
         }
       }
     }
-    // two accumulators (even and odd k-steps): two independent MMA chains
-    float acc[2][4];
+    if (ok) {
+      // two accumulators (even and odd k-steps): two independent MMA chains
+      float acc[2][4];
 #pragma unroll
-    for (int q2 = 0; q2 < 2; ++q2)
+      for (int q2 = 0; q2 < 2; ++q2)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[q2][e] = 0.f;
+        for (int e = 0; e < 4; ++e) acc[q2][e] = 0.f;
 #pragma unroll 4
-    for (int k0 = 0; k0 < MLA_LAT; k0 += 32) {
-      uint32_t af0[4], af1[4], bf[4];
-      {
-        const int row = (lm_mat & 1) * 8 + lm_row, col = k0 + (lm_mat >> 1) * 8;
-        ldmatrix_x4(af0, smem_u32(ol + row * WROW + col));
-        ldmatrix_x4(af1, smem_u32(ol + row * WROW + col + 16));
+      for (int k0 = 0; k0 < MLA_LAT; k0 += 32) {
+        uint32_t af0[4], af1[4], bf[4];
+        {
+          const int row = (lm_mat & 1) * 8 + lm_row, col = k0 + (lm_mat >> 1) * 8;
+          ldmatrix_x4(af0, smem_u32(ol + row * WROW + col));
+          ldmatrix_x4(af1, smem_u32(ol + row * WROW + col + 16));
+        }
+        {
+          // B = W_UV^T: W rows v (the n index, 8 of them), columns k0 .. k0 + 31 (two k-steps)
+          const int vrow = warp * 8 + lm_row, col = k0 + lm_mat * 8;
+          ldmatrix_x4(bf, smem_u32(w) + wsw(UV_PLANE, vrow, col));
+        }
+        mma_bf16_16816(acc[0], af0, bf[0], bf[1]);
+        mma_bf16_16816(acc[1], af1, bf[2], bf[3]);
       }
-      {
-        // B = W_UV^T: W rows v (the n index, 8 of them), columns k0 .. k0 + 31 (two k-steps)
-        const int vrow = warp * 8 + lm_row, col = k0 + lm_mat * 8;
-        ldmatrix_x4(bf, smem_u32(w) + wsw(UV_PLANE, vrow, col));
-      }
-      mma_bf16_16816(acc[0], af0, bf[0], bf[1]);
-      mma_bf16_16816(acc[1], af1, bf[2], bf[3]);
+      const int r0 = m0 + g, r1 = m0 + g + 8;
+      const int col = part * UV_ROWS + warp * 8 + 2 * tq;
+      if (r0 < a.B)
+        *reinterpret_cast<uint32_t *>(a.out + ((size_t)r0 * H + h) * MLA_V + col) =
+            pack_bf16x2(acc[0][0] + acc[1][0], acc[0][1] + acc[1][1]);
+      if (r1 < a.B)
+        *reinterpret_cast<uint32_t *>(a.out + ((size_t)r1 * H + h) * MLA_V + col) =
+            pack_bf16x2(acc[0][2] + acc[1][2], acc[0][3] + acc[1][3]);
     }
-    const int r0 = m0 + g, r1 = m0 + g + 8;
-    const int col = part * UV_ROWS + warp * 8 + 2 * tq;
-    if (r0 < B)
-      *reinterpret_cast<uint32_t *>(out + ((size_t)r0 * H + h) * MLA_V + col) =
-          pack_bf16x2(acc[0][0] + acc[1][0], acc[0][1] + acc[1][1]);
-    if (r1 < B)
-      *reinterpret_cast<uint32_t *>(out + ((size_t)r1 * H + h) * MLA_V + col) =
-          pack_bf16x2(acc[0][2] + acc[1][2], acc[0][3] + acc[1][3]);
-    __syncthreads();
+    cluster_sync();  // both blocks are done reading the tile before the next one is written
   }
 }
 
@@ -254,11 +419,12 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 struct MlaPlan {
   int ntile, rs, nparts_max;
-  size_t off_desc, off_part_lse, off_part_o, off_qabs, off_qlo, off_olat, total;
+  size_t off_desc, off_part_lse, off_part_o, off_qabs, off_qlo, off_olat, off_seq, total;
 };
 
 // The workspace: header, one descriptor per share, two fp32 partial slots (min(H, 128) heads x 256
-// columns) per share, q_abs [B, H, 576], q_lo [B, H, 512] and o_lat [B, 2, H, 256], all bf16.
+// columns) per share, q_abs [B, H, 576], q_lo [B, H, 512] and o_lat [B, 2, H, 256], all bf16, and
+// the two int32 tables [B, ntile] that say where each sequence's pieces are.
 int mla_shape(int batch, int H, int max_ctx, int P, int num_splits, MlaPlan *pl) {
   if (batch < 0 || H <= 0 || max_ctx < 0 || num_splits < 0) return PA_ERR_INVALID_ARGUMENT;
   if (num_splits > kMaxSplits) return PA_ERR_UNSUPPORTED;
@@ -280,6 +446,8 @@ int mla_shape(int batch, int H, int max_ctx, int P, int num_splits, MlaPlan *pl)
   off = round_up(off + B * (size_t)H * MLA_LAT * 2, 256);
   pl->off_olat = off;
   off = round_up(off + B * (size_t)H * MLA_LAT * 2, 256);
+  pl->off_seq = off;
+  off = round_up(off + 2 * B * (size_t)pl->ntile * sizeof(int32_t), 256);
   pl->total = off;
   return PA_OK;
 }
@@ -378,6 +546,8 @@ int mla_decode(const void *q, const void *cache, const void *w_uk, const void *w
   uint16_t *q_abs = reinterpret_cast<uint16_t *>(ws + pl.off_qabs);
   uint16_t *o_lat = reinterpret_cast<uint16_t *>(ws + pl.off_olat);
   uint16_t *q_lo = reinterpret_cast<uint16_t *>(ws + pl.off_qlo);
+  int32_t *seq_first = reinterpret_cast<int32_t *>(ws + pl.off_seq);
+  int32_t *seq_last = seq_first + (size_t)batch * pl.ntile;
   CUtensorMap tm_c, tm_q, tm_wuk, tm_wuv;
   if (!encode_cache_map(&tm_c, cache, num_pages, P, BH) || !encode_qabs_map(&tm_q, q_abs, (long long)batch * H) ||
       !encode_weight_map(&tm_wuk, w_uk, H, MLA_NOPE) || !encode_weight_map(&tm_wuv, w_uv, H, UV_ROWS))
@@ -422,6 +592,8 @@ int mla_decode(const void *q, const void *cache, const void *w_uk, const void *w
   ma.part_o = part_o;
   ma.part_lse = part_lse;
   ma.desc = desc;
+  ma.seq_first = seq_first;
+  ma.seq_last = seq_last;
   ma.batch = batch;
   ma.max_pages_per_seq = max_pages_per_seq;
   ma.num_pages = num_pages;
@@ -451,35 +623,38 @@ int mla_decode(const void *q, const void *cache, const void *w_uk, const void *w
     if (const cudaError_t ce = cudaEventRecord(ev_after, stream); ce != cudaSuccess) return pa::cuda_fail(ce);
   }
 
-  // merge of split sequences into o_lat (and lse)
+  // merge of split sequences and 7. o = W_UV . o_lat
   {
-    MlaCombineArgs ca;
-    ca.o_lat = o_lat;
-    ca.lse = lse;
-    ca.part_o = part_o;
-    ca.part_lse = part_lse;
-    ca.desc = desc;
-    ca.status = &hdr->status;
-    ca.H = H;
-    ca.rs = pl.rs;
-    ca.nparts = nparts;
-    ca.hg = ma.hg;
-    cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg =
-        pdl_config(dim3(nparts, MlaTcCfg::M / MLA_COMBINE_ROWS), dim3(MLA_COMBINE_THREADS), 0, stream, attr);
-    if (const cudaError_t ce = cudaLaunchKernelEx(&cfg, mla_combine_kernel, ca); ce != cudaSuccess)
-      return pa::cuda_fail(ce);
-  }
-  ++*launches;
-
-  // 7. o = W_UV . o_lat
-  {
-    cudaLaunchAttribute attr[1];
+    MlaUvArgs ua;
+    ua.o_lat = o_lat;
+    ua.part_o = part_o;
+    ua.part_lse = part_lse;
+    ua.seq_first = seq_first;
+    ua.seq_last = seq_last;
+    ua.desc = desc;
+    ua.context_lens = context_lens;
+    ua.q_lo = q_lo;
+    ua.out = static_cast<uint16_t *>(out);
+    ua.lse = lse;
+    ua.status = &hdr->status;
+    ua.scale = scale;
+    ua.B = batch;
+    ua.H = H;
+    ua.ntile = pl.ntile;
+    ua.rs = pl.rs;
+    ua.nparts = nparts;
+    ua.hg = ma.hg;
+    ua.max_context_len = max_context_len;
+    // the two blocks of a head form a cluster (they share the merged o_lat through distributed
+    // shared memory); a programmatic dependent of the split kernel like every launch here
+    cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = pdl_config(dim3(H * UV_PARTS), dim3(256), UV_SMEM, stream, attr);
-    if (const cudaError_t ce = cudaLaunchKernelEx(&cfg, mla_uv_kernel, tm_wuv, (const uint16_t *)o_lat,
-                                                  static_cast<uint16_t *>(out), (const uint16_t *)q_lo, lse, scale,
-                                                  batch, H, &hdr->status);
-        ce != cudaSuccess)
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = UV_PARTS;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+    if (const cudaError_t ce = cudaLaunchKernelEx(&cfg, mla_uv_kernel, tm_wuv, ua); ce != cudaSuccess)
       return pa::cuda_fail(ce);
   }
   ++*launches;

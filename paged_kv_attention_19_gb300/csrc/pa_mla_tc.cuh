@@ -52,6 +52,8 @@ struct MlaTcArgs {
   float *part_o;                // [nparts, 2, RS, 256] fp32
   float *part_lse;              // [nparts, 2, RS] fp32, log2 units
   GqaPartDesc *desc;            // [nparts]
+  int32_t *seq_first;           // [B, ntile]: -1 whole piece; else 2 x CTA + slot of the first piece
+  int32_t *seq_last;            // [B, ntile]: CTA holding the last piece of a split sequence
   int batch, max_pages_per_seq, num_pages, max_context_len;
   int H, ntile, rs;             // heads; sequences per row (2 x head tiles); rows per partial slot
   int log2_page, log2_bh, piece_cost, nparts, hg;
@@ -153,7 +155,7 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
   const uint32_t tmem = misc->tmem;
   // Only the query rows come from the absorb kernel: the producer waits for it (griddepcontrol)
   // just before their first copy, so the partition and the first cache stage overlap its tail.
-  pdl_launch_dependents();  // the combine kernel may be scheduled; it waits for this grid to finish
+  pdl_launch_dependents();  // the projection kernel may stage its weights; it waits for this grid to finish
   uint32_t *status = &misc->status;
 
   PartitionArgs pargs;
@@ -201,6 +203,15 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
       const int h0 = (cur.hs >> 1) * C::M, hv = cur.hs & 1;
       const int nh = min(C::M, a.H - h0);
       const int slot = (cur.starts && cur.ends) ? -1 : (npieces == 0 ? 0 : 1);
+      if (lane == 0) {
+        // where the projection kernel finds the sequence: written directly (whole piece), or
+        // merged from the partial slots of CTAs first, first + hg, ..., last
+        const size_t si = (size_t)cur.b * a.ntile + cur.hs;
+        if (cur.starts)
+          a.seq_first[si] = slot < 0 ? -1 : (int32_t)blockIdx.x * 2 + slot;
+        else if (cur.ends)
+          a.seq_last[si] = (int32_t)blockIdx.x;
+      }
       const int T0 = cur.ub << a.log2_bh;
       const int tok_lo = max(cur.lo, T0), tok_hi = min(cur.L, cur.ue << a.log2_bh);
       const int n_stages = (cur.ue - cur.ub + nbox - 1) / nbox;
@@ -626,102 +637,6 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
     float *po = a.part_o + (size_t)blockIdx.x * 2 * a.rs * C::DVH;
     for (int e = tid; e < a.rs * C::DVH; e += C::THREADS) po[e] = 0.f;
     for (int h = tid; h < a.rs; h += C::THREADS) a.part_lse[(size_t)blockIdx.x * 2 * a.rs + h] = -INFINITY;
-  }
-}
-
-// Merge of the pieces of split sequences: the CTA c whose last piece starts a sequence and does
-// not end it finds the sequence's later pieces in CTAs c + hg, c + 2 hg, ... (the same position
-// in the next groups) and merges them in that order.  Block (c, y) handles rows [8 y, 8 y + 8) of
-// the tile, one warp per row (the rows' dependent loads from L2 overlap instead of queueing); a
-// row's weights are exp2(lse_k - max), o = sum_k w_k o_k / sum_k w_k, each lane owning 8 of the
-// half's 256 columns.  The half-0 sequence writes the merged LSE.
-struct MlaCombineArgs {
-  uint16_t *o_lat;
-  float *lse;
-  const float *part_o, *part_lse;
-  const GqaPartDesc *desc;
-  uint32_t *status;
-  int H, rs, nparts, hg;
-};
-
-constexpr int MLA_COMBINE_THREADS = 256;
-constexpr int MLA_COMBINE_ROWS = MLA_COMBINE_THREADS / 32;  // rows per block: gridDim.y = 128 / 8
-
-__global__ void __launch_bounds__(MLA_COMBINE_THREADS) mla_combine_kernel(const MlaCombineArgs a) {
-  constexpr int DVH = MlaTcCfg::DVH, PER = DVH / 32;
-  pdl_wait();               // the split kernel's partials and descriptors are visible from here on
-  pdl_launch_dependents();  // the W_UV projection may stage its weights
-  const int c = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (c == 0 && blockIdx.y == 0 && warp == 0) {
-    uint32_t s = 0;
-    for (int i = lane; i < a.nparts; i += 32) s |= a.desc[i].status;
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) s |= __shfl_xor_sync(FULL, s, o);
-    if (lane == 0) *a.status = s;
-  }
-  const GqaPartDesc d0 = a.desc[c];
-  const uint32_t np = d0.flags & DESC_PIECES;
-  if (np == 0 || !(d0.flags & DESC_LAST_STARTS) || (d0.flags & DESC_LAST_ENDS)) return;
-  int k = -1;  // pieces: CTA c + i hg holds piece i, i < k
-  for (int base = 1; c + base * a.hg < a.nparts && k < 0; base += 32) {
-    const int i = c + (base + lane) * a.hg;
-    bool hit = false;
-    if (i < a.nparts) {
-      const uint32_t f = a.desc[i].flags;
-      hit = (f & DESC_PIECES) != 0 && (f & DESC_FIRST_ENDS) != 0;
-    }
-    const uint32_t msk = __ballot_sync(FULL, hit);
-    if (msk) k = base + __ffs(msk);
-  }
-  if (k < 0) return;  // not reachable for a consistent partition
-  const int first_slot = np >= 2 ? 1 : 0;
-  const int h0 = (d0.last_hs >> 1) * MlaTcCfg::M, hv = d0.last_hs & 1;
-  const int nh = min(MlaTcCfg::M, a.H - h0);
-  {
-    const int r = blockIdx.y * MLA_COMBINE_ROWS + warp;
-    if (r >= nh) return;
-    float M = -INFINITY;
-    for (int i = lane; i < k; i += 32) {
-      const size_t pi = i == 0 ? (size_t)c * 2 + first_slot : (size_t)(c + i * a.hg) * 2;
-      M = fmaxf(M, a.part_lse[pi * a.rs + r]);
-    }
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, o));
-    float Z = 0.f;
-    for (int i = lane; i < k; i += 32) {
-      const size_t pi = i == 0 ? (size_t)c * 2 + first_slot : (size_t)(c + i * a.hg) * 2;
-      const float l = a.part_lse[pi * a.rs + r];
-      Z += (l == -INFINITY || M == -INFINITY) ? 0.f : fast_exp2(l - M);
-    }
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) Z += __shfl_xor_sync(FULL, Z, o);
-    float acc[PER];
-#pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-#pragma unroll 4
-    for (int i = 0; i < k; ++i) {
-      const size_t pi = i == 0 ? (size_t)c * 2 + first_slot : (size_t)(c + i * a.hg) * 2;
-      const float l = a.part_lse[pi * a.rs + r];
-      const float wc = (l == -INFINITY || M == -INFINITY) ? 0.f : fast_exp2(l - M);
-      const float *po = a.part_o + (pi * a.rs + r) * DVH + lane * PER;
-#pragma unroll
-      for (int e = 0; e < PER; e += 4) {
-        const float4 x = *reinterpret_cast<const float4 *>(po + e);
-        acc[e] += wc * x.x;
-        acc[e + 1] += wc * x.y;
-        acc[e + 2] += wc * x.z;
-        acc[e + 3] += wc * x.w;
-      }
-    }
-    const float inv = Z > 0.f ? 1.f / Z : 0.f;
-    uint4 v;
-    v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-    v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-    v.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
-    v.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-    *reinterpret_cast<uint4 *>(a.o_lat + (((size_t)d0.last_b * 2 + hv) * a.H + h0 + r) * DVH + lane * PER) = v;
-    if (lane == 0 && hv == 0 && a.lse)
-      a.lse[(size_t)d0.last_b * a.H + h0 + r] = (M == -INFINITY || Z == 0.f) ? -INFINITY : (M + __log2f(Z)) * LN2;
   }
 }
 

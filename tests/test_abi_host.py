@@ -78,20 +78,22 @@ def test_workspace_size(pa):
 
 def test_mla_workspace_layout(pa):
     """The MLA workspace as the header describes it: per share two fp32 partial slots of
-    min(H, 128) heads x 256 columns (plus a 16-byte descriptor and the slots' LSEs), and per
-    (row, head) q_abs, q_lo and o_lat in bf16 (576 + 512 + 512 values); each region rounded up to
+    min(H, 128) heads x 256 columns (plus a 16-byte descriptor and the slots' LSEs), per
+    (row, head) q_abs, q_lo and o_lat in bf16 (576 + 512 + 512 values), and per (row, tile of 128
+    heads) two int32 entries for each of its two column-half sequences; each region rounded up to
     256 bytes."""
     ws = lambda B, H, n: pa.pa_workspace_size(pa.PA_KIND_MLA_ABSORBED, B, H, 0, 0, 8192, 64, n)
     per_row_head = (576 + 512 + 512) * 2
     for H in (1, 16, 128, 200, 256):
         rs = min(H, 128)
         per_share = 16 + 2 * rs * 4 + 2 * rs * 256 * 4
+        per_row_tables = 2 * 2 * ((H + 127) // 128) * 4
         # shares: an explicit count n grows the workspace by per_share bytes each (up to rounding)
         d = ws(16, H, 512) - ws(16, H, 256)
         assert abs(d - 256 * per_share) <= 3 * 256, (H, d)
-        # rows: each adds H * per_row_head bytes (up to rounding)
+        # rows: each adds H * per_row_head bytes plus its table entries (up to rounding)
         d = ws(32, H, 256) - ws(16, H, 256)
-        assert abs(d - 16 * H * per_row_head) <= 3 * 256, (H, d)
+        assert abs(d - 16 * (H * per_row_head + per_row_tables)) <= 4 * 256, (H, d)
         # automatic mode sizes for 256 shares
         assert ws(16, H, 0) == ws(16, H, 256)
         # the context length and page size do not enter
