@@ -111,7 +111,7 @@ typedef enum { PA_KIND_GQA = 0, PA_KIND_MLA_ABSORBED = 1 } pa_kind;
 /* Bits of the device status word (see pa_read_device_status). */
 #define PA_DEV_BAD_PAGE 0x1u /* a visited block-table entry was outside [0, num_pages) */
 #define PA_DEV_BAD_LEN 0x2u  /* a context length was < 0 or > max_context_len */
-#define PA_DEV_TIMEOUT 0x4u  /* a bounded wait inside a kernel gave up (never expected) */
+#define PA_DEV_TIMEOUT 0x4u  /* a bounded wait inside a kernel gave up (never expected at the default limit) */
 #define PA_DEV_BAD_SLOT 0x8u /* a cache write named a slot at or past num_pages * page_size */
 
 /*
@@ -318,6 +318,31 @@ int pa_set_profile_events(cudaEvent_t before_main, cudaEvent_t after_main);
 
 /* Number of kernel launches the last decode call on this host thread issued. */
 int pa_last_launch_count(void);
+
+/*
+ * Limit of the waits on the stage ring of the GQA split-KV kernels
+ * (pa_decode_gqa, pa_verify_gqa, pa_decode_gqa_fp8 and the no-alloc decode),
+ * in nanoseconds of the device's global timer, for later calls from the
+ * calling host thread.  The pages have no counterpart: it is a diagnostic
+ * for checking that the kernels leave cleanly when a wait does not complete.
+ * The default, PA_DEFAULT_WAIT_LIMIT_NS (1 s), is far beyond any legal wait;
+ * 0 makes a warp give up at the first wait it finds incomplete.
+ *
+ * A warp whose wait passes the limit records PA_DEV_TIMEOUT in the call's
+ * status word and gives up its work while keeping the ring's protocol: the
+ * producer issues no further copy and ends the ring once the slot it waited
+ * for is free; a consumer computes nothing more but still releases every
+ * stage and meets every barrier.  Copies already in flight land first
+ * (waiting up to another second), so no CTA ends with a copy in flight or
+ * leaves a warp waiting.  The call still returns normally, but its out and
+ * lse are unspecified.  The next call with a sufficient limit is
+ * unaffected.  The MLA kernels always use the default.  A call at the
+ * default limit runs kernels compiled with the 1 s bound fixed; a call with
+ * any other limit runs the same kernels compiled with it as an argument.
+ * Always returns PA_OK.
+ */
+#define PA_DEFAULT_WAIT_LIMIT_NS 1000000000ull
+int pa_set_wait_limit_ns(unsigned long long limit_ns);
 
 /*
  * The CUDA runtime error (a cudaError_t value) behind the most recent

@@ -8,7 +8,7 @@ library has not been built (``python paged_kv_attention_19_gb300/build.py``).
 Names follow the C ABI: ``pa_workspace_size``, ``pa_decode_gqa``,
 ``pa_decode_mla_absorbed``, ``pa_verify_gqa``, ``pa_decode_gqa_fp8``, ``pa_decode_gqa_noalloc``,
 ``pa_kv_write``, ``pa_kv_write_fp8``, ``pa_mla_cache_write``, ``pa_status_string``, ``pa_read_device_status``,
-``pa_set_profile_events``, ``pa_last_launch_count``, ``pa_last_cuda_error``,
+``pa_set_profile_events``, ``pa_last_launch_count``, ``pa_set_wait_limit_ns``, ``pa_last_cuda_error``,
 ``pa_last_cuda_error_string``.  The tensor-taking
 functions accept torch tensors (device memory, the layouts of the header) and
 infer every size from their shapes.
@@ -33,6 +33,7 @@ PA_DEV_BAD_PAGE = 0x1
 PA_DEV_BAD_LEN = 0x2
 PA_DEV_TIMEOUT = 0x4
 PA_DEV_BAD_SLOT = 0x8
+PA_DEFAULT_WAIT_LIMIT_NS = 1_000_000_000
 
 # Every symbol include/pa_decode.h declares, with its ctypes signature.
 _P, _I, _F, _Z, _U32P = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.POINTER(ctypes.c_uint32)
@@ -52,6 +53,7 @@ SIGNATURES = {
     "pa_read_device_status": (_I, [_P, _P, _U32P]),
     "pa_set_profile_events": (_I, [_P, _P]),
     "pa_last_launch_count": (_I, []),
+    "pa_set_wait_limit_ns": (_I, [ctypes.c_ulonglong]),
     "pa_last_cuda_error": (_I, []),
     "pa_last_cuda_error_string": (ctypes.c_char_p, []),
 }
@@ -233,6 +235,11 @@ def pa_set_profile_events(before=None, after=None) -> None:
 
 def pa_last_launch_count() -> int:
     return int(lib.pa_last_launch_count())
+
+
+def pa_set_wait_limit_ns(limit_ns: int = PA_DEFAULT_WAIT_LIMIT_NS) -> None:
+    """Limit (global-timer ns) of the GQA split kernels' ring waits for later calls from this thread."""
+    _check(lib.pa_set_wait_limit_ns(int(limit_ns)), "pa_set_wait_limit_ns")
 
 
 def pa_last_cuda_error() -> int:

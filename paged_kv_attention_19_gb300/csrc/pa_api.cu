@@ -34,6 +34,7 @@ thread_local cudaEvent_t t_ev_before = nullptr;
 thread_local cudaEvent_t t_ev_after = nullptr;
 thread_local int t_last_launches = 0;
 thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+thread_local unsigned long long t_wait_limit_ns = WAIT_LIMIT_NS;
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
@@ -265,6 +266,7 @@ int gqa_call(const void *q, const void *k_pool, const void *v_pool, const int32_
   }
   ga.qscale = scale * LOG2E * (f8.on ? f8.k : 1.f);
   ga.vscale = f8.on ? f8.v : 1.f;
+  ga.wait_ns = t_wait_limit_ns;
 
   CombineArgs ca;
   ca.out = static_cast<uint16_t *>(out);
@@ -391,6 +393,11 @@ int pa_set_profile_events(cudaEvent_t before_main, cudaEvent_t after_main) {
 }
 
 int pa_last_launch_count(void) { return t_last_launches; }
+
+int pa_set_wait_limit_ns(unsigned long long limit_ns) {
+  t_wait_limit_ns = limit_ns;
+  return PA_OK;
+}
 
 int pa_last_cuda_error(void) { return (int)t_last_cuda_error; }
 

@@ -26,7 +26,8 @@ struct WsHeader {
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
 constexpr unsigned FULL = 0xffffffffu;
-constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;  // 1 s: far beyond any legal wait
+constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;   // 1 s: far beyond any legal wait (the default limit)
+constexpr uint64_t DRAIN_LIMIT_NS = 1000000000ull;  // a wait after a give-up, for copies already in flight
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -69,6 +70,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking: has the phase of *bar with the given parity completed?  (try_wait above may hold
+// the thread for a while before it answers; test_wait answers at once.)
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for phase `parity` of `bar` to complete; false after WAIT_LIMIT_NS
 // (the timeout bit is then set in *status).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *status) {
@@ -81,6 +94,45 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
       return false;
     }
   }
+}
+
+// All 32 lanes of a converged warp: wait for phase `parity` of `bar` for at most `limit_ns` of the
+// global timer; every lane returns the same result.  A limit of 0 is one non-blocking test.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
+  if (limit_ns == 0) return __all_sync(FULL, mbar_test(bar, parity));
+  if (__all_sync(FULL, mbar_try_wait(bar, parity))) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (__all_sync(FULL, mbar_try_wait(bar, parity))) return true;
+    if (__any_sync(FULL, global_timer_ns() - t0 > limit_ns)) return false;
+  }
+}
+
+// One lane's wait for phase `parity` of `bar`, for at most `limit_ns` of the global timer (0: one
+// non-blocking test).
+__device__ __forceinline__ bool mbar_wait_lane(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
+  if (limit_ns == 0) return mbar_test(bar, parity);
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// A wait of the split kernels' stage ring under the call's limit (all lanes of a converged warp; the
+// result is the same in every lane).  RING_OK: the phase completed within the limit.  RING_LATE: the
+// wait passed the limit (PA_DEV_TIMEOUT is recorded) and the phase then completed within the drain
+// limit; the warp gives up its work but keeps the ring's protocol (a producer issues no further
+// stage, only the end marker, into that slot; a consumer computes nothing more but releases every
+// later stage and meets every end-of-piece barrier up to the end marker), so no copy is left in
+// flight and no barrier waits for a warp that has left.  RING_FAILED: the drain limit passed too.
+enum RingWait { RING_OK = 0, RING_LATE = 1, RING_FAILED = 2 };
+__device__ __forceinline__ int ring_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns, uint32_t *status) {
+  if (__all_sync(FULL, mbar_wait_lane(bar, parity, limit_ns))) return RING_OK;
+  if ((threadIdx.x & 31) == 0) atomicOr(status, PA_DEV_TIMEOUT);
+  __syncwarp();
+  return mbar_wait_warp(bar, parity, DRAIN_LIMIT_NS) ? RING_LATE : RING_FAILED;
 }
 
 // TMA: 4-D tiled copy global -> shared, completion counted on `bar`.

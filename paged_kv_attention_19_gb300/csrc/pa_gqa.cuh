@@ -90,6 +90,7 @@ struct GqaArgs {
   int hg;                       // CTAs per group: min(Hkv * ntile, nparts)
   float qscale;                 // scale * log2(e) (FP8: times the keys' scale)
   float vscale;                 // FP8: the values' scale; 1 for bf16 pools
+  unsigned long long wait_ns;   // limit of a stage-ring wait (global-timer ns) before the CTA gives up
 };
 
 // Layout of the bf16 split kernel: stage ring, token groups, consumer warps.  The FP8
@@ -223,8 +224,11 @@ __device__ __forceinline__ void gqa_setup(uint8_t *smem, const CUtensorMap *tm_k
 }
 
 // The producer warp: walks the CTA's pieces and fills the stage ring (a stage of the piece's
-// query rows, then its K/V stages), ends with an end marker.
-template <class C>
+// query rows, then its K/V stages), ends with an end marker.  LW: its waits for a free slot take
+// the call's limit (a.wait_ns) and follow the give-up protocol of ring_wait (a late wait: no
+// further stage, the end marker once the slot is free); otherwise they are bounded at 1 s.  The
+// consumers' waits follow the same rule.
+template <class C, bool LW>
 __device__ __forceinline__ void gqa_produce(uint8_t *smem, const CUtensorMap *tm_k, const CUtensorMap *tm_v,
                                             const CUtensorMap *tm_q, const GqaArgs &a, const PartitionArgs &pargs) {
   using S = GqaSmem<C>;
@@ -240,6 +244,12 @@ __device__ __forceinline__ void gqa_produce(uint8_t *smem, const CUtensorMap *tm
   const int nbox = C::ST >> a.log2_bh;  // boxes (units) per stage
   uint32_t j = 0;
   bool ok = true;
+  bool stop = false;  // LW: a wait passed the call's limit: no more stages, straight to the end marker
+  // a wait for a free slot: RING_OK, RING_LATE (LW only) or RING_FAILED
+  auto slot_wait = [&](int s, uint32_t parity) -> int {
+    if constexpr (LW) return ring_wait(&empty[s], parity, a.wait_ns, status);
+    else return mbar_wait(&empty[s], parity, status) ? RING_OK : RING_FAILED;
+  };
   int npieces = 0;
   Piece last_piece = {};
   bool first_ends = false;
@@ -261,7 +271,7 @@ __device__ __forceinline__ void gqa_produce(uint8_t *smem, const CUtensorMap *tm
     has_next = take_piece(nxt);
     if (has_next) nwin0 = piece_window(nxt);
   }
-  while (has_cur && ok) {
+  while (has_cur && ok && !stop) {
     // ---- emit the stages of `cur`
     const int g = cur.hs / a.ntile;
     const Tile tl = tile(cur);
@@ -283,8 +293,12 @@ __device__ __forceinline__ void gqa_produce(uint8_t *smem, const CUtensorMap *tm
       // consumers)
       const int s = j % C::NS;
       const uint32_t u = j / C::NS;
-      if (u > 0) ok = mbar_wait(&empty[s], (u - 1) & 1, status);
-      if (!ok) break;
+      if (u > 0) {
+        const int wr = slot_wait(s, (u - 1) & 1);
+        ok = wr != RING_FAILED;
+        stop = wr == RING_LATE;
+      }
+      if (!ok || stop) break;
       if (lane == 0) {
         StageMeta &m = meta[s];
         m.end = 0;
@@ -308,8 +322,12 @@ __device__ __forceinline__ void gqa_produce(uint8_t *smem, const CUtensorMap *tm
     for (int t = 0; t < n_stages && ok; ++t, ++j) {
       const int s = j % C::NS;
       const uint32_t u = j / C::NS;
-      if (u > 0) ok = mbar_wait(&empty[s], (u - 1) & 1, status);
-      if (!ok) break;
+      if (u > 0) {
+        const int wr = slot_wait(s, (u - 1) & 1);
+        ok = wr != RING_FAILED;
+        stop = wr == RING_LATE;
+      }
+      if (!ok || stop) break;
       const int unit0 = cur.ub + t * nbox;
       const int tok0 = unit0 << a.log2_bh;
       // the pages of one stage never straddle a 32-page window (nbox divides 32)
@@ -368,7 +386,7 @@ __device__ __forceinline__ void gqa_produce(uint8_t *smem, const CUtensorMap *tm
         }
       }
     }
-    if (!ok) break;
+    if (!ok || stop) break;
     if (npieces == 0) first_ends = cur.ends;
     if (npieces < (int)DESC_PIECES) ++npieces;
     last_piece = cur;
@@ -380,10 +398,11 @@ __device__ __forceinline__ void gqa_produce(uint8_t *smem, const CUtensorMap *tm
     if (has_next) nwin0 = piece_window(nxt);
   }
   if (ok) {
-    // end marker
+    // end marker (after a late wait too, into the slot that wait was for, which is free by then:
+    // the consumers finish the stages already issued and leave)
     const int s = j % C::NS;
     const uint32_t u = j / C::NS;
-    if (u > 0) ok = mbar_wait(&empty[s], (u - 1) & 1, status);
+    if (u > 0 && !stop) ok = slot_wait(s, (u - 1) & 1) != RING_FAILED;
     if (ok && lane == 0) {
       meta[s].end = 1;
       mbar_arrive(&full[s]);
@@ -458,6 +477,29 @@ __device__ __forceinline__ void gqa_merge_out(const float *mg, const float *sm_m
   }
 }
 
+// A consumer warp whose ring wait at stage j was late (it has completed since): it computes nothing
+// more, but releases this and every later stage and meets both end-of-piece barriers of every
+// piece's last stage, up to the end marker, as the warps still computing do.
+template <class C>
+__device__ __forceinline__ void gqa_consumer_drain(uint8_t *smem, uint32_t j) {
+  using S = GqaSmem<C>;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::OFF_BAR);
+  uint64_t *empty = full + C::NS;
+  const StageMeta *meta = reinterpret_cast<const StageMeta *>(smem + S::OFF_META);
+  for (bool first_stage = true;; ++j, first_stage = false) {
+    const int s = j % C::NS;
+    if (!first_stage && !mbar_wait_warp(&full[s], (j / C::NS) & 1, DRAIN_LIMIT_NS)) break;
+    const StageMeta &mt = meta[s];
+    if (mt.end) break;
+    if (mt.last) {
+      named_bar(1, C::NCW * 32);
+      named_bar(1, C::NCW * 32);
+    }
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&empty[s]);
+  }
+}
+
 // Descriptor of the CTA's pieces for the combine kernel; an idle CTA leaves slot 0 empty
 // (lse -inf, output 0), so a merge that spans it adds nothing.
 template <class C>
@@ -479,7 +521,8 @@ __device__ __forceinline__ void gqa_finish(uint8_t *smem, const GqaArgs &a) {
 }
 
 // MQ: several query positions per row (verify); false compiles the decode-only row logic.
-template <int D, bool MQ>
+// LW: the stage ring's waits take the call's limit (see gqa_produce).
+template <int D, bool MQ, bool LW>
 __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
     gqa_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_q, const GqaArgs a) {
@@ -500,7 +543,7 @@ __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
   gqa_setup<C>(smem, &tm_k, &tm_v, &tm_q, a, pargs);
 
   if (warp == C::NCW) {
-    gqa_produce<C>(smem, &tm_k, &tm_v, &tm_q, a, pargs);
+    gqa_produce<C, LW>(smem, &tm_k, &tm_v, &tm_q, a, pargs);
   } else {
     // ------------------------------------------------------------ consumers
     const int ct = tid;                               // consumer thread index
@@ -522,7 +565,13 @@ __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
     int lo0 = 0, hi0 = 0, lo1 = 0, hi1 = 0;
     for (uint32_t j = 0;; ++j) {
       const int s = j % C::NS;
-      if (!mbar_wait(&full[s], (j / C::NS) & 1, status)) break;
+      if constexpr (LW) {  // the call's limit, and the give-up protocol of ring_wait
+        const int wr = ring_wait(&full[s], (j / C::NS) & 1, a.wait_ns, status);
+        if (wr == RING_LATE) gqa_consumer_drain<C>(smem, j);
+        if (wr != RING_OK) break;
+      } else {
+        if (!mbar_wait(&full[s], (j / C::NS) & 1, status)) break;
+      }
       const StageMeta &mt = meta[s];
       if (mt.end) break;
       const uint32_t kbase = smem_u32(smem + S::OFF_STAGE + s * C::STAGE_BYTES);

@@ -118,7 +118,7 @@ __device__ __forceinline__ float bf16x2_absmax(uint32_t v) {
 __device__ __forceinline__ float pow2f(int s) { return __uint_as_float((uint32_t)(s + 127) << 23); }
 
 // MQ: several query positions per row (verify).  NH8: see GqaF8Cfg.
-template <int D, bool MQ, int NH8>
+template <int D, bool MQ, int NH8, bool LW>
 __global__ void __launch_bounds__(GqaF8Cfg<D, NH8>::THREADS, 1)
     gqa_f8_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                         const __grid_constant__ CUtensorMap tm_q, const GqaArgs a) {
@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(GqaF8Cfg<D, NH8>::THREADS, 1)
   gqa_setup<C>(smem, &tm_k, &tm_v, &tm_q, a, pargs);
 
   if (warp == C::NCW) {
-    gqa_produce<C>(smem, &tm_k, &tm_v, &tm_q, a, pargs);
+    gqa_produce<C, LW>(smem, &tm_k, &tm_v, &tm_q, a, pargs);
   } else {
     // ------------------------------------------------------------ consumers
     const int ct = tid;
@@ -177,7 +177,13 @@ __global__ void __launch_bounds__(GqaF8Cfg<D, NH8>::THREADS, 1)
       }
     for (uint32_t j = 0;; ++j) {
       const int s = j % C::NS;
-      if (!mbar_wait(&full[s], (j / C::NS) & 1, status)) break;
+      if constexpr (LW) {  // the call's limit, and the give-up protocol of ring_wait
+        const int wr = ring_wait(&full[s], (j / C::NS) & 1, a.wait_ns, status);
+        if (wr == RING_LATE) gqa_consumer_drain<C>(smem, j);
+        if (wr != RING_OK) break;
+      } else {
+        if (!mbar_wait(&full[s], (j / C::NS) & 1, status)) break;
+      }
       const StageMeta &mt = meta[s];
       if (mt.end) break;
       const uint32_t kbase = smem_u32(smem + S::OFF_STAGE + s * C::STAGE_BYTES);

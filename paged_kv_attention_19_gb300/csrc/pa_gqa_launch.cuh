@@ -45,22 +45,37 @@ cudaError_t launch_split_kernel(int grid, const CUtensorMap &tm_k, const CUtenso
   return cudaLaunchKernelEx(&cfg, kernel, tm_k, tm_v, tm_q, a);
 }
 
-// Q == 1 (decode) runs the kernel compiled without the per-position row logic.
+// Q == 1 (decode) runs the kernel compiled without the per-position row logic; a wait limit other
+// than the default runs the instantiation whose producer takes it as an argument (LW).
+template <int D, bool LW>
+cudaError_t launch_split_lw(int grid, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const CUtensorMap &tm_q,
+                            const GqaArgs &a, cudaStream_t stream) {
+  using C = GqaCfg<D>;
+  return a.Q > 1 ? launch_split_kernel<C, gqa_split_kernel<D, true, LW>>(grid, tm_k, tm_v, tm_q, a, stream)
+                 : launch_split_kernel<C, gqa_split_kernel<D, false, LW>>(grid, tm_k, tm_v, tm_q, a, stream);
+}
+
 template <int D>
 cudaError_t launch_split_any(int grid, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const CUtensorMap &tm_q,
                              const GqaArgs &a, cudaStream_t stream) {
-  using C = GqaCfg<D>;
-  return a.Q > 1 ? launch_split_kernel<C, gqa_split_kernel<D, true>>(grid, tm_k, tm_v, tm_q, a, stream)
-                 : launch_split_kernel<C, gqa_split_kernel<D, false>>(grid, tm_k, tm_v, tm_q, a, stream);
+  return a.wait_ns == WAIT_LIMIT_NS ? launch_split_lw<D, false>(grid, tm_k, tm_v, tm_q, a, stream)
+                                    : launch_split_lw<D, true>(grid, tm_k, tm_v, tm_q, a, stream);
 }
 
 // FP8 pools: NH8 = 1 when a tile has at most 8 (head, position) columns, else 2.
+template <int D, int NH8, bool LW>
+cudaError_t launch_f8_split_lw(int grid, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const CUtensorMap &tm_q,
+                               const GqaArgs &a, cudaStream_t stream) {
+  using C = GqaF8Cfg<D, NH8>;
+  return a.Q > 1 ? launch_split_kernel<C, gqa_f8_split_kernel<D, true, NH8, LW>>(grid, tm_k, tm_v, tm_q, a, stream)
+                 : launch_split_kernel<C, gqa_f8_split_kernel<D, false, NH8, LW>>(grid, tm_k, tm_v, tm_q, a, stream);
+}
+
 template <int D, int NH8>
 cudaError_t launch_f8_split(int grid, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const CUtensorMap &tm_q,
                             const GqaArgs &a, cudaStream_t stream) {
-  using C = GqaF8Cfg<D, NH8>;
-  return a.Q > 1 ? launch_split_kernel<C, gqa_f8_split_kernel<D, true, NH8>>(grid, tm_k, tm_v, tm_q, a, stream)
-                 : launch_split_kernel<C, gqa_f8_split_kernel<D, false, NH8>>(grid, tm_k, tm_v, tm_q, a, stream);
+  return a.wait_ns == WAIT_LIMIT_NS ? launch_f8_split_lw<D, NH8, false>(grid, tm_k, tm_v, tm_q, a, stream)
+                                    : launch_f8_split_lw<D, NH8, true>(grid, tm_k, tm_v, tm_q, a, stream);
 }
 
 template <int D>

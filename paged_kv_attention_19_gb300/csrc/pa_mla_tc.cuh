@@ -79,6 +79,7 @@ struct MlaTcCfg {
   static constexpr uint32_t IDESC_S = tc_idesc_bf16(M, ST, false);
   static constexpr uint32_t IDESC_PV = tc_idesc_bf16(M, DVH, true);
   static_assert(NQK % 3 == 0, "the scores are issued in chunks of 3 planes");
+  static_assert((ST & (ST - 1)) == 0, "a stage holds a whole number of TMA boxes of a power-of-two token count");
   static_assert(QT_BYTES <= STAGE_BYTES, "the query planes 5-8 fit a ring slot");
   static_assert(2 * ST + (NQK - NQS) * 4 * 8 + DVH <= (int)TM_COLS, "tensor-memory budget");
 };

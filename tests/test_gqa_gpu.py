@@ -193,3 +193,36 @@ def test_full_size_workload_every_output(name):
     o, l = gu.GqaDev(w).run()
     st, dl = gu.check_gqa(w, o, l)
     gu.report(name, o.shape, st, dl)
+
+
+@pytest.mark.parametrize("kind", ["decode", "verify", "fp8"])
+def test_wait_limit_zero_gives_up_cleanly_and_next_call_is_clean(kind):
+    """With a wait limit of 0 a CTA of the split kernel gives up at the first ring slot it finds
+    busy (4 shares: every CTA streams thousands of stages, so its producer soon waits for the
+    oldest one): the call returns, its status word reports PA_DEV_TIMEOUT, and (its outputs being
+    unspecified) the next call at the default limit on the same workspace is clean and matches the
+    oracle.  The bf16 decode, the multi-query verify and the FP8 kernel."""
+    import oracle
+    import paged_kv_attention_19_gb300 as pa
+    w = synth.make_gqa(960, LADDER + [20000] * 6, 16, 2, 128, 32, num_query=3 if kind == "verify" else 1,
+                       fp8=kind == "fp8")
+    g = gu.GqaDev(w)
+    ws = pa.workspace_for_gqa(g.q, g.k, g.bt)
+    try:
+        pa.pa_set_wait_limit_ns(0)
+        g.run_any(workspace=ws, num_splits=4)
+        assert pa.pa_read_device_status(ws) & pa.PA_DEV_TIMEOUT
+    finally:
+        pa.pa_set_wait_limit_ns(pa.PA_DEFAULT_WAIT_LIMIT_NS)
+    o, l = g.run_any(workspace=ws)
+    assert pa.pa_read_device_status(ws) == 0
+    lens, bt = w.layout.context_lens, w.layout.block_table
+    if kind == "fp8":
+        ro, rl = oracle.gqa_fp8(w.q, w.k_pool, w.v_pool, bt, lens, w.scale, w.k_scale, w.v_scale)
+    elif kind == "verify":
+        ro, rl = oracle.verify_gqa(w.q, w.k_pool, w.v_pool, bt, lens, w.scale, w.window)
+    else:
+        ro, rl = gu.gqa_oracle(w)
+    st = compare.compare(o.reshape(-1, w.head_dim), ro)
+    assert st.ok(), str(st)
+    assert compare.lse_max_abs(l.reshape(-1), rl) <= compare.LSE_ABS
