@@ -76,8 +76,8 @@
  *     contents need no initialisation and are overwritten by each call;
  *     calls sharing one workspace must be ordered on one stream.  The GQA
  *     workspace depends on head_dim and num_splits only (two fp32 partial
- *     results of 16 heads per share: 16 KB per share at head_dim 128, about
- *     4.2 MB in automatic mode).  The MLA workspace holds two fp32 partial
+ *     results of 32 rows -- two 16-row tiles of query rows -- per share: 32 KB
+ *     per share at head_dim 128, about 8.5 MB in automatic mode).  The MLA workspace holds two fp32 partial
  *     results of min(num_heads, 128) heads x 256 columns per share (256 KB
  *     per share for 128 heads, 64 MB in automatic mode), plus q_abs, q_lo and
  *     o_lat in bf16 (3.1 KB per (row, head)) and two int32 tables of where
@@ -228,7 +228,7 @@ int pa_decode_mla_absorbed(const void *q, const void *cache, const void *w_uk, c
  *   - A call whose pa_workspace_size(PA_KIND_GQA, ...) exceeds
  *     PA_NOALLOC_SCRATCH_BYTES returns PA_ERR_WORKSPACE_TOO_SMALL before any
  *     device work.  Automatic mode (num_splits 0) always fits; an explicit
- *     num_splits fits up to about 2000 shares at head_dim 128 (1000 at 256).
+ *     num_splits fits up to about 1000 shares at head_dim 128 (500 at 256).
  *   - The first call in a CUDA context (normally the device's primary
  *     context) looks up the array's device address in that context and
  *     caches it under the context's unique ID; make that first call before

@@ -55,8 +55,9 @@ struct GqaPlan {
 
 // Shape checks shared by pa_workspace_size and pa_decode_gqa; PA_OK or an error code.
 // The workspace holds the header, one descriptor per partition and two fp32
-// partial slots (16 heads x head_dim, plus their LSEs) per partition: its size
-// depends on head_dim and the partition count only, not on batch or context.
+// partial slots (32 rows -- two 16-row tiles -- x head_dim, plus their LSEs) per
+// partition: its size depends on head_dim and the partition count only, not on
+// batch or context.
 int gqa_shape(int batch, int Hq, int Hkv, int D, int max_ctx, int P, int num_splits, GqaPlan *pl) {
   if (batch < 0 || Hq <= 0 || Hkv <= 0 || max_ctx < 0 || num_splits < 0) return PA_ERR_INVALID_ARGUMENT;
   if (Hq % Hkv != 0) return PA_ERR_INVALID_ARGUMENT;
@@ -71,9 +72,9 @@ int gqa_shape(int batch, int Hq, int Hkv, int D, int max_ctx, int P, int num_spl
   pl->off_desc = off;
   off = round_up(off + np * sizeof(GqaPartDesc), 256);
   pl->off_part_lse = off;
-  off = round_up(off + np * 2 * PART_HEADS * sizeof(float), 256);
+  off = round_up(off + np * 2 * PART_ROWS * sizeof(float), 256);
   pl->off_part_o = off;
-  off = round_up(off + np * 2 * PART_HEADS * (size_t)D * sizeof(float), 256);
+  off = round_up(off + np * 2 * PART_ROWS * (size_t)D * sizeof(float), 256);
   pl->total = off;
   return PA_OK;
 }
@@ -214,6 +215,11 @@ int gqa_call(const void *q, const void *k_pool, const void *v_pool, const int32_
   const int gt = G < PART_HEADS ? G : PART_HEADS;
   const int qt = G < PART_HEADS ? (Q < PART_HEADS / G ? Q : PART_HEADS / G) : 1;
   const int ntile = G < PART_HEADS ? (Q + qt - 1) / qt : Q * pl.nsub;
+  // a KV head with more than one tile has its tiles paired in one sequence (bf16 pools, head_dim
+  // up to 128: both tiles' fragments fit the consumers' registers), so a page crosses shared
+  // memory once for all of the head's rows
+  const int mt = (!f8.on && D <= 128 && ntile >= 2) ? 2 : 1;
+  const int nseqh = (ntile + mt - 1) / mt;
   CUtensorMap tm_k, tm_v, tm_q;
   const int esz = f8.on ? 1 : 2;
   if (!encode_pool_map(&tm_k, k_pool, num_pages, P, num_kv_heads, D, BH, esz) ||
@@ -252,11 +258,13 @@ int gqa_call(const void *q, const void *k_pool, const void *v_pool, const int32_
   ga.gt = gt;
   ga.qt = qt;
   ga.ntile = ntile;
+  ga.mt = mt;
+  ga.nseqh = nseqh;
   ga.log2_page = ilog2(P);
   ga.log2_bh = ilog2(BH);
   ga.nparts = nparts;
   {
-    const int hs = num_kv_heads * ntile;
+    const int hs = num_kv_heads * nseqh;
     ga.hg = hs < nparts ? hs : nparts;
   }
   {
@@ -284,6 +292,8 @@ int gqa_call(const void *q, const void *k_pool, const void *v_pool, const int32_
   ca.gt = gt;
   ca.qt = qt;
   ca.ntile = ntile;
+  ca.mt = mt;
+  ca.nseqh = nseqh;
 
   cudaError_t e;
   if (t_ev_before) {

@@ -52,6 +52,8 @@
 //     CTAs that hold its pieces, in ascending order, one warp per row.
 #pragma once
 
+#include <type_traits>
+
 #include "pa_common.cuh"
 #include "pa_partition.cuh"
 
@@ -60,7 +62,7 @@ namespace pa {
 // What each split CTA leaves for the combine kernel.
 struct GqaPartDesc {
   int32_t last_b;   // row of the CTA's last piece
-  int32_t last_hs;  // KV head x tile (kv_head * ntile + tile) of the last piece
+  int32_t last_hs;  // sequence of the last piece in its row (kv_head * nseqh + tile pair)
   uint32_t flags;   // bits 0-15: pieces of the CTA (saturating); DESC_* bits
   uint32_t status;  // PA_DEV_* bits seen by the CTA
 };
@@ -69,7 +71,8 @@ constexpr uint32_t DESC_PIECES = 0xffffu;
 constexpr uint32_t DESC_LAST_STARTS = 1u << 16;  // the last piece begins its sequence
 constexpr uint32_t DESC_LAST_ENDS = 1u << 17;    // the last piece ends its sequence
 constexpr uint32_t DESC_FIRST_ENDS = 1u << 18;   // the first piece ends its sequence
-constexpr int PART_HEADS = 16;                   // heads per partial slot (one subgroup)
+constexpr int PART_HEADS = 16;                   // MMA rows of one tile (a 16-head subgroup)
+constexpr int PART_ROWS = 2 * PART_HEADS;        // rows of a partial slot: up to two tiles
 
 struct GqaArgs {
   const uint16_t *q;            // [B, Hq, D] bf16
@@ -84,10 +87,11 @@ struct GqaArgs {
   int Hq, Hkv, G, nsub;
   int Q;                        // query positions per row (1: decode; > 1: verify, causal within them)
   int gt, qt, ntile;            // a tile of MMA rows: qt positions x gt heads; ntile tiles per KV head
+  int mt, nseqh;                // tiles per sequence (1 or 2) and sequences per KV head (ntile / mt, rounded up)
   int log2_page, log2_bh;       // page size and tokens per unit (TMA box), as powers of two
   int piece_cost;               // partition cost of starting a piece, in units
   int nparts;                   // CTAs (shares); groups of hg consecutive CTAs
-  int hg;                       // CTAs per group: min(Hkv * ntile, nparts)
+  int hg;                       // CTAs per group: min(Hkv * nseqh, nparts)
   float qscale;                 // scale * log2(e) (FP8: times the keys' scale)
   float vscale;                 // FP8: the values' scale; 1 for bf16 pools
   unsigned long long wait_ns;   // limit of a stage-ring wait (global-timer ns) before the CTA gives up
@@ -116,7 +120,18 @@ struct GqaCfg {
   static constexpr int STAGE_BYTES = 2 * KV_BYTES;
   static constexpr int NS = (229376 / STAGE_BYTES) < 16 ? (229376 / STAGE_BYTES) : 16;  // 224 KB ring
   static constexpr int NACC = 2;                   // independent QK accumulators
+  static constexpr int QAREA = 0;                  // query rows kept outside the ring (none)
   static_assert(MR * D * 4 * MG <= STAGE_BYTES, "the end-of-piece merge fits the consumed stage");
+};
+
+// Two 16-row tiles per sequence (gqa_consume_pair): the piece's query rows of both tiles are copied
+// out of their ring stage into an area of their own, which takes one stage of the ring.
+template <int D_>
+struct GqaPairCfg : GqaCfg<D_> {
+  using B = GqaCfg<D_>;
+  static constexpr int QAREA = 2 * B::QNQ * B::M * 128;  // both tiles' rows, 128-byte swizzled planes
+  static constexpr int NS = (229376 - QAREA) / B::STAGE_BYTES;
+  static_assert(QAREA <= B::STAGE_BYTES, "a query stage holds both tiles' rows");
 };
 
 struct alignas(16) StageMeta {
@@ -124,7 +139,8 @@ struct alignas(16) StageMeta {
   int32_t b, hq0, ghead, slot;  // slot: -1 = whole sequence (final output), else partial slot 0 / 1
   int32_t tok0, tok_lo, tok_hi, L;  // L: the row's length (query position i attends below L - Q + 1 + i)
   uint32_t badmask;             // bit k: box k of the stage was not loaded
-  int32_t i0, nq, pad0;         // the tile's positions [i0, i0 + nq); ghead: its heads
+  int32_t i0, nq, aux;          // the (first) tile's positions [i0, i0 + nq); ghead: its heads; aux: GQA: the
+                                // sequence (hs of the piece), MLA score buffers: the ring slot of the stage
 };
 static_assert(sizeof(StageMeta) == 64, "stage meta is 64 bytes");
 
@@ -139,7 +155,8 @@ struct GqaMisc {
 template <class C>
 struct GqaSmem {
   static constexpr int OFF_STAGE = 0;
-  static constexpr int OFF_ML = OFF_STAGE + C::NS * C::STAGE_BYTES;
+  static constexpr int OFF_QAREA = OFF_STAGE + C::NS * C::STAGE_BYTES;  // 1024-byte aligned like the stages
+  static constexpr int OFF_ML = OFF_QAREA + C::QAREA;
   static constexpr int OFF_META = OFF_ML + C::MG * C::M * 2 * 4;
   static constexpr int OFF_BAR = OFF_META + C::NS * (int)sizeof(StageMeta);
   static constexpr int OFF_MISC = OFF_BAR + 2 * C::NS * 8;
@@ -217,7 +234,7 @@ __device__ __forceinline__ void gqa_setup(uint8_t *smem, const CUtensorMap *tm_k
   pargs.piece_cost = a.piece_cost;
   pargs.nparts = a.nparts;
   pargs.hg = a.hg;
-  pargs.hs = a.Hkv * a.ntile;  // sequences per row: KV heads x tiles
+  pargs.hs = a.Hkv * a.nseqh;  // sequences per row: KV heads x tile groups
   partition_prologue<C::THREADS>(pargs, &misc->part, &misc->status);
   zero_empty_rows<C::THREADS>(pargs, a.out, a.lse, a.Q * a.Hq * C::D, a.Q * a.Hq);
   __syncthreads();
@@ -228,7 +245,7 @@ __device__ __forceinline__ void gqa_setup(uint8_t *smem, const CUtensorMap *tm_k
 // the call's limit (a.wait_ns) and follow the give-up protocol of ring_wait (a late wait: no
 // further stage, the end marker once the slot is free); otherwise they are bounded at 1 s.  The
 // consumers' waits follow the same rule.
-template <class C, bool LW>
+template <class C, bool LW, int MT>
 __device__ __forceinline__ void gqa_produce(uint8_t *smem, const CUtensorMap *tm_k, const CUtensorMap *tm_v,
                                             const CUtensorMap *tm_q, const GqaArgs &a, const PartitionArgs &pargs) {
   using S = GqaSmem<C>;
@@ -255,7 +272,6 @@ __device__ __forceinline__ void gqa_produce(uint8_t *smem, const CUtensorMap *tm
   bool first_ends = false;
   PieceWalker walker(pargs, &misc->part, lane);
   auto take_piece = [&](Piece &pc) { return walker.take(pc); };
-  auto tile = [&](const Piece &p) { return tile_of(p.hs % a.ntile, a.G, a.nsub, a.Q, a.qt); };
   // block-table window 0 of a piece (lane l: entry l of its first page)
   auto piece_window = [&](const Piece &p) {
     const int pb = (p.ub << a.log2_bh) >> a.log2_page;
@@ -273,11 +289,14 @@ __device__ __forceinline__ void gqa_produce(uint8_t *smem, const CUtensorMap *tm
   }
   while (has_cur && ok && !stop) {
     // ---- emit the stages of `cur`
-    const int g = cur.hs / a.ntile;
-    const Tile tl = tile(cur);
+    const int g = cur.hs / a.nseqh;
+    const int t0 = (cur.hs % a.nseqh) * MT;                     // the sequence's first tile
+    const bool two = MT == 2 && t0 + 1 < a.ntile;                // and a second one
+    const Tile tl = tile_of(t0, a.G, a.nsub, a.Q, a.qt);
+    const Tile tlz = two ? tile_of(t0 + 1, a.G, a.nsub, a.Q, a.qt) : tl;  // the last tile
     const int hq0 = g * a.G + tl.h0;
-    // the tile's tightest key bounds: its first position ends first, its last starts last
-    const int hi_min = pos_hi(cur.L, a.Q, tl.i0), lo_max = pos_lo(cur.L, a.Q, tl.i0 + tl.nq - 1, a.window);
+    // the sequence's tightest key bounds: its first position ends first, its last starts last
+    const int hi_min = pos_hi(cur.L, a.Q, tl.i0), lo_max = pos_lo(cur.L, a.Q, tlz.i0 + tlz.nq - 1, a.window);
     const int slot = (cur.starts && cur.ends) ? -1 : (npieces == 0 ? 0 : 1);
     const int T0 = cur.ub << a.log2_bh;
     const int tok_lo = max(cur.lo, T0), tok_hi = min(cur.L, cur.ue << a.log2_bh);
@@ -309,12 +328,19 @@ __device__ __forceinline__ void gqa_produce(uint8_t *smem, const CUtensorMap *tm
         m.ghead = tl.nh;
         m.i0 = tl.i0;
         m.nq = tl.nq;
+        m.aux = cur.hs;
         m.L = cur.L;
-        mbar_arrive_expect_tx(&full[s], (uint32_t)(C::QNQ * a.gt * a.qt * 128));
+        mbar_arrive_expect_tx(&full[s], (uint32_t)(C::QNQ * a.gt * a.qt * 128 * (two ? 2 : 1)));
         uint8_t *qdst = smem + S::OFF_STAGE + s * C::STAGE_BYTES;
 #pragma unroll
         for (int dq = 0; dq < C::QNQ; ++dq)
           tma_load_3d(qdst + dq * (C::M * 128), tm_q, dq * 64, hq0, cur.b * a.Q + tl.i0, &full[s]);
+        if (two) {  // the second tile's rows follow the first's planes
+#pragma unroll
+          for (int dq = 0; dq < C::QNQ; ++dq)
+            tma_load_3d(qdst + (C::QNQ + dq) * (C::M * 128), tm_q, dq * 64, g * a.G + tlz.h0,
+                        cur.b * a.Q + tlz.i0, &full[s]);
+        }
       }
       __syncwarp();
       ++j;
@@ -365,6 +391,7 @@ __device__ __forceinline__ void gqa_produce(uint8_t *smem, const CUtensorMap *tm
         m.ghead = tl.nh;
         m.i0 = tl.i0;
         m.nq = tl.nq;
+        m.aux = cur.hs;
         m.L = cur.L;
         m.slot = slot;
         m.tok0 = tok0;
@@ -426,16 +453,22 @@ __device__ __forceinline__ void gqa_produce(uint8_t *smem, const CUtensorMap *tm
 // d ^ (4 (h & 7))): each thread takes 4 consecutive dims of one row and merges the groups
 // with weights exp2(m_w - M) / sum_w l_w exp2(m_w - M); a piece that covers its sequence writes
 // bf16 out and the LSE, any other an fp32 partial (times oscale / L either way).
+// The rows one merge writes: a tile of the piece's sequence (positions [i0, i0 + nq), heads
+// [hq0, hq0 + nh)) and where its rows start in a partial slot.
+struct MergeRows {
+  int slot, b, i0, nq, hq0, nh, prow0;
+};
+
 template <class C, bool MQ>
-__device__ __forceinline__ void gqa_merge_out(const float *mg, const float *sm_ml, const StageMeta &mt,
+__device__ __forceinline__ void gqa_merge_out(const float *mg, const float *sm_ml, const MergeRows &mt,
                                               const GqaArgs &a, int ct, float oscale) {
   constexpr int D = C::D;
   const int slot = mt.slot;
   const size_t pi = (size_t)blockIdx.x * 2 + (slot > 0 ? 1 : 0);  // partial slot (when slot >= 0)
-  const int nrows = MQ ? mt.nq * a.gt : mt.ghead;
+  const int nrows = MQ ? mt.nq * a.gt : mt.nh;
   for (int e = ct; e < nrows * (D / 4); e += C::NCW * 32) {
     const int h = e / (D / 4), d4 = (e % (D / 4)) * 4;  // h: the MMA row
-    if (MQ && h % a.gt >= mt.ghead) continue;          // not a head of this tile
+    if (MQ && h % a.gt >= mt.nh) continue;             // not a head of this tile
     float mw[C::MG], M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < C::MG; ++w) {
@@ -463,7 +496,7 @@ __device__ __forceinline__ void gqa_merge_out(const float *mg, const float *sm_m
       v.y = pack_bf16x2(o.z * inv, o.w * inv);
       *reinterpret_cast<uint2 *>(a.out + bh * D + d4) = v;
     } else {
-      *reinterpret_cast<float4 *>(a.part_o + (pi * C::M + h) * D + d4) =
+      *reinterpret_cast<float4 *>(a.part_o + (pi * PART_ROWS + mt.prow0 + h) * D + d4) =
           make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
     }
     if (d4 == 0) {
@@ -471,7 +504,7 @@ __device__ __forceinline__ void gqa_merge_out(const float *mg, const float *sm_m
       if (slot < 0) {
         if (a.lse) a.lse[bh] = lse2 * LN2;
       } else {
-        a.part_lse[pi * C::M + h] = lse2;
+        a.part_lse[pi * PART_ROWS + mt.prow0 + h] = lse2;
       }
     }
   }
@@ -480,8 +513,8 @@ __device__ __forceinline__ void gqa_merge_out(const float *mg, const float *sm_m
 // A consumer warp whose ring wait at stage j was late (it has completed since): it computes nothing
 // more, but releases this and every later stage and meets both end-of-piece barriers of every
 // piece's last stage, up to the end marker, as the warps still computing do.
-template <class C>
-__device__ __forceinline__ void gqa_consumer_drain(uint8_t *smem, uint32_t j) {
+template <class C, int MT>
+__device__ __forceinline__ void gqa_consumer_drain(uint8_t *smem, uint32_t j, const GqaArgs &a) {
   using S = GqaSmem<C>;
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::OFF_BAR);
   uint64_t *empty = full + C::NS;
@@ -491,9 +524,12 @@ __device__ __forceinline__ void gqa_consumer_drain(uint8_t *smem, uint32_t j) {
     if (!first_stage && !mbar_wait_warp(&full[s], (j / C::NS) & 1, DRAIN_LIMIT_NS)) break;
     const StageMeta &mt = meta[s];
     if (mt.end) break;
-    if (mt.last) {
-      named_bar(1, C::NCW * 32);
-      named_bar(1, C::NCW * 32);
+    if (mt.last) {  // one merge round (two barriers) per tile of the sequence
+      const bool two = MT == 2 && (mt.aux % a.nseqh) * MT + 1 < a.ntile;
+      for (int r = 0; r < (two ? 2 : 1); ++r) {
+        named_bar(1, C::NCW * 32);
+        named_bar(1, C::NCW * 32);
+      }
     }
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(&empty[s]);
@@ -515,127 +551,139 @@ __device__ __forceinline__ void gqa_finish(uint8_t *smem, const GqaArgs &a) {
     a.desc[blockIdx.x] = d;
   }
   if ((misc->desc.flags & DESC_PIECES) == 0) {
-    for (int e = tid; e < C::M * D; e += C::THREADS) a.part_o[(size_t)blockIdx.x * 2 * C::M * D + e] = 0.f;
-    for (int h = tid; h < C::M; h += C::THREADS) a.part_lse[(size_t)blockIdx.x * 2 * C::M + h] = -INFINITY;
+    for (int e = tid; e < PART_ROWS * D; e += C::THREADS) a.part_o[(size_t)blockIdx.x * 2 * PART_ROWS * D + e] = 0.f;
+    for (int h = tid; h < PART_ROWS; h += C::THREADS) a.part_lse[(size_t)blockIdx.x * 2 * PART_ROWS + h] = -INFINITY;
   }
 }
 
-// MQ: several query positions per row (verify); false compiles the decode-only row logic.
-// LW: the stage ring's waits take the call's limit (see gqa_produce).
-template <int D, bool MQ, bool LW>
-__global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
-    gqa_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                     const __grid_constant__ CUtensorMap tm_q, const GqaArgs a) {
-  using C = GqaCfg<D>;
+// Consumers of sequences of two 16-row tiles (MT = 2, configuration GqaPairCfg).  Warp w serves
+// tile w / TG over token group w % TG of every stage: it computes that tile's scores of the group's
+// 16 tokens and accumulates all D columns of its P.V (where the one-tile consumers split the columns
+// between two warps that both compute the scores), so the two warps of a token group read each K
+// and V fragment of the stage, one per tile, and no score is computed twice.  At the start of a
+// piece the consumers copy both tiles' query rows out of their ring stage into the query area
+// (the stage goes back at once: a ring stage held for a whole piece would be needed again before
+// the piece's end) and read the A fragments from there at every stage.  The end of a piece merges
+// the tiles one after the other through the consumed stage.
+template <class C, bool MQ, bool LW>
+__device__ __forceinline__ void gqa_consume_pair(uint8_t *smem, const GqaArgs &a) {
   using S = GqaSmem<C>;
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  // the 128-byte swizzle pattern repeats every 1024 bytes: start the stages on such a boundary
-  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  constexpr int D = C::D;
+  constexpr int NTF = D / 8;                 // P.V n-tiles: all columns of the tile
+  constexpr int QOFF1 = C::QNQ * C::M * 128;  // the second tile's rows in a query stage / the area
+  static_assert(C::NCW == 2 * C::TG, "one warp per (tile, token group)");
+  static_assert(C::QAREA == 2 * QOFF1, "the query area holds both tiles");
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::OFF_BAR);
   uint64_t *empty = full + C::NS;
-  StageMeta *meta = reinterpret_cast<StageMeta *>(smem + S::OFF_META);
+  const StageMeta *meta = reinterpret_cast<const StageMeta *>(smem + S::OFF_META);
   GqaMisc *misc = reinterpret_cast<GqaMisc *>(smem + S::OFF_MISC);
   uint32_t *status = &misc->status;
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
+  float *sm_ml = reinterpret_cast<float *>(smem + S::OFF_ML);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ct = tid;
+  const int g8 = lane >> 2, tq = lane & 3;          // MMA fragment row / column pair
+  const int lm_mat = lane >> 3, lm_row = lane & 7;  // ldmatrix: matrix / row this lane addresses
+  const int tgrp = warp % C::TG;                    // token group of this warp
+  const int x = warp / C::TG;                       // the tile it serves
+  const int wbase = tgrp * C::TW;                   // first stage token of this warp
+  const float TAU = 8.f;
+  const int bh_tokens = 1 << a.log2_bh;
+  const uint32_t qarea = smem_u32(smem + S::OFF_QAREA) + x * QOFF1;
+  // one QK accumulator per n-tile: the tile's 64 P.V accumulators fill the registers (two
+  // accumulators spilled and were 2 us slower on the 4-position verify workload)
+  constexpr int NACC = 1;
 
-  PartitionArgs pargs;
-  gqa_setup<C>(smem, &tm_k, &tm_v, &tm_q, a, pargs);
-
-  if (warp == C::NCW) {
-    gqa_produce<C, LW>(smem, &tm_k, &tm_v, &tm_q, a, pargs);
-  } else {
-    // ------------------------------------------------------------ consumers
-    const int ct = tid;                               // consumer thread index
-    const int g8 = lane >> 2, tq = lane & 3;          // MMA fragment row / column pair
-    const int lm_mat = lane >> 3, lm_row = lane & 7;  // ldmatrix: matrix / row this lane addresses
-    const int tgrp = warp % C::TG;                    // token group of this warp
-    const int dh = warp / C::TG;                      // which half of the P.V columns it owns
-    const int wbase = tgrp * C::TW;                   // first stage token of this warp
-    const int nd0 = dh * C::NT_PV;                    // first P.V n-tile of this warp
-    float *sm_ml = reinterpret_cast<float *>(smem + S::OFF_ML);
-    const float TAU = 8.f;
-    const int bh_tokens = 1 << a.log2_bh;
-
-    uint32_t qa[D / 16][4];  // Q A-fragments (rows = heads)
-    float acc[C::NT_PV][4];  // O C-fragments of this warp's columns: [n-tile][row g8 x2, row g8+8 x2]
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    // this thread's two fragment rows (g8, g8 + 8): real row?, key bounds [lo, hi) of its position
-    bool rv0 = false, rv1 = false;
-    int lo0 = 0, hi0 = 0, lo1 = 0, hi1 = 0;
-    for (uint32_t j = 0;; ++j) {
-      const int s = j % C::NS;
-      if constexpr (LW) {  // the call's limit, and the give-up protocol of ring_wait
-        const int wr = ring_wait(&full[s], (j / C::NS) & 1, a.wait_ns, status);
-        if (wr == RING_LATE) gqa_consumer_drain<C>(smem, j);
-        if (wr != RING_OK) break;
-      } else {
-        if (!mbar_wait(&full[s], (j / C::NS) & 1, status)) break;
-      }
-      const StageMeta &mt = meta[s];
-      if (mt.end) break;
-      const uint32_t kbase = smem_u32(smem + S::OFF_STAGE + s * C::STAGE_BYTES);
-      const uint32_t vbase = kbase + C::KV_BYTES;
-      if (mt.first) {
-        // a new piece: its query rows into the A-fragments (ldmatrix from the 128-byte
-        // swizzled planes of 16 rows x 64 dims), fresh softmax state, and the stage goes back
+  float acc[NTF][4];  // O C-fragments of the tile: [n-tile][row g8 x2, row g8+8 x2]
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  bool rv0 = false, rv1 = false;  // this thread's fragment rows (g8, g8 + 8): real rows?
+  int lo0 = 0, hi0 = 0, lo1 = 0, hi1 = 0;  // their key bounds [lo, hi)
+  bool two = false;     // the piece's sequence has a second tile (the same in every warp)
+  bool active = false;  // this warp's tile is in it
+  bool late = false;    // LW: a wait was late; from then on only the ring's protocol is kept
+  for (uint32_t j = 0;; ++j) {
+    const int s = j % C::NS;
+    if constexpr (LW) {
+      const int wr = ring_wait(&full[s], (j / C::NS) & 1, late ? DRAIN_LIMIT_NS : a.wait_ns, status);
+      if (wr == RING_FAILED) break;
+      late = late || wr == RING_LATE;
+    } else {
+      if (!mbar_wait(&full[s], (j / C::NS) & 1, status)) break;
+    }
+    const StageMeta &mt = meta[s];
+    if (mt.end) break;
+    const uint32_t kbase = smem_u32(smem + S::OFF_STAGE + s * C::STAGE_BYTES);
+    const uint32_t vbase = kbase + C::KV_BYTES;
+    const int t0 = (mt.aux % a.nseqh) * 2;
+    if (mt.first) {
+      // a new piece: both tiles' query rows into the query area (every warp passed the previous
+      // piece's merge, the last reads of the area, before this stage), fresh softmax state
+      two = t0 + 1 < a.ntile;
+      active = x == 0 || two;
+      if (!late) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(smem + S::OFF_STAGE + s * C::STAGE_BYTES);
+        uint4 *dst = reinterpret_cast<uint4 *>(smem + S::OFF_QAREA);
+        for (int e = ct; e < C::QAREA / 16; e += C::NCW * 32) dst[e] = src[e];
+        const Tile tl = tile_of(active ? t0 + x : t0, a.G, a.nsub, a.Q, a.qt);
         if constexpr (MQ) {
           const int iq0 = g8 / a.gt, hh0 = g8 % a.gt, iq1 = (g8 + 8) / a.gt, hh1 = (g8 + 8) % a.gt;
-          rv0 = iq0 < mt.nq && hh0 < mt.ghead;
-          rv1 = iq1 < mt.nq && hh1 < mt.ghead;
-          lo0 = pos_lo(mt.L, a.Q, mt.i0 + iq0, a.window);
-          hi0 = pos_hi(mt.L, a.Q, mt.i0 + iq0);
-          lo1 = pos_lo(mt.L, a.Q, mt.i0 + iq1, a.window);
-          hi1 = pos_hi(mt.L, a.Q, mt.i0 + iq1);
-        } else {  // one position: row r is head r, and the piece's bounds are the row's
-          rv0 = g8 < mt.ghead;
-          rv1 = g8 + 8 < mt.ghead;
+          rv0 = active && iq0 < tl.nq && hh0 < tl.nh;
+          rv1 = active && iq1 < tl.nq && hh1 < tl.nh;
+          lo0 = pos_lo(mt.L, a.Q, tl.i0 + iq0, a.window);
+          hi0 = pos_hi(mt.L, a.Q, tl.i0 + iq0);
+          lo1 = pos_lo(mt.L, a.Q, tl.i0 + iq1, a.window);
+          hi1 = pos_hi(mt.L, a.Q, tl.i0 + iq1);
+        } else {  // one position: row r is head r of the tile
+          rv0 = active && g8 < tl.nh;
+          rv1 = active && g8 + 8 < tl.nh;
         }
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const int row = (lm_mat & 1) * 8 + lm_row, chunk = 2 * ks + (lm_mat >> 1);
-          ldmatrix_x4(qa[ks], kbase + (chunk >> 3) * (C::M * 128) + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
-        }
-#pragma unroll
-        for (int n = 0; n < C::NT_PV; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+        for (int n = 0; n < NTF; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
         m0 = m1 = -INFINITY;
         l0 = l1 = 0.f;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-        continue;
       }
-
-      // ---- S = Q K^T for the group's 16 tokens (two n-tiles of 8); the k-steps are spread
-      // over NACC independent accumulators so no long chain of dependent MMAs forms
+      named_bar(1, C::NCW * 32);  // the area is complete before any warp reads it
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      continue;
+    }
+    const bool masked = mt.masked;
+    if (active && !late) {
+      // ---- S = Q K^T of this tile for the group's 16 tokens (two n-tiles of 8)
       float sv[2][4];
       {
-        float sp[C::NACC][2][4];
+        float sp[NACC][2][4];
 #pragma unroll
-        for (int q = 0; q < C::NACC; ++q)
+        for (int q = 0; q < NACC; ++q)
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) sp[q][nt][0] = sp[q][nt][1] = sp[q][nt][2] = sp[q][nt][3] = 0.f;
 #pragma unroll
         for (int ks2 = 0; ks2 < D / 32; ++ks2) {
+          uint32_t qf[2][4];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int ks = 2 * ks2 + h;
+            const int row = (lm_mat & 1) * 8 + lm_row, chunk = 2 * ks + (lm_mat >> 1);
+            ldmatrix_x4(qf[h], qarea + (chunk >> 3) * (C::M * 128) + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
+          }
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) {
             uint32_t b[4];
             ldmatrix_x4(b, kbase + kv_off<C>(wbase + nt * 8 + lm_row, 4 * ks2 + lm_mat));
-            mma_bf16_16816(sp[(2 * ks2) % C::NACC][nt], qa[2 * ks2], b[0], b[1]);
-            mma_bf16_16816(sp[(2 * ks2 + 1) % C::NACC][nt], qa[2 * ks2 + 1], b[2], b[3]);
+            mma_bf16_16816(sp[(2 * ks2) % NACC][nt], qf[0], b[0], b[1]);
+            mma_bf16_16816(sp[(2 * ks2 + 1) % NACC][nt], qf[1], b[2], b[3]);
           }
         }
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            float x = sp[0][nt][e];
+            float v = sp[0][nt][e];
 #pragma unroll
-            for (int q = 1; q < C::NACC; ++q) x += sp[q][nt][e];
-            sv[nt][e] = x;
+            for (int q = 1; q < NACC; ++q) v += sp[q][nt][e];
+            sv[nt][e] = v;
           }
       }
-      const bool masked = mt.masked;
-      // scale, mask (invalid tokens and padded head rows -> -inf)
+      // scale, mask (invalid tokens and padded rows -> -inf)
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -650,7 +698,7 @@ __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
           }
           sv[nt][e] = valid ? v : -INFINITY;
         }
-      // ---- online softmax per head row (rows g8 and g8 + 8)
+      // ---- online softmax per row (rows g8 and g8 + 8)
       float x0 = fmaxf(fmaxf(sv[0][0], sv[0][1]), fmaxf(sv[1][0], sv[1][1]));
       float x1 = fmaxf(fmaxf(sv[0][2], sv[0][3]), fmaxf(sv[1][2], sv[1][3]));
       x0 = fmaxf(x0, __shfl_xor_sync(FULL, x0, 1));
@@ -666,7 +714,7 @@ __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
         l0 *= a0;
         l1 *= a1;
 #pragma unroll
-        for (int n = 0; n < C::NT_PV; ++n) {
+        for (int n = 0; n < NTF; ++n) {
           acc[n][0] *= a0;
           acc[n][1] *= a0;
           acc[n][2] *= a1;
@@ -692,61 +740,317 @@ __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
         l1 += (p[0][2] + p[0][3]) + (p[1][2] + p[1][3]);
       }
       if (masked) {
-        // V rows of keys that are not attended (outside [lo, L), unloaded boxes) may hold
-        // anything, NaN included: zero this warp's columns of them so that 0 x row stays 0.
+        // V rows of keys that are not attended may hold anything, NaN included: zero them (all
+        // columns of the group's rows; the other tile's warp of the group writes the same zeros)
+        // so that 0 x row stays 0
         uint8_t *vgen = smem + S::OFF_STAGE + s * C::STAGE_BYTES + C::KV_BYTES;
-        constexpr int CPW = C::NQ * 8 / C::DSPLIT;  // 16-byte chunks of a row owned by this warp
-        for (int e = lane; e < C::TW * CPW; e += 32) {
-          const int stok = wbase + e / CPW;
-          const int chunk = dh * CPW + e % CPW;
+        constexpr int CPR = C::NQ * 8;  // 16-byte chunks of a row
+        for (int e = lane; e < C::TW * CPR; e += 32) {
+          const int stok = wbase + e / CPR;
+          const int chunk = e % CPR;
           const int ltok = mt.tok0 + stok;
           if (ltok < mt.tok_lo || ltok >= mt.tok_hi || ((mt.badmask >> (stok / bh_tokens)) & 1u))
             *reinterpret_cast<uint4 *>(vgen + kv_off<C>(stok, chunk)) = make_uint4(0, 0, 0, 0);
         }
         __syncwarp();
       }
-      // ---- O += P V (k = the group's 16 tokens), this warp's columns
+      // ---- O += P V (k = the group's 16 tokens), all columns
       {
         const int tok = wbase + (lm_mat & 1) * 8 + lm_row;
 #pragma unroll
-        for (int nd = 0; nd < C::NT_PV; nd += 2) {
+        for (int nd = 0; nd < NTF; nd += 2) {
           uint32_t b[4];
-          ldmatrix_x4_trans(b, vbase + kv_off<C>(tok, nd0 + nd + (lm_mat >> 1)));
+          ldmatrix_x4_trans(b, vbase + kv_off<C>(tok, nd + (lm_mat >> 1)));
           mma_bf16_16816(acc[nd], pa, b[0], b[1]);
           mma_bf16_16816(acc[nd + 1], pa, b[2], b[3]);
         }
       }
+    }
 
-      if (mt.last) {
-        // ---- end of a piece: merge the token groups through this stage's buffer
+    if (mt.last) {
+      // ---- end of a piece: the tiles one after the other, through this stage's buffer
+      float *mg = reinterpret_cast<float *>(smem + S::OFF_STAGE + s * C::STAGE_BYTES);
+      const int g = mt.aux / a.nseqh;
+      if (active && !late) {
         l0 += __shfl_xor_sync(FULL, l0, 1);
         l0 += __shfl_xor_sync(FULL, l0, 2);
         l1 += __shfl_xor_sync(FULL, l1, 1);
         l1 += __shfl_xor_sync(FULL, l1, 2);
-        named_bar(1, C::NCW * 32);  // all warps are done reading this stage
-        float *mg = reinterpret_cast<float *>(smem + S::OFF_STAGE + s * C::STAGE_BYTES);
+      }
+      for (int xr = 0; xr < (two ? 2 : 1); ++xr) {
+        named_bar(1, C::NCW * 32);  // all warps are done reading this stage (or the last merge)
+        if (x == xr && !late) {
 #pragma unroll
-        for (int n = 0; n < C::NT_PV; ++n) {
-          const int d = ((nd0 + n) * 8 + 2 * tq) ^ (4 * g8);
-          *reinterpret_cast<float2 *>(mg + (tgrp * C::M + g8) * D + d) = make_float2(acc[n][0], acc[n][1]);
-          *reinterpret_cast<float2 *>(mg + (tgrp * C::M + g8 + 8) * D + d) = make_float2(acc[n][2], acc[n][3]);
-        }
-        if (tq == 0 && dh == 0) {  // both column halves of a token group hold the same (m, l)
-          sm_ml[(tgrp * C::M + g8) * 2] = m0;
-          sm_ml[(tgrp * C::M + g8) * 2 + 1] = l0;
-          sm_ml[(tgrp * C::M + g8 + 8) * 2] = m1;
-          sm_ml[(tgrp * C::M + g8 + 8) * 2 + 1] = l1;
+          for (int n = 0; n < NTF; ++n) {
+            const int d = (n * 8 + 2 * tq) ^ (4 * g8);
+            *reinterpret_cast<float2 *>(mg + (tgrp * C::M + g8) * D + d) = make_float2(acc[n][0], acc[n][1]);
+            *reinterpret_cast<float2 *>(mg + (tgrp * C::M + g8 + 8) * D + d) = make_float2(acc[n][2], acc[n][3]);
+          }
+          if (tq == 0) {
+            sm_ml[(tgrp * C::M + g8) * 2] = m0;
+            sm_ml[(tgrp * C::M + g8) * 2 + 1] = l0;
+            sm_ml[(tgrp * C::M + g8 + 8) * 2] = m1;
+            sm_ml[(tgrp * C::M + g8 + 8) * 2 + 1] = l1;
+          }
         }
         named_bar(1, C::NCW * 32);
-        gqa_merge_out<C, MQ>(mg, sm_ml, mt, a, ct, 1.f);
-        // no CTA barrier before the release: every warp arrives on the stage's empty barrier
-        // after its own reads, and the producer refills the stage only once all have arrived
-        fence_proxy_async_smem();  // generic writes to the stage buffer precede its next TMA fill
-      } else if (masked) {
-        fence_proxy_async_smem();  // the zeroed V rows precede the next TMA fill of this stage
+        if (!late) {
+          const Tile tl = tile_of(t0 + xr, a.G, a.nsub, a.Q, a.qt);
+          const MergeRows rows = {mt.slot, mt.b, tl.i0, tl.nq, g * a.G + tl.h0, tl.nh, xr * C::M};
+          gqa_merge_out<C, MQ>(mg, sm_ml, rows, a, ct, 1.f);
+        }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
+      // no CTA barrier before the release: every warp arrives on the stage's empty barrier
+      // after its own reads, and the producer refills the stage only once all have arrived
+      fence_proxy_async_smem();  // generic writes to the stage buffer precede its next TMA fill
+    } else if (masked) {
+      fence_proxy_async_smem();  // the zeroed V rows precede the next TMA fill of this stage
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+  }
+}
+
+// MQ: several query positions per row (verify); false compiles the decode-only row logic.
+// LW: the stage ring's waits take the call's limit (see gqa_produce).
+// MT: tiles per sequence.  With MT = 2 a sequence is a pair of 16-row tiles of one KV head (32
+// (position, head) rows: verify with more than 16 rows per KV head, or more than 16 heads per
+// group): each K or V fragment a warp loads from the stage feeds the MMAs of both tiles, so a page
+// crosses shared memory once for all of the head's rows.
+template <int D, int MT>
+using GqaCfgOf = std::conditional_t<MT == 2, GqaPairCfg<D>, GqaCfg<D>>;
+
+template <int D, bool MQ, bool LW, int MT>
+__global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
+    gqa_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ CUtensorMap tm_q, const GqaArgs a) {
+  using C = GqaCfgOf<D, MT>;
+  using S = GqaSmem<C>;
+  static_assert(MT == 1 || MT == 2, "one or two tiles per sequence");
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // the 128-byte swizzle pattern repeats every 1024 bytes: start the stages on such a boundary
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::OFF_BAR);
+  uint64_t *empty = full + C::NS;
+  StageMeta *meta = reinterpret_cast<StageMeta *>(smem + S::OFF_META);
+  GqaMisc *misc = reinterpret_cast<GqaMisc *>(smem + S::OFF_MISC);
+  uint32_t *status = &misc->status;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+
+  PartitionArgs pargs;
+  gqa_setup<C>(smem, &tm_k, &tm_v, &tm_q, a, pargs);
+
+  if (warp == C::NCW) {
+    gqa_produce<C, LW, MT>(smem, &tm_k, &tm_v, &tm_q, a, pargs);
+  } else {
+    if constexpr (MT == 2) {
+      gqa_consume_pair<C, MQ, LW>(smem, a);
+    } else {
+      // ------------------------------------------------------------ consumers
+      const int ct = tid;                               // consumer thread index
+      const int g8 = lane >> 2, tq = lane & 3;          // MMA fragment row / column pair
+      const int lm_mat = lane >> 3, lm_row = lane & 7;  // ldmatrix: matrix / row this lane addresses
+      const int tgrp = warp % C::TG;                    // token group of this warp
+      const int dh = warp / C::TG;                      // which half of the P.V columns it owns
+      const int wbase = tgrp * C::TW;                   // first stage token of this warp
+      const int nd0 = dh * C::NT_PV;                    // first P.V n-tile of this warp
+      float *sm_ml = reinterpret_cast<float *>(smem + S::OFF_ML);
+      const float TAU = 8.f;
+      const int bh_tokens = 1 << a.log2_bh;
+
+      uint32_t qa[D / 16][4];  // Q A-fragments (rows = heads)
+      float acc[C::NT_PV][4];  // O C-fragments of this warp's columns: [n-tile][row g8 x2, row g8+8 x2]
+      float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+      // this thread's two fragment rows (g8, g8 + 8): real row?, key bounds [lo, hi) of its position
+      bool rv0 = false, rv1 = false;
+      int lo0 = 0, hi0 = 0, lo1 = 0, hi1 = 0;
+      for (uint32_t j = 0;; ++j) {
+        const int s = j % C::NS;
+        if constexpr (LW) {  // the call's limit, and the give-up protocol of ring_wait
+          const int wr = ring_wait(&full[s], (j / C::NS) & 1, a.wait_ns, status);
+          if (wr == RING_LATE) gqa_consumer_drain<C, 1>(smem, j, a);
+          if (wr != RING_OK) break;
+        } else {
+          if (!mbar_wait(&full[s], (j / C::NS) & 1, status)) break;
+        }
+        const StageMeta &mt = meta[s];
+        if (mt.end) break;
+        const uint32_t kbase = smem_u32(smem + S::OFF_STAGE + s * C::STAGE_BYTES);
+        const uint32_t vbase = kbase + C::KV_BYTES;
+        if (mt.first) {
+          // a new piece: its query rows into the A-fragments (ldmatrix from the 128-byte
+          // swizzled planes of 16 rows x 64 dims), fresh softmax state, and the stage goes back
+          if constexpr (MQ) {
+            const int iq0 = g8 / a.gt, hh0 = g8 % a.gt, iq1 = (g8 + 8) / a.gt, hh1 = (g8 + 8) % a.gt;
+            rv0 = iq0 < mt.nq && hh0 < mt.ghead;
+            rv1 = iq1 < mt.nq && hh1 < mt.ghead;
+            lo0 = pos_lo(mt.L, a.Q, mt.i0 + iq0, a.window);
+            hi0 = pos_hi(mt.L, a.Q, mt.i0 + iq0);
+            lo1 = pos_lo(mt.L, a.Q, mt.i0 + iq1, a.window);
+            hi1 = pos_hi(mt.L, a.Q, mt.i0 + iq1);
+          } else {  // one position: row r is head r, and the piece's bounds are the row's
+            rv0 = g8 < mt.ghead;
+            rv1 = g8 + 8 < mt.ghead;
+          }
+  #pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const int row = (lm_mat & 1) * 8 + lm_row, chunk = 2 * ks + (lm_mat >> 1);
+            ldmatrix_x4(qa[ks], kbase + (chunk >> 3) * (C::M * 128) + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
+          }
+  #pragma unroll
+          for (int n = 0; n < C::NT_PV; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+          m0 = m1 = -INFINITY;
+          l0 = l1 = 0.f;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[s]);
+          continue;
+        }
+
+        // ---- S = Q K^T for the group's 16 tokens (two n-tiles of 8); the k-steps are spread
+        // over NACC independent accumulators so no long chain of dependent MMAs forms
+        float sv[2][4];
+        {
+          float sp[C::NACC][2][4];
+  #pragma unroll
+          for (int q = 0; q < C::NACC; ++q)
+  #pragma unroll
+            for (int nt = 0; nt < 2; ++nt) sp[q][nt][0] = sp[q][nt][1] = sp[q][nt][2] = sp[q][nt][3] = 0.f;
+  #pragma unroll
+          for (int ks2 = 0; ks2 < D / 32; ++ks2) {
+  #pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+              uint32_t b[4];
+              ldmatrix_x4(b, kbase + kv_off<C>(wbase + nt * 8 + lm_row, 4 * ks2 + lm_mat));
+              mma_bf16_16816(sp[(2 * ks2) % C::NACC][nt], qa[2 * ks2], b[0], b[1]);
+              mma_bf16_16816(sp[(2 * ks2 + 1) % C::NACC][nt], qa[2 * ks2 + 1], b[2], b[3]);
+            }
+          }
+  #pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+  #pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float x = sp[0][nt][e];
+  #pragma unroll
+              for (int q = 1; q < C::NACC; ++q) x += sp[q][nt][e];
+              sv[nt][e] = x;
+            }
+        }
+        const bool masked = mt.masked;
+        // scale, mask (invalid tokens and padded head rows -> -inf)
+  #pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+  #pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float v = sv[nt][e] * a.qscale;
+            bool valid = (e < 2) ? rv0 : rv1;
+            if (masked) {
+              const int stok = wbase + nt * 8 + 2 * tq + (e & 1);
+              const int ltok = mt.tok0 + stok;
+              valid = valid && ltok >= mt.tok_lo && ltok < mt.tok_hi && !((mt.badmask >> (stok / bh_tokens)) & 1u);
+              if constexpr (MQ) valid = valid && ltok >= ((e < 2) ? lo0 : lo1) && ltok < ((e < 2) ? hi0 : hi1);
+            }
+            sv[nt][e] = valid ? v : -INFINITY;
+          }
+        // ---- online softmax per head row (rows g8 and g8 + 8)
+        float x0 = fmaxf(fmaxf(sv[0][0], sv[0][1]), fmaxf(sv[1][0], sv[1][1]));
+        float x1 = fmaxf(fmaxf(sv[0][2], sv[0][3]), fmaxf(sv[1][2], sv[1][3]));
+        x0 = fmaxf(x0, __shfl_xor_sync(FULL, x0, 1));
+        x0 = fmaxf(x0, __shfl_xor_sync(FULL, x0, 2));
+        x1 = fmaxf(x1, __shfl_xor_sync(FULL, x1, 1));
+        x1 = fmaxf(x1, __shfl_xor_sync(FULL, x1, 2));
+        if (__any_sync(FULL, (x0 > m0 + TAU) || (x1 > m1 + TAU))) {
+          const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+          const float a0 = (n0 == -INFINITY) ? 1.f : fast_exp2(m0 - n0);
+          const float a1 = (n1 == -INFINITY) ? 1.f : fast_exp2(m1 - n1);
+          m0 = n0;
+          m1 = n1;
+          l0 *= a0;
+          l1 *= a1;
+  #pragma unroll
+          for (int n = 0; n < C::NT_PV; ++n) {
+            acc[n][0] *= a0;
+            acc[n][1] *= a0;
+            acc[n][2] *= a1;
+            acc[n][3] *= a1;
+          }
+        }
+        uint32_t pa[4];
+        {
+          float p[2][4];
+  #pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+  #pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float mr = (e < 2) ? m0 : m1;
+              p[nt][e] = (sv[nt][e] == -INFINITY) ? 0.f : fast_exp2(sv[nt][e] - mr);
+            }
+          pa[0] = pack_bf16x2(p[0][0], p[0][1]);
+          pa[1] = pack_bf16x2(p[0][2], p[0][3]);
+          pa[2] = pack_bf16x2(p[1][0], p[1][1]);
+          pa[3] = pack_bf16x2(p[1][2], p[1][3]);
+          // the denominator (and so the LSE) sums the fp32 weights; only the MMA operand is rounded
+          l0 += (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
+          l1 += (p[0][2] + p[0][3]) + (p[1][2] + p[1][3]);
+        }
+        if (masked) {
+          // V rows of keys that are not attended (outside [lo, L), unloaded boxes) may hold
+          // anything, NaN included: zero this warp's columns of them so that 0 x row stays 0.
+          uint8_t *vgen = smem + S::OFF_STAGE + s * C::STAGE_BYTES + C::KV_BYTES;
+          constexpr int CPW = C::NQ * 8 / C::DSPLIT;  // 16-byte chunks of a row owned by this warp
+          for (int e = lane; e < C::TW * CPW; e += 32) {
+            const int stok = wbase + e / CPW;
+            const int chunk = dh * CPW + e % CPW;
+            const int ltok = mt.tok0 + stok;
+            if (ltok < mt.tok_lo || ltok >= mt.tok_hi || ((mt.badmask >> (stok / bh_tokens)) & 1u))
+              *reinterpret_cast<uint4 *>(vgen + kv_off<C>(stok, chunk)) = make_uint4(0, 0, 0, 0);
+          }
+          __syncwarp();
+        }
+        // ---- O += P V (k = the group's 16 tokens), this warp's columns
+        {
+          const int tok = wbase + (lm_mat & 1) * 8 + lm_row;
+  #pragma unroll
+          for (int nd = 0; nd < C::NT_PV; nd += 2) {
+            uint32_t b[4];
+            ldmatrix_x4_trans(b, vbase + kv_off<C>(tok, nd0 + nd + (lm_mat >> 1)));
+            mma_bf16_16816(acc[nd], pa, b[0], b[1]);
+            mma_bf16_16816(acc[nd + 1], pa, b[2], b[3]);
+          }
+        }
+
+        if (mt.last) {
+          // ---- end of a piece: merge the token groups through this stage's buffer
+          l0 += __shfl_xor_sync(FULL, l0, 1);
+          l0 += __shfl_xor_sync(FULL, l0, 2);
+          l1 += __shfl_xor_sync(FULL, l1, 1);
+          l1 += __shfl_xor_sync(FULL, l1, 2);
+          named_bar(1, C::NCW * 32);  // all warps are done reading this stage
+          float *mg = reinterpret_cast<float *>(smem + S::OFF_STAGE + s * C::STAGE_BYTES);
+  #pragma unroll
+          for (int n = 0; n < C::NT_PV; ++n) {
+            const int d = ((nd0 + n) * 8 + 2 * tq) ^ (4 * g8);
+            *reinterpret_cast<float2 *>(mg + (tgrp * C::M + g8) * D + d) = make_float2(acc[n][0], acc[n][1]);
+            *reinterpret_cast<float2 *>(mg + (tgrp * C::M + g8 + 8) * D + d) = make_float2(acc[n][2], acc[n][3]);
+          }
+          if (tq == 0 && dh == 0) {  // both column halves of a token group hold the same (m, l)
+            sm_ml[(tgrp * C::M + g8) * 2] = m0;
+            sm_ml[(tgrp * C::M + g8) * 2 + 1] = l0;
+            sm_ml[(tgrp * C::M + g8 + 8) * 2] = m1;
+            sm_ml[(tgrp * C::M + g8 + 8) * 2 + 1] = l1;
+          }
+          named_bar(1, C::NCW * 32);
+          const MergeRows rows = {mt.slot, mt.b, mt.i0, mt.nq, mt.hq0, mt.ghead, 0};
+          gqa_merge_out<C, MQ>(mg, sm_ml, rows, a, ct, 1.f);
+          // no CTA barrier before the release: every warp arrives on the stage's empty barrier
+          // after its own reads, and the producer refills the stage only once all have arrived
+          fence_proxy_async_smem();  // generic writes to the stage buffer precede its next TMA fill
+        } else if (masked) {
+          fence_proxy_async_smem();  // the zeroed V rows precede the next TMA fill of this stage
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+      }
     }
   }
   gqa_finish<C>(smem, a);
@@ -760,7 +1064,7 @@ struct CombineArgs {
   const GqaPartDesc *desc;
   uint32_t *status;  // the workspace status word: OR of every CTA's bits
   int Hq, G, nsub, nparts, hg;
-  int Q, gt, qt, ntile;
+  int Q, gt, qt, ntile, mt, nseqh;
 };
 
 // One block per split CTA c.  Block c merges the sequence that CTA c's last
@@ -768,10 +1072,11 @@ struct CombineArgs {
 // CTA c's slot (1 if the CTA has several pieces, else 0) and slot 0 of CTAs
 // c + hg, c + 2 hg, ... (the same head in the following groups) up to the
 // first one whose first piece ends the sequence.
-// Warp w handles MMA row w (one warp per row, so the rows' few dependent
-// loads from L2 overlap instead of queueing): weights exp2(lse_k - M), then
+// Warp w handles row w of the sequence's partial slots, i.e. MMA row w % 16 of its tile w / 16
+// (one warp per row, so the rows' few dependent loads from L2 overlap instead of queueing; the
+// block has 16 warps per tile of a sequence): weights exp2(lse_k - M), then
 // o = sum_k w_k o_k / sum_k w_k in ascending k, each lane owning D/32 dims.
-constexpr int COMBINE_THREADS = PART_HEADS * 32;
+constexpr int COMBINE_THREADS = PART_ROWS * 32;  // the largest block: two tiles
 template <int D>
 __global__ void __launch_bounds__(COMBINE_THREADS) gqa_combine_kernel(const CombineArgs a) {
   pdl_wait();               // the split kernel's partials and descriptors are visible from here on
@@ -801,24 +1106,27 @@ __global__ void __launch_bounds__(COMBINE_THREADS) gqa_combine_kernel(const Comb
   }
   if (k < 0) return;  // not reachable for a consistent partition
   const int first_slot = np >= 2 ? 1 : 0;
-  const int g = d0.last_hs / a.ntile;
-  const Tile tl = tile_of(d0.last_hs % a.ntile, a.G, a.nsub, a.Q, a.qt);
+  const int g = d0.last_hs / a.nseqh;
+  const int h = warp;                                   // the row of the partial slots
+  const int t = (d0.last_hs % a.nseqh) * a.mt + h / PART_HEADS;  // its tile
+  if (t >= a.ntile) return;                             // a sequence with one tile of two
+  const Tile tl = tile_of(t, a.G, a.nsub, a.Q, a.qt);
   const int hq0 = g * a.G + tl.h0;
   constexpr int PER = D / 32;  // 2, 4 or 8 consecutive dims per lane
   {
-    const int h = warp;  // the MMA row
-    if (h >= tl.nq * a.gt || h % a.gt >= tl.nh) return;
+    const int r = h % PART_HEADS;  // the MMA row of the tile
+    if (r >= tl.nq * a.gt || r % a.gt >= tl.nh) return;
     float M = -INFINITY;
     for (int i = lane; i < k; i += 32) {
       const size_t pi = i == 0 ? (size_t)c * 2 + first_slot : (size_t)(c + i * a.hg) * 2;
-      M = fmaxf(M, a.part_lse[pi * PART_HEADS + h]);
+      M = fmaxf(M, a.part_lse[pi * PART_ROWS + h]);
     }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, o));
     float Z = 0.f;
     for (int i = lane; i < k; i += 32) {
       const size_t pi = i == 0 ? (size_t)c * 2 + first_slot : (size_t)(c + i * a.hg) * 2;
-      const float l = a.part_lse[pi * PART_HEADS + h];
+      const float l = a.part_lse[pi * PART_ROWS + h];
       Z += (l == -INFINITY || M == -INFINITY) ? 0.f : fast_exp2(l - M);
     }
 #pragma unroll
@@ -829,9 +1137,9 @@ __global__ void __launch_bounds__(COMBINE_THREADS) gqa_combine_kernel(const Comb
 #pragma unroll 4
     for (int i = 0; i < k; ++i) {
       const size_t pi = i == 0 ? (size_t)c * 2 + first_slot : (size_t)(c + i * a.hg) * 2;
-      const float l = a.part_lse[pi * PART_HEADS + h];
+      const float l = a.part_lse[pi * PART_ROWS + h];
       const float wc = (l == -INFINITY || M == -INFINITY) ? 0.f : fast_exp2(l - M);
-      const float *po = a.part_o + (pi * PART_HEADS + h) * D + lane * PER;
+      const float *po = a.part_o + (pi * PART_ROWS + h) * D + lane * PER;
       if constexpr (PER == 2) {
         const float2 x = *reinterpret_cast<const float2 *>(po);
         acc[0] += wc * x.x;
@@ -848,7 +1156,7 @@ __global__ void __launch_bounds__(COMBINE_THREADS) gqa_combine_kernel(const Comb
       }
     }
     const float inv = Z > 0.f ? 1.f / Z : 0.f;
-    const size_t bh = ((size_t)d0.last_b * a.Q + tl.i0 + h / a.gt) * a.Hq + hq0 + h % a.gt;
+    const size_t bh = ((size_t)d0.last_b * a.Q + tl.i0 + r / a.gt) * a.Hq + hq0 + r % a.gt;
     uint32_t *dst = reinterpret_cast<uint32_t *>(a.out + bh * D + lane * PER);
 #pragma unroll
     for (int e = 0; e < PER; e += 2) dst[e / 2] = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);

@@ -70,6 +70,7 @@ struct GqaF8Cfg {
   static_assert(MR * D * 4 * MG <= STAGE_BYTES, "the end-of-piece merge fits the consumed stage");
   static_assert(QNQ * M * 128 <= STAGE_BYTES, "the query rows fit one stage");
   static_assert(D % 128 == 0, "FP8 rows are whole 128-byte planes");
+  static constexpr int QAREA = 0;                  // no query rows kept outside the ring
 };
 
 // D += A(16x32, row) * B(32x8, col), E4M3 inputs (4 per register), fp32 accumulation.  Fragments
@@ -138,7 +139,7 @@ __global__ void __launch_bounds__(GqaF8Cfg<D, NH8>::THREADS, 1)
   gqa_setup<C>(smem, &tm_k, &tm_v, &tm_q, a, pargs);
 
   if (warp == C::NCW) {
-    gqa_produce<C, LW>(smem, &tm_k, &tm_v, &tm_q, a, pargs);
+    gqa_produce<C, LW, 1>(smem, &tm_k, &tm_v, &tm_q, a, pargs);
   } else {
     // ------------------------------------------------------------ consumers
     const int ct = tid;
@@ -179,7 +180,7 @@ __global__ void __launch_bounds__(GqaF8Cfg<D, NH8>::THREADS, 1)
       const int s = j % C::NS;
       if constexpr (LW) {  // the call's limit, and the give-up protocol of ring_wait
         const int wr = ring_wait(&full[s], (j / C::NS) & 1, a.wait_ns, status);
-        if (wr == RING_LATE) gqa_consumer_drain<C>(smem, j);
+        if (wr == RING_LATE) gqa_consumer_drain<C, 1>(smem, j, a);
         if (wr != RING_OK) break;
       } else {
         if (!mbar_wait(&full[s], (j / C::NS) & 1, status)) break;
@@ -422,7 +423,8 @@ __global__ void __launch_bounds__(GqaF8Cfg<D, NH8>::THREADS, 1)
             }
         }
         named_bar(1, C::NCW * 32);
-        gqa_merge_out<C, MQ>(mg, sm_ml, mt, a, ct, a.vscale / PSCALE);
+        const MergeRows rows = {mt.slot, mt.b, mt.i0, mt.nq, mt.hq0, mt.ghead, 0};
+        gqa_merge_out<C, MQ>(mg, sm_ml, rows, a, ct, a.vscale / PSCALE);
         fence_proxy_async_smem();  // generic writes to the stage buffer precede its next TMA fill
       } else if (masked && own) {
         fence_proxy_async_smem();  // the zeroed V rows precede the next TMA fill of this stage

@@ -47,12 +47,22 @@ cudaError_t launch_split_kernel(int grid, const CUtensorMap &tm_k, const CUtenso
 
 // Q == 1 (decode) runs the kernel compiled without the per-position row logic; a wait limit other
 // than the default runs the instantiation whose producer takes it as an argument (LW).
+template <int D, bool LW, int MT>
+cudaError_t launch_split_mt(int grid, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const CUtensorMap &tm_q,
+                            const GqaArgs &a, cudaStream_t stream) {
+  using C = GqaCfgOf<D, MT>;
+  return a.Q > 1 ? launch_split_kernel<C, gqa_split_kernel<D, true, LW, MT>>(grid, tm_k, tm_v, tm_q, a, stream)
+                 : launch_split_kernel<C, gqa_split_kernel<D, false, LW, MT>>(grid, tm_k, tm_v, tm_q, a, stream);
+}
+
+// Tiles paired in one sequence (a.mt == 2) exist for head_dim up to 128.
 template <int D, bool LW>
 cudaError_t launch_split_lw(int grid, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const CUtensorMap &tm_q,
                             const GqaArgs &a, cudaStream_t stream) {
-  using C = GqaCfg<D>;
-  return a.Q > 1 ? launch_split_kernel<C, gqa_split_kernel<D, true, LW>>(grid, tm_k, tm_v, tm_q, a, stream)
-                 : launch_split_kernel<C, gqa_split_kernel<D, false, LW>>(grid, tm_k, tm_v, tm_q, a, stream);
+  if constexpr (D <= 128) {
+    if (a.mt == 2) return launch_split_mt<D, LW, 2>(grid, tm_k, tm_v, tm_q, a, stream);
+  }
+  return launch_split_mt<D, LW, 1>(grid, tm_k, tm_v, tm_q, a, stream);
 }
 
 template <int D>
@@ -88,7 +98,7 @@ cudaError_t launch_f8_split_any(int grid, const CUtensorMap &tm_k, const CUtenso
 template <int D>
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t stream) {
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = pdl_config(dim3(a.nparts), dim3(COMBINE_THREADS), 0, stream, attr);
+  cudaLaunchConfig_t cfg = pdl_config(dim3(a.nparts), dim3(a.mt * PART_HEADS * 32), 0, stream, attr);
   return cudaLaunchKernelEx(&cfg, gqa_combine_kernel<D>, a);
 }
 

@@ -107,7 +107,7 @@ struct MlaTcSmem {
   static_assert(BYTES <= 232448, "fits the 227 KB opt-in shared memory of one CTA");
 };
 
-// StageMeta fields as used here: nq = 1 marks a query stage; pad0 (score buffers) = the ring slot
+// StageMeta fields as used here: nq = 1 marks a query stage; aux (score buffers) = the ring slot
 // holding the stage's cache rows.
 __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
     mla_tc_split_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_q,
@@ -463,7 +463,7 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
             StageMeta &si = sinfo[sb];
             si = mt;
             si.end = 0;
-            si.pad0 = s;
+            si.aux = s;
             if (sb) rs1 = s; else rs0 = s;
             mbar_arrive(&s_full[sb]);  // releases sinfo; the phase completes with the scores' commit
             last_js = mt.last;
@@ -506,7 +506,7 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
       const bool first = mt.first, last = mt.last, masked = mt.masked;
       const int tok0 = mt.tok0, tok_lo = mt.tok_lo, tok_hi = mt.tok_hi;
       const uint32_t badmask = mt.badmask;
-      const int b = mt.b, h0 = mt.hq0, nh = mt.ghead, hv = mt.i0, slot = mt.slot, rslot = mt.pad0;
+      const int b = mt.b, h0 = mt.hq0, nh = mt.ghead, hv = mt.i0, slot = mt.slot, rslot = mt.aux;
       if (first) {
         m = -INFINITY;
         l = 0.f;

@@ -57,12 +57,12 @@ def test_workspace_size(pa):
     ws = lambda *a: pa.pa_workspace_size(pa.PA_KIND_GQA, *a)
     g = ws(32, 64, 8, 128, 16384, 32, 0)
     assert g > 0
-    # two partial slots of 16 heads per share: independent of batch, heads and context,
-    # growing with head_dim and with an explicit share count (automatic mode: 256 shares)
+    # two partial slots of 32 rows (two 16-row tiles) per share: independent of batch, heads and
+    # context, growing with head_dim and with an explicit share count (automatic mode: 256 shares)
     assert ws(64, 64, 8, 128, 16384, 32, 0) == g
     assert ws(32, 64, 8, 128, 131072, 32, 0) == g
     assert ws(32, 64, 8, 128, 16384, 32, 256) == g
-    assert 256 * 2 * 16 * 128 * 4 <= g < 256 * 2 * 16 * 128 * 4 + (1 << 16)
+    assert 256 * 2 * 32 * 128 * 4 <= g < 256 * 2 * 32 * 128 * 4 + (1 << 17)  # + descriptors and LSEs
     assert ws(32, 64, 8, 128, 16384, 32, 4) < g
     assert ws(32, 64, 8, 128, 16384, 32, 512) > g
     assert ws(32, 64, 8, 256, 16384, 32, 0) > g

@@ -28,10 +28,10 @@ def _noalloc(pa, g, w, out, lse, num_splits=0):
         int(num_splits), torch.cuda.current_stream().cuda_stream)
 
 
-@pytest.mark.parametrize("window,num_splits", [(0, 0), (100, 0), (0, 2000)])
+@pytest.mark.parametrize("window,num_splits", [(0, 0), (100, 0), (0, 960)])
 def test_noalloc_matches_workspace_entry_point_twice(window, num_splits):
-    """Automatic shares, a window, and 2000 explicit shares: a workspace of about 31.5 MiB, so the
-    last shares' partials sit at the top of the 32 MiB array."""
+    """Automatic shares, a window, and 960 explicit shares: a workspace of about 31.7 MB of the
+    33.5 MB array, so the last shares' partials sit near its top."""
     import paged_kv_attention_19_gb300 as pa
     w = synth.make_gqa(4242 + window, [1, 31, 32, 33, 64, 100, 685, 1000, 5000, 20000], 16, 2, 128, 32,
                        window=window)
@@ -53,7 +53,7 @@ def test_noalloc_matches_workspace_entry_point_twice(window, num_splits):
         assert np.array_equal(l.view(np.uint32), ref_l.view(np.uint32)), "lse bits differ from pa_decode_gqa"
 
 
-@pytest.mark.parametrize("num_splits", [1100, 4096])
+@pytest.mark.parametrize("num_splits", [600, 4096])
 def test_noalloc_refuses_a_workspace_larger_than_its_scratch(num_splits):
     """A valid small workload (head_dim 256, pools sized to its pages) whose share count needs more
     than the array: refused before any device work, outputs untouched.  Were the size check ever
