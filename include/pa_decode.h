@@ -75,9 +75,11 @@
  *     the same (kind, shape, max_context_len, page_size, num_splits).  Its
  *     contents need no initialisation and are overwritten by each call;
  *     calls sharing one workspace must be ordered on one stream.  The GQA
- *     workspace depends on head_dim and num_splits only (two fp32 partial
- *     results of 32 rows -- two 16-row tiles of query rows -- per share: 32 KB
- *     per share at head_dim 128, about 8.5 MB in automatic mode).  The MLA workspace holds two fp32 partial
+ *     workspace holds two fp32 partial results of 32 rows -- two 16-row tiles
+ *     of query rows -- per share (32 KB per share at head_dim 128, about 8.5 MB
+ *     in automatic mode) and two int32 tables with an entry per (row, KV head,
+ *     tile) for up to 64 query positions (2 KB per (row, KV head)); it does
+ *     not depend on the context lengths.  The MLA workspace holds two fp32 partial
  *     results of min(num_heads, 128) heads x 256 columns per share (256 KB
  *     per share for 128 heads, 64 MB in automatic mode), plus q_abs, q_lo and
  *     o_lat in bf16 (3.1 KB per (row, head)) and two int32 tables of where

@@ -50,14 +50,15 @@ int gqa_stage_tokens(int D, bool fp8) { return fp8 ? (D <= 128 ? 128 : 64) : (D 
 
 struct GqaPlan {
   int nsub, nparts_max;
-  size_t off_desc, off_part_lse, off_part_o, total;
+  size_t off_desc, off_part_lse, off_part_o, off_seq, total;
 };
 
 // Shape checks shared by pa_workspace_size and pa_decode_gqa; PA_OK or an error code.
-// The workspace holds the header, one descriptor per partition and two fp32
-// partial slots (32 rows -- two 16-row tiles -- x head_dim, plus their LSEs) per
-// partition: its size depends on head_dim and the partition count only, not on
-// batch or context.
+// The workspace holds the header, one descriptor per partition, two fp32 partial
+// slots (32 rows -- two 16-row tiles -- x head_dim, plus their LSEs) per
+// partition, and two int32 tables of where each sequence's pieces are: one
+// entry each per (row, KV head, tile) for the largest query count a call may
+// have (kMaxQueryPositions).  Its size does not depend on the context lengths.
 int gqa_shape(int batch, int Hq, int Hkv, int D, int max_ctx, int P, int num_splits, GqaPlan *pl) {
   if (batch < 0 || Hq <= 0 || Hkv <= 0 || max_ctx < 0 || num_splits < 0) return PA_ERR_INVALID_ARGUMENT;
   if (Hq % Hkv != 0) return PA_ERR_INVALID_ARGUMENT;
@@ -75,6 +76,9 @@ int gqa_shape(int batch, int Hq, int Hkv, int D, int max_ctx, int P, int num_spl
   off = round_up(off + np * 2 * PART_ROWS * sizeof(float), 256);
   pl->off_part_o = off;
   off = round_up(off + np * 2 * PART_ROWS * (size_t)D * sizeof(float), 256);
+  pl->off_seq = off;
+  const size_t max_seqs = (size_t)(batch > 0 ? batch : 1) * Hkv * kMaxQueryPositions * pl->nsub;
+  off = round_up(off + 2 * max_seqs * sizeof(int32_t), 256);
   pl->total = off;
   return PA_OK;
 }
@@ -235,6 +239,9 @@ int gqa_call(const void *q, const void *k_pool, const void *v_pool, const int32_
   GqaPartDesc *desc = reinterpret_cast<GqaPartDesc *>(ws + pl.off_desc);
   float *part_lse = reinterpret_cast<float *>(ws + pl.off_part_lse);
   float *part_o = reinterpret_cast<float *>(ws + pl.off_part_o);
+  const int hs = num_kv_heads * nseqh;  // sequences per row
+  int32_t *seq_first = reinterpret_cast<int32_t *>(ws + pl.off_seq);
+  int32_t *seq_last = seq_first + (size_t)batch * hs;
 
   GqaArgs ga;
   ga.q = static_cast<const uint16_t *>(q);
@@ -245,6 +252,8 @@ int gqa_call(const void *q, const void *k_pool, const void *v_pool, const int32_
   ga.part_o = part_o;
   ga.part_lse = part_lse;
   ga.desc = desc;
+  ga.seq_first = seq_first;
+  ga.seq_last = seq_last;
   ga.batch = batch;
   ga.max_pages_per_seq = max_pages_per_seq;
   ga.num_pages = num_pages;
@@ -263,10 +272,7 @@ int gqa_call(const void *q, const void *k_pool, const void *v_pool, const int32_
   ga.log2_page = ilog2(P);
   ga.log2_bh = ilog2(BH);
   ga.nparts = nparts;
-  {
-    const int hs = num_kv_heads * nseqh;
-    ga.hg = hs < nparts ? hs : nparts;
-  }
+  ga.hg = hs < nparts ? hs : nparts;
   {
     const long long unit_bytes = (long long)BH * D * 2 * esz;  // K and V of one unit of one KV head
     const long long piece_bytes = f8.on ? kPieceCostBytesF8 : kPieceCostBytes;
@@ -282,6 +288,9 @@ int gqa_call(const void *q, const void *k_pool, const void *v_pool, const int32_
   ca.part_o = part_o;
   ca.part_lse = part_lse;
   ca.desc = desc;
+  ca.seq_first = seq_first;
+  ca.seq_last = seq_last;
+  ca.context_lens = context_lens;
   ca.status = &hdr->status;
   ca.Hq = num_q_heads;
   ca.G = ga.G;
@@ -294,6 +303,9 @@ int gqa_call(const void *q, const void *k_pool, const void *v_pool, const int32_
   ca.ntile = ntile;
   ca.mt = mt;
   ca.nseqh = nseqh;
+  ca.hs = hs;
+  ca.max_context_len = max_context_len;
+  ca.nblocks = batch * hs;
 
   cudaError_t e;
   if (t_ev_before) {

@@ -83,6 +83,8 @@ struct GqaArgs {
   float *part_o;                // [nparts, 2, 16, D] fp32
   float *part_lse;              // [nparts, 2, 16] fp32, log2 units
   GqaPartDesc *desc;            // [nparts]
+  int32_t *seq_first;           // [B, sequences per row]: -1 whole piece; else 2 x CTA + slot of the first piece
+  int32_t *seq_last;            // [B, sequences per row]: CTA holding the last piece of a split sequence
   int batch, max_pages_per_seq, num_pages, max_context_len, window;
   int Hq, Hkv, G, nsub;
   int Q;                        // query positions per row (1: decode; > 1: verify, causal within them)
@@ -298,6 +300,15 @@ __device__ __forceinline__ void gqa_produce(uint8_t *smem, const CUtensorMap *tm
     // the sequence's tightest key bounds: its first position ends first, its last starts last
     const int hi_min = pos_hi(cur.L, a.Q, tl.i0), lo_max = pos_lo(cur.L, a.Q, tlz.i0 + tlz.nq - 1, a.window);
     const int slot = (cur.starts && cur.ends) ? -1 : (npieces == 0 ? 0 : 1);
+    if (lane == 0) {
+      // where the combine kernel finds the sequence: written whole (one piece), or merged from the
+      // partial slots of CTAs first, first + hg, ..., last
+      const size_t si = (size_t)cur.b * pargs.hs + cur.hs;
+      if (cur.starts)
+        a.seq_first[si] = slot < 0 ? -1 : (int32_t)blockIdx.x * 2 + slot;
+      else if (cur.ends)
+        a.seq_last[si] = (int32_t)blockIdx.x;
+    }
     const int T0 = cur.ub << a.log2_bh;
     const int tok_lo = max(cur.lo, T0), tok_hi = min(cur.L, cur.ue << a.log2_bh);
     const int n_stages = (cur.ue - cur.ub + nbox - 1) / nbox;
@@ -1062,106 +1073,91 @@ struct CombineArgs {
   const float *part_o;
   const float *part_lse;
   const GqaPartDesc *desc;
+  const int32_t *seq_first, *seq_last;  // where each sequence's pieces are (written by the split kernel)
+  const int32_t *context_lens;
   uint32_t *status;  // the workspace status word: OR of every CTA's bits
   int Hq, G, nsub, nparts, hg;
   int Q, gt, qt, ntile, mt, nseqh;
+  int hs, max_context_len;  // sequences per row; the call's bound on the context lengths
+  int nblocks;              // batch x hs: one block per sequence
 };
 
-// One block per split CTA c.  Block c merges the sequence that CTA c's last
-// piece begins, if that piece does not also end it: the sequence's pieces are
-// CTA c's slot (1 if the CTA has several pieces, else 0) and slot 0 of CTAs
-// c + hg, c + 2 hg, ... (the same head in the following groups) up to the
-// first one whose first piece ends the sequence.
-// Warp w handles row w of the sequence's partial slots, i.e. MMA row w % 16 of its tile w / 16
-// (one warp per row, so the rows' few dependent loads from L2 overlap instead of queueing; the
-// block has 16 warps per tile of a sequence): weights exp2(lse_k - M), then
-// o = sum_k w_k o_k / sum_k w_k in ascending k, each lane owning D/32 dims.
+// One block per sequence (row b, sequence q of the row).  A sequence that one piece covered was
+// written by the split kernel; a split one is merged here from the partial slots of CTAs first,
+// first + hg, ..., last (its pieces in ascending token order; a CTA in between whose range held no
+// visible key left an empty slot, lse -inf, that weighs nothing).  Warp w handles row w of the
+// sequence's slots, i.e. MMA row w % 16 of its tile w / 16, each lane owning D/32 dims: an online
+// log-sum-exp merge (running max, rescaled sum and accumulator) whose loads of one partial -- its
+// LSE and values -- are independent of the others', so after the table lookup the merge is one
+// trip to L2.  The indices read from the tables are range-checked.
 constexpr int COMBINE_THREADS = PART_ROWS * 32;  // the largest block: two tiles
 template <int D>
 __global__ void __launch_bounds__(COMBINE_THREADS) gqa_combine_kernel(const CombineArgs a) {
-  pdl_wait();               // the split kernel's partials and descriptors are visible from here on
-  pdl_launch_dependents();  // a following kernel (MLA: the W_UV projection) may stage its inputs
-  const int c = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (c == 0 && warp == 0) {
-    uint32_t s = 0;
-    for (int i = lane; i < a.nparts; i += 32) s |= a.desc[i].status;
+  pdl_wait();               // the split kernel's partials, tables and descriptors are visible from here on
+  pdl_launch_dependents();  // a following kernel may stage its inputs
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (blockIdx.x == 0 && warp == 0) {
+    uint32_t st = 0;
+    for (int i = lane; i < a.nparts; i += 32) st |= a.desc[i].status;
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) s |= __shfl_xor_sync(FULL, s, o);
-    if (lane == 0) *a.status = s;
+    for (int o = 16; o >= 1; o >>= 1) st |= __shfl_xor_sync(FULL, st, o);
+    if (lane == 0) *a.status = st;
   }
-  const GqaPartDesc d0 = a.desc[c];
-  const uint32_t np = d0.flags & DESC_PIECES;
-  if (np == 0 || !(d0.flags & DESC_LAST_STARTS) || (d0.flags & DESC_LAST_ENDS)) return;
-  // the later pieces of the sequence are in CTAs c + hg, c + 2 hg, ... (same head, next groups)
-  int k = -1;  // pieces: CTA c + i hg holds piece i, i < k
-  for (int base = 1; c + base * a.hg < a.nparts && k < 0; base += 32) {
-    const int i = c + (base + lane) * a.hg;
-    bool hit = false;
-    if (i < a.nparts) {
-      const uint32_t f = a.desc[i].flags;
-      hit = (f & DESC_PIECES) != 0 && (f & DESC_FIRST_ENDS) != 0;
-    }
-    const uint32_t m = __ballot_sync(FULL, hit);
-    if (m) k = base + __ffs(m);
-  }
-  if (k < 0) return;  // not reachable for a consistent partition
-  const int first_slot = np >= 2 ? 1 : 0;
-  const int g = d0.last_hs / a.nseqh;
-  const int h = warp;                                   // the row of the partial slots
-  const int t = (d0.last_hs % a.nseqh) * a.mt + h / PART_HEADS;  // its tile
-  if (t >= a.ntile) return;                             // a sequence with one tile of two
+  const int b = blockIdx.x / a.hs, q = blockIdx.x % a.hs;
+  const size_t si = (size_t)b * a.hs + q;
+  const int L = a.context_lens[b], f = a.seq_first[si], cl = a.seq_last[si];
+  const int c0 = f >> 1;
+  if (clamp_len(L, a.max_context_len) == 0 || f < 0 || c0 >= a.nparts || cl < c0 || cl >= a.nparts ||
+      (cl - c0) % a.hg != 0)
+    return;  // an empty row, a sequence written whole, or (only if the split kernel gave up) a stale entry
+  const int k = (cl - c0) / a.hg + 1;  // pieces
+  const int g = q / a.nseqh;
+  const int h = warp;                                // the row of the partial slots
+  const int t = (q % a.nseqh) * a.mt + h / PART_HEADS;  // its tile
+  if (t >= a.ntile) return;                          // a sequence with one tile of two
   const Tile tl = tile_of(t, a.G, a.nsub, a.Q, a.qt);
-  const int hq0 = g * a.G + tl.h0;
+  const int r = h % PART_HEADS;  // the MMA row of the tile
+  if (r >= tl.nq * a.gt || r % a.gt >= tl.nh) return;
   constexpr int PER = D / 32;  // 2, 4 or 8 consecutive dims per lane
-  {
-    const int r = h % PART_HEADS;  // the MMA row of the tile
-    if (r >= tl.nq * a.gt || r % a.gt >= tl.nh) return;
-    float M = -INFINITY;
-    for (int i = lane; i < k; i += 32) {
-      const size_t pi = i == 0 ? (size_t)c * 2 + first_slot : (size_t)(c + i * a.hg) * 2;
-      M = fmaxf(M, a.part_lse[pi * PART_ROWS + h]);
-    }
+  float M = -INFINITY, Z = 0.f, acc[PER];
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, o));
-    float Z = 0.f;
-    for (int i = lane; i < k; i += 32) {
-      const size_t pi = i == 0 ? (size_t)c * 2 + first_slot : (size_t)(c + i * a.hg) * 2;
-      const float l = a.part_lse[pi * PART_ROWS + h];
-      Z += (l == -INFINITY || M == -INFINITY) ? 0.f : fast_exp2(l - M);
-    }
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) Z += __shfl_xor_sync(FULL, Z, o);
-    float acc[PER];
-#pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+  for (int e = 0; e < PER; ++e) acc[e] = 0.f;
 #pragma unroll 4
-    for (int i = 0; i < k; ++i) {
-      const size_t pi = i == 0 ? (size_t)c * 2 + first_slot : (size_t)(c + i * a.hg) * 2;
-      const float l = a.part_lse[pi * PART_ROWS + h];
-      const float wc = (l == -INFINITY || M == -INFINITY) ? 0.f : fast_exp2(l - M);
-      const float *po = a.part_o + (pi * PART_ROWS + h) * D + lane * PER;
-      if constexpr (PER == 2) {
-        const float2 x = *reinterpret_cast<const float2 *>(po);
-        acc[0] += wc * x.x;
-        acc[1] += wc * x.y;
-      } else {
+  for (int i = 0; i < k; ++i) {
+    const size_t pi = i == 0 ? (size_t)f : (size_t)(c0 + i * a.hg) * 2;
+    const float l = a.part_lse[pi * PART_ROWS + h];
+    float x[PER];
+    const float *po = a.part_o + (pi * PART_ROWS + h) * D + lane * PER;
+    if constexpr (PER == 2) {
+      const float2 v = *reinterpret_cast<const float2 *>(po);
+      x[0] = v.x;
+      x[1] = v.y;
+    } else {
 #pragma unroll
-        for (int e = 0; e < PER; e += 4) {
-          const float4 x = *reinterpret_cast<const float4 *>(po + e);
-          acc[e] += wc * x.x;
-          acc[e + 1] += wc * x.y;
-          acc[e + 2] += wc * x.z;
-          acc[e + 3] += wc * x.w;
-        }
+      for (int e = 0; e < PER; e += 4) {
+        const float4 v = *reinterpret_cast<const float4 *>(po + e);
+        x[e] = v.x;
+        x[e + 1] = v.y;
+        x[e + 2] = v.z;
+        x[e + 3] = v.w;
       }
     }
-    const float inv = Z > 0.f ? 1.f / Z : 0.f;
-    const size_t bh = ((size_t)d0.last_b * a.Q + tl.i0 + r / a.gt) * a.Hq + hq0 + r % a.gt;
-    uint32_t *dst = reinterpret_cast<uint32_t *>(a.out + bh * D + lane * PER);
+    if (l != -INFINITY) {
+      const float mn = fmaxf(M, l);
+      const float sc = M == -INFINITY ? 0.f : fast_exp2(M - mn);
+      const float wc = fast_exp2(l - mn);
+      M = mn;
+      Z = Z * sc + wc;
 #pragma unroll
-    for (int e = 0; e < PER; e += 2) dst[e / 2] = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
-    if (lane == 0 && a.lse) a.lse[bh] = (M == -INFINITY || Z == 0.f) ? -INFINITY : (M + __log2f(Z)) * LN2;
+      for (int e = 0; e < PER; ++e) acc[e] = acc[e] * sc + wc * x[e];
+    }
   }
+  const float inv = Z > 0.f ? 1.f / Z : 0.f;
+  const size_t bh = ((size_t)b * a.Q + tl.i0 + r / a.gt) * a.Hq + g * a.G + tl.h0 + r % a.gt;
+  uint32_t *dst = reinterpret_cast<uint32_t *>(a.out + bh * D + lane * PER);
+#pragma unroll
+  for (int e = 0; e < PER; e += 2) dst[e / 2] = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+  if (lane == 0 && a.lse) a.lse[bh] = (M == -INFINITY || Z == 0.f) ? -INFINITY : (M + __log2f(Z)) * LN2;
 }
 
 }  // namespace pa

@@ -98,7 +98,7 @@ cudaError_t launch_f8_split_any(int grid, const CUtensorMap &tm_k, const CUtenso
 template <int D>
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t stream) {
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = pdl_config(dim3(a.nparts), dim3(a.mt * PART_HEADS * 32), 0, stream, attr);
+  cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)a.nblocks), dim3(a.mt * PART_HEADS * 32), 0, stream, attr);
   return cudaLaunchKernelEx(&cfg, gqa_combine_kernel<D>, a);
 }
 

@@ -57,12 +57,14 @@ def test_workspace_size(pa):
     ws = lambda *a: pa.pa_workspace_size(pa.PA_KIND_GQA, *a)
     g = ws(32, 64, 8, 128, 16384, 32, 0)
     assert g > 0
-    # two partial slots of 32 rows (two 16-row tiles) per share: independent of batch, heads and
-    # context, growing with head_dim and with an explicit share count (automatic mode: 256 shares)
-    assert ws(64, 64, 8, 128, 16384, 32, 0) == g
+    # two partial slots of 32 rows (two 16-row tiles) per share, growing with head_dim and with an
+    # explicit share count (automatic mode: 256 shares), plus two int32 tables with one entry per
+    # (row, KV head, tile) for up to 64 query positions; independent of the context
+    assert abs(ws(64, 64, 8, 128, 16384, 32, 0) - g - 32 * 8 * 64 * 2 * 4) <= 256
     assert ws(32, 64, 8, 128, 131072, 32, 0) == g
     assert ws(32, 64, 8, 128, 16384, 32, 256) == g
-    assert 256 * 2 * 32 * 128 * 4 <= g < 256 * 2 * 32 * 128 * 4 + (1 << 17)  # + descriptors and LSEs
+    tables = 32 * 8 * 64 * 2 * 4
+    assert 256 * 2 * 32 * 128 * 4 + tables <= g < 256 * 2 * 32 * 128 * 4 + tables + (1 << 17)  # + descriptors, LSEs
     assert ws(32, 64, 8, 128, 16384, 32, 4) < g
     assert ws(32, 64, 8, 128, 16384, 32, 512) > g
     assert ws(32, 64, 8, 256, 16384, 32, 0) > g
