@@ -9,12 +9,14 @@
 // skipped.  The FP8 variant (row KERNEL-KV-QUANT) stores E4M3 codes of
 // value / scale, one float scale per pool.
 //
-// GB300 mapping: a pure copy, bound by HBM.  Each thread moves one 16-byte
-// vector; consecutive threads cover consecutive vectors of one (token, head)
-// row, so the reads of the new tokens and the writes into a page are
-// coalesced.  The grid is a multiple of the SM count with a grid-stride loop.
+// GB300 mapping: a pure copy, bound by HBM.  Each thread moves 16-byte vectors,
+// two per iteration with all their loads in flight together; consecutive
+// threads cover consecutive vectors of one (token, head) row, so the reads of
+// the new tokens and the writes into a page are coalesced.  The grid is the SM count times the blocks of the kernel that one
+// SM holds at once (one wave), with a grid-stride loop.
 #include <cmath>
 #include <cstdint>
+#include <cstring>
 
 #include "pa_common.cuh"
 #include "pa_decode.h"
@@ -24,25 +26,73 @@ namespace pa {
 
 namespace {
 
+struct Uint4x2 {
+  uint4 a, b;
+};
+__device__ __forceinline__ Uint4x2 make_uint4x2(uint4 a, uint4 b) { return {a, b}; }
+
+// Grid-stride loop over n_vec vectors of vec_per_token per token, U vectors per thread and
+// iteration: the loads of all U vectors (load(i, t, e) for vector e of token t, in bounds
+// whatever the slot) and of their tokens' slots are issued before any is stored
+// (store(dst, data)), so an iteration waits for one memory latency.  The (token, vector) pair
+// of each index advances by the grid stride without a division.  A negative slot is a padding
+// token; a slot past the pool is skipped and flagged.
+template <int U, typename Load, typename Store>
+__device__ __forceinline__ void write_loop(long long n_vec, int vec_per_token, const int64_t *__restrict__ slots,
+                                           long long n_slots, uint32_t *status, Load load, Store store) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  const long long i0 = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i0 >= n_vec) return;
+  const long long dt = stride / vec_per_token;
+  const int de = (int)(stride - dt * vec_per_token);
+  long long t = i0 / vec_per_token;
+  int e = (int)(i0 - t * vec_per_token);
+  for (long long i = i0; i < n_vec; i += U * stride) {
+    using Data = decltype(load(i, t, e));
+    Data d[U];
+    long long tu[U];
+    int eu[U];
+    bool has[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      has[u] = i + u * stride < n_vec;
+      tu[u] = has[u] ? t : tu[0];
+      eu[u] = has[u] ? e : eu[0];
+      d[u] = load(has[u] ? i + u * stride : i, tu[u], eu[u]);
+      t += dt;
+      e += de;
+      if (e >= vec_per_token) {
+        e -= vec_per_token;
+        ++t;
+      }
+    }
+    int64_t sl[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) sl[u] = slots[tu[u]];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (!has[u] || sl[u] < 0) continue;
+      if (sl[u] >= n_slots) {
+        if (status && eu[u] == 0) atomicOr(status, PA_DEV_BAD_SLOT);
+        continue;
+      }
+      store(sl[u] * (long long)vec_per_token + eu[u], d[u]);
+    }
+  }
+}
+
 // K and V rows: token t, head h, 16-byte vector e of D * 2 bytes.
 __global__ void __launch_bounds__(256) kv_write_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
                                                        const int64_t *__restrict__ slots, uint4 *k_pool,
                                                        uint4 *v_pool, long long n_vec, int vec_per_token,
                                                        long long n_slots, uint32_t *status) {
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_vec;
-       i += (long long)gridDim.x * blockDim.x) {
-    const long long t = i / vec_per_token;
-    const int e = (int)(i - t * vec_per_token);
-    const int64_t s = slots[t];
-    if (s < 0) continue;  // padding token
-    if (s >= n_slots) {
-      if (status && e == 0) atomicOr(status, PA_DEV_BAD_SLOT);
-      continue;
-    }
-    const long long dst = s * (long long)vec_per_token + e;
-    k_pool[dst] = k[i];
-    v_pool[dst] = v[i];
-  }
+  write_loop<2>(
+      n_vec, vec_per_token, slots, n_slots, status,
+      [&](long long i, long long, int) { return make_uint4x2(k[i], v[i]); },
+      [&](long long dst, const Uint4x2 &d) {
+        k_pool[dst] = d.a;
+        v_pool[dst] = d.b;
+      });
 }
 
 // MLA cache rows of 576 bf16 = 72 vectors: 64 from the latent (512) and 8 from the rope key (64).
@@ -52,63 +102,68 @@ __global__ void __launch_bounds__(256) mla_cache_write_kernel(const uint4 *__res
                                                               long long n_vec, long long n_slots,
                                                               uint32_t *status) {
   constexpr int ROW = 72, LAT = 64, ROPE = 8;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_vec;
-       i += (long long)gridDim.x * blockDim.x) {
-    const long long t = i / ROW;
-    const int e = (int)(i - t * ROW);
-    const int64_t s = slots[t];
-    if (s < 0) continue;
-    if (s >= n_slots) {
-      if (status && e == 0) atomicOr(status, PA_DEV_BAD_SLOT);
-      continue;
-    }
-    cache[s * ROW + e] = e < LAT ? c_lat[t * LAT + e] : k_rope[t * ROPE + (e - LAT)];
-  }
+  write_loop<2>(
+      n_vec, ROW, slots, n_slots, status,
+      [&](long long, long long t, int e) { return e < LAT ? c_lat[t * LAT + e] : k_rope[t * ROPE + (e - LAT)]; },
+      [&](long long dst, const uint4 &d) { cache[dst] = d; });
 }
 
-// FP8: thread i converts 16 values (two 16-byte bf16 vectors) of k and of v into one 16-byte
-// vector of E4M3 codes each: the fp32 quotient x / scale (correctly rounded division), then the
-// nearest code (ties to even), magnitudes beyond 448 saturated.
-__device__ __forceinline__ uint32_t quant4(uint32_t x0, uint32_t x1, float sc) {
-  const float2 a = make_float2(__fdiv_rn(__uint_as_float(x0 << 16), sc), __fdiv_rn(__uint_as_float(x0 & 0xffff0000u), sc));
-  const float2 b = make_float2(__fdiv_rn(__uint_as_float(x1 << 16), sc), __fdiv_rn(__uint_as_float(x1 & 0xffff0000u), sc));
+// FP8: thread i converts 8 values (one 16-byte bf16 vector) of k and of v into 8 bytes of E4M3
+// codes each, so that a warp's loads and its stores are both contiguous: the fp32 quotient
+// x / scale (correctly rounded division), then the nearest code (ties to even), magnitudes
+// beyond 448 saturated.  A pool scale that is a power of
+// two with a normal reciprocal (the host checks) divides as a product with that reciprocal: both
+// round the same exact value once, so the codes are identical.
+struct Fp8Scale {
+  float sc;   // the pool's scale
+  float rcp;  // 1 / sc when exact, else 0
+};
+
+__device__ __forceinline__ float quot(float x, Fp8Scale s) { return s.rcp != 0.f ? x * s.rcp : __fdiv_rn(x, s.sc); }
+
+__device__ __forceinline__ uint32_t quant4(uint32_t x0, uint32_t x1, Fp8Scale s) {
+  const float2 a = make_float2(quot(__uint_as_float(x0 << 16), s), quot(__uint_as_float(x0 & 0xffff0000u), s));
+  const float2 b = make_float2(quot(__uint_as_float(x1 << 16), s), quot(__uint_as_float(x1 & 0xffff0000u), s));
   const uint32_t lo = __nv_cvt_float2_to_fp8x2(a, __NV_SATFINITE, __NV_E4M3);
   const uint32_t hi = __nv_cvt_float2_to_fp8x2(b, __NV_SATFINITE, __NV_E4M3);
   return (lo & 0xffffu) | (hi << 16);
 }
 
-__device__ __forceinline__ uint4 quant16(uint4 x0, uint4 x1, float sc) {
-  return make_uint4(quant4(x0.x, x0.y, sc), quant4(x0.z, x0.w, sc), quant4(x1.x, x1.y, sc), quant4(x1.z, x1.w, sc));
-}
+__device__ __forceinline__ uint2 quant8(uint4 x, Fp8Scale s) { return make_uint2(quant4(x.x, x.y, s), quant4(x.z, x.w, s)); }
 
 __global__ void __launch_bounds__(256) kv_write_fp8_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
-                                                           const int64_t *__restrict__ slots, uint4 *k_pool,
-                                                           uint4 *v_pool, long long n_vec, int vec_per_token,
-                                                           long long n_slots, float k_scale, float v_scale,
-                                                           uint32_t *status) {
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_vec;
-       i += (long long)gridDim.x * blockDim.x) {
-    const long long t = i / vec_per_token;
-    const int e = (int)(i - t * vec_per_token);
-    const int64_t s = slots[t];
-    if (s < 0) continue;
-    if (s >= n_slots) {
-      if (status && e == 0) atomicOr(status, PA_DEV_BAD_SLOT);
-      continue;
-    }
-    const long long dst = s * (long long)vec_per_token + e;
-    k_pool[dst] = quant16(k[2 * i], k[2 * i + 1], k_scale);
-    v_pool[dst] = quant16(v[2 * i], v[2 * i + 1], v_scale);
-  }
+                                                           const int64_t *__restrict__ slots, uint2 *k_pool,
+                                                           uint2 *v_pool, long long n_vec, int vec_per_token,
+                                                           long long n_slots, Fp8Scale k_scale,
+                                                           Fp8Scale v_scale, uint32_t *status) {
+  write_loop<2>(
+      n_vec, vec_per_token, slots, n_slots, status,
+      [&](long long i, long long, int) { return make_uint4x2(k[i], v[i]); },
+      [&](long long dst, const Uint4x2 &d) {
+        k_pool[dst] = quant8(d.a, k_scale);
+        v_pool[dst] = quant8(d.b, v_scale);
+      });
 }
 
-int grid_for(long long n_vec) {
-  int dev = 0, sms = 0;
+// Blocks of 256 threads for n_vec vectors: at most one wave of the kernel's resident blocks.
+template <typename Kernel>
+int grid_for(Kernel kernel, long long n_vec) {
+  int dev = 0, sms = 0, per_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return -1;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, 0) != cudaSuccess || per_sm <= 0) return -1;
   const long long want = (n_vec + 255) / 256;
-  const long long cap = (long long)sms * 8;
+  const long long cap = (long long)sms * per_sm;
   return (int)(want < cap ? want : cap);
+}
+
+// The reciprocal of a scale that is a normal power of two (exact and normal itself), else 0.
+Fp8Scale fp8_scale(float sc) {
+  uint32_t b;
+  std::memcpy(&b, &sc, 4);
+  const uint32_t e = (b >> 23) & 0xffu;
+  const bool pow2 = (b & 0x807fffffu) == 0 && e >= 1 && e <= 253;  // sc = 2^(e - 127), 1 / sc = 2^(127 - e)
+  return {sc, pow2 ? 1.0f / sc : 0.f};
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -130,8 +185,8 @@ extern "C" int pa_kv_write(const void *k, const void *v, const int64_t *slot_map
     return PA_ERR_MISALIGNED;
   const int vec_per_token = num_kv_heads * head_dim / 8;
   const long long n_vec = (long long)num_tokens * vec_per_token;
-  const int grid = pa::grid_for(n_vec);
-  if (grid <= 0) return pa::cuda_fail(cudaSuccess);
+  const int grid = pa::grid_for(pa::kv_write_kernel, n_vec);
+  if (grid <= 0) return pa::cuda_fail(cudaGetLastError());
   pa::note_launches(0);
   if (const cudaError_t ce = pa::profile_mark(true, stream); ce != cudaSuccess) return pa::cuda_fail(ce);
   pa::kv_write_kernel<<<grid, 256, 0, stream>>>(
@@ -157,16 +212,16 @@ extern "C" int pa_kv_write_fp8(const void *k, const void *v, const int64_t *slot
   if (!pa::aligned16(k) || !pa::aligned16(v) || !pa::aligned16(k_pool) || !pa::aligned16(v_pool) ||
       (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) || (reinterpret_cast<uintptr_t>(status) & 3u))
     return PA_ERR_MISALIGNED;
-  const int vec_per_token = num_kv_heads * head_dim / 16;  // 16-byte vectors of codes
+  const int vec_per_token = num_kv_heads * head_dim / 8;  // 16-byte bf16 vectors, 8 bytes of codes each
   const long long n_vec = (long long)num_tokens * vec_per_token;
-  const int grid = pa::grid_for(n_vec);
-  if (grid <= 0) return pa::cuda_fail(cudaSuccess);
+  const int grid = pa::grid_for(pa::kv_write_fp8_kernel, n_vec);
+  if (grid <= 0) return pa::cuda_fail(cudaGetLastError());
   pa::note_launches(0);
   if (const cudaError_t ce = pa::profile_mark(true, stream); ce != cudaSuccess) return pa::cuda_fail(ce);
   pa::kv_write_fp8_kernel<<<grid, 256, 0, stream>>>(
-      static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping, static_cast<uint4 *>(k_pool),
-      static_cast<uint4 *>(v_pool), n_vec, vec_per_token, (long long)num_pages * page_size, k_scale, v_scale,
-      status);
+      static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping, static_cast<uint2 *>(k_pool),
+      static_cast<uint2 *>(v_pool), n_vec, vec_per_token, (long long)num_pages * page_size,
+      pa::fp8_scale(k_scale), pa::fp8_scale(v_scale), status);
   if (const cudaError_t ce = cudaGetLastError(); ce != cudaSuccess) return pa::cuda_fail(ce);
   pa::note_launches(1);
   if (const cudaError_t ce = pa::profile_mark(false, stream); ce != cudaSuccess) return pa::cuda_fail(ce);
@@ -183,8 +238,8 @@ extern "C" int pa_mla_cache_write(const void *c_lat, const void *k_rope, const i
       (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) || (reinterpret_cast<uintptr_t>(status) & 3u))
     return PA_ERR_MISALIGNED;
   const long long n_vec = (long long)num_tokens * 72;
-  const int grid = pa::grid_for(n_vec);
-  if (grid <= 0) return pa::cuda_fail(cudaSuccess);
+  const int grid = pa::grid_for(pa::mla_cache_write_kernel, n_vec);
+  if (grid <= 0) return pa::cuda_fail(cudaGetLastError());
   pa::note_launches(0);
   if (const cudaError_t ce = pa::profile_mark(true, stream); ce != cudaSuccess) return pa::cuda_fail(ce);
   pa::mla_cache_write_kernel<<<grid, 256, 0, stream>>>(

@@ -115,15 +115,21 @@ def test_fp8_full_size_every_output():
 
 
 # ------------------------------------------------------------------------- the quantizing write
+@pytest.mark.filterwarnings("ignore:overflow encountered in divide:RuntimeWarning")  # the saturating cases
 @pytest.mark.parametrize("T,Hkv,D,P,pages,pad,ks,vs", [(1, 1, 16, 8, 1, 0, 1.0, 1.0),
                                                        (37, 2, 128, 16, 8, 5, 1.0, 0.5),
                                                        (300, 8, 128, 32, 16, 7, 0.37, 1.0 / 3),
                                                        (64, 4, 256, 32, 4, 0, 1.0 / 512, 2.5e-3),
-                                                       (1000, 3, 64, 256, 5, 11, 3e-5, 7.0)])
+                                                       (1000, 3, 64, 256, 5, 11, 3e-5, 7.0),
+                                                       (50, 2, 32, 16, 4, 3, 2.0 ** -126, 2.0 ** 127),
+                                                       (40, 2, 64, 16, 4, 0, 2.0 ** 126, 1e-40),
+                                                       (33, 1, 16, 8, 8, 2, 0.125, 2.0 ** -9)])
 def test_kv_write_fp8_bit_exact(T, Hkv, D, P, pages, pad, ks, vs):
     """Scale 1 divides exactly (the bf16 inputs hit E4M3 ties often: ties to even); 1/512 pushes
     |x| > 0.875 past 448 and 3e-5 nearly every value (saturation); 7 reaches the subnormal codes
-    and zero."""
+    and zero.  Powers of two from 2^-126 to 2^126 divide as products with their reciprocal; 2^127
+    (whose reciprocal is subnormal) and the subnormal scale 1e-40 take the division, and
+    0.125 / 2^-9 the product, each against the oracle's float32 quotient."""
     import paged_kv_attention_19_gb300 as pa
     w = synth.make_kv_write(600 + T, T, Hkv, D, P, pages, pad_every=pad)
     kp0 = np.full(w.pool_shape(), synth.E4M3_NAN, dtype=np.uint8)
