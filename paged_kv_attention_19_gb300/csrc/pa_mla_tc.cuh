@@ -26,9 +26,11 @@
 //     tokens, 128-byte swizzle, 72 KB) into the 2-slot ring;
 //   * warp 1, one thread issues the tensor-core work from a polling loop: the tcgen05.cp of a query
 //     stage, the 36 score MMAs of a stage (S = Q C^T, M = 128 heads, N = 64 tokens, K = 576) into
-//     one of two score buffers, in chunks of 3 planes, and, as soon as a stage's probabilities are
-//     in tensor memory, its P.V (P: 128 x 64 bf16 written over the stage's own scores, V: the
-//     stage's latent columns of this half, MN-major, N = 256) into the O columns;
+//     one of two score buffers, and, as soon as a stage's probabilities are in tensor memory, its
+//     P.V (P: 128 x 64 bf16 written over the stage's own scores, V: the stage's latent columns of
+//     this half, MN-major, N = 256) into the O columns.  With both operands in shared memory a
+//     score MMA reads 6 KB, so the MMAs keep the shared-memory port busy and every mbarrier test
+//     or shared-memory access of this thread waits behind them: the loop makes few of them;
 //   * warps 2-5, softmax: one thread per head row reads its 64 scores, keeps the fp32 running max
 //     and sum (rescaling its O row in tensor memory only when the max grows by more than 2^8),
 //     writes the probabilities as bf16 over the scores, and at the end of a piece reads O, divides
@@ -107,8 +109,8 @@ struct MlaTcSmem {
   static_assert(BYTES <= 232448, "fits the 227 KB opt-in shared memory of one CTA");
 };
 
-// StageMeta fields as used here: nq = 1 marks a query stage; aux (score buffers) = the ring slot
-// holding the stage's cache rows.
+// StageMeta fields as used here: nq = 1 marks a query stage; sinfo[b].aux = the ring slot whose
+// metadata and cache rows belong to the stage in score buffer b.
 __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
     mla_tc_split_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_q,
                         const MlaTcArgs a) {
@@ -355,8 +357,9 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ tensor-core issue (one thread)
     // A polling loop over the events the tensor-core work waits for.  P.V of the oldest stage goes
-    // first (it frees a ring slot and a score buffer); the 36 score MMAs of a stage go out in
-    // chunks of 3 planes, so a P.V whose probabilities are ready waits for at most one chunk.
+    // first (it frees a ring slot and a score buffer); the 36 score MMAs of a stage go out together.
+    // The metadata of a stage is read once, as two 16-byte words; what P.V needs of it stays in
+    // registers, and the softmax warps find the rest through the ring slot left in sinfo.
     if (lane == 0) {
       const uint64_t qd0 = tc_sdesc_sw128(smem_u32(smem + S::OFF_Q), 16, 1024);
       const uint32_t stage0 = smem_u32(smem + S::OFF_STAGE);
@@ -367,20 +370,21 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
       uint32_t kf = 0;    // pieces whose first scores were issued (q_full phases)
       uint32_t npp = 0;   // pieces whose first P.V was issued (o_free phases: one per earlier piece)
       uint32_t rs0 = 0, rs1 = 0;  // ring slots of the stages in score buffers 0 and 1
-      int plane = -1;     // >= 0: the scores of stage js are being issued, next plane
+      bool scores_due = false;  // stage js has started: its scores go out next
       bool last_js = false, ended = false;
+      uint32_t pvinfo = 0;  // per score buffer b: bit 2b = the stage is a piece's first, bit 2b + 1 = its column half
       uint64_t idle_since = 0;
       while (!(ended && jp == js)) {
         bool progress = false;
         if (jp < js && mbar_test(p_full, jp & 1)) {
           const int bp = jp & 1;
-          const StageMeta &ip = sinfo[bp];
-          const bool first = ip.first;
+          const bool first = (pvinfo >> (2 * bp)) & 1u;
+          const uint32_t hvp = (pvinfo >> (2 * bp + 1)) & 1u;
           if (!first || npp == 0 || mbar_test(o_free, (npp - 1) & 1)) {
             tc_fence_after();
             if (first) ++npp;
             const uint32_t sp = bp ? rs1 : rs0;
-            const uint64_t vd = tc_sdesc_sw128(stage0 + sp * C::STAGE_BYTES + ip.i0 * 4 * C::PLANE, C::PLANE, 1024);
+            const uint64_t vd = tc_sdesc_sw128(stage0 + sp * C::STAGE_BYTES + hvp * 4 * C::PLANE, C::PLANE, 1024);
 #pragma unroll
             for (int kk = 0; kk < C::ST / 16; ++kk)
               tc_mma_ts(tmem + C::TM_O, tmem + C::TM_S + bp * C::ST + 8 * kk, vd + (uint64_t)((kk * 16 * 128) >> 4),
@@ -392,48 +396,36 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
             progress = true;
           }
         }
-        if (!progress && plane >= 0) {
+        if (!progress && scores_due) {
           const int sb = js & 1;
           const uint64_t cd0 = tc_sdesc_sw128(stage0 + (sb ? rs1 : rs0) * C::STAGE_BYTES, 16, 1024);
           const uint32_t dS = tmem + C::TM_S + sb * C::ST;
-          // planes [P0, P0 + 3) with compile-time operand offsets
-          auto chunk = [&](auto p0c) {
-            constexpr int P0 = decltype(p0c)::value;
+          // all planes, with compile-time operand offsets
 #pragma unroll
-            for (int pp = 0; pp < 3; ++pp) {
+          for (int p = 0; p < C::NQK; ++p) {
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const int p = P0 + pp;
-                const uint64_t bd = cd0 + (uint64_t)((p * C::PLANE + 32 * kk) >> 4);
-                if (p < C::NQS)
-                  tc_mma_ss(dS, qd0 + (uint64_t)((p * C::QPLANE + 32 * kk) >> 4), bd, C::IDESC_S,
-                            (p | kk) != 0 ? 1u : 0u);
-                else
-                  tc_mma_ts(dS, tmem + C::TM_QT + ((p - C::NQS) * 4 + kk) * 8, bd, C::IDESC_S, 1u);
-              }
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t bd = cd0 + (uint64_t)((p * C::PLANE + 32 * kk) >> 4);
+              if (p < C::NQS)
+                tc_mma_ss(dS, qd0 + (uint64_t)((p * C::QPLANE + 32 * kk) >> 4), bd, C::IDESC_S,
+                          (p | kk) != 0 ? 1u : 0u);
+              else
+                tc_mma_ts(dS, tmem + C::TM_QT + ((p - C::NQS) * 4 + kk) * 8, bd, C::IDESC_S, 1u);
             }
-          };
-          if (plane == 0)
-            chunk(std::integral_constant<int, 0>{});
-          else if (plane == 3)
-            chunk(std::integral_constant<int, 3>{});
-          else
-            chunk(std::integral_constant<int, 6>{});
-          plane += 3;
-          if (plane == C::NQK) {
-            tc_commit(&s_full[sb]);
-            if (last_js) tc_commit(q_empty);  // the query may be replaced by the next piece's
-            plane = -1;
-            ++js;
           }
+          tc_commit(&s_full[sb]);
+          if (last_js) tc_commit(q_empty);  // the query may be replaced by the next piece's
+          scores_due = false;
+          ++js;
           progress = true;
         }
-        if (!progress && plane < 0 && !ended && mbar_test(&full[r % C::NS], (r / C::NS) & 1)) {
+        if (!progress && !scores_due && !ended && mbar_test(&full[r % C::NS], (r / C::NS) & 1)) {
           const int s = r % C::NS;
-          const StageMeta &mt = meta[s];
+          const int4 mf = *reinterpret_cast<const int4 *>(&meta[s].end);      // end, first, last, masked
+          const int4 mg = *reinterpret_cast<const int4 *>(&meta[s].badmask);  // badmask, i0, nq, aux
           const int sb = js & 1;
           const bool buf_free = js < 2 || mbar_test(&sbuf_free[sb], ((js >> 1) - 1) & 1);
-          if (mt.nq) {
+          if (mg.z) {
             // a query stage: planes 5-8 into tensor memory once the previous piece's scores are done
             if (kq == 0 || mbar_test(q_empty, (kq - 1) & 1)) {
               tc_fence_after();
@@ -448,26 +440,25 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
               ++r;
               progress = true;
             }
-          } else if (mt.end) {
+          } else if (mf.x) {
             if (buf_free) {
               tc_fence_after();
-              sinfo[sb].end = 1;
+              sinfo[sb].aux = s;  // the end marker's slot
               mbar_arrive(&s_full[sb]);  // the softmax warps stop at this stage
               mbar_arrive(&s_full[sb]);
               ended = true;
               progress = true;
             }
-          } else if (buf_free && (!mt.first || mbar_test(q_full, kf & 1))) {
+          } else if (buf_free && (!mf.y || mbar_test(q_full, kf & 1))) {
             tc_fence_after();
-            if (mt.first) ++kf;
-            StageMeta &si = sinfo[sb];
-            si = mt;
-            si.end = 0;
-            si.aux = s;
+            if (mf.y) ++kf;
+            sinfo[sb].aux = s;
+            pvinfo = (pvinfo & ~(3u << (2 * sb))) | ((uint32_t)(mf.y != 0) << (2 * sb)) |
+                     ((uint32_t)(mg.y & 1) << (2 * sb + 1));
             if (sb) rs1 = s; else rs0 = s;
             mbar_arrive(&s_full[sb]);  // releases sinfo; the phase completes with the scores' commit
-            last_js = mt.last;
-            plane = 0;
+            last_js = mf.z != 0;
+            scores_due = true;
             ++r;
             progress = true;
           }
@@ -501,12 +492,14 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
       const int sb = j & 1;
       if (!mbar_wait(&s_full[sb], (j >> 1) & 1, status)) break;
       tc_fence_after();
-      const StageMeta &mt = sinfo[sb];
+      // the stage's metadata stays in its ring slot until the stage's P.V has completed
+      const int rslot = sinfo[sb].aux;
+      const StageMeta &mt = meta[rslot];
       if (mt.end) break;
       const bool first = mt.first, last = mt.last, masked = mt.masked;
       const int tok0 = mt.tok0, tok_lo = mt.tok_lo, tok_hi = mt.tok_hi;
       const uint32_t badmask = mt.badmask;
-      const int b = mt.b, h0 = mt.hq0, nh = mt.ghead, hv = mt.i0, slot = mt.slot, rslot = mt.aux;
+      const int b = mt.b, h0 = mt.hq0, nh = mt.ghead, hv = mt.i0, slot = mt.slot;
       if (first) {
         m = -INFINITY;
         l = 0.f;
