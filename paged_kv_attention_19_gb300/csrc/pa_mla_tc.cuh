@@ -357,7 +357,8 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ tensor-core issue (one thread)
     // A polling loop over the events the tensor-core work waits for.  P.V of the oldest stage goes
-    // first (it frees a ring slot and a score buffer); the 36 score MMAs of a stage go out together.
+    // first (it frees a ring slot and a score buffer); the 36 score MMAs of a stage go out together,
+    // in the iteration that starts the stage.
     // The metadata of a stage is read once, as two 16-byte words; what P.V needs of it stays in
     // registers, and the softmax warps find the rest through the ring slot left in sinfo.
     if (lane == 0) {
@@ -395,29 +396,6 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
             ++jp;
             progress = true;
           }
-        }
-        if (!progress && scores_due) {
-          const int sb = js & 1;
-          const uint64_t cd0 = tc_sdesc_sw128(stage0 + (sb ? rs1 : rs0) * C::STAGE_BYTES, 16, 1024);
-          const uint32_t dS = tmem + C::TM_S + sb * C::ST;
-          // all planes, with compile-time operand offsets
-#pragma unroll
-          for (int p = 0; p < C::NQK; ++p) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t bd = cd0 + (uint64_t)((p * C::PLANE + 32 * kk) >> 4);
-              if (p < C::NQS)
-                tc_mma_ss(dS, qd0 + (uint64_t)((p * C::QPLANE + 32 * kk) >> 4), bd, C::IDESC_S,
-                          (p | kk) != 0 ? 1u : 0u);
-              else
-                tc_mma_ts(dS, tmem + C::TM_QT + ((p - C::NQS) * 4 + kk) * 8, bd, C::IDESC_S, 1u);
-            }
-          }
-          tc_commit(&s_full[sb]);
-          if (last_js) tc_commit(q_empty);  // the query may be replaced by the next piece's
-          scores_due = false;
-          ++js;
-          progress = true;
         }
         if (!progress && !scores_due && !ended && mbar_test(&full[r % C::NS], (r / C::NS) & 1)) {
           const int s = r % C::NS;
@@ -462,6 +440,29 @@ __global__ void __launch_bounds__(MlaTcCfg::THREADS, 1)
             ++r;
             progress = true;
           }
+        }
+        if (scores_due) {  // in the iteration that started the stage
+          const int sb = js & 1;
+          const uint64_t cd0 = tc_sdesc_sw128(stage0 + (sb ? rs1 : rs0) * C::STAGE_BYTES, 16, 1024);
+          const uint32_t dS = tmem + C::TM_S + sb * C::ST;
+          // all planes, with compile-time operand offsets
+#pragma unroll
+          for (int p = 0; p < C::NQK; ++p) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t bd = cd0 + (uint64_t)((p * C::PLANE + 32 * kk) >> 4);
+              if (p < C::NQS)
+                tc_mma_ss(dS, qd0 + (uint64_t)((p * C::QPLANE + 32 * kk) >> 4), bd, C::IDESC_S,
+                          (p | kk) != 0 ? 1u : 0u);
+              else
+                tc_mma_ts(dS, tmem + C::TM_QT + ((p - C::NQS) * 4 + kk) * 8, bd, C::IDESC_S, 1u);
+            }
+          }
+          tc_commit(&s_full[sb]);
+          if (last_js) tc_commit(q_empty);  // the query may be replaced by the next piece's
+          scores_due = false;
+          ++js;
+          progress = true;
         }
         if (progress) {
           idle_since = 0;
