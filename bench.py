@@ -54,7 +54,8 @@ WORKLOADS = ["tiny", "llama3-8b", "qwen3-32b", "hd256-window", "mla", "kv-write"
 KERNEL_SOURCES = {"gqa": ("pa_gqa.cuh", "pa_partition.cuh", "pa_common.cuh"),
                   "gqa_f8": ("pa_gqa_f8.cuh", "pa_gqa.cuh", "pa_partition.cuh", "pa_common.cuh"),
                   "mla": ("pa_mla_tc.cuh", "pa_tcgen05.cuh", "pa_mla.cu", "pa_gqa.cuh", "pa_partition.cuh",
-                          "pa_common.cuh")}
+                          "pa_common.cuh"),
+                  "write": ("pa_kv_write.cu", "pa_common.cuh")}
 
 
 def compute_dtype(w):
@@ -68,6 +69,8 @@ def compute_dtype(w):
 
 
 def kernel_kind(workload: str) -> str:
+    if workload.startswith("kv-write"):
+        return "write"
     return "mla" if workload == "mla" else "gqa_f8" if workload.endswith("-fp8") else "gqa"
 
 
