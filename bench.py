@@ -51,8 +51,8 @@ DEFAULT_WORKLOAD = "qwen3-32b"
 WORKLOADS = ["tiny", "llama3-8b", "qwen3-32b", "hd256-window", "mla", "kv-write", "qwen3-32b-verify4",
              "qwen3-32b-fp8", "kv-write-fp8"]
 # sources of the kernel each roofline line profiles (a change voids its committed ncu traffic)
-KERNEL_SOURCES = {"gqa": ("pa_gqa.cuh", "pa_partition.cuh", "pa_common.cuh"),
-                  "gqa_f8": ("pa_gqa_f8.cuh", "pa_gqa.cuh", "pa_partition.cuh", "pa_common.cuh"),
+KERNEL_SOURCES = {"gqa": ("pa_gqa.cuh", "pa_partition.cuh", "pa_common.cuh", "pa_api.cu"),
+                  "gqa_f8": ("pa_gqa_f8.cuh", "pa_gqa.cuh", "pa_partition.cuh", "pa_common.cuh", "pa_api.cu"),
                   "mla": ("pa_mla_tc.cuh", "pa_tcgen05.cuh", "pa_mla.cu", "pa_gqa.cuh", "pa_partition.cuh",
                           "pa_common.cuh"),
                   "write": ("pa_kv_write.cu", "pa_common.cuh")}

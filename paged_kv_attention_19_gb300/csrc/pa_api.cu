@@ -23,9 +23,14 @@ using namespace pa;
 constexpr int kMaxSplits = 4096;     // largest accepted explicit num_splits (partitions)
 constexpr int kAutoPartsMax = 256;   // automatic mode: one partition per SM, at most this many
 constexpr int kMaxQueryPositions = 64;  // verify: query positions per row
-// Fixed cost of one piece of work in the GQA partition (the Q load and the end-of-piece
-// merge, about 0.8 us of one SM), expressed as the KV bytes the SM streams meanwhile.
-constexpr long long kPieceCostBytes = 32 << 10;
+// Fixed cost of one piece of work in the GQA partition, expressed as the KV bytes an SM
+// streams meanwhile: the query load, the end-of-piece merge and the partial's share of the
+// combine, and the start-up and tail of a piece's stages.  Set by measurement (sweeps of the
+// qwen3-32b, hd256-window and llama3-8b decodes, and of the 4-position verify): a sequence of
+// one 16-row tile...
+constexpr long long kPieceCostBytes = 80 << 10;
+// ...and one of two paired tiles, whose pieces copy both tiles' query rows and merge twice.
+constexpr long long kPieceCostBytesPair = 192 << 10;
 // The same for FP8 pools, whose pieces cost more (the query split and a merge over twice
 // the token groups) while each byte carries twice the tokens.
 constexpr long long kPieceCostBytesF8 = 128 << 10;
@@ -275,7 +280,7 @@ int gqa_call(const void *q, const void *k_pool, const void *v_pool, const int32_
   ga.hg = hs < nparts ? hs : nparts;
   {
     const long long unit_bytes = (long long)BH * D * 2 * esz;  // K and V of one unit of one KV head
-    const long long piece_bytes = f8.on ? kPieceCostBytesF8 : kPieceCostBytes;
+    const long long piece_bytes = f8.on ? kPieceCostBytesF8 : mt == 2 ? kPieceCostBytesPair : kPieceCostBytes;
     ga.piece_cost = (int)((piece_bytes + unit_bytes - 1) / unit_bytes);
   }
   ga.qscale = scale * LOG2E * (f8.on ? f8.k : 1.f);
