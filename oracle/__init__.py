@@ -269,6 +269,146 @@ def kv_write_fp8(k, v, slots, k_pool, v_pool, k_scale: float, v_scale: float):
     return kv_write(e4m3_encode(kf.astype(np.float64)), e4m3_encode(vf.astype(np.float64)), slots, k_pool, v_pool)
 
 
+# ---------------------------------------------------------------------------------------------
+# NVFP4 KV cache (vllm.cpp kernel-matrix, row KERNEL-KV-QUANT: "Quantized KV cache, including FP8
+# and NVFP4").  The pages name the format only; this is the published NVFP4 layout read plainly:
+# 4-bit E2M1 values (1 sign, 2 exponent, 1 mantissa bit: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6),
+# one E4M3 scale per block of 16 consecutive values, and one fp32 scale per pool, so that
+# value = e2m1(code) * e4m3(block scale) * pool_scale.  A pool row (page slot, KV head) of D
+# values is D / 2 bytes of code pairs (the even dim in the low nibble), then D / 16 scale codes,
+# then zero bytes up to a multiple of 16 bytes (nvfp4_row_bytes).
+
+_E2M1_MAG = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def nvfp4_row_bytes(D: int) -> int:
+    """Bytes of one NVFP4 pool row of D values: codes and block scales, padded to 16 bytes."""
+    return (D // 2 + D // 16 + 15) // 16 * 16
+
+
+def e2m1_decode(codes) -> np.ndarray:
+    """Value of each 4-bit E2M1 code (float64), from the format's definition: exponent e, mantissa
+    m; e = 0: m / 2 (subnormal), else (1 + m / 2) * 2^(e - 1); bit 3 the sign."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64) & 15
+    e = (c >> 1) & 3
+    m = (c & 1).astype(np.float64)
+    val = np.where(e == 0, m * 0.5, (1.0 + m / 2.0) * np.exp2(e.astype(np.float64) - 1))
+    return np.where(c >> 3, -val, val)
+
+
+def e2m1_encode(y) -> np.ndarray:
+    """Nearest E2M1 code of each value: round to nearest, ties to the code with an even mantissa,
+    magnitudes above 6 saturate to 6, NaN maps to +0 (E2M1 has no NaN; a NaN input also makes its
+    block's scale NaN)."""
+    y = np.asarray(y, dtype=np.float64)
+    a = np.minimum(np.abs(np.nan_to_num(y, nan=0.0)), 6.0)
+    idx = np.searchsorted(_E2M1_MAG, a)                        # first magnitude >= a
+    hi = np.minimum(idx, 7)
+    lo = np.maximum(hi - 1, 0)
+    d_hi = _E2M1_MAG[hi] - a
+    d_lo = a - _E2M1_MAG[lo]
+    pick_lo = (d_lo < d_hi) | ((d_lo == d_hi) & ((lo & 1) == 0))
+    code = np.where(pick_lo, lo, hi)
+    code = code | np.where(np.signbit(y) & ~np.isnan(y), 8, 0)
+    return code.astype(np.uint8)
+
+
+def nvfp4_quantize_rows(x32, pool_scale: float):
+    """NVFP4 codes and block scales of float32 rows x32 [..., D] (D a multiple of 16), in float32
+    arithmetic, each step correctly rounded: per block of 16, its amax a, the scale code
+    e4m3((a / pool_scale) / 6); each value's code e2m1((x / pool_scale) / e4m3(scale)), all codes 0
+    where the scale decodes to 0.  Returns (codes [..., D] uint8 (one per value), scales [..., D / 16])."""
+    x = np.asarray(x32, dtype=np.float32)
+    D = x.shape[-1]
+    blocks = x.reshape(x.shape[:-1] + (D // 16, 16))
+    ps = np.float32(pool_scale)
+    with np.errstate(over="ignore", invalid="ignore", divide="ignore"):
+        a = np.max(np.abs(blocks), axis=-1)
+        t = (a / ps) / np.float32(6.0)
+        sc = e4m3_encode(t.astype(np.float64))
+        ds = e4m3_decode(sc).astype(np.float32)
+        y = (blocks / ps) / ds[..., None]
+    codes = e2m1_encode(y.astype(np.float64))
+    codes = np.where((ds == 0)[..., None], np.uint8(0), codes)
+    return codes.reshape(x.shape), sc
+
+
+def nvfp4_pack_rows(codes, scales) -> np.ndarray:
+    """Pool rows [..., nvfp4_row_bytes(D)] from per-value codes [..., D] and scales [..., D / 16]."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    D = codes.shape[-1]
+    R = nvfp4_row_bytes(D)
+    out = np.zeros(codes.shape[:-1] + (R,), dtype=np.uint8)
+    out[..., : D // 2] = (codes[..., 0::2] & 15) | ((codes[..., 1::2] & 15) << 4)
+    out[..., D // 2: D // 2 + D // 16] = scales
+    return out
+
+
+def nvfp4_decode_rows(rows, D: int, pool_scale: float) -> np.ndarray:
+    """Values (float64 [..., D]) of NVFP4 pool rows: e2m1(code) * e4m3(block scale) * pool_scale."""
+    r = np.asarray(rows, dtype=np.uint8)
+    pairs = r[..., : D // 2]
+    codes = np.stack([pairs & 15, pairs >> 4], axis=-1).reshape(r.shape[:-1] + (D,))
+    sc = e4m3_decode(r[..., D // 2: D // 2 + D // 16])
+    v = e2m1_decode(codes).reshape(r.shape[:-1] + (D // 16, 16)) * sc[..., None]
+    return v.reshape(r.shape[:-1] + (D,)) * float(np.float32(pool_scale))
+
+
+def kv_write_nvfp4(k, v, slots, k_pool, v_pool, k_scale: float, v_scale: float):
+    """NVFP4 paged KV write: token t's bf16 rows k[t], v[t] ([T, Hkv, D]) are quantized per KV
+    head (nvfp4_quantize_rows) and stored as pool rows at slot slots[t] (negative: padding).
+    Returns new pools ([num_pages, P, Hkv, nvfp4_row_bytes(D)])."""
+    kq = nvfp4_pack_rows(*nvfp4_quantize_rows(synth_bf16_to_f32(k), k_scale))
+    vq = nvfp4_pack_rows(*nvfp4_quantize_rows(synth_bf16_to_f32(v), v_scale))
+    return kv_write(kq, vq, slots, k_pool, v_pool)
+
+
+def gqa_nvfp4(q, k_rows, v_rows, block_table, context_lens, scale: float, k_scale: float, v_scale: float,
+              window: int = 0, rows=None, num_query: int = 1):
+    """GQA decode (or multi-query verify) over an NVFP4 cache, in float64: the attention of the
+    decode oracle with keys and values nvfp4_decode_rows of their pool rows.  Returns
+    (o [n, D], lse [n])."""
+    q = np.asarray(q, dtype=np.uint16)
+    D = q.shape[-1]
+    K = nvfp4_decode_rows(k_rows, D, k_scale)
+    V = nvfp4_decode_rows(v_rows, D, v_scale)
+    return _gqa_dense_values(q, K, V, block_table, context_lens, scale, window, rows, num_query)
+
+
+def _gqa_dense_values(q, K, V, block_table, context_lens, scale, window, rows, num_query):
+    """The decode oracle over pools of float64 values K, V [num_pages, P, Hkv, D], per (row,
+    position, head): scores over the row's visible keys, max, exp, sum, weighted values."""
+    if num_query == 1 and q.ndim == 3:
+        q = q[:, None]
+    B, Q, Hq, D = q.shape
+    npg, P, Hkv, _ = K.shape
+    G = Hq // Hkv
+    qf = synth_bf16_to_f32(q).astype(np.float64)
+    bt = np.asarray(block_table, dtype=np.int64)
+    lens = np.asarray(context_lens, dtype=np.int64)
+    if rows is None:
+        rows = [(b, i, h) for b in range(B) for i in range(Q) for h in range(Hq)]
+    elif len(rows) and len(rows[0]) == 2:
+        rows = [(b, 0, h) for b, h in rows]
+    o = np.zeros((len(rows), D))
+    lse = np.full(len(rows), -np.inf)
+    for n, (b, i, h) in enumerate(rows):
+        hi = max(int(lens[b]) - Q + 1 + i, 0)
+        lo = max(hi - window, 0) if window > 0 else 0
+        if hi <= lo:
+            continue
+        t = np.arange(lo, hi)
+        pages = bt[b, t // P]
+        k = K[pages, t % P, h // G]
+        v = V[pages, t % P, h // G]
+        s = float(scale) * (k @ qf[b, i, h])
+        m = s.max()
+        p = np.exp(s - m)
+        o[n] = (p / p.sum()) @ v
+        lse[n] = m + np.log(p.sum())
+    return o, lse
+
+
 def synth_bf16_to_f32(bits) -> np.ndarray:
     """bf16 bit patterns (uint16) to float32 values (exact)."""
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
