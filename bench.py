@@ -49,10 +49,11 @@ FLUSH_BYTES = 512 << 20
 CLEAN_BYTES = 512 << 20
 DEFAULT_WORKLOAD = "qwen3-32b"
 WORKLOADS = ["tiny", "llama3-8b", "qwen3-32b", "hd256-window", "mla", "kv-write", "qwen3-32b-verify4",
-             "qwen3-32b-fp8", "kv-write-fp8"]
+             "qwen3-32b-fp8", "kv-write-fp8", "qwen3-32b-nvfp4", "kv-write-nvfp4"]
 # sources of the kernel each roofline line profiles (a change voids its committed ncu traffic)
 KERNEL_SOURCES = {"gqa": ("pa_gqa.cuh", "pa_partition.cuh", "pa_common.cuh", "pa_api.cu"),
                   "gqa_f8": ("pa_gqa_f8.cuh", "pa_gqa.cuh", "pa_partition.cuh", "pa_common.cuh", "pa_api.cu"),
+                  "gqa_fp4": ("pa_gqa_fp4.cuh", "pa_gqa.cuh", "pa_partition.cuh", "pa_common.cuh", "pa_api.cu"),
                   "mla": ("pa_mla_tc.cuh", "pa_tcgen05.cuh", "pa_mla.cu", "pa_gqa.cuh", "pa_partition.cuh",
                           "pa_common.cuh"),
                   "write": ("pa_kv_write.cu", "pa_common.cuh")}
@@ -62,7 +63,11 @@ def compute_dtype(w):
     """(dtype, description) of the arithmetic the timed path computes in."""
     import synth
     if isinstance(w, synth.KVWriteWorkload):
+        if w.nvfp4:
+            return "f32", "fp32 divides by the pool and block scales, e4m3 block-scale and e2m1 encode"
         return ("f32", "fp32 divide by the scale, e4m3 encode") if w.fp8 else ("bf16", "bf16 copy")
+    if getattr(w, "nvfp4", False):
+        return "bf16", "e2m1 x e4m3 block values dequantized exactly to bf16, bf16 tensor-core mma, f32 softmax"
     if getattr(w, "fp8", False):
         return "e4m3", "e4m3 tensor-core mma (two-term q and p), f32 softmax and accumulation"
     return "bf16", "bf16 tensor-core mma, f32 softmax and accumulation"
@@ -71,6 +76,8 @@ def compute_dtype(w):
 def kernel_kind(workload: str) -> str:
     if workload.startswith("kv-write"):
         return "write"
+    if workload.endswith("-nvfp4"):
+        return "gqa_fp4"
     return "mla" if workload == "mla" else "gqa_f8" if workload.endswith("-fp8") else "gqa"
 
 
@@ -147,7 +154,9 @@ def describe(w, name):
                 "head_dim": int(w.k.shape[2]), "page_size": w.page_size, "pool_pages": w.num_pages,
                 "slots": "prefill order: token t at position t % P of page perm[t // P]",
                 "algorithmic_bytes": w.algorithmic_bytes(), "seed": w.seed,
-                **({"pools": "fp8 e4m3 codes", "k_scale": w.k_scale, "v_scale": w.v_scale} if w.fp8 else {})}
+                **({"pools": "fp8 e4m3 codes", "k_scale": w.k_scale, "v_scale": w.v_scale} if w.fp8 else {}),
+                **({"pools": "nvfp4 rows (e2m1 code pairs, e4m3 scale per 16 values, 16-byte padding)",
+                    "k_scale": w.k_scale, "v_scale": w.v_scale} if w.nvfp4 else {})}
     if isinstance(w, synth.MLAWorkload):
         return {"workload": name, "batch": w.batch, "heads": w.num_heads, "q_dim": 192, "cache_dim": 576,
                 "v_dim": 128, "page_size": w.layout.page_size, "context": "uniform[1024,8192]",
@@ -157,13 +166,17 @@ def describe(w, name):
            "qwen3-32b": "loguniform[128,16384]", "hd256-window": "uniform[2048,32768], window 4096",
            "qwen3-32b-verify4": "loguniform[128,16384] (the qwen3-32b lengths), 4 query positions per row, "
                                 "causal among them",
-           "qwen3-32b-fp8": "loguniform[128,16384] (the qwen3-32b lengths)"}[name]
+           "qwen3-32b-fp8": "loguniform[128,16384] (the qwen3-32b lengths)",
+           "qwen3-32b-nvfp4": "loguniform[128,16384] (the qwen3-32b lengths)"}[name]
     return {"workload": name, "batch": w.batch, "query_positions": w.num_query, "q_heads": w.num_q_heads,
             "kv_heads": w.num_kv_heads,
             "head_dim": w.head_dim, "page_size": w.layout.page_size, "context": ctx, "window": w.window,
             "visible_tokens": w.visible_tokens(), "algorithmic_bytes": w.algorithmic_bytes(), "seed": w.seed,
             **({"kv_cache": "fp8 e4m3 codes, per-pool scales", "k_scale": w.k_scale, "v_scale": w.v_scale}
-               if w.fp8 else {"kv_cache": "bf16"})}
+               if w.fp8 else
+               {"kv_cache": "nvfp4 rows: e2m1 codes, e4m3 scale per 16 values, per-pool scales; algorithmic "
+                            "bytes count 9/16 byte per value, not the row padding",
+                "k_scale": w.k_scale, "v_scale": w.v_scale} if w.nvfp4 else {"kv_cache": "bf16"})}
 
 
 class ClockSampler:
@@ -234,7 +247,9 @@ class OracleSample:
         if isinstance(w, synth.KVWriteWorkload):
             # the oracle writes token by token into copies of the pools: time it on all tokens
             kp, vp = w.empty_pool(), w.empty_pool()
-            if w.fp8:
+            if w.nvfp4:
+                self.fn = lambda rows: oracle.kv_write_nvfp4(w.k, w.v, w.slots, kp, vp, w.k_scale, w.v_scale)
+            elif w.fp8:
                 self.fn = lambda rows: oracle.kv_write_fp8(w.k, w.v, w.slots, kp, vp, w.k_scale, w.v_scale)
             else:
                 self.fn = lambda rows: oracle.kv_write(w.k, w.v, w.slots, kp, vp)
@@ -249,7 +264,12 @@ class OracleSample:
         win = 0 if is_mla else w.window
         vis = [synth.visible_range(int(L), win, Q) for L in w.layout.context_lens]
         total_work = sum(hi - lo for lo, hi in vis) * H
-        if not is_mla and w.fp8:
+        if not is_mla and w.nvfp4:
+            self.fn = lambda rows: oracle.gqa_nvfp4(w.q, w.k_pool, w.v_pool, w.layout.block_table,
+                                                    w.layout.context_lens, w.scale, w.k_scale, w.v_scale,
+                                                    w.window, rows=[(b, i, h) for b, h in rows for i in range(Q)],
+                                                    num_query=Q)
+        elif not is_mla and w.fp8:
             self.fn = lambda rows: oracle.gqa_fp8(w.q, w.k_pool, w.v_pool, w.layout.block_table,
                                                   w.layout.context_lens, w.scale, w.k_scale, w.v_scale, w.window,
                                                   rows=[(b, i, h) for b, h in rows for i in range(Q)],
@@ -343,6 +363,9 @@ def run_ours(args, rank, local_rank, world):
         if w.mla:
             def call(c, r, s):
                 pa.pa_mla_cache_write(c, r, s, kp, status=status)
+        elif w.nvfp4:
+            def call(k, v, s):
+                pa.pa_kv_write_nvfp4(k, v, s, kp, vp, k_scale=w.k_scale, v_scale=w.v_scale, status=status)
         elif w.fp8:
             def call(k, v, s):
                 pa.pa_kv_write_fp8(k, v, s, kp, vp, k_scale=w.k_scale, v_scale=w.v_scale, status=status)
@@ -366,7 +389,12 @@ def run_ours(args, rank, local_rank, world):
         lse = torch.empty(w.q.shape[:-1], dtype=torch.float32, device="cuda")
         ws = pa.workspace_for_gqa(d.q, d.k, d.bt, args.num_splits)
         ins, outs = [d.q, d.bt, d.lens], [out, lse]
-        if w.fp8:
+        if w.nvfp4:
+            def call(q, bt, lens):
+                pa.pa_decode_gqa_nvfp4(q, d.k, d.v, bt, lens, out, lse, scale=w.scale, k_scale=w.k_scale,
+                                       v_scale=w.v_scale, window=w.window, workspace=ws,
+                                       num_splits=args.num_splits)
+        elif w.fp8:
             def call(q, bt, lens):
                 pa.pa_decode_gqa_fp8(q, d.k, d.v, bt, lens, out, lse, scale=w.scale, k_scale=w.k_scale,
                                      v_scale=w.v_scale, window=w.window, workspace=ws, num_splits=args.num_splits)
@@ -468,8 +496,10 @@ def run_ours(args, rank, local_rank, world):
         "config": dict(cfg, num_splits=args.num_splits or "auto", parallelism=f"replicas x{world}",
                        l2="between timed calls, outside the timed events: a 512 MB buffer written, then another 512 MB read"),
         "roofline": {"bound": "alu" if is_mla else "hbm",
-                     "kernel": (("kv_write_fp8_kernel" if w.fp8 else "kv_write_kernel") if is_write
+                     "kernel": (("kv_write_nvfp4_kernel" if w.nvfp4 else "kv_write_fp8_kernel" if w.fp8
+                                 else "kv_write_kernel") if is_write
                                 else "mla_tc_split_kernel" if is_mla
+                                else "gqa_fp4_split_kernel" if getattr(w, "nvfp4", False)
                                 else "gqa_f8_split_kernel" if getattr(w, "fp8", False) else "gqa_split_kernel"),
                      "achieved": round(kernel_gbs, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(kernel_gbs / peak, 4), "peak_source": f"hbm_gbs of {peak_kind}",

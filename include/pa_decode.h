@@ -7,8 +7,10 @@
  *   pa_decode_gqa           grouped-query attention, optional sliding window
  *   pa_verify_gqa           the same for several query positions per row
  *   pa_decode_gqa_fp8       both over an FP8 (E4M3) cache with per-pool scales
+ *   pa_decode_gqa_nvfp4     both over an NVFP4 cache (E2M1 values, E4M3 block scales)
  *   pa_decode_mla_absorbed  multi-head latent attention in the absorbed form
- *   pa_kv_write, pa_kv_write_fp8, pa_mla_cache_write   the paged writes
+ *   pa_kv_write, pa_kv_write_fp8, pa_kv_write_nvfp4, pa_mla_cache_write
+ *                           the paged writes
  *
  * The operations are the ones the following pages describe:
  *   - paged cache: K/V pools [pages, block_size, Hkv, D], per-request
@@ -29,8 +31,8 @@
  *     PR #938 "warp-cooperative two-pass MLA absorbed decode kernel",
  *     Schedule section, steps 1-7; kernel-matrix row KERNEL-ATTN-MLA-SPARSE,
  *     weight absorption as two batched contractions);
- *   - the paged writes and the FP8 form of the cache (kernel-matrix rows
- *     KERNEL-KV-CACHE and KERNEL-KV-QUANT);
+ *   - the paged writes and the FP8 and NVFP4 forms of the cache (kernel-matrix
+ *     rows KERNEL-KV-CACHE and KERNEL-KV-QUANT);
  *   - the raw pointer / shape / scalar / workspace / stream calling
  *     convention of the planned drop-in kernel ABI (kernel-matrix preamble).
  *
@@ -197,6 +199,36 @@ int pa_decode_gqa_fp8(const void *q, const void *k_pool, const void *v_pool,
                       int num_splits, void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * GQA decode and multi-query verify over an NVFP4 KV cache (vllm.cpp
+ * kernel-matrix, row KERNEL-KV-QUANT, "Quantized KV cache, including FP8 and
+ * NVFP4").  The pages name the format only; it is read as the published NVFP4
+ * layout: 4-bit E2M1 values (1 sign, 2 exponent, 1 mantissa bit: magnitudes 0,
+ * 0.5, 1, 1.5, 2, 3, 4, 6), one E4M3 scale per block of 16 consecutive values
+ * of a row, and one float scale per pool:
+ *   key = E2M1(code) * E4M3(block scale) * k_scale   (values: v_scale)
+ *   k_pool, v_pool [num_pages, page_size, num_kv_heads, R] uint8 rows,
+ *                R = round_up(head_dim / 2 + head_dim / 16, 16) (48, 80, 144 at
+ *                head_dim 64, 128, 256): head_dim / 2 bytes of code pairs (dim
+ *                2i in the low nibble of byte i, 2i + 1 in the high nibble),
+ *                then head_dim / 16 block-scale codes, then padding (not read)
+ *   k_scale, v_scale finite and > 0 (else PA_ERR_INVALID_ARGUMENT)
+ *   num_query    query positions per row as for pa_verify_gqa
+ * Every other argument, the workspace (pa_workspace_size(PA_KIND_GQA, ...)),
+ * the window and the error codes are those of pa_verify_gqa; head_dim in
+ * {64, 128, 256}.  Each E2M1 value times its E4M3 block scale is an exact
+ * bf16 value, so the keys and values enter bf16 tensor-core MMAs unrounded;
+ * the pool scales multiply the fp32 scores and outputs.  A block scale that
+ * decodes to NaN makes the values of its block NaN (as the format defines);
+ * such a row is read only where it is attended.
+ */
+int pa_decode_gqa_nvfp4(const void *q, const void *k_pool, const void *v_pool,
+                        const int32_t *block_table, const int32_t *context_lens, void *out,
+                        float *lse, int batch, int num_query, int num_q_heads, int num_kv_heads,
+                        int head_dim, int page_size, int num_pages, int max_pages_per_seq,
+                        int max_context_len, float scale, float k_scale, float v_scale, int window,
+                        int num_splits, void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * MLA absorbed decode (DeepSeek-V2-style geometry: 128 nope + 64 rope query
  * dims, 512 latent + 64 rope cache dims, 128 value dims per head).
  *   q            [batch, num_heads, 192] bf16: q_nope (128) || q_rope (64)
@@ -287,6 +319,30 @@ int pa_kv_write_fp8(const void *k, const void *v, const int64_t *slot_mapping, v
                     void *v_pool, int num_tokens, int num_kv_heads, int head_dim, int page_size,
                     int num_pages, float k_scale, float v_scale, uint32_t *status,
                     cudaStream_t stream);
+
+/*
+ * NVFP4 paged KV write: as pa_kv_write into NVFP4 pools (the row layout of
+ * pa_decode_gqa_nvfp4).  Each block of 16 consecutive bf16 values x of a
+ * (token, head) row of k (v) is quantized in fp32 arithmetic, every step
+ * correctly rounded, with s = k_scale (v_scale):
+ *   block scale code c = E4M3((amax / s) / 6), amax = the largest |x| of the
+ *                block; round to nearest, ties to even, saturating at 448; a
+ *                NaN in the block gives the NaN code 0x7F
+ *   value code   E2M1((x / s) / E4M3(c)), round to nearest, ties to even
+ *                (the code with the even mantissa bit), magnitudes above 6
+ *                saturating to 6, the sign bit taken from the quotient; every
+ *                code of the block 0 where E4M3(c) is 0 or NaN
+ *   k_pool, v_pool [num_pages, page_size, num_kv_heads, R] uint8 rows; the whole
+ *                row of a named slot is written, its padding bytes as zeros
+ *   k_scale, v_scale finite and > 0 (else PA_ERR_INVALID_ARGUMENT)
+ * head_dim in {64, 128, 256} (else PA_ERR_UNSUPPORTED); k and v 16-byte
+ * aligned, the pools 16-byte aligned.  slot_mapping, status and num_tokens as
+ * for pa_kv_write.
+ */
+int pa_kv_write_nvfp4(const void *k, const void *v, const int64_t *slot_mapping, void *k_pool,
+                      void *v_pool, int num_tokens, int num_kv_heads, int head_dim, int page_size,
+                      int num_pages, float k_scale, float v_scale, uint32_t *status,
+                      cudaStream_t stream);
 
 /*
  * MLA cache write: the 576-wide cache row of each new token is its latent

@@ -6,8 +6,8 @@ There is no CPU fallback: importing this package fails with ImportError if the
 library has not been built (``python paged_kv_attention_19_gb300/build.py``).
 
 Names follow the C ABI: ``pa_workspace_size``, ``pa_decode_gqa``,
-``pa_decode_mla_absorbed``, ``pa_verify_gqa``, ``pa_decode_gqa_fp8``, ``pa_decode_gqa_noalloc``,
-``pa_kv_write``, ``pa_kv_write_fp8``, ``pa_mla_cache_write``, ``pa_status_string``, ``pa_read_device_status``,
+``pa_decode_mla_absorbed``, ``pa_verify_gqa``, ``pa_decode_gqa_fp8``, ``pa_decode_gqa_nvfp4``,
+``pa_decode_gqa_noalloc``, ``pa_kv_write``, ``pa_kv_write_fp8``, ``pa_kv_write_nvfp4``, ``pa_mla_cache_write``, ``pa_status_string``, ``pa_read_device_status``,
 ``pa_set_profile_events``, ``pa_last_launch_count``, ``pa_set_wait_limit_ns``, ``pa_last_cuda_error``,
 ``pa_last_cuda_error_string``.  The tensor-taking
 functions accept torch tensors (device memory, the layouts of the header) and
@@ -46,6 +46,9 @@ SIGNATURES = {
                            _P]),
     "pa_decode_gqa_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _F, _F, _F, _I,
                                _I, _P, _Z, _P]),
+    "pa_decode_gqa_nvfp4": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _F, _F, _F, _I,
+                                 _I, _P, _Z, _P]),
+    "pa_kv_write_nvfp4": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _F, _P, _P]),
     "pa_kv_write": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
     "pa_kv_write_fp8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _F, _P, _P]),
     "pa_mla_cache_write": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
@@ -170,6 +173,36 @@ def pa_decode_gqa_fp8(q, k_pool, v_pool, block_table, context_lens, out, lse=Non
     _check(rc, "pa_decode_gqa_fp8")
 
 
+def pa_decode_gqa_nvfp4(q, k_pool, v_pool, block_table, context_lens, out, lse=None, *, scale: float,
+                        k_scale: float, v_scale: float, workspace, window: int = 0, num_splits: int = 0,
+                        max_context_len=None, stream=None) -> None:
+    """GQA decode (q [B, Hq, D]) or multi-query verify (q [B, Q, Hq, D]) over NVFP4 pools
+    [pages, P, Hkv, R] uint8 (R = nvfp4_row_bytes(D): code pairs, block scales, padding) whose
+    values are e2m1(code) * e4m3(block scale) * k_scale (keys; v_scale for values); out and lse
+    shaped like q without / with its last dim; the rest as for pa_verify_gqa."""
+    if q.dim() == 3:
+        B, Hq, D = q.shape
+        Q = 1
+    else:
+        B, Q, Hq, D = q.shape
+    num_pages, P, Hkv, _ = k_pool.shape
+    max_pages = block_table.shape[1]
+    if max_context_len is None:
+        max_context_len = max_pages * P
+    rc = lib.pa_decode_gqa_nvfp4(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table), _ptr(context_lens),
+                                 _ptr(out), _ptr(lse), B, Q, Hq, Hkv, D, P, num_pages, max_pages,
+                                 int(max_context_len), float(scale), float(k_scale), float(v_scale), int(window),
+                                 int(num_splits), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                 _stream(stream))
+    _check(rc, "pa_decode_gqa_nvfp4")
+
+
+def nvfp4_row_bytes(head_dim: int) -> int:
+    """Bytes of one NVFP4 pool row: head_dim / 2 code bytes and head_dim / 16 scale codes,
+    padded to a multiple of 16."""
+    return (head_dim // 2 + head_dim // 16 + 15) // 16 * 16
+
+
 def pa_decode_mla_absorbed(q, cache, w_uk, w_uv, block_table, context_lens, out, lse=None, *, scale: float,
                            workspace, num_splits: int = 0, max_context_len=None, stream=None) -> None:
     """MLA absorbed decode.  q [B, H, 192], cache [pages, P, 576], w_uk / w_uv [H, 128, 512] bf16;
@@ -205,6 +238,18 @@ def pa_kv_write_fp8(k, v, slot_mapping, k_pool, v_pool, *, k_scale: float, v_sca
     _check(lib.pa_kv_write_fp8(_ptr(k), _ptr(v), _ptr(slot_mapping), _ptr(k_pool), _ptr(v_pool), T, Hkv, D, P,
                                num_pages, float(k_scale), float(v_scale), _ptr(status), _stream(stream)),
            "pa_kv_write_fp8")
+
+
+def pa_kv_write_nvfp4(k, v, slot_mapping, k_pool, v_pool, *, k_scale: float, v_scale: float, status=None,
+                      stream=None) -> None:
+    """NVFP4 paged KV write.  k, v [T, Hkv, D] bf16; pools [pages, P, Hkv, nvfp4_row_bytes(D)] uint8
+    rows (E2M1 code pairs and E4M3 block scales of value / pool scale); the rest as for
+    pa_kv_write."""
+    T, Hkv, D = k.shape
+    num_pages, P, _, _ = k_pool.shape
+    _check(lib.pa_kv_write_nvfp4(_ptr(k), _ptr(v), _ptr(slot_mapping), _ptr(k_pool), _ptr(v_pool), T, Hkv, D,
+                                 P, num_pages, float(k_scale), float(v_scale), _ptr(status), _stream(stream)),
+           "pa_kv_write_nvfp4")
 
 
 def pa_mla_cache_write(c_lat, k_rope, slot_mapping, cache, *, status=None, stream=None) -> None:

@@ -34,6 +34,9 @@ constexpr long long kPieceCostBytesPair = 192 << 10;
 // The same for FP8 pools, whose pieces cost more (the query split and a merge over twice
 // the token groups) while each byte carries twice the tokens.
 constexpr long long kPieceCostBytesF8 = 128 << 10;
+// NVFP4 pools: a byte carries about 3.2 times the tokens of bf16 (head_dim 128: 80-byte rows),
+// so a piece's fixed cost is fewer bytes (a first setting near the bf16 figure times 80 / 256).
+constexpr long long kPieceCostBytesFp4 = 32 << 10;
 
 thread_local cudaEvent_t t_ev_before = nullptr;
 thread_local cudaEvent_t t_ev_after = nullptr;
@@ -50,8 +53,16 @@ int ilog2(int x) {
 }
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Tokens per stage of the split kernel (must match GqaCfg<D>::ST and GqaF8Cfg<D, *>::ST).
-int gqa_stage_tokens(int D, bool fp8) { return fp8 ? (D <= 128 ? 128 : 64) : (D <= 128 ? 64 : 32); }
+// Element formats of the K/V pools.
+enum PoolFmt { FMT_BF16 = 0, FMT_FP8 = 1, FMT_NVFP4 = 2 };
+
+// Tokens per stage of the split kernel (must match GqaCfg<D>::ST, GqaF8Cfg<D, *>::ST and
+// GqaFp4Cfg<D>::ST).
+int gqa_stage_tokens(int D, int fmt) { return fmt == FMT_FP8 ? (D <= 128 ? 128 : 64) : (D <= 128 ? 64 : 32); }
+
+// Bytes of an NVFP4 pool row of D values (must match nvfp4_row_bytes in pa_gqa_fp4.cuh): D / 2
+// bytes of code pairs, D / 16 block scales, zero padding to a multiple of 16 bytes.
+int nvfp4_row(int D) { return (D / 2 + D / 16 + 15) / 16 * 16; }
 
 struct GqaPlan {
   int nsub, nparts_max;
@@ -115,6 +126,21 @@ bool encode_pool_map(CUtensorMap *m, const void *base, int num_pages, int P, int
   cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
   CUresult r = fn(m, esz == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 4-D map over a [num_pages, P, H, R] pool of NVFP4 rows (R bytes each); box = (one whole row,
+// 1 head, BH tokens, 1 page), no swizzle: the box's rows land as consecutive R-byte rows.
+bool encode_nvfp4_map(CUtensorMap *m, const void *base, int num_pages, int P, int H, int R, int BH) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)R, (cuuint64_t)H, (cuuint64_t)P, (cuuint64_t)num_pages};
+  cuuint64_t strides[3] = {(cuuint64_t)R, (cuuint64_t)H * R, (cuuint64_t)P * H * R};
+  cuuint32_t box[4] = {(cuuint32_t)R, 1u, (cuuint32_t)BH, 1u};
+  cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -184,28 +210,29 @@ size_t pa_workspace_size(int kind, int batch, int num_q_heads, int num_kv_heads,
 
 namespace {
 
-// FP8 pool scales: one float per pool, each finite and positive.
-struct Fp8Scales {
-  bool on;
+// Pool format and scales: one float per pool (FP8 and NVFP4), each finite and positive.
+struct PoolScales {
+  int fmt;
   float k, v;
 };
 
 // GQA decode (Q == 1) and verify (Q > 1 query positions per row, causal among them), over
-// bf16 pools or (f8.on) FP8 E4M3 pools with per-pool scales.
+// bf16 pools, FP8 E4M3 pools or NVFP4 pools, the last two with per-pool scales.
 int gqa_call(const void *q, const void *k_pool, const void *v_pool, const int32_t *block_table,
              const int32_t *context_lens, void *out, float *lse, int batch, int Q, int num_q_heads,
              int num_kv_heads, int head_dim, int page_size, int num_pages, int max_pages_per_seq,
              int max_context_len, float scale, int window, int num_splits, void *workspace,
-             size_t workspace_bytes, cudaStream_t stream, Fp8Scales f8 = {false, 1.f, 1.f}) {
+             size_t workspace_bytes, cudaStream_t stream, PoolScales f8 = {FMT_BF16, 1.f, 1.f}) {
   t_last_launches = 0;
+  const bool fp8 = f8.fmt == FMT_FP8, fp4 = f8.fmt == FMT_NVFP4, scaled = fp8 || fp4;
   if (Q <= 0 || Q > kMaxQueryPositions) return Q <= 0 ? PA_ERR_INVALID_ARGUMENT : PA_ERR_UNSUPPORTED;
-  if (f8.on && !(std::isfinite(f8.k) && f8.k > 0.f && std::isfinite(f8.v) && f8.v > 0.f))
+  if (scaled && !(std::isfinite(f8.k) && f8.k > 0.f && std::isfinite(f8.v) && f8.v > 0.f))
     return PA_ERR_INVALID_ARGUMENT;
   if (batch == 0) return PA_OK;
   GqaPlan pl;
   int rc = gqa_shape(batch, num_q_heads, num_kv_heads, head_dim, max_context_len, page_size, num_splits, &pl);
   if (rc != PA_OK) return rc;
-  if (f8.on && head_dim != 128 && head_dim != 256) return PA_ERR_UNSUPPORTED;
+  if (fp8 && head_dim != 128 && head_dim != 256) return PA_ERR_UNSUPPORTED;
   if (!q || !k_pool || !v_pool || !block_table || !context_lens || !out || !workspace)
     return PA_ERR_INVALID_ARGUMENT;
   if (num_pages <= 0 || max_pages_per_seq <= 0 || !std::isfinite(scale)) return PA_ERR_INVALID_ARGUMENT;
@@ -217,7 +244,7 @@ int gqa_call(const void *q, const void *k_pool, const void *v_pool, const int32_
   if (workspace_bytes < pl.total) return PA_ERR_WORKSPACE_TOO_SMALL;
 
   const int D = head_dim, P = page_size;
-  const int ST = gqa_stage_tokens(D, f8.on);
+  const int ST = gqa_stage_tokens(D, f8.fmt);
   const int BH = P < ST ? P : ST;  // tokens per TMA box = per work unit
   // query tiles of at most 16 MMA rows: qt positions x gt heads of one KV head's group
   const int G = num_q_heads / num_kv_heads;
@@ -227,14 +254,16 @@ int gqa_call(const void *q, const void *k_pool, const void *v_pool, const int32_
   // a KV head with more than one tile has its tiles paired in one sequence (bf16 pools, head_dim
   // up to 128: both tiles' fragments fit the consumers' registers), so a page crosses shared
   // memory once for all of the head's rows
-  const int mt = (!f8.on && D <= 128 && ntile >= 2) ? 2 : 1;
+  const int mt = (!scaled && D <= 128 && ntile >= 2) ? 2 : 1;
   const int nseqh = (ntile + mt - 1) / mt;
   CUtensorMap tm_k, tm_v, tm_q;
-  const int esz = f8.on ? 1 : 2;
-  if (!encode_pool_map(&tm_k, k_pool, num_pages, P, num_kv_heads, D, BH, esz) ||
-      !encode_pool_map(&tm_v, v_pool, num_pages, P, num_kv_heads, D, BH, esz) ||
-      !encode_q_map(&tm_q, q, (long long)batch * Q, num_q_heads, D, gt, qt))
-    return PA_ERR_UNSUPPORTED;
+  const int esz = fp8 ? 1 : 2;
+  const bool maps_ok =
+      fp4 ? encode_nvfp4_map(&tm_k, k_pool, num_pages, P, num_kv_heads, nvfp4_row(D), BH) &&
+                encode_nvfp4_map(&tm_v, v_pool, num_pages, P, num_kv_heads, nvfp4_row(D), BH)
+          : encode_pool_map(&tm_k, k_pool, num_pages, P, num_kv_heads, D, BH, esz) &&
+                encode_pool_map(&tm_v, v_pool, num_pages, P, num_kv_heads, D, BH, esz);
+  if (!maps_ok || !encode_q_map(&tm_q, q, (long long)batch * Q, num_q_heads, D, gt, qt)) return PA_ERR_UNSUPPORTED;
   const int sms = sm_count();
   if (sms <= 0) return pa::cuda_fail(cudaSuccess);
   const int nparts = num_splits > 0 ? num_splits : (sms < kAutoPartsMax ? sms : kAutoPartsMax);
@@ -279,12 +308,15 @@ int gqa_call(const void *q, const void *k_pool, const void *v_pool, const int32_
   ga.nparts = nparts;
   ga.hg = hs < nparts ? hs : nparts;
   {
-    const long long unit_bytes = (long long)BH * D * 2 * esz;  // K and V of one unit of one KV head
-    const long long piece_bytes = f8.on ? kPieceCostBytesF8 : mt == 2 ? kPieceCostBytesPair : kPieceCostBytes;
+    // K and V of one unit of one KV head
+    const long long unit_bytes = (long long)BH * 2 * (fp4 ? nvfp4_row(D) : D * esz);
+    const long long piece_bytes = fp8 ? kPieceCostBytesF8
+                                  : fp4 ? kPieceCostBytesFp4
+                                        : mt == 2 ? kPieceCostBytesPair : kPieceCostBytes;
     ga.piece_cost = (int)((piece_bytes + unit_bytes - 1) / unit_bytes);
   }
-  ga.qscale = scale * LOG2E * (f8.on ? f8.k : 1.f);
-  ga.vscale = f8.on ? f8.v : 1.f;
+  ga.qscale = scale * LOG2E * (scaled ? f8.k : 1.f);
+  ga.vscale = scaled ? f8.v : 1.f;
   ga.wait_ns = t_wait_limit_ns;
 
   CombineArgs ca;
@@ -316,7 +348,9 @@ int gqa_call(const void *q, const void *k_pool, const void *v_pool, const int32_
   if (t_ev_before) {
     if (const cudaError_t ce = cudaEventRecord(t_ev_before, stream); ce != cudaSuccess) return pa::cuda_fail(ce);
   }
-  if (f8.on) {
+  if (fp4) {
+    e = launch_gqa_split_nvfp4(D, nparts, tm_k, tm_v, tm_q, ga, stream);
+  } else if (fp8) {
     e = D == 128 ? launch_gqa_split_fp8_d128(nparts, tm_k, tm_v, tm_q, ga, stream)
                  : launch_gqa_split_fp8_d256(nparts, tm_k, tm_v, tm_q, ga, stream);
   } else {
@@ -373,7 +407,18 @@ int pa_decode_gqa_fp8(const void *q, const void *k_pool, const void *v_pool, con
                       cudaStream_t stream) {
   return gqa_call(q, k_pool, v_pool, block_table, context_lens, out, lse, batch, num_query, num_q_heads,
                   num_kv_heads, head_dim, page_size, num_pages, max_pages_per_seq, max_context_len, scale, window,
-                  num_splits, workspace, workspace_bytes, stream, Fp8Scales{true, k_scale, v_scale});
+                  num_splits, workspace, workspace_bytes, stream, PoolScales{FMT_FP8, k_scale, v_scale});
+}
+
+int pa_decode_gqa_nvfp4(const void *q, const void *k_pool, const void *v_pool, const int32_t *block_table,
+                        const int32_t *context_lens, void *out, float *lse, int batch, int num_query,
+                        int num_q_heads, int num_kv_heads, int head_dim, int page_size, int num_pages,
+                        int max_pages_per_seq, int max_context_len, float scale, float k_scale, float v_scale,
+                        int window, int num_splits, void *workspace, size_t workspace_bytes,
+                        cudaStream_t stream) {
+  return gqa_call(q, k_pool, v_pool, block_table, context_lens, out, lse, batch, num_query, num_q_heads,
+                  num_kv_heads, head_dim, page_size, num_pages, max_pages_per_seq, max_context_len, scale, window,
+                  num_splits, workspace, workspace_bytes, stream, PoolScales{FMT_NVFP4, k_scale, v_scale});
 }
 
 int pa_decode_mla_absorbed(const void *q, const void *cache, const void *w_uk, const void *w_uv,

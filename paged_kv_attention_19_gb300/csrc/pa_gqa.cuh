@@ -105,6 +105,8 @@ template <int D_>
 struct GqaCfg {
   static constexpr int D = D_;
   static constexpr bool F8 = false;                // pools of bf16 values
+  static constexpr int ROWB = 128;                 // bytes of a token's row in one plane of a stage
+  static constexpr int XSTEP = 64;                 // tensor-map x of consecutive planes (bf16 values)
   static constexpr int M = PART_HEADS;             // MMA rows = query heads per subgroup
   static constexpr int MR = M;                     // rows per token group in the end-of-piece merge
   static constexpr int ST = D <= 128 ? 64 : 32;    // tokens per stage
@@ -251,8 +253,6 @@ template <class C, bool LW, int MT>
 __device__ __forceinline__ void gqa_produce(uint8_t *smem, const CUtensorMap *tm_k, const CUtensorMap *tm_v,
                                             const CUtensorMap *tm_q, const GqaArgs &a, const PartitionArgs &pargs) {
   using S = GqaSmem<C>;
-  constexpr int D = C::D;
-  constexpr bool F8 = C::F8;
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::OFF_BAR);
   uint64_t *empty = full + C::NS;
   StageMeta *meta = reinterpret_cast<StageMeta *>(smem + S::OFF_META);
@@ -410,15 +410,15 @@ __device__ __forceinline__ void gqa_produce(uint8_t *smem, const CUtensorMap *tm
         m.tok_hi = tok_hi;
         m.badmask = bad;
         m.masked = (tok0 < max(tok_lo, lo_max)) || (tok0 + C::ST > min(tok_hi, hi_min)) || bad != 0;
-        mbar_arrive_expect_tx(&full[s], (uint32_t)nvalid * (uint32_t)((D * (F8 ? 1 : 2) * 2) << a.log2_bh));
+        mbar_arrive_expect_tx(&full[s], (uint32_t)nvalid * (uint32_t)((C::NQ * C::ROWB * 2) << a.log2_bh));
       }
       __syncwarp();
       if (load) {
         const int pslot = btok & (P - 1);
-        uint8_t *dst = kdst + (lane << a.log2_bh) * 128;
+        uint8_t *dst = kdst + (lane << a.log2_bh) * C::ROWB;
 #pragma unroll
         for (int dq = 0; dq < C::NQ; ++dq) {
-          const int x = dq * (F8 ? 128 : 64);  // 128 bytes of the row per plane
+          const int x = dq * C::XSTEP;  // C::ROWB bytes of the row per plane
           tma_load_4d(dst + dq * C::PLANE, tm_k, x, g, pslot, phys, &full[s]);
           tma_load_4d(dst + dq * C::PLANE + C::KV_BYTES, tm_v, x, g, pslot, phys, &full[s]);
         }

@@ -43,6 +43,8 @@ template <int D_, int NH8_>
 struct GqaF8Cfg {
   static constexpr int D = D_;
   static constexpr bool F8 = true;                 // pools of E4M3 codes
+  static constexpr int ROWB = 128;                 // bytes of a token's row in one plane of a stage
+  static constexpr int XSTEP = 128;                // tensor-map x of consecutive planes (one-byte codes)
   static constexpr int NH8 = NH8_;
   static constexpr int M = PART_HEADS;             // rows of a partial slot
   static constexpr int MR = 8 * NH8;               // rows per token group in the end-of-piece merge

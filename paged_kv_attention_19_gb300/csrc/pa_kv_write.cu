@@ -34,7 +34,7 @@ __device__ __forceinline__ Uint4x2 make_uint4x2(uint4 a, uint4 b) { return {a, b
 // Grid-stride loop over n_vec vectors of vec_per_token per token, U vectors per thread and
 // iteration: the loads of all U vectors (load(i, t, e) for vector e of token t, in bounds
 // whatever the slot) and of their tokens' slots are issued before any is stored
-// (store(dst, data)), so an iteration waits for one memory latency.  The (token, vector) pair
+// (store(slot, e, data): vector e of the row at that slot), so an iteration waits for one memory latency.  The (token, vector) pair
 // of each index advances by the grid stride without a division.  A negative slot is a padding
 // token; a slot past the pool is skipped and flagged.
 template <int U, typename Load, typename Store>
@@ -76,7 +76,7 @@ __device__ __forceinline__ void write_loop(long long n_vec, int vec_per_token, c
         if (status && eu[u] == 0) atomicOr(status, PA_DEV_BAD_SLOT);
         continue;
       }
-      store(sl[u] * (long long)vec_per_token + eu[u], d[u]);
+      store(sl[u], eu[u], d[u]);
     }
   }
 }
@@ -89,9 +89,9 @@ __global__ void __launch_bounds__(256) kv_write_kernel(const uint4 *__restrict__
   write_loop<2>(
       n_vec, vec_per_token, slots, n_slots, status,
       [&](long long i, long long, int) { return make_uint4x2(k[i], v[i]); },
-      [&](long long dst, const Uint4x2 &d) {
-        k_pool[dst] = d.a;
-        v_pool[dst] = d.b;
+      [&](long long slot, int e, const Uint4x2 &d) {
+        k_pool[slot * vec_per_token + e] = d.a;
+        v_pool[slot * vec_per_token + e] = d.b;
       });
 }
 
@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(256) mla_cache_write_kernel(const uint4 *__res
   write_loop<2>(
       n_vec, ROW, slots, n_slots, status,
       [&](long long, long long t, int e) { return e < LAT ? c_lat[t * LAT + e] : k_rope[t * ROPE + (e - LAT)]; },
-      [&](long long dst, const uint4 &d) { cache[dst] = d; });
+      [&](long long slot, int e, const uint4 &d) { cache[slot * ROW + e] = d; });
 }
 
 // FP8: thread i converts 8 values (one 16-byte bf16 vector) of k and of v into 8 bytes of E4M3
@@ -139,9 +139,99 @@ __global__ void __launch_bounds__(256) kv_write_fp8_kernel(const uint4 *__restri
   write_loop<2>(
       n_vec, vec_per_token, slots, n_slots, status,
       [&](long long i, long long, int) { return make_uint4x2(k[i], v[i]); },
-      [&](long long dst, const Uint4x2 &d) {
-        k_pool[dst] = quant8(d.a, k_scale);
-        v_pool[dst] = quant8(d.b, v_scale);
+      [&](long long slot, int e, const Uint4x2 &d) {
+        k_pool[slot * vec_per_token + e] = quant8(d.a, k_scale);
+        v_pool[slot * vec_per_token + e] = quant8(d.b, v_scale);
+      });
+}
+
+// NVFP4: thread i quantizes block i (16 consecutive values of one (token, head) row: two 16-byte
+// bf16 vectors) of k and of v into 8 bytes of E2M1 code pairs and one E4M3 scale code, in fp32
+// with every step correctly rounded: the scale code of (amax / s) / 6, then each value's code of
+// (x / s) / E4M3(scale code).  The thread of a row's block 0 also writes the row's padding.
+struct Nvfp4Row {
+  int nb;        // blocks per row: head_dim / 16
+  int code_off;  // byte offset of the block scales in a row: head_dim / 2
+  int row;       // bytes per row (a multiple of 16)
+};
+
+// Nearest E2M1 code of y: ties to the code with the even mantissa bit, saturating at 6, the sign
+// bit from y's sign (y is never NaN here).
+__device__ __forceinline__ uint32_t e2m1_code(float y) {
+  const float a = fabsf(y);
+  const uint32_t m = a <= 0.25f ? 0u : a < 0.75f ? 1u : a <= 1.25f ? 2u : a < 1.75f ? 3u
+                   : a <= 2.5f ? 4u : a < 3.5f ? 5u : a <= 5.f ? 6u : 7u;
+  return m | ((__float_as_uint(y) >> 28) & 8u);
+}
+
+// Value of a non-negative, non-NaN E4M3 code (exact in fp32).
+__device__ __forceinline__ float e4m3_value(uint32_t c) {
+  const uint32_t e = c >> 3, m = c & 7u;
+  return e == 0 ? (float)m * 0.001953125f : __uint_as_float(((e + 120u) << 23) | (m << 20));
+}
+
+struct Nvfp4Block {
+  uint2 codes;
+  uint32_t scale;
+};
+
+__device__ __forceinline__ Nvfp4Block quant_nvfp4(uint4 x0, uint4 x1, Fp8Scale s) {
+  const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+  float y[16];
+  float amax = 0.f;
+  bool nan = false;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
+    amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
+    nan = nan || lo != lo || hi != hi;
+    y[2 * i] = quot(lo, s);
+    y[2 * i + 1] = quot(hi, s);
+  }
+  Nvfp4Block b;
+  if (nan) {
+    b.scale = 0x7Fu;
+    b.codes = make_uint2(0u, 0u);
+    return b;
+  }
+  b.scale = (uint32_t)__nv_cvt_float_to_fp8(__fdiv_rn(quot(amax, s), 6.f), __NV_SATFINITE, __NV_E4M3);
+  const float ds = e4m3_value(b.scale);
+  uint32_t c[2] = {0u, 0u};
+  if (ds != 0.f) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) c[i >> 3] |= e2m1_code(__fdiv_rn(y[i], ds)) << (4 * (i & 7));
+  }
+  b.codes = make_uint2(c[0], c[1]);
+  return b;
+}
+
+struct Uint4x4 {
+  uint4 k0, k1, v0, v1;
+};
+
+__global__ void __launch_bounds__(256) kv_write_nvfp4_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
+                                                             const int64_t *__restrict__ slots, uint8_t *k_pool,
+                                                             uint8_t *v_pool, long long n_blk, int blk_per_token,
+                                                             long long n_slots, Nvfp4Row r, Fp8Scale k_scale,
+                                                             Fp8Scale v_scale, uint32_t *status) {
+  write_loop<1>(
+      n_blk, blk_per_token, slots, n_slots, status,
+      [&](long long i, long long, int) { return Uint4x4{k[2 * i], k[2 * i + 1], v[2 * i], v[2 * i + 1]}; },
+      [&](long long slot, int e, const Uint4x4 &d) {
+        const int h = e / r.nb, blk = e - h * r.nb;
+        const long long row0 = (slot * (blk_per_token / r.nb) + h) * r.row;
+        const Nvfp4Block kb = quant_nvfp4(d.k0, d.k1, k_scale);
+        const Nvfp4Block vb = quant_nvfp4(d.v0, d.v1, v_scale);
+        *reinterpret_cast<uint2 *>(k_pool + row0 + blk * 8) = kb.codes;
+        *reinterpret_cast<uint2 *>(v_pool + row0 + blk * 8) = vb.codes;
+        k_pool[row0 + r.code_off + blk] = (uint8_t)kb.scale;
+        v_pool[row0 + r.code_off + blk] = (uint8_t)vb.scale;
+        if (blk == 0) {
+          for (int p = r.code_off + r.nb; p < r.row; p += 4) {
+            *reinterpret_cast<uint32_t *>(k_pool + row0 + p) = 0u;
+            *reinterpret_cast<uint32_t *>(v_pool + row0 + p) = 0u;
+          }
+        }
       });
 }
 
@@ -221,6 +311,37 @@ extern "C" int pa_kv_write_fp8(const void *k, const void *v, const int64_t *slot
   pa::kv_write_fp8_kernel<<<grid, 256, 0, stream>>>(
       static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping, static_cast<uint2 *>(k_pool),
       static_cast<uint2 *>(v_pool), n_vec, vec_per_token, (long long)num_pages * page_size,
+      pa::fp8_scale(k_scale), pa::fp8_scale(v_scale), status);
+  if (const cudaError_t ce = cudaGetLastError(); ce != cudaSuccess) return pa::cuda_fail(ce);
+  pa::note_launches(1);
+  if (const cudaError_t ce = pa::profile_mark(false, stream); ce != cudaSuccess) return pa::cuda_fail(ce);
+  return PA_OK;
+}
+
+extern "C" int pa_kv_write_nvfp4(const void *k, const void *v, const int64_t *slot_mapping, void *k_pool,
+                                 void *v_pool, int num_tokens, int num_kv_heads, int head_dim, int page_size,
+                                 int num_pages, float k_scale, float v_scale, uint32_t *status,
+                                 cudaStream_t stream) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || page_size <= 0 || num_pages <= 0)
+    return PA_ERR_INVALID_ARGUMENT;
+  if (!(std::isfinite(k_scale) && k_scale > 0.f && std::isfinite(v_scale) && v_scale > 0.f))
+    return PA_ERR_INVALID_ARGUMENT;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return PA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PA_OK;
+  if (!k || !v || !slot_mapping || !k_pool || !v_pool) return PA_ERR_INVALID_ARGUMENT;
+  if (!pa::aligned16(k) || !pa::aligned16(v) || !pa::aligned16(k_pool) || !pa::aligned16(v_pool) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) || (reinterpret_cast<uintptr_t>(status) & 3u))
+    return PA_ERR_MISALIGNED;
+  const pa::Nvfp4Row r = {head_dim / 16, head_dim / 2, (head_dim / 2 + head_dim / 16 + 15) / 16 * 16};
+  const int blk_per_token = num_kv_heads * r.nb;
+  const long long n_blk = (long long)num_tokens * blk_per_token;
+  const int grid = pa::grid_for(pa::kv_write_nvfp4_kernel, n_blk);
+  if (grid <= 0) return pa::cuda_fail(cudaGetLastError());
+  pa::note_launches(0);
+  if (const cudaError_t ce = pa::profile_mark(true, stream); ce != cudaSuccess) return pa::cuda_fail(ce);
+  pa::kv_write_nvfp4_kernel<<<grid, 256, 0, stream>>>(
+      static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping, static_cast<uint8_t *>(k_pool),
+      static_cast<uint8_t *>(v_pool), n_blk, blk_per_token, (long long)num_pages * page_size, r,
       pa::fp8_scale(k_scale), pa::fp8_scale(v_scale), status);
   if (const cudaError_t ce = cudaGetLastError(); ce != cudaSuccess) return pa::cuda_fail(ce);
   pa::note_launches(1);

@@ -29,6 +29,9 @@ cudaError_t launch_gqa_split_fp8_d128(int grid, const CUtensorMap &tm_k, const C
                                       const CUtensorMap &tm_q, const GqaArgs &a, cudaStream_t stream);
 cudaError_t launch_gqa_split_fp8_d256(int grid, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                                       const CUtensorMap &tm_q, const GqaArgs &a, cudaStream_t stream);
+// NVFP4 pools (head_dim 64, 128 or 256)
+cudaError_t launch_gqa_split_nvfp4(int D, int grid, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                                   const CUtensorMap &tm_q, const GqaArgs &a, cudaStream_t stream);
 cudaError_t launch_gqa_combine_d64(const CombineArgs &a, cudaStream_t stream);
 cudaError_t launch_gqa_combine_d128(const CombineArgs &a, cudaStream_t stream);
 cudaError_t launch_gqa_combine_d256(const CombineArgs &a, cudaStream_t stream);

@@ -29,6 +29,13 @@ Recipe (all counter-based, so any element can be regenerated on its own):
   127 finite ones (zeros, subnormals, 448 included), else one uniform over
   0x28..0x6F (values 0.25 .. 120, log-uniform).  Slots that must not be read
   hold the NaN code 0x7F.
+* NVFP4 pools hold row bytes drawn directly the same way.  A row of D values is
+  D / 2 code bytes, D / 16 block-scale codes and zero padding to a multiple of
+  16 bytes.  Output ``x`` of a code byte's stream gives the byte (``x & 255``:
+  two uniform 4-bit codes).  A scale byte's ``x`` gives, with probability 1/32
+  (bits 8-12 all zero), a code uniform over 0x00..0x4F (zero, the subnormals,
+  normals up to 7.5), else one uniform over 0x28..0x47 (0.25 .. 3.75).  Slots
+  that must not be read hold 0x7F in every byte (a NaN block scale).
 
 The workloads mirror the decode shapes of the pages: the Llama-3-8B / Qwen3-32B
 GQA geometries and the 576-wide (512 latent + 64 rope) MLA cache of
@@ -140,6 +147,33 @@ def _codes_range(state: int, start: int, n: int, chunk: int = 1 << 18) -> np.nda
     return out
 
 
+def nvfp4_row_bytes(head_dim: int) -> int:
+    """Bytes of one NVFP4 row (layout only): head_dim / 2 code bytes, head_dim / 16 scale codes,
+    zero padding to a multiple of 16."""
+    return (head_dim // 2 + head_dim // 16 + 15) // 16 * 16
+
+
+def nvfp4_bytes(state: int, index: np.ndarray, head_dim: int) -> np.ndarray:
+    """NVFP4 row bytes (uint8), one per ``index`` (its place in a row is index % row bytes), by
+    the recipe in the module docstring."""
+    R = nvfp4_row_bytes(head_dim)
+    o = (np.asarray(index, dtype=np.uint64) % np.uint64(R)).astype(np.int64)
+    x = splitmix64(state, index)
+    code = (x & np.uint64(255)).astype(np.uint8)
+    wide = ((x >> np.uint64(8)) & np.uint64(31)) == 0
+    r = x >> np.uint64(16)
+    sc = np.where(wide, r % np.uint64(0x50), np.uint64(0x28) + r % np.uint64(0x20)).astype(np.uint8)
+    return np.where(o < head_dim // 2, code, np.where(o < head_dim // 2 + head_dim // 16, sc, np.uint8(0)))
+
+
+def _nvfp4_range(state: int, start: int, n: int, head_dim: int, chunk: int = 1 << 18) -> np.ndarray:
+    out = np.empty(n, dtype=np.uint8)
+    for s in range(0, n, chunk):
+        e = min(n, s + chunk)
+        out[s:e] = nvfp4_bytes(state, np.arange(start + s, start + e, dtype=np.uint64), head_dim)
+    return out
+
+
 def permutation(state: int, n: int) -> np.ndarray:
     """Seeded Fisher-Yates shuffle of range(n) (Durstenfeld form, j drawn from [0, i])."""
     perm = np.arange(n, dtype=np.int64)
@@ -217,12 +251,13 @@ def make_layout(seed: int, context_lens: np.ndarray, page_size: int, pool_factor
 
 
 def _fill_pool(state: int, layout: PagedLayout, row_width: int, std: float, window: int,
-               visible_only: bool, num_query: int = 1, fp8: bool = False) -> np.ndarray:
-    """Pool [num_pages, P, row_width] bf16 bits (fp8: E4M3 codes); values drawn per logical
-    (page, slot, element)."""
+               visible_only: bool, num_query: int = 1, fp8: bool = False, nvfp4_dim: int = 0) -> np.ndarray:
+    """Pool [num_pages, P, row_width] bf16 bits (fp8: E4M3 codes; nvfp4_dim > 0: NVFP4 row bytes of
+    that head_dim); values drawn per logical (page, slot, element)."""
     P = layout.page_size
-    poison = E4M3_NAN if fp8 else BF16_NAN
-    pool = np.full((layout.num_pages, P, row_width), poison, dtype=np.uint8 if fp8 else np.uint16)
+    byte_pool = fp8 or nvfp4_dim > 0
+    poison = E4M3_NAN if byte_pool else BF16_NAN
+    pool = np.full((layout.num_pages, P, row_width), poison, dtype=np.uint8 if byte_pool else np.uint16)
     per_page = P * row_width
     for b in range(layout.batch):
         L = int(layout.context_lens[b])
@@ -231,7 +266,9 @@ def _fill_pool(state: int, layout: PagedLayout, row_width: int, std: float, wind
         lo, hi = visible_range(L, window, num_query) if visible_only else (0, L)
         p0, p1 = lo // P, (hi + P - 1) // P
         g0 = int(layout.logical_page_of_row[b])
-        if fp8:
+        if nvfp4_dim > 0:
+            vals = _nvfp4_range(state, (g0 + p0) * per_page, (p1 - p0) * per_page, nvfp4_dim)
+        elif fp8:
             vals = _codes_range(state, (g0 + p0) * per_page, (p1 - p0) * per_page)
         else:
             vals = _normal_bf16_range(state, (g0 + p0) * per_page, (p1 - p0) * per_page, std)
@@ -249,8 +286,8 @@ class GQAWorkload:
     name: str
     seed: int
     q: np.ndarray            # [B, Hq, D] bf16 bits ([B, Q, Hq, D] when num_query > 1)
-    k_pool: np.ndarray       # [num_pages, P, Hkv, D] bf16 bits (fp8: uint8 E4M3 codes)
-    v_pool: np.ndarray       # [num_pages, P, Hkv, D] bf16 bits (fp8: uint8 E4M3 codes)
+    k_pool: np.ndarray       # [num_pages, P, Hkv, D] bf16 bits (fp8: uint8 E4M3 codes; nvfp4: [.., Hkv, R] uint8 rows)
+    v_pool: np.ndarray       # the same for the values
     layout: PagedLayout
     num_q_heads: int
     num_kv_heads: int
@@ -260,8 +297,9 @@ class GQAWorkload:
     k_std: float = 1.0
     num_query: int = 1
     fp8: bool = False
-    k_scale: float = 1.0     # fp8: key = E4M3(code) * k_scale
+    k_scale: float = 1.0     # fp8: key = E4M3(code) * k_scale (nvfp4: the pool scale)
     v_scale: float = 1.0     # fp8: value = E4M3(code) * v_scale
+    nvfp4: bool = False
 
     @property
     def batch(self):
@@ -274,7 +312,10 @@ class GQAWorkload:
     def algorithmic_bytes(self) -> int:
         """Bytes the method must move: every visible K and V row of each kv head once, all of q, and
         the output (every query position of a row shares the one walk over its keys)."""
-        kv = self.visible_tokens() * self.num_kv_heads * self.head_dim * 2 * (1 if self.fp8 else 2)
+        # per row: 2 bytes per value (bf16), 1 (FP8), or 9 / 16 (NVFP4: half a byte per value and a
+        # scale byte per 16 values; the row's padding to 16 bytes is not counted)
+        row = self.head_dim * 9 // 16 if self.nvfp4 else self.head_dim * (1 if self.fp8 else 2)
+        kv = self.visible_tokens() * self.num_kv_heads * row * 2
         qb = self.batch * self.num_query * self.num_q_heads * self.head_dim * 2
         ob = self.batch * self.num_query * self.num_q_heads * (self.head_dim * 2 + 4)
         return kv + qb + ob
@@ -284,25 +325,30 @@ def make_gqa(seed: int, context_lens, num_q_heads: int, num_kv_heads: int, head_
              page_size: int, window: int = 0, k_std: float = 1.0, pool_factor: int = 1,
              scale: Optional[float] = None, scramble: bool = True, name: str = "gqa",
              visible_only: bool = True, extra_table_cols: int = 0, num_query: int = 1,
-             fp8: bool = False, k_scale: float = 1.0 / 64, v_scale: float = 1.0 / 128) -> GQAWorkload:
-    """GQA decode / verify inputs; fp8: E4M3 code pools with the given per-pool scales (k_std
-    does not apply to them)."""
+             fp8: bool = False, k_scale: float = 1.0 / 64, v_scale: float = 1.0 / 128,
+             nvfp4: bool = False) -> GQAWorkload:
+    """GQA decode / verify inputs; fp8: E4M3 code pools, nvfp4: NVFP4 row pools, either with the
+    given per-pool scales (k_std does not apply to them)."""
     lens = np.asarray(context_lens, dtype=np.int32)
     layout = make_layout(seed, lens, page_size, pool_factor, scramble, extra_table_cols)
     B = lens.shape[0]
     Q = num_query
     q = _normal_bf16_dense(stream_seed(seed, TAG_Q), B * Q * num_q_heads * head_dim, 1.0)
     q = q.reshape(B, num_q_heads, head_dim) if Q == 1 else q.reshape(B, Q, num_q_heads, head_dim)
-    w = num_kv_heads * head_dim
-    k = _fill_pool(stream_seed(seed, TAG_K), layout, w, k_std, window, visible_only, Q, fp8)
-    v = _fill_pool(stream_seed(seed, TAG_V), layout, w, 1.0, window, visible_only, Q, fp8)
-    k = k.reshape(layout.num_pages, page_size, num_kv_heads, head_dim)
-    v = v.reshape(layout.num_pages, page_size, num_kv_heads, head_dim)
+    row = nvfp4_row_bytes(head_dim) if nvfp4 else head_dim
+    w = num_kv_heads * row
+    nd = head_dim if nvfp4 else 0
+    k = _fill_pool(stream_seed(seed, TAG_K), layout, w, k_std, window, visible_only, Q, fp8, nd)
+    v = _fill_pool(stream_seed(seed, TAG_V), layout, w, 1.0, window, visible_only, Q, fp8, nd)
+    k = k.reshape(layout.num_pages, page_size, num_kv_heads, row)
+    v = v.reshape(layout.num_pages, page_size, num_kv_heads, row)
+    scaled = fp8 or nvfp4
     if scale is None:
         scale = 1.0 / math.sqrt(head_dim)
     return GQAWorkload(name, seed, q, k, v, layout, num_q_heads, num_kv_heads, head_dim,
                        float(scale), int(window), float(k_std), int(Q), bool(fp8),
-                       float(np.float32(k_scale)) if fp8 else 1.0, float(np.float32(v_scale)) if fp8 else 1.0)
+                       float(np.float32(k_scale)) if scaled else 1.0, float(np.float32(v_scale)) if scaled else 1.0,
+                       bool(nvfp4))
 
 
 MLA_NOPE, MLA_ROPE, MLA_LATENT, MLA_VDIM = 128, 64, 512, 128
@@ -377,6 +423,7 @@ class KVWriteWorkload:
     fp8: bool = False          # quantizing write into E4M3 pools
     k_scale: float = 1.0
     v_scale: float = 1.0
+    nvfp4: bool = False        # quantizing write into NVFP4 row pools
 
     @property
     def num_tokens(self) -> int:
@@ -385,19 +432,25 @@ class KVWriteWorkload:
     def pool_shape(self):
         if self.mla:
             return (self.num_pages, self.page_size, 576)
+        if self.nvfp4:
+            return (self.num_pages, self.page_size, self.k.shape[1], nvfp4_row_bytes(self.k.shape[2]))
         return (self.num_pages, self.page_size) + tuple(self.k.shape[1:])
 
     def empty_pool(self) -> np.ndarray:
-        if self.fp8:
+        if self.fp8 or self.nvfp4:
             return np.full(self.pool_shape(), E4M3_NAN, dtype=np.uint8)
         return np.full(self.pool_shape(), BF16_NAN, dtype=np.uint16)
 
     def algorithmic_bytes(self) -> int:
         """Bytes read (the bf16 new rows of the written tokens) plus bytes written (the same rows
-        in the pools: one byte per value for FP8 pools)."""
+        in the pools: one byte per value for FP8 pools, whole rows with their padding for NVFP4
+        pools)."""
         written = int((self.slots >= 0).sum())
         row_in = (576 * 2) if self.mla else 2 * int(np.prod(self.k.shape[1:])) * 2
-        row_out = row_in // 2 if self.fp8 else row_in
+        if self.nvfp4:
+            row_out = 2 * self.k.shape[1] * nvfp4_row_bytes(self.k.shape[2])
+        else:
+            row_out = row_in // 2 if self.fp8 else row_in
         return written * (row_in + row_out)
 
 
@@ -420,7 +473,7 @@ def make_kv_write(seed: int, num_tokens: int, num_kv_heads: int, head_dim: int, 
 
 
 WORKLOADS = ("tiny", "llama3-8b", "qwen3-32b", "hd256-window", "mla", "kv-write", "qwen3-32b-verify4",
-             "qwen3-32b-fp8", "kv-write-fp8")
+             "qwen3-32b-fp8", "kv-write-fp8", "qwen3-32b-nvfp4", "kv-write-nvfp4")
 
 
 def workload(name: str, seed: Optional[int] = None, scramble: bool = True):
@@ -454,6 +507,15 @@ def workload(name: str, seed: Optional[int] = None, scramble: bool = True):
         # the kv-write prefill chunk quantized into E4M3 pools (scales 1/64, 1/128)
         w = make_kv_write(20265 if seed == 20268 else seed, 16384, 8, 128, 32, 1024, name=name)
         return dataclasses.replace(w, fp8=True, k_scale=float(np.float32(1 / 64)), v_scale=float(np.float32(1 / 128)))
+    if name == "qwen3-32b-nvfp4":
+        # the qwen3-32b rows (same lengths) over an NVFP4 cache (pool scales 1/4 and 1/16)
+        lens = context_lengths(20262 if seed == 20269 else seed, 32, "loguniform", 128, 16384)
+        return make_gqa(seed, lens, 64, 8, 128, 32, name=name, scramble=scramble, nvfp4=True, k_scale=0.25,
+                        v_scale=1.0 / 16)
+    if name == "kv-write-nvfp4":
+        # the kv-write prefill chunk quantized into NVFP4 pools (pool scales 1/4, 1/2)
+        w = make_kv_write(20265 if seed == 20270 else seed, 16384, 8, 128, 32, 1024, name=name)
+        return dataclasses.replace(w, nvfp4=True, k_scale=0.25, v_scale=0.5)
     if name == "kv-write":
         # a 16384-token prefill chunk into a Qwen3-32B-shaped cache (8 KV heads, D 128, page 32)
         return make_kv_write(seed, 16384, 8, 128, 32, 1024, name=name)

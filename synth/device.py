@@ -60,8 +60,8 @@ class GqaDev:
         return bits(out), lse.cpu().numpy()
 
     def run_any(self, num_splits=0, window=None, workspace=None):
-        """One call of the entry point that serves the workload: pa_decode_gqa_fp8 for FP8
-        pools, pa_verify_gqa for several query positions, else pa_decode_gqa."""
+        """One call of the entry point that serves the workload: pa_decode_gqa_nvfp4 for NVFP4
+        pools, pa_decode_gqa_fp8 for FP8 pools, pa_verify_gqa for several query positions, else pa_decode_gqa."""
         import torch
         import paged_kv_attention_19_gb300 as pa
         w = self.w
@@ -70,7 +70,11 @@ class GqaDev:
         lse = torch.full(w.q.shape[:-1], float("nan"), dtype=torch.float32, device="cuda")
         if workspace is None:
             workspace = pa.workspace_for_gqa(self.q, self.k, self.bt, num_splits)
-        if w.fp8:
+        if w.nvfp4:
+            pa.pa_decode_gqa_nvfp4(self.q, self.k, self.v, self.bt, self.lens, out, lse, scale=w.scale,
+                                   k_scale=w.k_scale, v_scale=w.v_scale, window=win, num_splits=num_splits,
+                                   workspace=workspace)
+        elif w.fp8:
             pa.pa_decode_gqa_fp8(self.q, self.k, self.v, self.bt, self.lens, out, lse, scale=w.scale,
                                  k_scale=w.k_scale, v_scale=w.v_scale, window=win, num_splits=num_splits,
                                  workspace=workspace)
