@@ -58,7 +58,11 @@ enum PoolFmt { FMT_BF16 = 0, FMT_FP8 = 1, FMT_NVFP4 = 2 };
 
 // Tokens per stage of the split kernel (must match GqaCfg<D>::ST, GqaF8Cfg<D, *>::ST and
 // GqaFp4Cfg<D>::ST).
-int gqa_stage_tokens(int D, int fmt) { return fmt == FMT_FP8 ? (D <= 128 ? 128 : 64) : (D <= 128 ? 64 : 32); }
+int gqa_stage_tokens(int D, int fmt) {
+  if (fmt == FMT_FP8) return D <= 128 ? 128 : 64;
+  if (fmt == FMT_NVFP4) return D <= 128 ? 128 : 32;
+  return D <= 128 ? 64 : 32;
+}
 
 // Bytes of an NVFP4 pool row of D values (must match nvfp4_row_bytes in pa_gqa_fp4.cuh): D / 2
 // bytes of code pairs, D / 16 block scales, zero padding to a multiple of 16 bytes.

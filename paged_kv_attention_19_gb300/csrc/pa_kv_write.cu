@@ -18,6 +18,8 @@
 #include <cstdint>
 #include <cstring>
 
+#include <cuda_fp4.h>
+
 #include "pa_common.cuh"
 #include "pa_decode.h"
 #include "pa_launch.h"
@@ -111,15 +113,36 @@ __global__ void __launch_bounds__(256) mla_cache_write_kernel(const uint4 *__res
 // FP8: thread i converts 8 values (one 16-byte bf16 vector) of k and of v into 8 bytes of E4M3
 // codes each, so that a warp's loads and its stores are both contiguous: the fp32 quotient
 // x / scale (correctly rounded division), then the nearest code (ties to even), magnitudes
-// beyond 448 saturated.  A pool scale that is a power of
-// two with a normal reciprocal (the host checks) divides as a product with that reciprocal: both
-// round the same exact value once, so the codes are identical.
+// beyond 448 saturated.
+//
+// The correctly rounded quotient a / b is taken in one of three ways (the host picks per scale):
+//   * b a normal power of two with a normal reciprocal: the product a * (1 / b), exact;
+//   * b in [2^-100, 2^100]: Markstein's correction (P. Markstein, "Computation of elementary
+//     functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990): with
+//     y = RN(1 / b), q = RN(a y) is within one ulp of a / b, the remainder r = a - b q is exact
+//     (one fma), and RN(q + r y) is RN(a / b) whenever a and the quotient are normal numbers.  A
+//     quotient that overflows (q infinite) stays infinite.  Where a or the quotient is subnormal
+//     the result may be an ulp off, which changes no code derived from it: the quotient is then
+//     below 2^-26 and rounds to the zero code of E4M3 and of E2M1 (its sign is a's), and a block
+//     scale derived from it is the zero code;
+//   * otherwise the correctly rounded division.
 struct Fp8Scale {
-  float sc;   // the pool's scale
-  float rcp;  // 1 / sc when exact, else 0
+  float sc;    // the pool's scale b
+  float rcp;   // 1 / b when exact (a power of two), else 0
+  float rcpn;  // RN(1 / b) when b and 1 / b are normal and b is not a power of two, else 0
 };
 
-__device__ __forceinline__ float quot(float x, Fp8Scale s) { return s.rcp != 0.f ? x * s.rcp : __fdiv_rn(x, s.sc); }
+__device__ __forceinline__ float markstein_quot(float a, float b, float y) {
+  const float q = a * y;
+  const float r = fmaf(-q, b, a);
+  return fabsf(q) == INFINITY ? q : fmaf(r, y, q);
+}
+
+__device__ __forceinline__ float quot(float x, Fp8Scale s) {
+  if (s.rcp != 0.f) return x * s.rcp;
+  if (s.rcpn != 0.f) return markstein_quot(x, s.sc, s.rcpn);
+  return __fdiv_rn(x, s.sc);
+}
 
 __device__ __forceinline__ uint32_t quant4(uint32_t x0, uint32_t x1, Fp8Scale s) {
   const float2 a = make_float2(quot(__uint_as_float(x0 << 16), s), quot(__uint_as_float(x0 & 0xffff0000u), s));
@@ -155,13 +178,11 @@ struct Nvfp4Row {
   int row;       // bytes per row (a multiple of 16)
 };
 
-// Nearest E2M1 code of y: ties to the code with the even mantissa bit, saturating at 6, the sign
-// bit from y's sign (y is never NaN here).
-__device__ __forceinline__ uint32_t e2m1_code(float y) {
-  const float a = fabsf(y);
-  const uint32_t m = a <= 0.25f ? 0u : a < 0.75f ? 1u : a <= 1.25f ? 2u : a < 1.75f ? 3u
-                   : a <= 2.5f ? 4u : a < 3.5f ? 5u : a <= 5.f ? 6u : 7u;
-  return m | ((__float_as_uint(y) >> 28) & 8u);
+// Nearest E2M1 codes of two values (never NaN here): the conversion instruction rounds to nearest
+// with ties to the even mantissa bit, saturates at 6 and keeps the sign (a negative value that
+// rounds to zero gives the negative-zero code); lo goes to the low nibble.
+__device__ __forceinline__ uint32_t e2m1_pair(float lo, float hi) {
+  return (uint32_t)__nv_cvt_float2_to_fp4x2(make_float2(lo, hi), __NV_E2M1, cudaRoundNearest) & 0xffu;
 }
 
 // Value of a non-negative, non-NaN E4M3 code (exact in fp32).
@@ -198,8 +219,14 @@ __device__ __forceinline__ Nvfp4Block quant_nvfp4(uint4 x0, uint4 x1, Fp8Scale s
   const float ds = e4m3_value(b.scale);
   uint32_t c[2] = {0u, 0u};
   if (ds != 0.f) {
+    // y / ds by Markstein's correction (ds is normal or an E4M3 subnormal, at least 2^-9, so its
+    // reciprocal is normal); an infinite y (x / s overflowed) stays infinite
+    const float r = __frcp_rn(ds);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) c[i >> 3] |= e2m1_code(__fdiv_rn(y[i], ds)) << (4 * (i & 7));
+    for (int i = 0; i < 16; i += 2) {
+      const uint32_t pr = e2m1_pair(markstein_quot(y[i], ds, r), markstein_quot(y[i + 1], ds, r));
+      c[i >> 3] |= pr << (4 * (i & 7));
+    }
   }
   b.codes = make_uint2(c[0], c[1]);
   return b;
@@ -247,13 +274,18 @@ int grid_for(Kernel kernel, long long n_vec) {
   return (int)(want < cap ? want : cap);
 }
 
-// The reciprocal of a scale that is a normal power of two (exact and normal itself), else 0.
+// How x / sc is divided (see Fp8Scale): the exact reciprocal of a normal power of two whose
+// reciprocal is normal, else RN(1 / sc) for Markstein's correction when sc and 1 / sc are normal,
+// else neither (the correctly rounded division).
 Fp8Scale fp8_scale(float sc) {
   uint32_t b;
   std::memcpy(&b, &sc, 4);
   const uint32_t e = (b >> 23) & 0xffu;
   const bool pow2 = (b & 0x807fffffu) == 0 && e >= 1 && e <= 253;  // sc = 2^(e - 127), 1 / sc = 2^(127 - e)
-  return {sc, pow2 ? 1.0f / sc : 0.f};
+  if (pow2) return {sc, 1.0f / sc, 0.f};
+  const float y = 1.0f / sc;  // host IEEE division: correctly rounded
+  const bool in_range = sc >= 0x1p-100f && sc <= 0x1p100f;
+  return {sc, 0.f, in_range ? y : 0.f};
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
