@@ -115,7 +115,15 @@ struct GqaCfg {
   static constexpr int MG = TG;                    // groups merged at the end of a piece
   static constexpr int DSPLIT = 2;                 // warps sharing a token group (each: D / 2 of P.V)
   static constexpr int NCW = TG * DSPLIT;          // consumer warps
-  static constexpr int THREADS = (NCW + 1) * 32;   // + producer warp
+  // + producer warp.  With eight consumer warps the block is three warpgroups instead (the
+  // producer warp and three idle ones): one producer warp beside them would put three warps on one
+  // SM sub-partition and cap every thread at 168 registers, where the producer's warpgroup gives
+  // registers back and the consumers' two take them (launch: 384 x 168 = 256 x 208 + 128 x 88).
+  static constexpr bool REG_SPLIT = NCW == 8;
+  static constexpr int THREADS = REG_SPLIT ? (NCW + 4) * 32 : (NCW + 1) * 32;
+  static constexpr int CONSUMER_REGS = 208, PRODUCER_REGS = 88;
+  static_assert(!REG_SPLIT || NCW * 32 * CONSUMER_REGS + 128 * PRODUCER_REGS <= THREADS * 168,
+                "the register split stays within the launch's registers");
   static constexpr int NT_PV = D / 8 / DSPLIT;     // P.V n-tiles per warp
   static constexpr int NQ = D / 64;                // 128-byte swizzle planes along D
   static constexpr int QNQ = NQ;                   // the same for the query rows
@@ -852,9 +860,11 @@ __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
   PartitionArgs pargs;
   gqa_setup<C>(smem, &tm_k, &tm_v, &tm_q, a, pargs);
 
-  if (warp == C::NCW) {
-    gqa_produce<C, LW, MT>(smem, &tm_k, &tm_v, &tm_q, a, pargs);
+  if (warp >= C::NCW) {
+    if constexpr (C::REG_SPLIT) setmaxnreg_dec<C::PRODUCER_REGS>();
+    if (warp == C::NCW) gqa_produce<C, LW, MT>(smem, &tm_k, &tm_v, &tm_q, a, pargs);
   } else {
+    if constexpr (C::REG_SPLIT) setmaxnreg_inc<C::CONSUMER_REGS>();
     if constexpr (MT == 2) {
       gqa_consume_pair<C, MQ, LW>(smem, a);
     } else {

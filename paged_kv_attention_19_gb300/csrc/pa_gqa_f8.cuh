@@ -61,7 +61,15 @@ struct GqaF8Cfg {
   static constexpr int WS = NH8 == 1 ? 2 : 1;
   static constexpr int MG = TG * WS;               // groups merged at the end of a piece
   static constexpr int NCW = TG * DSPLIT * WS;     // consumer warps
-  static constexpr int THREADS = (NCW + 1) * 32;   // + producer warp
+  // + producer warp.  With eight consumer warps the block is three warpgroups instead (the
+  // producer warp and three idle ones): one producer warp beside them would put three warps on one
+  // SM sub-partition and cap every thread at 168 registers, where the producer's warpgroup gives
+  // registers back and the consumers' two take them (launch: 384 x 168 = 256 x 208 + 128 x 88).
+  static constexpr bool REG_SPLIT = NCW == 8;
+  static constexpr int THREADS = REG_SPLIT ? (NCW + 4) * 32 : (NCW + 1) * 32;
+  static constexpr int CONSUMER_REGS = 208, PRODUCER_REGS = 88;
+  static_assert(!REG_SPLIT || NCW * 32 * CONSUMER_REGS + 128 * PRODUCER_REGS <= THREADS * 168,
+                "the register split stays within the launch's registers");
   static constexpr int CH = D / DSPLIT / 16;       // 16-dim chunks (M tiles of O^T) per warp
   static constexpr int NQ = D / 128;               // 128-byte swizzle planes along D (K, V)
   static constexpr int QNQ = D / 64;               // the same for the bf16 query rows
@@ -140,9 +148,11 @@ __global__ void __launch_bounds__(GqaF8Cfg<D, NH8>::THREADS, 1)
   PartitionArgs pargs;
   gqa_setup<C>(smem, &tm_k, &tm_v, &tm_q, a, pargs);
 
-  if (warp == C::NCW) {
-    gqa_produce<C, LW, 1>(smem, &tm_k, &tm_v, &tm_q, a, pargs);
+  if (warp >= C::NCW) {
+    if constexpr (C::REG_SPLIT) setmaxnreg_dec<C::PRODUCER_REGS>();
+    if (warp == C::NCW) gqa_produce<C, LW, 1>(smem, &tm_k, &tm_v, &tm_q, a, pargs);
   } else {
+    if constexpr (C::REG_SPLIT) setmaxnreg_inc<C::CONSUMER_REGS>();
     // ------------------------------------------------------------ consumers
     const int ct = tid;
     const int g8 = lane >> 2, tq = lane & 3;          // fragment row / column pair

@@ -55,7 +55,15 @@ struct GqaFp4Cfg {
   static constexpr int MG = TG;
   static constexpr int DSPLIT = 2;
   static constexpr int NCW = TG * DSPLIT;
-  static constexpr int THREADS = (NCW + 1) * 32;
+  // With eight consumer warps, one producer warp would put three warps on one SM sub-partition and
+  // cap every thread at 168 registers (a sub-partition holds 16384).  Instead the block is three
+  // warpgroups: the producer's (the producer warp and three idle ones) gives registers back and
+  // the consumers' two take them (launch: 384 x 168 = 64512 = 256 x 208 + 128 x 88).
+  static constexpr bool REG_SPLIT = NCW == 8;
+  static constexpr int THREADS = REG_SPLIT ? (NCW + 4) * 32 : (NCW + 1) * 32;
+  static constexpr int CONSUMER_REGS = 208, PRODUCER_REGS = 88;
+  static_assert(!REG_SPLIT || NCW * 32 * CONSUMER_REGS + 128 * PRODUCER_REGS <= THREADS * 168,
+                "the register split stays within the launch's registers");
   static constexpr int NT_PV = D / 8 / DSPLIT;
   static constexpr int KSH = D / 16 / DSPLIT;      // score k-steps (16-value blocks) per warp
   static constexpr int NACC = KSH >= 2 ? 2 : 1;
@@ -209,9 +217,11 @@ __global__ void __launch_bounds__(GqaFp4Cfg<D>::THREADS, 1)
   PartitionArgs pargs;
   gqa_setup<C>(smem, &tm_k, &tm_v, &tm_q, a, pargs);
 
-  if (warp == C::NCW) {
-    gqa_produce<C, LW, 1>(smem, &tm_k, &tm_v, &tm_q, a, pargs);
+  if (warp >= C::NCW) {
+    if constexpr (C::REG_SPLIT) setmaxnreg_dec<C::PRODUCER_REGS>();
+    if (warp == C::NCW) gqa_produce<C, LW, 1>(smem, &tm_k, &tm_v, &tm_q, a, pargs);
   } else {
+    if constexpr (C::REG_SPLIT) setmaxnreg_inc<C::CONSUMER_REGS>();
     // ------------------------------------------------------------ consumers
     const int ct = tid;
     const int g8 = lane >> 2, tq = lane & 3;

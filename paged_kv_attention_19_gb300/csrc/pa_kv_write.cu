@@ -215,7 +215,9 @@ __device__ __forceinline__ Nvfp4Block quant_nvfp4(uint4 x0, uint4 x1, Fp8Scale s
     b.codes = make_uint2(0u, 0u);
     return b;
   }
-  b.scale = (uint32_t)__nv_cvt_float_to_fp8(__fdiv_rn(quot(amax, s), 6.f), __NV_SATFINITE, __NV_E4M3);
+  // (amax / s) / 6: the second division by Markstein's correction with RN(1 / 6)
+  b.scale = (uint32_t)__nv_cvt_float_to_fp8(markstein_quot(quot(amax, s), 6.f, 1.f / 6.f), __NV_SATFINITE,
+                                            __NV_E4M3);
   const float ds = e4m3_value(b.scale);
   uint32_t c[2] = {0u, 0u};
   if (ds != 0.f) {
