@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(256) kv_write_fp8_kernel(const uint4 *__restri
 // with every step correctly rounded: the scale code of (amax / s) / 6, then each value's code of
 // (x / s) / E4M3(scale code).  The thread of a row's block 0 also writes the row's padding.
 struct Nvfp4Row {
-  int nb;        // blocks per row: head_dim / 16
+  int log2_nb;   // blocks per row, head_dim / 16, as a power of two
   int code_off;  // byte offset of the block scales in a row: head_dim / 2
   int row;       // bytes per row (a multiple of 16)
 };
@@ -198,16 +198,18 @@ struct Nvfp4Block {
 
 __device__ __forceinline__ Nvfp4Block quant_nvfp4(uint4 x0, uint4 x1, Fp8Scale s) {
   const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+  // the largest magnitude as bf16 bits: the bits of |x| order like the values, NaN above infinity
+  uint32_t m2 = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m2 = __vmaxu2(m2, w[i] & 0x7fff7fffu);
+  const uint32_t mh = max(m2 & 0xffffu, m2 >> 16);
+  const bool nan = mh > 0x7f80u;
+  const float amax = __uint_as_float(mh << 16);
   float y[16];
-  float amax = 0.f;
-  bool nan = false;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
-    amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
-    nan = nan || lo != lo || hi != hi;
-    y[2 * i] = quot(lo, s);
-    y[2 * i + 1] = quot(hi, s);
+    y[2 * i] = quot(__uint_as_float(w[i] << 16), s);
+    y[2 * i + 1] = quot(__uint_as_float(w[i] & 0xffff0000u), s);
   }
   Nvfp4Block b;
   if (nan) {
@@ -238,7 +240,7 @@ struct Uint4x4 {
   uint4 k0, k1, v0, v1;
 };
 
-__global__ void __launch_bounds__(256) kv_write_nvfp4_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
+__global__ void __launch_bounds__(256, 4) kv_write_nvfp4_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
                                                              const int64_t *__restrict__ slots, uint8_t *k_pool,
                                                              uint8_t *v_pool, long long n_blk, int blk_per_token,
                                                              long long n_slots, Nvfp4Row r, Fp8Scale k_scale,
@@ -247,8 +249,8 @@ __global__ void __launch_bounds__(256) kv_write_nvfp4_kernel(const uint4 *__rest
       n_blk, blk_per_token, slots, n_slots, status,
       [&](long long i, long long, int) { return Uint4x4{k[2 * i], k[2 * i + 1], v[2 * i], v[2 * i + 1]}; },
       [&](long long slot, int e, const Uint4x4 &d) {
-        const int h = e / r.nb, blk = e - h * r.nb;
-        const long long row0 = (slot * (blk_per_token / r.nb) + h) * r.row;
+        const int h = e >> r.log2_nb, blk = e & ((1 << r.log2_nb) - 1);
+        const long long row0 = (slot * (blk_per_token >> r.log2_nb) + h) * r.row;
         const Nvfp4Block kb = quant_nvfp4(d.k0, d.k1, k_scale);
         const Nvfp4Block vb = quant_nvfp4(d.v0, d.v1, v_scale);
         *reinterpret_cast<uint2 *>(k_pool + row0 + blk * 8) = kb.codes;
@@ -256,7 +258,7 @@ __global__ void __launch_bounds__(256) kv_write_nvfp4_kernel(const uint4 *__rest
         k_pool[row0 + r.code_off + blk] = (uint8_t)kb.scale;
         v_pool[row0 + r.code_off + blk] = (uint8_t)vb.scale;
         if (blk == 0) {
-          for (int p = r.code_off + r.nb; p < r.row; p += 4) {
+          for (int p = r.code_off + (1 << r.log2_nb); p < r.row; p += 4) {
             *reinterpret_cast<uint32_t *>(k_pool + row0 + p) = 0u;
             *reinterpret_cast<uint32_t *>(v_pool + row0 + p) = 0u;
           }
@@ -366,8 +368,9 @@ extern "C" int pa_kv_write_nvfp4(const void *k, const void *v, const int64_t *sl
   if (!pa::aligned16(k) || !pa::aligned16(v) || !pa::aligned16(k_pool) || !pa::aligned16(v_pool) ||
       (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) || (reinterpret_cast<uintptr_t>(status) & 3u))
     return PA_ERR_MISALIGNED;
-  const pa::Nvfp4Row r = {head_dim / 16, head_dim / 2, (head_dim / 2 + head_dim / 16 + 15) / 16 * 16};
-  const int blk_per_token = num_kv_heads * r.nb;
+  const pa::Nvfp4Row r = {head_dim == 64 ? 2 : head_dim == 128 ? 3 : 4, head_dim / 2,
+                          (head_dim / 2 + head_dim / 16 + 15) / 16 * 16};
+  const int blk_per_token = num_kv_heads << r.log2_nb;
   const long long n_blk = (long long)num_tokens * blk_per_token;
   const int grid = pa::grid_for(pa::kv_write_nvfp4_kernel, n_blk);
   if (grid <= 0) return pa::cuda_fail(cudaGetLastError());
