@@ -138,6 +138,12 @@ __device__ __forceinline__ float markstein_quot(float a, float b, float y) {
   return fabsf(q) == INFINITY ? q : fmaf(r, y, q);
 }
 
+// The same for a quotient known to be finite (no infinite q to keep).
+__device__ __forceinline__ float markstein_quot_finite(float a, float b, float y) {
+  const float q = a * y;
+  return fmaf(fmaf(-q, b, a), y, q);
+}
+
 __device__ __forceinline__ float quot(float x, Fp8Scale s) {
   if (s.rcp != 0.f) return x * s.rcp;
   if (s.rcpn != 0.f) return markstein_quot(x, s.sc, s.rcpn);
@@ -205,11 +211,20 @@ __device__ __forceinline__ Nvfp4Block quant_nvfp4(uint4 x0, uint4 x1, Fp8Scale s
   const uint32_t mh = max(m2 & 0xffffu, m2 >> 16);
   const bool nan = mh > 0x7f80u;
   const float amax = __uint_as_float(mh << 16);
+  // x / s for the 16 values, the scale's way of dividing chosen once (it is the same for the launch)
   float y[16];
+  if (s.rcp != 0.f) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    y[2 * i] = quot(__uint_as_float(w[i] << 16), s);
-    y[2 * i + 1] = quot(__uint_as_float(w[i] & 0xffff0000u), s);
+    for (int i = 0; i < 8; ++i) {
+      y[2 * i] = __uint_as_float(w[i] << 16) * s.rcp;
+      y[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u) * s.rcp;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      y[2 * i] = quot(__uint_as_float(w[i] << 16), s);
+      y[2 * i + 1] = quot(__uint_as_float(w[i] & 0xffff0000u), s);
+    }
   }
   Nvfp4Block b;
   if (nan) {
@@ -218,18 +233,27 @@ __device__ __forceinline__ Nvfp4Block quant_nvfp4(uint4 x0, uint4 x1, Fp8Scale s
     return b;
   }
   // (amax / s) / 6: the second division by Markstein's correction with RN(1 / 6)
-  b.scale = (uint32_t)__nv_cvt_float_to_fp8(markstein_quot(quot(amax, s), 6.f, 1.f / 6.f), __NV_SATFINITE,
-                                            __NV_E4M3);
+  const float qa = quot(amax, s);
+  b.scale = (uint32_t)__nv_cvt_float_to_fp8(markstein_quot(qa, 6.f, 1.f / 6.f), __NV_SATFINITE, __NV_E4M3);
   const float ds = e4m3_value(b.scale);
   uint32_t c[2] = {0u, 0u};
   if (ds != 0.f) {
     // y / ds by Markstein's correction (ds is normal or an E4M3 subnormal, at least 2^-9, so its
-    // reciprocal is normal); an infinite y (x / s overflowed) stays infinite
+    // reciprocal is normal).  Some y is infinite (an x / s overflowed) only if amax / s is: then the
+    // infinite ones stay infinite
     const float r = __frcp_rn(ds);
+    if (fabsf(qa) != INFINITY) {
 #pragma unroll
-    for (int i = 0; i < 16; i += 2) {
-      const uint32_t pr = e2m1_pair(markstein_quot(y[i], ds, r), markstein_quot(y[i + 1], ds, r));
-      c[i >> 3] |= pr << (4 * (i & 7));
+      for (int i = 0; i < 16; i += 2) {
+        const uint32_t pr = e2m1_pair(markstein_quot_finite(y[i], ds, r), markstein_quot_finite(y[i + 1], ds, r));
+        c[i >> 3] |= pr << (4 * (i & 7));
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; i += 2) {
+        const uint32_t pr = e2m1_pair(markstein_quot(y[i], ds, r), markstein_quot(y[i + 1], ds, r));
+        c[i >> 3] |= pr << (4 * (i & 7));
+      }
     }
   }
   b.codes = make_uint2(c[0], c[1]);

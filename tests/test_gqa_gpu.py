@@ -195,17 +195,19 @@ def test_full_size_workload_every_output(name):
     gu.report(name, o.shape, st, dl)
 
 
-@pytest.mark.parametrize("kind", ["decode", "verify", "fp8"])
+@pytest.mark.parametrize("kind", ["decode", "verify", "fp8", "nvfp4"])
 def test_wait_limit_zero_gives_up_cleanly_and_next_call_is_clean(kind):
     """With a wait limit of 0 a CTA of the split kernel gives up at the first ring slot it finds
     busy (4 shares: every CTA streams thousands of stages, so its producer soon waits for the
     oldest one): the call returns, its status word reports PA_DEV_TIMEOUT, and (its outputs being
     unspecified) the next call at the default limit on the same workspace is clean and matches the
-    oracle.  The bf16 decode, the multi-query verify and the FP8 kernel."""
+    oracle.  The bf16 decode, the multi-query verify, the FP8 kernel and the NVFP4 kernel (whose
+    late warps keep meeting their token group's score-exchange barrier)."""
     import oracle
     import paged_kv_attention_19_gb300 as pa
+    scales = dict(k_scale=0.25, v_scale=1.0 / 16) if kind == "nvfp4" else {}
     w = synth.make_gqa(960, LADDER + [20000] * 6, 16, 2, 128, 32, num_query=3 if kind == "verify" else 1,
-                       fp8=kind == "fp8")
+                       fp8=kind == "fp8", nvfp4=kind == "nvfp4", **scales)
     g = gu.GqaDev(w)
     ws = pa.workspace_for_gqa(g.q, g.k, g.bt)
     try:
@@ -219,6 +221,8 @@ def test_wait_limit_zero_gives_up_cleanly_and_next_call_is_clean(kind):
     lens, bt = w.layout.context_lens, w.layout.block_table
     if kind == "fp8":
         ro, rl = oracle.gqa_fp8(w.q, w.k_pool, w.v_pool, bt, lens, w.scale, w.k_scale, w.v_scale)
+    elif kind == "nvfp4":
+        ro, rl = oracle.gqa_nvfp4(w.q, w.k_pool, w.v_pool, bt, lens, w.scale, w.k_scale, w.v_scale)
     elif kind == "verify":
         ro, rl = oracle.verify_gqa(w.q, w.k_pool, w.v_pool, bt, lens, w.scale, w.window)
     else:
