@@ -87,3 +87,37 @@ def test_fp8_codes_recipe():
         assert np.array_equal(pk, wi.k_pool[wi.layout.block_table[b, t // P], t % P])
         seen[bt[b, t // P], t % P] = True
     assert np.all(w.k_pool[~seen] == synth.E4M3_NAN) and np.all(w.v_pool[~seen] == synth.E4M3_NAN)
+
+
+def test_nvfp4_rows_recipe():
+    """NVFP4 pools: visible rows hold uniform code bytes, block-scale codes drawn per the recipe
+    (about 1/32 from 0x00..0x4F, the rest from 0x28..0x47, never NaN) and zero padding; every
+    slot no row may read holds 0x7F in every byte; the same logical rows under any page order."""
+    D = 128
+    R = synth.nvfp4_row_bytes(D)
+    assert R == 80 and synth.nvfp4_row_bytes(64) == 48 and synth.nvfp4_row_bytes(256) == 144
+    b = synth.nvfp4_bytes(synth.stream_seed(5, synth.TAG_K), np.arange(R * 4000, dtype=np.uint64), D)
+    rows = b.reshape(4000, R)
+    codes, scales, pad = rows[:, : D // 2], rows[:, D // 2: D // 2 + D // 16], rows[:, D // 2 + D // 16:]
+    assert not pad.any()
+    assert len(np.unique(codes)) == 256                     # every code byte occurs
+    assert scales.max() <= 0x4F and not np.any(scales == 0x7F)
+    wide = (scales < 0x28) | (scales > 0x47)
+    assert 0.005 < wide.mean() < 0.04
+    assert {0x00, 0x01} <= set(np.unique(scales).tolist())  # zero and the smallest subnormal scale
+    w = synth.make_gqa(9, [1, 31, 40], 8, 2, D, 16, nvfp4=True, window=20)
+    wi = synth.make_gqa(9, [1, 31, 40], 8, 2, D, 16, nvfp4=True, window=20, scramble=False)
+    assert w.k_pool.shape[2:] == (2, R) and w.k_pool.dtype == np.uint8
+    bt, P = w.layout.block_table, w.layout.page_size
+    seen = np.zeros(w.k_pool.shape[:2], dtype=bool)
+    for bi, L in enumerate(w.layout.context_lens):
+        lo, hi = synth.visible_range(int(L), w.window)
+        t = np.arange(lo, hi)
+        pk = w.k_pool[bt[bi, t // P], t % P]
+        assert not pk[..., D // 2 + D // 16:].any()
+        assert np.array_equal(pk, wi.k_pool[wi.layout.block_table[bi, t // P], t % P])
+        seen[bt[bi, t // P], t % P] = True
+    assert np.all(w.k_pool[~seen] == 0x7F) and np.all(w.v_pool[~seen] == 0x7F)
+    # the algorithmic bytes count 9/16 byte per cached value
+    vis = w.visible_tokens()
+    assert w.algorithmic_bytes() == vis * 2 * 2 * (D * 9 // 16) + 3 * 8 * D * 2 + 3 * 8 * (D * 2 + 4)
