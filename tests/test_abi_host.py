@@ -226,3 +226,47 @@ def test_last_cuda_error_starts_clean(pa):
     # no call on this thread has returned PA_ERR_CUDA: no error recorded
     assert pa.pa_last_cuda_error() == 0
     assert isinstance(pa.pa_last_cuda_error_string(), str)
+
+
+def _gqa_nvfp4(pa, **kw):
+    a = dict(q=0x10000, k=0x20000, v=0x30000, bt=0x40000, lens=0x50000, out=0x60000, lse=None, batch=2, nq=1,
+             hq=8, hkv=2, d=128, p=16, pages=10, maxp=5, maxctx=80, scale=0.1, ks=0.25, vs=0.5, window=0,
+             splits=0, ws=0x70000, wsb=1 << 30)
+    a.update(kw)
+    return pa.lib.pa_decode_gqa_nvfp4(a["q"], a["k"], a["v"], a["bt"], a["lens"], a["out"], a["lse"], a["batch"],
+                                      a["nq"], a["hq"], a["hkv"], a["d"], a["p"], a["pages"], a["maxp"],
+                                      a["maxctx"], a["scale"], a["ks"], a["vs"], a["window"], a["splits"], a["ws"],
+                                      a["wsb"], None)
+
+
+def test_gqa_nvfp4_host_validation(pa):
+    """Every rejection happens on the host, before any CUDA call (this machine has no GPU)."""
+    assert _gqa_nvfp4(pa, batch=0) == pa.PA_OK
+    assert _gqa_nvfp4(pa, ks=0.0) == pa.PA_ERR_INVALID_ARGUMENT
+    assert _gqa_nvfp4(pa, vs=-1.0) == pa.PA_ERR_INVALID_ARGUMENT
+    assert _gqa_nvfp4(pa, ks=float("inf")) == pa.PA_ERR_INVALID_ARGUMENT
+    assert _gqa_nvfp4(pa, vs=float("nan"), batch=0) == pa.PA_ERR_INVALID_ARGUMENT  # scales checked first
+    assert _gqa_nvfp4(pa, d=96) == pa.PA_ERR_UNSUPPORTED
+    assert _gqa_nvfp4(pa, p=12) == pa.PA_ERR_UNSUPPORTED
+    assert _gqa_nvfp4(pa, nq=0) == pa.PA_ERR_INVALID_ARGUMENT
+    assert _gqa_nvfp4(pa, nq=65) == pa.PA_ERR_UNSUPPORTED
+    assert _gqa_nvfp4(pa, k=None) == pa.PA_ERR_INVALID_ARGUMENT
+    assert _gqa_nvfp4(pa, v=0x30008) == pa.PA_ERR_MISALIGNED
+    assert _gqa_nvfp4(pa, wsb=1024) == pa.PA_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_kv_write_nvfp4_host_validation(pa):
+    kw = lambda **a: pa.lib.pa_kv_write_nvfp4(a.get("k", 0x10000), a.get("v", 0x20000), a.get("s", 0x30000),
+                                              a.get("kp", 0x40000), a.get("vp", 0x50000), a.get("T", 4),
+                                              a.get("H", 2), a.get("D", 64), a.get("P", 16), a.get("pages", 4),
+                                              a.get("ks", 0.5), a.get("vs", 0.5), a.get("st", None), None)
+    assert kw(T=0) == pa.PA_OK
+    assert kw(T=-1) == pa.PA_ERR_INVALID_ARGUMENT
+    assert kw(ks=0.0) == pa.PA_ERR_INVALID_ARGUMENT
+    assert kw(vs=float("nan")) == pa.PA_ERR_INVALID_ARGUMENT
+    assert kw(D=96) == pa.PA_ERR_UNSUPPORTED           # head_dim 64, 128 or 256
+    assert kw(D=32) == pa.PA_ERR_UNSUPPORTED
+    assert kw(kp=None) == pa.PA_ERR_INVALID_ARGUMENT
+    assert kw(vp=0x50008) == pa.PA_ERR_MISALIGNED
+    assert kw(s=0x30004) == pa.PA_ERR_MISALIGNED
+    assert kw(st=0x60002) == pa.PA_ERR_MISALIGNED
