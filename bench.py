@@ -196,7 +196,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             threading.Thread(target=self._read, daemon=True).start()
         except Exception:
@@ -217,7 +217,7 @@ class ClockSampler:
     def summary(self):
         rows = [(t, s.split(", ")) for t, s in self.samples]
         if self.t0 is not None:
-            inside = [(t, r) for t, r in rows if self.t0 - 0.15 <= t <= self.t1 + 0.15]
+            inside = [(t, r) for t, r in rows if self.t0 - 0.05 <= t <= self.t1 + 0.05]
             rows = inside or rows
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
