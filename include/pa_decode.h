@@ -379,7 +379,8 @@ int pa_last_launch_count(void);
 
 /*
  * Limit of the waits on the stage ring of the GQA split-KV kernels
- * (pa_decode_gqa, pa_verify_gqa, pa_decode_gqa_fp8 and the no-alloc decode),
+ * (pa_decode_gqa, pa_verify_gqa, pa_decode_gqa_fp8, pa_decode_gqa_nvfp4 and the
+ * no-alloc decode),
  * in nanoseconds of the device's global timer, for later calls from the
  * calling host thread.  The pages have no counterpart: it is a diagnostic
  * for checking that the kernels leave cleanly when a wait does not complete.
