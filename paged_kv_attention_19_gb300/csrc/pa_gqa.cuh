@@ -1097,9 +1097,10 @@ struct CombineArgs {
 // first + hg, ..., last (its pieces in ascending token order; a CTA in between whose range held no
 // visible key left an empty slot, lse -inf, that weighs nothing).  Warp w handles row w of the
 // sequence's slots, i.e. MMA row w % 16 of its tile w / 16, each lane owning D/32 dims: an online
-// log-sum-exp merge (running max, rescaled sum and accumulator) whose loads of one partial -- its
-// LSE and values -- are independent of the others', so after the table lookup the merge is one
-// trip to L2.  The indices read from the tables are range-checked.
+// log-sum-exp merge (running max, rescaled sum and accumulator).  The partials (LSE and values) of
+// up to four pieces are loaded together before any of them is merged, so after the table lookup a
+// sequence of at most four pieces costs one trip to L2.  The indices read from the tables are
+// range-checked.
 constexpr int COMBINE_THREADS = PART_ROWS * 32;  // the largest block: two tiles
 template <int D>
 __global__ void __launch_bounds__(COMBINE_THREADS) gqa_combine_kernel(const CombineArgs a) {
@@ -1129,37 +1130,51 @@ __global__ void __launch_bounds__(COMBINE_THREADS) gqa_combine_kernel(const Comb
   const int r = h % PART_HEADS;  // the MMA row of the tile
   if (r >= tl.nq * a.gt || r % a.gt >= tl.nh) return;
   constexpr int PER = D / 32;  // 2, 4 or 8 consecutive dims per lane
+  constexpr int CHUNK = 4;     // pieces whose partials are loaded together (one trip to L2)
   float M = -INFINITY, Z = 0.f, acc[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-#pragma unroll 4
-  for (int i = 0; i < k; ++i) {
-    const size_t pi = i == 0 ? (size_t)f : (size_t)(c0 + i * a.hg) * 2;
-    const float l = a.part_lse[pi * PART_ROWS + h];
-    float x[PER];
-    const float *po = a.part_o + (pi * PART_ROWS + h) * D + lane * PER;
-    if constexpr (PER == 2) {
-      const float2 v = *reinterpret_cast<const float2 *>(po);
-      x[0] = v.x;
-      x[1] = v.y;
-    } else {
+  for (int i0 = 0; i0 < k; i0 += CHUNK) {
+    float lc[CHUNK], x[CHUNK][PER];
 #pragma unroll
-      for (int e = 0; e < PER; e += 4) {
-        const float4 v = *reinterpret_cast<const float4 *>(po + e);
-        x[e] = v.x;
-        x[e + 1] = v.y;
-        x[e + 2] = v.z;
-        x[e + 3] = v.w;
+    for (int u = 0; u < CHUNK; ++u) {
+      const int i = i0 + u;
+      lc[u] = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < PER; ++e) x[u][e] = 0.f;
+      if (i < k) {
+        const size_t pi = i == 0 ? (size_t)f : (size_t)(c0 + i * a.hg) * 2;
+        lc[u] = a.part_lse[pi * PART_ROWS + h];
+        const float *po = a.part_o + (pi * PART_ROWS + h) * D + lane * PER;
+        if constexpr (PER == 2) {
+          const float2 v = *reinterpret_cast<const float2 *>(po);
+          x[u][0] = v.x;
+          x[u][1] = v.y;
+        } else {
+#pragma unroll
+          for (int e = 0; e < PER; e += 4) {
+            const float4 v = *reinterpret_cast<const float4 *>(po + e);
+            x[u][e] = v.x;
+            x[u][e + 1] = v.y;
+            x[u][e + 2] = v.z;
+            x[u][e + 3] = v.w;
+          }
+        }
       }
     }
-    if (l != -INFINITY) {
-      const float mn = fmaxf(M, l);
-      const float sc = M == -INFINITY ? 0.f : fast_exp2(M - mn);
-      const float wc = fast_exp2(l - mn);
-      M = mn;
-      Z = Z * sc + wc;
+    // the online merge in ascending piece order, as before
 #pragma unroll
-      for (int e = 0; e < PER; ++e) acc[e] = acc[e] * sc + wc * x[e];
+    for (int u = 0; u < CHUNK; ++u) {
+      const float l = lc[u];
+      if (l != -INFINITY) {
+        const float mn = fmaxf(M, l);
+        const float sc = M == -INFINITY ? 0.f : fast_exp2(M - mn);
+        const float wc = fast_exp2(l - mn);
+        M = mn;
+        Z = Z * sc + wc;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc[e] = acc[e] * sc + wc * x[u][e];
+      }
     }
   }
   const float inv = Z > 0.f ? 1.f / Z : 0.f;
