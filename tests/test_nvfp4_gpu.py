@@ -53,7 +53,8 @@ def _check(w, o, l, rows=None):
 
 
 @pytest.mark.parametrize("hq,hkv,D,P", [(8, 2, 128, 32), (64, 8, 128, 32), (16, 4, 256, 32), (32, 2, 128, 16),
-                                        (4, 4, 64, 8), (40, 2, 256, 64), (12, 2, 64, 256), (32, 1, 256, 16)])
+                                        (4, 4, 64, 8), (40, 2, 256, 64), (12, 2, 64, 256), (32, 1, 256, 16),
+                                        (8, 2, 256, 8), (16, 2, 128, 8), (20, 1, 128, 128)])
 def test_nvfp4_decode_ladder(hq, hkv, D, P):
     w = _gqa(700 + hq + D + P, LADDER, hq, hkv, D, P)
     o, l = _run(w)
