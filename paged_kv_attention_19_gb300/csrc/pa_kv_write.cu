@@ -202,7 +202,13 @@ struct Nvfp4Block {
   uint32_t scale;
 };
 
-__device__ __forceinline__ Nvfp4Block quant_nvfp4(uint4 x0, uint4 x1, Fp8Scale s) {
+// The value of each non-negative E4M3 scale code and its correctly rounded reciprocal (0 for the
+// zero code), tabulated once per thread block.
+struct E4m3Table {
+  float val[128], rcp[128];
+};
+
+__device__ __forceinline__ Nvfp4Block quant_nvfp4(uint4 x0, uint4 x1, Fp8Scale s, const E4m3Table &tab) {
   const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
   // the largest magnitude as bf16 bits: the bits of |x| order like the values, NaN above infinity
   uint32_t m2 = 0;
@@ -235,13 +241,14 @@ __device__ __forceinline__ Nvfp4Block quant_nvfp4(uint4 x0, uint4 x1, Fp8Scale s
   // (amax / s) / 6: the second division by Markstein's correction with RN(1 / 6)
   const float qa = quot(amax, s);
   b.scale = (uint32_t)__nv_cvt_float_to_fp8(markstein_quot(qa, 6.f, 1.f / 6.f), __NV_SATFINITE, __NV_E4M3);
-  const float ds = e4m3_value(b.scale);
+  // the code is never NaN here (a NaN block returned above): 0 .. 126
+  const float ds = tab.val[b.scale];
   uint32_t c[2] = {0u, 0u};
   if (ds != 0.f) {
     // y / ds by Markstein's correction (ds is normal or an E4M3 subnormal, at least 2^-9, so its
     // reciprocal is normal).  Some y is infinite (an x / s overflowed) only if amax / s is: then the
     // infinite ones stay infinite
-    const float r = __frcp_rn(ds);
+    const float r = tab.rcp[b.scale];
     if (fabsf(qa) != INFINITY) {
 #pragma unroll
       for (int i = 0; i < 16; i += 2) {
@@ -269,14 +276,21 @@ __global__ void __launch_bounds__(256, 4) kv_write_nvfp4_kernel(const uint4 *__r
                                                              uint8_t *v_pool, long long n_blk, int blk_per_token,
                                                              long long n_slots, Nvfp4Row r, Fp8Scale k_scale,
                                                              Fp8Scale v_scale, uint32_t *status) {
+  __shared__ E4m3Table tab;
+  if (threadIdx.x < 128) {
+    const float x = e4m3_value(threadIdx.x);
+    tab.val[threadIdx.x] = x;
+    tab.rcp[threadIdx.x] = x != 0.f ? __frcp_rn(x) : 0.f;
+  }
+  __syncthreads();
   write_loop<1>(
       n_blk, blk_per_token, slots, n_slots, status,
       [&](long long i, long long, int) { return Uint4x4{k[2 * i], k[2 * i + 1], v[2 * i], v[2 * i + 1]}; },
       [&](long long slot, int e, const Uint4x4 &d) {
         const int h = e >> r.log2_nb, blk = e & ((1 << r.log2_nb) - 1);
         const long long row0 = (slot * (blk_per_token >> r.log2_nb) + h) * r.row;
-        const Nvfp4Block kb = quant_nvfp4(d.k0, d.k1, k_scale);
-        const Nvfp4Block vb = quant_nvfp4(d.v0, d.v1, v_scale);
+        const Nvfp4Block kb = quant_nvfp4(d.k0, d.k1, k_scale, tab);
+        const Nvfp4Block vb = quant_nvfp4(d.v0, d.v1, v_scale, tab);
         *reinterpret_cast<uint2 *>(k_pool + row0 + blk * 8) = kb.codes;
         *reinterpret_cast<uint2 *>(v_pool + row0 + blk * 8) = vb.codes;
         k_pool[row0 + r.code_off + blk] = (uint8_t)kb.scale;
