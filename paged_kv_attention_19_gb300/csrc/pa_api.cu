@@ -135,6 +135,24 @@ bool encode_pool_map(CUtensorMap *m, const void *base, int num_pages, int P, int
   return r == CUDA_SUCCESS;
 }
 
+// 5-D map over a [num_pages, P, H, D] pool of bf16 values seen as (64 dims, P tokens, D / 64
+// planes, H heads, pages): the plane stride (128 bytes) is below the token stride.  Box = (64 dims,
+// BH tokens, all planes, 1 head, 1 page): one copy brings a unit's rows of every plane, landing as
+// the planes' BH 128-byte rows one after the other, with the 128-byte swizzle (the unit-major stage
+// blocks of the bf16 split kernel, head_dim 128 and 256).
+bool encode_pool_units_map(CUtensorMap *m, const void *base, int num_pages, int P, int H, int D, int BH) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[5] = {64u, (cuuint64_t)P, (cuuint64_t)(D / 64), (cuuint64_t)H, (cuuint64_t)num_pages};
+  cuuint64_t strides[4] = {(cuuint64_t)H * D * 2, 128u, (cuuint64_t)D * 2, (cuuint64_t)P * H * D * 2};
+  cuuint32_t box[5] = {64u, (cuuint32_t)BH, (cuuint32_t)(D / 64), 1u, 1u};
+  cuuint32_t estr[5] = {1u, 1u, 1u, 1u, 1u};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 4-D map over a [num_pages, P, H, R] pool of NVFP4 rows (R bytes each); box = (one whole row,
 // 1 head, BH tokens, 1 page), no swizzle: the box's rows land as consecutive R-byte rows.
 bool encode_nvfp4_map(CUtensorMap *m, const void *base, int num_pages, int P, int H, int R, int BH) {
@@ -263,10 +281,15 @@ int gqa_call(const void *q, const void *k_pool, const void *v_pool, const int32_
   const int nseqh = (ntile + mt - 1) / mt;
   CUtensorMap tm_k, tm_v, tm_q;
   const int esz = fp8 ? 1 : 2;
+  // decode over bf16 pages of fewer than 32 tokens with more than one 64-dim plane: the unit-major
+  // kernel, whose producer fills a unit of all planes by one 5-D copy
+  const bool units = !fp8 && !fp4 && D > 64 && BH < 32 && Q == 1 && mt == 1;
   const bool maps_ok =
-      fp4 ? encode_nvfp4_map(&tm_k, k_pool, num_pages, P, num_kv_heads, nvfp4_row(D), BH) &&
+      fp4     ? encode_nvfp4_map(&tm_k, k_pool, num_pages, P, num_kv_heads, nvfp4_row(D), BH) &&
                 encode_nvfp4_map(&tm_v, v_pool, num_pages, P, num_kv_heads, nvfp4_row(D), BH)
-          : encode_pool_map(&tm_k, k_pool, num_pages, P, num_kv_heads, D, BH, esz) &&
+      : units ? encode_pool_units_map(&tm_k, k_pool, num_pages, P, num_kv_heads, D, BH) &&
+                encode_pool_units_map(&tm_v, v_pool, num_pages, P, num_kv_heads, D, BH)
+              : encode_pool_map(&tm_k, k_pool, num_pages, P, num_kv_heads, D, BH, esz) &&
                 encode_pool_map(&tm_v, v_pool, num_pages, P, num_kv_heads, D, BH, esz);
   if (!maps_ok || !encode_q_map(&tm_q, q, (long long)batch * Q, num_q_heads, D, gt, qt)) return PA_ERR_UNSUPPORTED;
   const int sms = sm_count();
@@ -310,6 +333,7 @@ int gqa_call(const void *q, const void *k_pool, const void *v_pool, const int32_
   ga.nseqh = nseqh;
   ga.log2_page = ilog2(P);
   ga.log2_bh = ilog2(BH);
+  ga.unit_copy = units ? 1 : 0;
   ga.nparts = nparts;
   ga.hg = hs < nparts ? hs : nparts;
   {

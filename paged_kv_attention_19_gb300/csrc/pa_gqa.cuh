@@ -91,6 +91,7 @@ struct GqaArgs {
   int gt, qt, ntile;            // a tile of MMA rows: qt positions x gt heads; ntile tiles per KV head
   int mt, nseqh;                // tiles per sequence (1 or 2) and sequences per KV head (ntile / mt, rounded up)
   int log2_page, log2_bh;       // page size and tokens per unit (TMA box), as powers of two
+  int unit_copy;                // 1: the unit-major kernel (GqaUnitCfg) and a 5-D pool map
   int piece_cost;               // partition cost of starting a piece, in units
   int nparts;                   // CTAs (shares); groups of hg consecutive CTAs
   int hg;                       // CTAs per group: min(Hkv * nseqh, nparts)
@@ -107,6 +108,8 @@ struct GqaCfg {
   static constexpr bool F8 = false;                // pools of bf16 values
   static constexpr int ROWB = 128;                 // bytes of a token's row in one plane of a stage
   static constexpr int XSTEP = 64;                 // tensor-map x of consecutive planes (bf16 values)
+  // A stage's K (and V) block is plane-major: its NQ planes of ST 128-byte rows (see kv_off).
+  static constexpr bool UNIT_MAJOR = false;
   static constexpr int M = PART_HEADS;             // MMA rows = query heads per subgroup
   static constexpr int MR = M;                     // rows per token group in the end-of-piece merge
   static constexpr int ST = D <= 128 ? 64 : 32;    // tokens per stage
@@ -134,6 +137,15 @@ struct GqaCfg {
   static constexpr int NACC = 2;                   // independent QK accumulators
   static constexpr int QAREA = 0;                  // query rows kept outside the ring (none)
   static_assert(MR * D * 4 * MG <= STAGE_BYTES, "the end-of-piece merge fits the consumed stage");
+};
+
+// Unit-major stage blocks (decode over pages of fewer than 32 tokens, head_dim 128 and 256): per
+// unit (one box of BH tokens) its NQ planes of BH 128-byte rows, so that one 5-D copy brings all
+// planes of a unit.  A copy costs the producer about the same whatever its size, and the
+// plane-major order takes NQ copies per unit (16 per stage at page 16, head_dim 128).
+template <int D_>
+struct GqaUnitCfg : GqaCfg<D_> {
+  static constexpr bool UNIT_MAJOR = true;
 };
 
 // Two 16-row tiles per sequence (gqa_consume_pair): the piece's query rows of both tiles are copied
@@ -177,12 +189,20 @@ struct GqaSmem {
   static_assert(BYTES <= 232448, "fits the 227 KB opt-in shared memory of one CTA");
 };
 
-// Byte offset of 16-byte chunk `chunk` (along D) of token row `tok` in a
-// stage's K or V block: planes of 64 dims, 128-byte rows, chunk ^ (row & 7)
-// (the TMA 128-byte swizzle; every box starts on a 1024-byte boundary).
+// Byte offset of 16-byte chunk `chunk` (along D) of token row `tok` in a stage's K or V block of
+// 128-byte rows, chunk ^ (row & 7) (the TMA 128-byte swizzle; every plane of a box starts on a
+// 1024-byte boundary since a unit holds at least 8 tokens).  Plane-major (C::UNIT_MAJOR false):
+// the stage's planes of 64 dims one after the other.  Unit-major: per unit of 2^lbh tokens its
+// planes one after the other (the two orders agree when a unit is the whole stage).
 template <class C>
-__device__ __forceinline__ uint32_t kv_off(int tok, int chunk) {
-  return (uint32_t)((chunk >> 3) * C::PLANE + tok * 128 + (((chunk & 7) ^ (tok & 7)) << 4));
+__device__ __forceinline__ uint32_t kv_off(int tok, int chunk, int lbh) {
+  if constexpr (C::UNIT_MAJOR && C::NQ > 1) {
+    constexpr int LNQ = C::NQ == 4 ? 2 : 1;
+    const int row = ((tok >> lbh) << (lbh + LNQ)) + ((chunk >> 3) << lbh) + (tok & ((1 << lbh) - 1));
+    return (uint32_t)(row * 128 + (((chunk & 7) ^ (tok & 7)) << 4));
+  } else {
+    return (uint32_t)((chunk >> 3) * C::PLANE + tok * 128 + (((chunk & 7) ^ (tok & 7)) << 4));
+  }
 }
 
 // Tile t of a KV head's query rows: positions [i0, i0 + nq), heads [h0, h0 + nh) of the
@@ -423,12 +443,19 @@ __device__ __forceinline__ void gqa_produce(uint8_t *smem, const CUtensorMap *tm
       __syncwarp();
       if (load) {
         const int pslot = btok & (P - 1);
-        uint8_t *dst = kdst + (lane << a.log2_bh) * C::ROWB;
+        if constexpr (C::UNIT_MAJOR && C::NQ > 1) {
+          // one copy per unit and pool: (64 dims, the unit's tokens, all planes, head g, page)
+          uint8_t *dst = kdst + (lane << a.log2_bh) * (C::NQ * C::ROWB);
+          tma_load_5d(dst, tm_k, 0, pslot, 0, g, phys, &full[s]);
+          tma_load_5d(dst + C::KV_BYTES, tm_v, 0, pslot, 0, g, phys, &full[s]);
+        } else {
+          uint8_t *dst = kdst + (lane << a.log2_bh) * C::ROWB;
 #pragma unroll
-        for (int dq = 0; dq < C::NQ; ++dq) {
-          const int x = dq * C::XSTEP;  // C::ROWB bytes of the row per plane
-          tma_load_4d(dst + dq * C::PLANE, tm_k, x, g, pslot, phys, &full[s]);
-          tma_load_4d(dst + dq * C::PLANE + C::KV_BYTES, tm_v, x, g, pslot, phys, &full[s]);
+          for (int dq = 0; dq < C::NQ; ++dq) {
+            const int x = dq * C::XSTEP;  // C::ROWB bytes of the row per plane
+            tma_load_4d(dst + dq * C::PLANE, tm_k, x, g, pslot, phys, &full[s]);
+            tma_load_4d(dst + dq * C::PLANE + C::KV_BYTES, tm_v, x, g, pslot, phys, &full[s]);
+          }
         }
       }
     }
@@ -607,6 +634,7 @@ __device__ __forceinline__ void gqa_consume_pair(uint8_t *smem, const GqaArgs &a
   const int wbase = tgrp * C::TW;                   // first stage token of this warp
   const float TAU = 8.f;
   const int bh_tokens = 1 << a.log2_bh;
+  const int lbh = a.log2_bh;  // tokens per unit, log2 (the stage layout of kv_off)
   const uint32_t qarea = smem_u32(smem + S::OFF_QAREA) + x * QOFF1;
   // one QK accumulator per n-tile: the tile's 64 P.V accumulators fill the registers (two
   // accumulators spilled and were 2 us slower on the 4-position verify workload)
@@ -687,7 +715,7 @@ __device__ __forceinline__ void gqa_consume_pair(uint8_t *smem, const GqaArgs &a
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) {
             uint32_t b[4];
-            ldmatrix_x4(b, kbase + kv_off<C>(wbase + nt * 8 + lm_row, 4 * ks2 + lm_mat));
+            ldmatrix_x4(b, kbase + kv_off<C>(wbase + nt * 8 + lm_row, 4 * ks2 + lm_mat, lbh));
             mma_bf16_16816(sp[(2 * ks2) % NACC][nt], qf[0], b[0], b[1]);
             mma_bf16_16816(sp[(2 * ks2 + 1) % NACC][nt], qf[1], b[2], b[3]);
           }
@@ -769,7 +797,7 @@ __device__ __forceinline__ void gqa_consume_pair(uint8_t *smem, const GqaArgs &a
           const int chunk = e % CPR;
           const int ltok = mt.tok0 + stok;
           if (ltok < mt.tok_lo || ltok >= mt.tok_hi || ((mt.badmask >> (stok / bh_tokens)) & 1u))
-            *reinterpret_cast<uint4 *>(vgen + kv_off<C>(stok, chunk)) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4 *>(vgen + kv_off<C>(stok, chunk, lbh)) = make_uint4(0, 0, 0, 0);
         }
         __syncwarp();
       }
@@ -779,7 +807,7 @@ __device__ __forceinline__ void gqa_consume_pair(uint8_t *smem, const GqaArgs &a
 #pragma unroll
         for (int nd = 0; nd < NTF; nd += 2) {
           uint32_t b[4];
-          ldmatrix_x4_trans(b, vbase + kv_off<C>(tok, nd + (lm_mat >> 1)));
+          ldmatrix_x4_trans(b, vbase + kv_off<C>(tok, nd + (lm_mat >> 1), lbh));
           mma_bf16_16816(acc[nd], pa, b[0], b[1]);
           mma_bf16_16816(acc[nd + 1], pa, b[2], b[3]);
         }
@@ -836,14 +864,16 @@ __device__ __forceinline__ void gqa_consume_pair(uint8_t *smem, const GqaArgs &a
 // (position, head) rows: verify with more than 16 rows per KV head, or more than 16 heads per
 // group): each K or V fragment a warp loads from the stage feeds the MMAs of both tiles, so a page
 // crosses shared memory once for all of the head's rows.
-template <int D, int MT>
-using GqaCfgOf = std::conditional_t<MT == 2, GqaPairCfg<D>, GqaCfg<D>>;
+// UM: unit-major stage blocks (GqaUnitCfg; one-tile sequences).
+template <int D, int MT, bool UM = false>
+using GqaCfgOf = std::conditional_t<MT == 2, GqaPairCfg<D>, std::conditional_t<UM, GqaUnitCfg<D>, GqaCfg<D>>>;
 
-template <int D, bool MQ, bool LW, int MT>
+template <int D, bool MQ, bool LW, int MT, bool UM = false>
 __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
     gqa_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_q, const GqaArgs a) {
-  using C = GqaCfgOf<D, MT>;
+  using C = GqaCfgOf<D, MT, UM>;
+  static_assert(!UM || MT == 1, "unit-major stage blocks serve one-tile sequences");
   using S = GqaSmem<C>;
   static_assert(MT == 1 || MT == 2, "one or two tiles per sequence");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -879,6 +909,7 @@ __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
       float *sm_ml = reinterpret_cast<float *>(smem + S::OFF_ML);
       const float TAU = 8.f;
       const int bh_tokens = 1 << a.log2_bh;
+      const int lbh = a.log2_bh;  // tokens per unit, log2 (the stage layout of kv_off)
 
       uint32_t qa[D / 16][4];  // Q A-fragments (rows = heads)
       float acc[C::NT_PV][4];  // O C-fragments of this warp's columns: [n-tile][row g8 x2, row g8+8 x2]
@@ -942,7 +973,7 @@ __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
   #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
               uint32_t b[4];
-              ldmatrix_x4(b, kbase + kv_off<C>(wbase + nt * 8 + lm_row, 4 * ks2 + lm_mat));
+              ldmatrix_x4(b, kbase + kv_off<C>(wbase + nt * 8 + lm_row, 4 * ks2 + lm_mat, lbh));
               mma_bf16_16816(sp[(2 * ks2) % C::NACC][nt], qa[2 * ks2], b[0], b[1]);
               mma_bf16_16816(sp[(2 * ks2 + 1) % C::NACC][nt], qa[2 * ks2 + 1], b[2], b[3]);
             }
@@ -1024,7 +1055,7 @@ __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
             const int chunk = dh * CPW + e % CPW;
             const int ltok = mt.tok0 + stok;
             if (ltok < mt.tok_lo || ltok >= mt.tok_hi || ((mt.badmask >> (stok / bh_tokens)) & 1u))
-              *reinterpret_cast<uint4 *>(vgen + kv_off<C>(stok, chunk)) = make_uint4(0, 0, 0, 0);
+              *reinterpret_cast<uint4 *>(vgen + kv_off<C>(stok, chunk, lbh)) = make_uint4(0, 0, 0, 0);
           }
           __syncwarp();
         }
@@ -1034,7 +1065,7 @@ __global__ void __launch_bounds__(GqaCfg<D>::THREADS, 1)
   #pragma unroll
           for (int nd = 0; nd < C::NT_PV; nd += 2) {
             uint32_t b[4];
-            ldmatrix_x4_trans(b, vbase + kv_off<C>(tok, nd0 + nd + (lm_mat >> 1)));
+            ldmatrix_x4_trans(b, vbase + kv_off<C>(tok, nd0 + nd + (lm_mat >> 1), lbh));
             mma_bf16_16816(acc[nd], pa, b[0], b[1]);
             mma_bf16_16816(acc[nd + 1], pa, b[2], b[3]);
           }

@@ -45,6 +45,7 @@ struct GqaF8Cfg {
   static constexpr bool F8 = true;                 // pools of E4M3 codes
   static constexpr int ROWB = 128;                 // bytes of a token's row in one plane of a stage
   static constexpr int XSTEP = 128;                // tensor-map x of consecutive planes (one-byte codes)
+  static constexpr bool UNIT_MAJOR = false;        // plane-major stage blocks, one copy per plane
   static constexpr int NH8 = NH8_;
   static constexpr int M = PART_HEADS;             // rows of a partial slot
   static constexpr int MR = 8 * NH8;               // rows per token group in the end-of-piece merge
@@ -284,7 +285,7 @@ __global__ void __launch_bounds__(GqaF8Cfg<D, NH8>::THREADS, 1)
 #pragma unroll
           for (int k = 0; k < D / 32; ++k) {
             uint32_t ak[4];
-            ldmatrix_x4(ak, kbase + kv_off<C>(wbase + 16 * m + (lm_mat & 1) * 8 + lm_row, 2 * k + (lm_mat >> 1)));
+            ldmatrix_x4(ak, kbase + kv_off<C>(wbase + 16 * m + (lm_mat & 1) * 8 + lm_row, 2 * k + (lm_mat >> 1), a.log2_bh));
 #pragma unroll
             for (int n = 0; n < NH8; ++n) {
               mma_e4m3_16832(sv[m][n], ak, qh[k][n][0], qh[k][n][1]);
@@ -379,7 +380,7 @@ __global__ void __launch_bounds__(GqaF8Cfg<D, NH8>::THREADS, 1)
             const int chunk = dh * CPW + e % CPW;
             const int ltok = mt.tok0 + stok;
             if (ltok < mt.tok_lo || ltok >= mt.tok_hi || ((mt.badmask >> (stok / bh_tokens)) & 1u))
-              *reinterpret_cast<uint4 *>(vgen + kv_off<C>(stok, chunk)) = make_uint4(0, 0, 0, 0);
+              *reinterpret_cast<uint4 *>(vgen + kv_off<C>(stok, chunk, a.log2_bh)) = make_uint4(0, 0, 0, 0);
           }
           __syncwarp();
         }
@@ -389,7 +390,7 @@ __global__ void __launch_bounds__(GqaF8Cfg<D, NH8>::THREADS, 1)
 #pragma unroll
         for (int c = 0; c < C::CH; ++c) {
           uint32_t r[4];  // token octets 0-7, 8-15, 16-23, 24-31
-          ldmatrix_x4_trans(r, vbase + kv_off<C>(wbase + lane, dh * C::CH + c));
+          ldmatrix_x4_trans(r, vbase + kv_off<C>(wbase + lane, dh * C::CH + c, a.log2_bh));
           const uint32_t av[4] = {prmt(r[0], r[1], 0x6420u), prmt(r[0], r[1], 0x7531u), prmt(r[2], r[3], 0x6420u),
                                   prmt(r[2], r[3], 0x7531u)};
 #pragma unroll

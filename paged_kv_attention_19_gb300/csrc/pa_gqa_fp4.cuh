@@ -46,6 +46,7 @@ struct GqaFp4Cfg {
   static constexpr bool F8 = false;
   static constexpr int ROWB = nvfp4_row_bytes(D);  // bytes of a token's row (codes, scales, padding)
   static constexpr int XSTEP = 0;                  // one plane: the whole row
+  static constexpr bool UNIT_MAJOR = false;        // (one plane: either order)
   static constexpr int M = PART_HEADS;
   static constexpr int MR = M;
   static constexpr int ST = D <= 128 ? 128 : 32;   // tokens per stage

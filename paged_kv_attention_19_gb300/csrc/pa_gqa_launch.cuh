@@ -51,6 +51,11 @@ template <int D, bool LW, int MT>
 cudaError_t launch_split_mt(int grid, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const CUtensorMap &tm_q,
                             const GqaArgs &a, cudaStream_t stream) {
   using C = GqaCfgOf<D, MT>;
+  if constexpr (MT == 1 && D > 64) {
+    if (a.unit_copy)  // decode over small pages: the unit-major kernel (its pool maps are 5-D)
+      return launch_split_kernel<GqaCfgOf<D, 1, true>, gqa_split_kernel<D, false, LW, 1, true>>(grid, tm_k, tm_v,
+                                                                                              tm_q, a, stream);
+  }
   return a.Q > 1 ? launch_split_kernel<C, gqa_split_kernel<D, true, LW, MT>>(grid, tm_k, tm_v, tm_q, a, stream)
                  : launch_split_kernel<C, gqa_split_kernel<D, false, LW, MT>>(grid, tm_k, tm_v, tm_q, a, stream);
 }

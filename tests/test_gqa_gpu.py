@@ -63,10 +63,25 @@ def test_window_at_least_length_is_no_window_bitwise():
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
-def test_scrambled_vs_identity_pages_bitwise():
+@pytest.mark.parametrize("D", [128, 256])
+@pytest.mark.parametrize("P", [8, 16])
+@pytest.mark.parametrize("window", [0, 5, 33, 100])
+def test_unit_major_stages(D, P, window):
+    """Decode over pages of fewer than 32 tokens at head_dim 128 and 256 runs the kernel whose stage
+    blocks are unit-major (a unit's planes filled by one 5-D copy): the ladder, with windows that
+    mask stages at every offset within a unit, and several split counts."""
+    w = synth.make_gqa(1100 + D + P + window, LADDER + [4096], 8, 2, D, P, window=window)
+    g = gu.GqaDev(w)
+    for splits in (0, 5, 64):
+        o, l = g.run(num_splits=splits)
+        gu.check_gqa(w, o, l)
+
+
+@pytest.mark.parametrize("P", [16, 32])
+def test_scrambled_vs_identity_pages_bitwise(P):
     for splits in (0, 3):
-        a = synth.make_gqa(400, LADDER, 8, 2, 128, 32, scramble=True)
-        b = synth.make_gqa(400, LADDER, 8, 2, 128, 32, scramble=False)
+        a = synth.make_gqa(400, LADDER, 8, 2, 128, P, scramble=True)
+        b = synth.make_gqa(400, LADDER, 8, 2, 128, P, scramble=False)
         assert not np.array_equal(a.layout.block_table, b.layout.block_table)
         oa, la = gu.GqaDev(a).run(num_splits=splits)
         ob, lb = gu.GqaDev(b).run(num_splits=splits)
@@ -195,18 +210,20 @@ def test_full_size_workload_every_output(name):
     gu.report(name, o.shape, st, dl)
 
 
-@pytest.mark.parametrize("kind", ["decode", "verify", "fp8", "nvfp4"])
+@pytest.mark.parametrize("kind", ["decode", "decode-page16", "verify", "fp8", "nvfp4"])
 def test_wait_limit_zero_gives_up_cleanly_and_next_call_is_clean(kind):
     """With a wait limit of 0 a CTA of the split kernel gives up at the first ring slot it finds
     busy (4 shares: every CTA streams thousands of stages, so its producer soon waits for the
     oldest one): the call returns, its status word reports PA_DEV_TIMEOUT, and (its outputs being
     unspecified) the next call at the default limit on the same workspace is clean and matches the
-    oracle.  The bf16 decode, the multi-query verify, the FP8 kernel and the NVFP4 kernel (whose
-    late warps keep meeting their token group's score-exchange barrier)."""
+    oracle.  The bf16 decode (plane-major stages at page 32, unit-major at page 16), the multi-query
+    verify, the FP8 kernel and the NVFP4 kernel (whose late warps keep meeting their token group's
+    score-exchange barrier)."""
     import oracle
     import paged_kv_attention_19_gb300 as pa
     scales = dict(k_scale=0.25, v_scale=1.0 / 16) if kind == "nvfp4" else {}
-    w = synth.make_gqa(960, LADDER + [20000] * 6, 16, 2, 128, 32, num_query=3 if kind == "verify" else 1,
+    w = synth.make_gqa(960, LADDER + [20000] * 6, 16, 2, 128, 16 if kind == "decode-page16" else 32,
+                       num_query=3 if kind == "verify" else 1,
                        fp8=kind == "fp8", nvfp4=kind == "nvfp4", **scales)
     g = gu.GqaDev(w)
     ws = pa.workspace_for_gqa(g.q, g.k, g.bt)
